@@ -1,0 +1,277 @@
+"""Seeded synthetic inputs for decode attention, shared by the tests, the
+benchmark and the smoke check.
+
+This module holds no attention arithmetic: it only draws random numbers,
+rounds them to the device storage types and lays them out in the shapes the
+IncreFlashAttention / SparseFlashAttention pages define.  Host arrays use
+``numpy.float16`` for fp16, ``numpy.uint16`` bit patterns for bf16 and
+``numpy.int8`` for int8.
+
+Workload recipes (value distributions and structure follow the decode
+workloads this library is measured on):
+
+* ``tiny_mha``      B=1, N=KV_N=8, D=64, BNSD fp16, S=128, lengths [128]
+* ``gqa_padded``    B=16, N=32, KV_N=8, D=128, BSH bf16, Smax=4096,
+                    lengths ~ U{1..4096}, bool mask (B,1,1,S) true past each length
+* ``paged_gqa``     B=64, N=32, KV_N=8, D=128, bf16, blockSize=128,
+                    cache (blocknum, KV_N, 128, D), blockTable a random permutation
+                    of the physical blocks, lengths ~ U{512..32768}
+* ``int8_leftpad``  B=32, N=64, KV_N=8, D=128, fp16 query, BNSD int8 K/V ~ U{-127..127},
+                    per-channel scale ~ U[0.005,0.02], offset ~ U[-4,4], Smax=8192,
+                    lengths ~ U{256..8192}, kvPaddingSize = Smax - length - U{0..64}
+* ``sfa_mla``       B=32, Q_N=128, KV_N=1, D=512 + rope 64, bf16, PA_BSND block 64,
+                    KV length 32768, sparse_indices (B,1,1,2048): U{1024..2048} distinct
+                    indices < length in random order, then a -1 tail
+
+Every generator takes shrink arguments so tests can build the same structure
+at sizes the CPU oracle finishes in seconds.
+"""
+from __future__ import annotations
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+from typing import Any, Dict, Optional
+
+import numpy as np
+
+_CHUNK = 1 << 22  # elements per independently seeded chunk (fixed: results do not depend on threads)
+
+
+def _pool_map(fn, n):
+    workers = max(1, min(32, os.cpu_count() or 1))
+    if n <= 1 or workers == 1:
+        return [fn(i) for i in range(n)]
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(fn, range(n)))
+
+
+def _children(seed: int, tag: int, n: int):
+    return np.random.SeedSequence(entropy=int(seed), spawn_key=(int(tag),)).spawn(n)
+
+
+def normal_f32(seed: int, tag: int, shape) -> np.ndarray:
+    """N(0,1) float32 array, filled in fixed-size chunks with spawned seeds."""
+    size = int(np.prod(shape))
+    out = np.empty(size, dtype=np.float32)
+    n = max(1, math.ceil(size / _CHUNK))
+    kids = _children(seed, tag, n)
+
+    def fill(i):
+        lo, hi = i * _CHUNK, min(size, (i + 1) * _CHUNK)
+        np.random.default_rng(kids[i]).standard_normal(out=out[lo:hi], dtype=np.float32)
+
+    _pool_map(fill, n)
+    return out.reshape(shape)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16 (round to nearest even), returned as uint16 bits."""
+    flat = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    out = np.empty(flat.size, dtype=np.uint16)
+    n = max(1, math.ceil(flat.size / _CHUNK))
+
+    def conv(i):
+        lo, hi = i * _CHUNK, min(flat.size, (i + 1) * _CHUNK)
+        u = flat[lo:hi].view(np.uint32)
+        r = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+        out[lo:hi] = ((u + r) >> np.uint32(16)).astype(np.uint16)
+
+    _pool_map(conv, n)
+    return out.reshape(x.shape)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "fp16":
+        return x.astype(np.float16)
+    if dtype == "bf16":
+        return f32_to_bf16_bits(x)
+    raise ValueError(dtype)
+
+
+def random_storage(seed: int, tag: int, shape, dtype: str) -> np.ndarray:
+    return to_storage(normal_f32(seed, tag, shape), dtype)
+
+
+def uniform_int8(seed: int, tag: int, shape, lo: int = -127, hi: int = 127) -> np.ndarray:
+    size = int(np.prod(shape))
+    out = np.empty(size, dtype=np.int8)
+    n = max(1, math.ceil(size / _CHUNK))
+    kids = _children(seed, tag, n)
+
+    def fill(i):
+        a, b = i * _CHUNK, min(size, (i + 1) * _CHUNK)
+        out[a:b] = np.random.default_rng(kids[i]).integers(lo, hi + 1, size=b - a, dtype=np.int8)
+
+    _pool_map(fill, n)
+    return out.reshape(shape)
+
+
+@dataclass
+class IfaCase:
+    """One incremental-attention problem: host arrays plus the call attributes."""
+    name: str
+    query: np.ndarray
+    key: np.ndarray
+    value: np.ndarray
+    num_heads: int
+    num_kv_heads: int
+    scale: float
+    layout: str = "BNSD"          # query layout (and contiguous key/value layout)
+    kv_format: str = "contig"     # contig | paged_nbsd | paged_bsh
+    q_dtype: str = "bf16"
+    kv_dtype: str = "bf16"        # bf16 | fp16 | int8
+    max_seq_len: int = 0          # contiguous S (Smax)
+    block_size: int = 0
+    block_table: Optional[np.ndarray] = None
+    atten_mask: Optional[np.ndarray] = None
+    actual_seq_lengths: Optional[np.ndarray] = None
+    kv_padding_size: Optional[np.ndarray] = None
+    antiquant: str = "none"       # none | per_channel | per_tensor
+    antiquant_scale: Optional[np.ndarray] = None
+    antiquant_offset: Optional[np.ndarray] = None
+    meta: Dict[str, Any] = field(default_factory=dict)
+
+    @property
+    def B(self) -> int:
+        return self.query.shape[0]
+
+    @property
+    def D(self) -> int:
+        return self.query.size // (self.B * self.num_heads)
+
+
+@dataclass
+class SfaCase:
+    name: str
+    query: np.ndarray           # (B, 1, Q_N, D)
+    query_rope: np.ndarray      # (B, 1, Q_N, Dr)
+    key: np.ndarray             # (block_num, block_size, 1, D)
+    key_rope: np.ndarray        # (block_num, block_size, 1, Dr)
+    value: np.ndarray           # (block_num, block_size, 1, D)
+    sparse_indices: np.ndarray  # (B, 1, 1, sparse_size) int32
+    block_table: np.ndarray     # (B, cols) int32
+    actual_seq_lengths_kv: np.ndarray  # (B,) int32
+    scale: float
+    dtype: str = "bf16"
+    meta: Dict[str, Any] = field(default_factory=dict)
+
+    @property
+    def B(self) -> int:
+        return self.query.shape[0]
+
+
+def _lengths(rng, B, lo, hi):
+    return rng.integers(lo, hi + 1, size=B, dtype=np.int64)
+
+
+def _block_table(rng, lens, block_size, cols):
+    """Random permutation of exactly the blocks the lengths need; -1 elsewhere."""
+    need = [(int(l) + block_size - 1) // block_size for l in lens]
+    blocknum = max(1, sum(need))
+    perm = rng.permutation(blocknum).astype(np.int32)
+    bt = np.full((len(lens), cols), -1, dtype=np.int32)
+    off = 0
+    for b, nb in enumerate(need):
+        bt[b, :nb] = perm[off:off + nb]
+        off += nb
+    return bt, blocknum
+
+
+def query_shape(layout, B, N, D):
+    if layout == "BNSD":
+        return (B, N, 1, D)
+    if layout == "BSND":
+        return (B, 1, N, D)
+    return (B, 1, N * D)
+
+
+def kv_shape(layout, B, KV_N, S, D):
+    if layout == "BNSD":
+        return (B, KV_N, S, D)
+    if layout == "BSND":
+        return (B, S, KV_N, D)
+    return (B, S, KV_N * D)
+
+
+def tiny_mha(seed: int = 0, B=1, N=8, D=64, S=128, dtype="fp16") -> IfaCase:
+    lens = np.full(B, S, dtype=np.int64)
+    return IfaCase("tiny_mha", random_storage(seed, 1, query_shape("BNSD", B, N, D), dtype),
+                   random_storage(seed, 2, kv_shape("BNSD", B, N, S, D), dtype),
+                   random_storage(seed, 3, kv_shape("BNSD", B, N, S, D), dtype),
+                   num_heads=N, num_kv_heads=N, scale=1.0 / math.sqrt(D), layout="BNSD",
+                   q_dtype=dtype, kv_dtype=dtype, max_seq_len=S, actual_seq_lengths=lens)
+
+
+def gqa_padded(seed: int = 0, B=16, N=32, KV_N=8, D=128, Smax=4096, layout="BSH", dtype="bf16",
+               mask=True, len_lo=1, len_hi=None) -> IfaCase:
+    rng = np.random.default_rng(seed)
+    lens = _lengths(rng, B, len_lo, Smax if len_hi is None else len_hi)
+    m = None
+    if mask:
+        m = (np.arange(Smax)[None, :] >= lens[:, None]).reshape(B, 1, 1, Smax)
+    return IfaCase("gqa_padded", random_storage(seed, 1, query_shape(layout, B, N, D), dtype),
+                   random_storage(seed, 2, kv_shape(layout, B, KV_N, Smax, D), dtype),
+                   random_storage(seed, 3, kv_shape(layout, B, KV_N, Smax, D), dtype),
+                   num_heads=N, num_kv_heads=KV_N, scale=1.0 / math.sqrt(D), layout=layout,
+                   q_dtype=dtype, kv_dtype=dtype, max_seq_len=Smax, atten_mask=m,
+                   actual_seq_lengths=lens)
+
+
+def paged_gqa(seed: int = 0, B=64, N=32, KV_N=8, D=128, block_size=128, len_lo=512,
+              len_hi=32768, dtype="bf16", kv_format="paged_nbsd", bt_cols=None) -> IfaCase:
+    rng = np.random.default_rng(seed)
+    lens = _lengths(rng, B, len_lo, len_hi)
+    cols = bt_cols or (len_hi + block_size - 1) // block_size
+    bt, blocknum = _block_table(rng, lens, block_size, cols)
+    if kv_format == "paged_nbsd":
+        shape = (blocknum, KV_N, block_size, D)
+    else:
+        shape = (blocknum, block_size, KV_N * D)
+    return IfaCase("paged_gqa", random_storage(seed, 1, (B, N, 1, D), dtype),
+                   random_storage(seed, 2, shape, dtype), random_storage(seed, 3, shape, dtype),
+                   num_heads=N, num_kv_heads=KV_N, scale=1.0 / math.sqrt(D), layout="BNSD",
+                   kv_format=kv_format, q_dtype=dtype, kv_dtype=dtype, block_size=block_size,
+                   block_table=bt, actual_seq_lengths=lens, meta={"blocknum": blocknum})
+
+
+def int8_leftpad(seed: int = 0, B=32, N=64, KV_N=8, D=128, Smax=8192, len_lo=256, len_hi=8192,
+                 pad_extra=64, per_tensor=False, q_dtype="fp16") -> IfaCase:
+    rng = np.random.default_rng(seed)
+    lens = _lengths(rng, B, len_lo, len_hi)
+    u = rng.integers(0, pad_extra + 1, size=B, dtype=np.int64)
+    pads = Smax - lens - u  # may be negative near Smax; the operator clamps it
+    pshape = (2,) if per_tensor else (2, KV_N, 1, D)
+    scale = to_storage(rng.uniform(0.005, 0.02, size=pshape).astype(np.float32), q_dtype)
+    offset = to_storage(rng.uniform(-4.0, 4.0, size=pshape).astype(np.float32), q_dtype)
+    return IfaCase("int8_leftpad", random_storage(seed, 1, (B, N, 1, D), q_dtype),
+                   uniform_int8(seed, 2, (B, KV_N, Smax, D)),
+                   uniform_int8(seed, 3, (B, KV_N, Smax, D)),
+                   num_heads=N, num_kv_heads=KV_N, scale=1.0 / math.sqrt(D), layout="BNSD",
+                   q_dtype=q_dtype, kv_dtype="int8", max_seq_len=Smax, actual_seq_lengths=lens,
+                   kv_padding_size=pads, antiquant="per_tensor" if per_tensor else "per_channel",
+                   antiquant_scale=scale, antiquant_offset=offset)
+
+
+def sfa_mla(seed: int = 0, B=32, Q_N=128, D=512, Dr=64, block_size=64, kv_len=32768,
+            sparse_size=2048, nvalid_lo=1024, nvalid_hi=2048, dtype="bf16") -> SfaCase:
+    rng = np.random.default_rng(seed)
+    cols = (kv_len + block_size - 1) // block_size
+    block_num = B * cols
+    bt = rng.permutation(block_num).astype(np.int32).reshape(B, cols)
+    idx = np.full((B, 1, 1, sparse_size), -1, dtype=np.int32)
+    for b in range(B):
+        nv = int(rng.integers(nvalid_lo, nvalid_hi + 1))
+        idx[b, 0, 0, :nv] = rng.choice(kv_len, size=nv, replace=False).astype(np.int32)
+    lens = np.full(B, kv_len, dtype=np.int32)
+    return SfaCase("sfa_mla", random_storage(seed, 1, (B, 1, Q_N, D), dtype),
+                   random_storage(seed, 4, (B, 1, Q_N, Dr), dtype),
+                   random_storage(seed, 2, (block_num, block_size, 1, D), dtype),
+                   random_storage(seed, 5, (block_num, block_size, 1, Dr), dtype),
+                   random_storage(seed, 3, (block_num, block_size, 1, D), dtype),
+                   idx, bt, lens, scale=1.0 / math.sqrt(D + Dr), dtype=dtype)

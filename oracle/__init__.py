@@ -1,0 +1,174 @@
+"""CPU oracle for single-query decode attention (IncreFlashAttention) and for
+sparse-index MLA-absorb decode (SparseFlashAttention).
+
+TEST INFRASTRUCTURE: only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package.  The product path (the
+CUDA library and its binding) never loads it, and this package imports
+nothing from the product.
+
+The arithmetic lives in ``ifa_oracle.c`` (plain double-precision loops, see
+its header for the definitions and readings).  This module compiles it with
+gcc on first use and marshals numpy arrays into it.
+
+Dtype conventions of the inputs (shared with the seeded input generators):
+fp16 arrays are ``numpy.float16``; bf16 arrays are ``numpy.uint16`` holding
+the bf16 bit patterns; int8 arrays are ``numpy.int8``; masks are one byte per
+element (bool, int8 or uint8), nonzero meaning "excluded".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ifa_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "libifa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F16, BF16, I8 = 0, 1, 2
+BSH, BSND, BNSD = 0, 1, 2
+CONTIG, PAGED_NBSD, PAGED_BSH = 0, 1, 2
+AQ_NONE, AQ_PER_CHANNEL, AQ_PER_TENSOR = 0, 1, 2
+
+_LAYOUT = {"BSH": BSH, "BSND": BSND, "BNSD": BNSD}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build`` (plain C, -O2, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-Wall",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, ip, vp, dp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_double
+            lib.ifa_oracle_run.restype = ctypes.c_int
+            lib.ifa_oracle_run.argtypes = [i64, i64, i64, i64, ip, ip, ip, ip, i64, i64, i64, i64,
+                                           vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, vp, ip,
+                                           vp, vp, dp, vp]
+            lib.sfa_oracle_run.restype = ctypes.c_int
+            lib.sfa_oracle_run.argtypes = [i64, i64, i64, i64, ip, i64, i64, i64, i64,
+                                           vp, vp, vp, vp, vp, vp, vp, vp, dp, vp]
+            _lib = lib
+    return _lib
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float16:
+        return F16
+    if a.dtype == np.uint16:
+        return BF16
+    if a.dtype == np.int8:
+        return I8
+    raise TypeError(f"unsupported oracle input dtype {a.dtype}")
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype=None):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a if dtype is None else np.asarray(a, dtype=dtype))
+    return a
+
+
+def ifa_ref(query, key, value, *, num_heads, num_kv_heads=0, scale, layout="BNSD",
+            kv_format=CONTIG, block_size=0, block_table=None, atten_mask=None,
+            actual_seq_lengths=None, kv_padding_size=None, antiquant=AQ_NONE,
+            antiquant_scale=None, antiquant_offset=None):
+    """Reference output, float64 array of shape (B, numHeads, D).
+
+    query: (B,N,1,D) BNSD, (B,1,N,D) BSND or (B,1,H) BSH.
+    key/value: contiguous in the same layout, or a paged cache
+    (blocknum, KV_N, blockSize, D) for ``PAGED_NBSD`` / (blocknum, blockSize, H)
+    for ``PAGED_BSH``.  atten_mask: (Bm, Nm, 1, S) with Bm in {1, B}, Nm in
+    {1, numHeads}.  antiquant_scale/offset: (2, KV_N, D)-shaped memory
+    (per channel) or (2,) (per tensor), in the query dtype.
+    """
+    lib = _load()
+    q = _c(query)
+    k = _c(key)
+    v = _c(value)
+    B = q.shape[0]
+    N = int(num_heads)
+    kvn = int(num_kv_heads) or N
+    D = q.size // (B * N)
+    lay = _LAYOUT[layout]
+    if kv_format == CONTIG:
+        if lay == BNSD:
+            smax = k.shape[2]
+        else:
+            smax = k.shape[1]
+        block_num = 0
+        bt_cols = 0
+    else:
+        block_num = k.shape[0]
+        smax = 0
+        bt_cols = np.asarray(block_table).shape[1]
+    bt = _c(block_table, np.int32) if block_table is not None else None
+    m = None
+    mB = mN = mS = 0
+    if atten_mask is not None:
+        m = _c(atten_mask).view(np.uint8)
+        mB, mN, mS = m.shape[0], m.shape[1], m.shape[-1]
+    lens = _c(actual_seq_lengths, np.int64)
+    pads = _c(kv_padding_size, np.int64)
+    if pads is not None:
+        pads = pads.reshape(-1)
+    sc = _c(antiquant_scale)
+    of = _c(antiquant_offset)
+    out = np.zeros((B, N, D), dtype=np.float64)
+    rc = lib.ifa_oracle_run(B, N, kvn, D, _dtype_code(q), _dtype_code(k), lay, kv_format, smax,
+                            int(block_size), bt_cols, block_num, _ptr(q), _ptr(k), _ptr(v),
+                            _ptr(m), mB, mN, mS, _ptr(lens), _ptr(pads),
+                            0 if pads is None else pads.size, _ptr(bt), int(antiquant),
+                            _ptr(sc), _ptr(of), float(scale), _ptr(out))
+    if rc < 0:
+        raise ValueError("oracle rejected its arguments")
+    return out
+
+
+def sfa_ref(query, query_rope, key, key_rope, value, sparse_indices, block_table,
+            actual_seq_lengths_kv, *, scale):
+    """Reference sparse MLA-absorb decode output, float64 (B, Q_N, D).
+
+    query (B,1,Q_N,D), query_rope (B,1,Q_N,Dr), key/value (block_num, block_size, 1, D),
+    key_rope (block_num, block_size, 1, Dr), sparse_indices (B,1,1,sparse_size) int32,
+    block_table (B, cols) int32, actual_seq_lengths_kv (B,) int32.
+    """
+    lib = _load()
+    q = _c(query)
+    qr = _c(query_rope)
+    k = _c(key)
+    kr = _c(key_rope)
+    v = _c(value)
+    idx = _c(sparse_indices, np.int32)
+    bt = _c(block_table, np.int32)
+    lens = _c(actual_seq_lengths_kv, np.int32)
+    B, Q_N, D = q.shape[0], q.shape[2], q.shape[3]
+    Dr = qr.shape[3]
+    block_num, block_size = k.shape[0], k.shape[1]
+    out = np.zeros((B, Q_N, D), dtype=np.float64)
+    rc = lib.sfa_oracle_run(B, Q_N, D, Dr, _dtype_code(q), block_size, block_num, bt.shape[1],
+                            idx.shape[-1], _ptr(q), _ptr(qr), _ptr(k), _ptr(kr), _ptr(v),
+                            _ptr(idx), _ptr(bt), _ptr(lens), float(scale), _ptr(out))
+    if rc < 0:
+        raise ValueError("oracle rejected its arguments")
+    return out

@@ -1,0 +1,477 @@
+"""Pins of the CPU oracle to facts the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: the worked
+example of the aclnnIncreFlashAttentionV2 page, closed forms of softmax
+attention, invariants the IncreFlashAttention / SparseFlashAttention pages
+state (GQA head sharing, page-attention addressing, left padding, masking,
+sparse selection), and torch's float64 softmax on small shapes.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_cache_incremental_split_gb300 import inputs as gen
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def as_f64(a, dtype):
+    if dtype == "fp16":
+        return np.asarray(a, dtype=np.float16).astype(np.float64)
+    if dtype == "bf16":
+        return gen.bf16_bits_to_f32(a).astype(np.float64)
+    return np.asarray(a).astype(np.float64)
+
+
+def torch_attention(q, k, v, scale, valid=None):
+    """float64 softmax(q k^T * scale) v for one head; q (D,), k/v (T, D)."""
+    q = torch.as_tensor(q, dtype=torch.float64)
+    k = torch.as_tensor(k, dtype=torch.float64)
+    v = torch.as_tensor(v, dtype=torch.float64)
+    if valid is not None:
+        sel = torch.as_tensor(np.nonzero(valid)[0])
+        k, v = k[sel], v[sel]
+    if k.shape[0] == 0:
+        return np.zeros(v.shape[1])
+    p = torch.softmax((k @ q) * scale, dim=0)
+    return (p @ v).numpy()
+
+
+def run(case, **over):
+    kw = dict(num_heads=case.num_heads, num_kv_heads=case.num_kv_heads, scale=case.scale,
+              layout=case.layout, atten_mask=case.atten_mask,
+              actual_seq_lengths=case.actual_seq_lengths, kv_padding_size=case.kv_padding_size)
+    kw.update(over)
+    return oracle.ifa_ref(case.query, case.key, case.value, **kw)
+
+
+# ---------------------------------------------------------------- worked example
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *rest = line.split()
+            vals[key] = rest
+    return vals
+
+
+def test_worked_example_of_the_v2_page():
+    g = _read_golden("aclnn_ifa_v2_example.txt")
+    B, N, KV_N, D, S = (int(g[k][0]) for k in ("B", "N", "KV_N", "D", "S"))
+    fill = float(g["fill"][0])
+    q = np.full((B, N, 1, D), fill, dtype=np.float16)
+    k = np.full((B, KV_N, S, D), fill, dtype=np.float16)
+    v = np.full((B, KV_N, S, D), fill, dtype=np.float16)
+    mask = np.full([int(x) for x in g["mask_shape"]], int(g["mask_fill"][0]), dtype=np.int8)
+    lens = np.array([int(x) for x in g["actual_seq_lengths"]], dtype=np.int64)
+    out = oracle.ifa_ref(q, k, v, num_heads=N, num_kv_heads=KV_N, scale=float(g["scale"][0]),
+                         layout=g["layout"][0], atten_mask=mask, actual_seq_lengths=lens)
+    expected = np.array([float(x) for x in g["expected"]])
+    assert out.size == expected.size == 32
+    assert np.array_equal(out.reshape(-1), expected)
+
+
+# ---------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_matches_torch_float64_softmax(dtype):
+    """Small GQA problems against torch's float64 softmax on the same widened values."""
+    for seed in range(3):
+        case = gen.gqa_padded(seed, B=3, N=6, KV_N=2, D=16, Smax=37, layout="BNSD", dtype=dtype,
+                              mask=False, len_lo=1)
+        out = run(case)
+        q = as_f64(case.query, dtype).reshape(3, 6, 16)
+        k = as_f64(case.key, dtype)
+        v = as_f64(case.value, dtype)
+        for b in range(3):
+            L = int(case.actual_seq_lengths[b])
+            for n in range(6):
+                h = n // 3
+                ref = torch_attention(q[b, n], k[b, h, :L], v[b, h, :L], case.scale)
+                np.testing.assert_allclose(out[b, n], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_constant_value_rows_give_that_constant():
+    case = gen.gqa_padded(4, B=2, N=4, KV_N=2, D=32, Smax=50, layout="BNSD", dtype="fp16", mask=False)
+    case.value = np.full_like(case.value, np.float16(0.375))
+    out = run(case)
+    np.testing.assert_allclose(out, 0.375, rtol=1e-14, atol=0)
+
+
+def test_identical_keys_give_mean_of_values():
+    case = gen.gqa_padded(5, B=2, N=4, KV_N=2, D=16, Smax=40, layout="BNSD", dtype="fp16", mask=False)
+    case.key = np.broadcast_to(case.key[:, :, :1, :], case.key.shape).copy()
+    out = run(case)
+    v = as_f64(case.value, "fp16")
+    for b in range(2):
+        L = int(case.actual_seq_lengths[b])
+        for n in range(4):
+            np.testing.assert_allclose(out[b, n], v[b, n // 2, :L].mean(axis=0), rtol=1e-12, atol=1e-14)
+
+
+def test_zero_query_gives_mean_of_values():
+    case = gen.gqa_padded(6, B=2, N=2, KV_N=1, D=16, Smax=33, layout="BSND", dtype="bf16", mask=False)
+    case.query = np.zeros_like(case.query)
+    out = run(case)
+    v = as_f64(case.value, "bf16")  # (B, S, KV_N, D)
+    for b in range(2):
+        L = int(case.actual_seq_lengths[b])
+        for n in range(2):
+            np.testing.assert_allclose(out[b, n], v[b, :L, 0].mean(axis=0), rtol=1e-12, atol=1e-14)
+
+
+def test_single_valid_token_returns_its_value_row():
+    case = gen.gqa_padded(7, B=3, N=4, KV_N=2, D=16, Smax=20, layout="BNSD", dtype="bf16", mask=False)
+    case.actual_seq_lengths = np.array([1, 1, 1], dtype=np.int64)
+    out = run(case)
+    v = as_f64(case.value, "bf16")
+    for b in range(3):
+        for n in range(4):
+            assert np.array_equal(out[b, n], v[b, n // 2, 0])
+    # the same through the mask: only position 5 survives
+    case.actual_seq_lengths = np.array([20, 20, 20], dtype=np.int64)
+    m = np.ones((3, 1, 1, 20), dtype=bool)
+    m[:, :, :, 5] = False
+    out = run(case, atten_mask=m)
+    for b in range(3):
+        for n in range(4):
+            assert np.array_equal(out[b, n], v[b, n // 2, 5])
+
+
+# ---------------------------------------------------------------- invariants on the pages
+
+def test_gqa_equals_explicitly_repeated_kv_heads():
+    """numHeads a multiple of numKeyValueHeads (IncreFlashAttention README constraints)."""
+    case = gen.gqa_padded(8, B=2, N=8, KV_N=2, D=16, Smax=30, layout="BNSD", dtype="fp16", mask=False)
+    out_gqa = run(case)
+    G = 4
+    rep_k = np.repeat(case.key, G, axis=1)   # head n <- kv head n // G
+    rep_v = np.repeat(case.value, G, axis=1)
+    out_mha = oracle.ifa_ref(case.query, rep_k, rep_v, num_heads=8, num_kv_heads=8,
+                             scale=case.scale, layout="BNSD",
+                             actual_seq_lengths=case.actual_seq_lengths)
+    assert np.array_equal(out_gqa, out_mha)
+
+
+def test_num_kv_heads_zero_means_equal_to_num_heads():
+    case = gen.gqa_padded(9, B=2, N=3, KV_N=3, D=16, Smax=12, layout="BNSD", dtype="fp16", mask=False)
+    assert np.array_equal(run(case, num_kv_heads=0), run(case, num_kv_heads=3))
+
+
+@pytest.mark.parametrize("layout", ["BSH", "BSND"])
+def test_layouts_describe_the_same_problem(layout):
+    ref = gen.gqa_padded(10, B=2, N=4, KV_N=2, D=16, Smax=21, layout="BNSD", dtype="bf16", mask=False)
+    q = ref.query.reshape(2, 4, 16)
+    k = np.transpose(ref.key, (0, 2, 1, 3))   # (B, S, KV_N, D)
+    v = np.transpose(ref.value, (0, 2, 1, 3))
+    if layout == "BSH":
+        q2, k2, v2 = q.reshape(2, 1, 64), k.reshape(2, 21, 32), v.reshape(2, 21, 32)
+    else:
+        q2, k2, v2 = q.reshape(2, 1, 4, 16), k, v
+    out = oracle.ifa_ref(q2, k2, v2, num_heads=4, num_kv_heads=2, scale=ref.scale, layout=layout,
+                         actual_seq_lengths=ref.actual_seq_lengths)
+    assert np.array_equal(out, run(ref))
+
+
+@pytest.mark.parametrize("block_size", [16, 48, 5])
+def test_paged_equals_contiguous(block_size):
+    """Token t of batch b lives in block blockTable[b][t // blockSize], slot t % blockSize."""
+    rng = np.random.default_rng(11)
+    case = gen.gqa_padded(11, B=3, N=4, KV_N=2, D=16, Smax=100, layout="BNSD", dtype="bf16", mask=False)
+    lens = case.actual_seq_lengths
+    nblk = [(int(l) + block_size - 1) // block_size for l in lens]
+    total = sum(nblk) + 3  # a few unused physical blocks
+    perm = rng.permutation(total)
+    cols = (100 + block_size - 1) // block_size
+    bt = np.full((3, cols), -1, dtype=np.int32)
+    cache_k = np.zeros((total, 2, block_size, 16), dtype=np.uint16)
+    cache_v = np.zeros_like(cache_k)
+    off = 0
+    for b in range(3):
+        for j in range(nblk[b]):
+            blk = perm[off]; off += 1
+            bt[b, j] = blk
+            n_tok = min(block_size, int(lens[b]) - j * block_size)
+            cache_k[blk, :, :n_tok] = case.key[b, :, j * block_size:j * block_size + n_tok]
+            cache_v[blk, :, :n_tok] = case.value[b, :, j * block_size:j * block_size + n_tok]
+    out_nbsd = oracle.ifa_ref(case.query, cache_k, cache_v, num_heads=4, num_kv_heads=2,
+                              scale=case.scale, layout="BNSD", kv_format=oracle.PAGED_NBSD,
+                              block_size=block_size, block_table=bt, actual_seq_lengths=lens)
+    bsh_k = np.transpose(cache_k, (0, 2, 1, 3)).reshape(total, block_size, 32)
+    bsh_v = np.transpose(cache_v, (0, 2, 1, 3)).reshape(total, block_size, 32)
+    out_bsh = oracle.ifa_ref(case.query, bsh_k, bsh_v, num_heads=4, num_kv_heads=2,
+                             scale=case.scale, layout="BNSD", kv_format=oracle.PAGED_BSH,
+                             block_size=block_size, block_table=bt, actual_seq_lengths=lens)
+    ref = run(case)
+    assert np.array_equal(out_nbsd, ref)
+    assert np.array_equal(out_bsh, ref)
+
+
+def test_left_padded_window_equals_right_padded_cache():
+    """Window [Smax - pad - len, Smax - pad) (IncreFlashAttention README, kv left padding)."""
+    rng = np.random.default_rng(12)
+    B, Smax = 3, 40
+    right = gen.gqa_padded(12, B=B, N=4, KV_N=2, D=16, Smax=Smax, layout="BNSD", dtype="fp16", mask=False)
+    lens = right.actual_seq_lengths
+    pads = np.array([int(rng.integers(0, Smax - l + 1)) for l in lens], dtype=np.int64)
+    k = gen.random_storage(99, 1, right.key.shape, "fp16")
+    v = gen.random_storage(99, 2, right.value.shape, "fp16")
+    for b in range(B):
+        st = Smax - pads[b] - lens[b]
+        k[b, :, st:st + lens[b]] = right.key[b, :, :lens[b]]
+        v[b, :, st:st + lens[b]] = right.value[b, :, :lens[b]]
+    out = oracle.ifa_ref(right.query, k, v, num_heads=4, num_kv_heads=2, scale=right.scale,
+                         layout="BNSD", actual_seq_lengths=lens, kv_padding_size=pads)
+    assert np.array_equal(out, run(right))
+
+
+def test_left_pad_out_of_range_window_is_zero_and_negative_pad_is_zero_pad():
+    case = gen.gqa_padded(13, B=3, N=2, KV_N=1, D=16, Smax=30, layout="BNSD", dtype="fp16", mask=False)
+    case.actual_seq_lengths = np.array([25, 10, 30], dtype=np.int64)
+    # b0: start = 30 - 8 - 25 < 0 -> zeros; b1: regular; b2: pad -5 -> treated as 0
+    pads = np.array([8, 3, -5], dtype=np.int64)
+    out = run(case, kv_padding_size=pads)
+    assert np.all(out[0] == 0.0)
+    assert not np.all(out[1] == 0.0)
+    out0 = run(case, kv_padding_size=np.array([8, 3, 0], dtype=np.int64))
+    assert np.array_equal(out[2], out0[2])
+    # a single broadcast pad value applies to every batch
+    one = run(case, kv_padding_size=np.array([0], dtype=np.int64))
+    assert np.array_equal(one, run(case, kv_padding_size=np.zeros(3, dtype=np.int64)))
+
+
+def test_mask_semantics():
+    case = gen.gqa_padded(14, B=2, N=4, KV_N=2, D=16, Smax=24, layout="BNSD", dtype="bf16", mask=False)
+    base = run(case)
+    zeros = np.zeros((2, 1, 1, 24), dtype=bool)
+    assert np.array_equal(run(case, atten_mask=zeros), base)
+    # a mask true past each length equals the length-limited problem
+    full = np.full(2, 24, dtype=np.int64)
+    past = (np.arange(24)[None, :] >= case.actual_seq_lengths[:, None]).reshape(2, 1, 1, 24)
+    assert np.array_equal(run(case, actual_seq_lengths=full, atten_mask=past), base)
+    # per-head mask (B, N, 1, S): excluding everything for head 1 only
+    m = np.zeros((2, 4, 1, 24), dtype=np.uint8)
+    m[:, 1] = 1
+    out = run(case, atten_mask=m)
+    assert np.all(out[:, 1] == 0.0)
+    assert np.array_equal(out[:, [0, 2, 3]], base[:, [0, 2, 3]])
+    # a broadcast (1, N, 1, S) mask equals the same mask repeated over B
+    m1 = (np.random.default_rng(3).random((1, 4, 1, 24)) < 0.3).astype(np.int8)
+    assert np.array_equal(run(case, atten_mask=m1), run(case, atten_mask=np.repeat(m1, 2, axis=0)))
+    # masked positions are simply dropped: compare with torch on the survivors
+    q = as_f64(case.query, "bf16").reshape(2, 4, 16)
+    k, v = as_f64(case.key, "bf16"), as_f64(case.value, "bf16")
+    got = run(case, atten_mask=m1)
+    for b in range(2):
+        L = int(case.actual_seq_lengths[b])
+        for n in range(4):
+            valid = m1[0, n, 0, :L] == 0
+            ref = torch_attention(q[b, n], k[b, n // 2, :L], v[b, n // 2, :L], case.scale, valid)
+            np.testing.assert_allclose(got[b, n], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_zero_length_row_is_zero():
+    case = gen.gqa_padded(15, B=2, N=2, KV_N=1, D=16, Smax=10, layout="BNSD", dtype="fp16", mask=False)
+    case.actual_seq_lengths = np.array([0, 4], dtype=np.int64)
+    out = run(case)
+    assert np.all(out[0] == 0.0)
+    assert not np.all(out[1] == 0.0)
+
+
+def test_permuting_tokens_together_leaves_output_unchanged():
+    case = gen.gqa_padded(16, B=1, N=2, KV_N=1, D=16, Smax=64, layout="BNSD", dtype="fp16", mask=False)
+    case.actual_seq_lengths = np.array([64], dtype=np.int64)
+    perm = np.random.default_rng(0).permutation(64)
+    out = run(case)
+    case.key, case.value = case.key[:, :, perm], case.value[:, :, perm]
+    np.testing.assert_allclose(run(case), out, rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------------- antiquant
+
+def _int8_case(seed, per_tensor=False):
+    return gen.int8_leftpad(seed, B=2, N=4, KV_N=2, D=16, Smax=48, len_lo=5, len_hi=40, pad_extra=4,
+                            per_tensor=per_tensor)
+
+
+def _aq(case, **over):
+    kw = dict(antiquant=oracle.AQ_PER_TENSOR if case.antiquant == "per_tensor" else oracle.AQ_PER_CHANNEL,
+              antiquant_scale=case.antiquant_scale, antiquant_offset=case.antiquant_offset)
+    kw.update(over)
+    return run(case, **kw)
+
+
+def test_antiquant_value_formula_on_constant_rows():
+    """With every int8 value row equal to c, out[d] = (c + offset_V[h,d]) * scale_V[h,d] exactly."""
+    case = _int8_case(20)
+    case.value = np.full_like(case.value, 7)
+    out = _aq(case)
+    s = case.antiquant_scale.astype(np.float64).reshape(2, 2, 16)
+    o = case.antiquant_offset.astype(np.float64).reshape(2, 2, 16)
+    for b in range(2):
+        for n in range(4):
+            np.testing.assert_allclose(out[b, n], (7 + o[1, n // 2]) * s[1, n // 2], rtol=1e-14)
+
+
+def test_antiquant_scales_against_torch_on_dequantised_values():
+    """Zero offsets: softmax over k*scale_K against v*scale_V, computed by torch in float64."""
+    case = _int8_case(21)
+    case.antiquant_offset = np.zeros_like(case.antiquant_offset)
+    out = _aq(case)
+    s = case.antiquant_scale.astype(np.float64).reshape(2, 2, 16)
+    q = case.query.astype(np.float64).reshape(2, 4, 16)
+    k = case.key.astype(np.float64)
+    v = case.value.astype(np.float64)
+    for b in range(2):
+        pad = max(int(case.kv_padding_size[b]), 0)
+        st = 48 - pad - int(case.actual_seq_lengths[b])
+        en = 48 - pad
+        for n in range(4):
+            h = n // 2
+            if st < 0:
+                assert np.all(out[b, n] == 0)
+                continue
+            ref = torch_attention(q[b, n], k[b, h, st:en] * s[0, h], v[b, h, st:en] * s[1, h], case.scale)
+            np.testing.assert_allclose(out[b, n], ref, rtol=1e-11, atol=1e-13)
+
+
+def test_antiquant_key_offset_only_shifts_scores():
+    """A per-channel key offset adds the same constant to every score of a row."""
+    case = _int8_case(22)
+    a = _aq(case)
+    off = case.antiquant_offset.copy()
+    off[0] = np.float16(0.0)
+    b = _aq(case, antiquant_offset=off)
+    np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-12)
+
+
+def test_antiquant_per_tensor_equals_broadcast_per_channel():
+    case = _int8_case(23, per_tensor=True)
+    pt = _aq(case)
+    sc = np.repeat(case.antiquant_scale.reshape(2, 1), 2 * 16, axis=1).reshape(2, 2, 1, 16)
+    of = np.repeat(case.antiquant_offset.reshape(2, 1), 2 * 16, axis=1).reshape(2, 2, 1, 16)
+    pc = _aq(case, antiquant=oracle.AQ_PER_CHANNEL, antiquant_scale=sc, antiquant_offset=of)
+    assert np.array_equal(pt, pc)
+
+
+def test_antiquant_identity_params_equal_plain_fp16():
+    case = _int8_case(24)
+    one = np.ones_like(case.antiquant_scale)
+    zero = np.zeros_like(case.antiquant_offset)
+    a = _aq(case, antiquant_scale=one, antiquant_offset=zero)
+    kf = case.key.astype(np.float16)
+    vf = case.value.astype(np.float16)
+    b = oracle.ifa_ref(case.query, kf, vf, num_heads=4, num_kv_heads=2, scale=case.scale,
+                       layout="BNSD", actual_seq_lengths=case.actual_seq_lengths,
+                       kv_padding_size=case.kv_padding_size)
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- sparse MLA decode
+
+def _sfa(seed=0, **kw):
+    base = dict(B=2, Q_N=4, D=32, Dr=8, block_size=16, kv_len=64, sparse_size=16, nvalid_lo=4,
+                nvalid_hi=16)
+    base.update(kw)
+    return gen.sfa_mla(seed, **base)
+
+
+def sref(c, **over):
+    a = dict(query=c.query, query_rope=c.query_rope, key=c.key, key_rope=c.key_rope, value=c.value,
+             sparse_indices=c.sparse_indices, block_table=c.block_table,
+             actual_seq_lengths_kv=c.actual_seq_lengths_kv)
+    a.update(over)
+    return oracle.sfa_ref(a["query"], a["query_rope"], a["key"], a["key_rope"], a["value"],
+                          a["sparse_indices"], a["block_table"], a["actual_seq_lengths_kv"], scale=c.scale)
+
+
+def _rows(c, b, idx):
+    bs = c.key.shape[1]
+    return np.array([c.block_table[b, i // bs] * bs + i % bs for i in idx])
+
+
+def test_sfa_dense_indices_match_torch_mla():
+    c = _sfa(30)
+    c.sparse_indices[:] = np.arange(16, dtype=np.int32)
+    out = sref(c)
+    q = as_f64(c.query, "bf16")[:, 0]
+    qr = as_f64(c.query_rope, "bf16")[:, 0]
+    k = as_f64(c.key, "bf16").reshape(-1, 32)
+    kr = as_f64(c.key_rope, "bf16").reshape(-1, 8)
+    v = as_f64(c.value, "bf16").reshape(-1, 32)
+    for b in range(2):
+        rows = _rows(c, b, range(16))
+        for n in range(4):
+            ref = torch_attention(np.concatenate([q[b, n], qr[b, n]]),
+                                  np.concatenate([k[rows], kr[rows]], axis=1), v[rows], c.scale)
+            np.testing.assert_allclose(out[b, n], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_sfa_single_index_returns_value_row_and_all_invalid_is_zero():
+    c = _sfa(31)
+    c.sparse_indices[:] = -1
+    c.sparse_indices[0, 0, 0, 0] = 37
+    out = sref(c)
+    v = as_f64(c.value, "bf16").reshape(-1, 32)
+    row = _rows(c, 0, [37])[0]
+    for n in range(4):
+        assert np.array_equal(out[0, n], v[row])
+    assert np.all(out[1] == 0.0)
+
+
+def test_sfa_selected_set_exact_mean():
+    """Q = 0 and value row = integer code of its token: the output is the exact mean of the
+    codes of exactly the valid selected tokens (invalid entries anywhere are skipped)."""
+    c = _sfa(32)
+    c.query[:] = 0
+    c.query_rope[:] = 0
+    bs = 16
+    codes = np.zeros(c.value.shape, dtype=np.float32)
+    # code(token) = token index of the row within its batch, recovered from the block table
+    for b in range(2):
+        for t in range(64):
+            blk = c.block_table[b, t // bs]
+            codes[blk, t % bs, 0, :] = t
+    c.value = gen.to_storage(codes, "bf16")
+    sel = np.array([3, 60, 17, 8, -1, 70, 5, 9], dtype=np.int32)   # 70 >= length, -1 invalid
+    idx = np.full((2, 1, 1, 16), -1, dtype=np.int32)
+    idx[0, 0, 0, :8] = sel
+    idx[1, 0, 0, :4] = [1, 2, 3, 6]
+    lens = np.array([64, 64], dtype=np.int32)
+    out = sref(c, sparse_indices=idx, actual_seq_lengths_kv=lens)
+    valid0 = [3, 60, 17, 8, 5, 9]
+    assert np.all(out[0] == np.mean(valid0))
+    assert np.all(out[1] == 3.0)
+    # a shorter actual length drops index 60 as well
+    out2 = sref(c, sparse_indices=idx, actual_seq_lengths_kv=np.array([40, 64], dtype=np.int32))
+    assert np.all(out2[0] == np.mean([3, 17, 8, 5, 9]))
+
+
+def test_sfa_index_order_is_irrelevant_and_duplicates_count_twice():
+    c = _sfa(33, nvalid_lo=10, nvalid_hi=10)
+    out = sref(c)
+    idx = c.sparse_indices.copy()
+    idx[:, :, :, :10] = idx[:, :, :, :10][..., ::-1]
+    np.testing.assert_allclose(sref(c, sparse_indices=idx), out, rtol=1e-13, atol=1e-15)
+    dup = c.sparse_indices.copy()
+    dup[:, :, :, 10] = dup[:, :, :, 0]
+    got = sref(c, sparse_indices=dup)
+    q = as_f64(c.query, "bf16")[:, 0]
+    qr = as_f64(c.query_rope, "bf16")[:, 0]
+    k = as_f64(c.key, "bf16").reshape(-1, 32)
+    kr = as_f64(c.key_rope, "bf16").reshape(-1, 8)
+    v = as_f64(c.value, "bf16").reshape(-1, 32)
+    for b in range(2):
+        rows = _rows(c, b, dup[b, 0, 0, :11])
+        for n in range(4):
+            ref = torch_attention(np.concatenate([q[b, n], qr[b, n]]),
+                                  np.concatenate([k[rows], kr[rows]], axis=1), v[rows], c.scale)
+            np.testing.assert_allclose(got[b, n], ref, rtol=1e-12, atol=1e-13)
