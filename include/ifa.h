@@ -1,0 +1,169 @@
+/*
+ * ifa.h -- C ABI of the GB300 (sm_103a) incremental flash attention library.
+ *
+ * Single-query decode attention
+ *
+ *     attentionOut[b, n, :] = softmax(scaleValue * q[b, n, :] . K_b^T) . V_b
+ *
+ * over the valid key/value tokens of batch b, with GQA (query head n reads
+ * key/value head n / (numHeads / numKeyValueHeads)), per-batch
+ * actualSeqLengths, an optional attenMask, key/value left padding
+ * (kvPaddingSize), a paged cache addressed through blockTable/blockSize, and
+ * int8 key/value "antiquant" with per-channel or per-tensor scale and offset.
+ *
+ * Sources (titles of the pages that define the operation):
+ *  - "IncreFlashAttention" README: 功能说明 (function and formula), 约束说明
+ *    (constraints: GQA multiple, page attention, kv左padding, antiquant shapes).
+ *  - "aclnnIncreFlashAttentionV2": Function (formula), Function Prototype
+ *    (two-phase workspace/run API), Parameters (query/key/value/attenMask/
+ *    actualSeqLengths/numHeads/scaleValue/inputLayout/numKeyValueHeads),
+ *    Return Value (error codes), Constraints (S_q = 1, determinism).
+ *
+ * Readings of points the pages leave open:
+ *  - a nonzero attenMask byte EXCLUDES its position; the mask is indexed in
+ *    the key/value S coordinate (absolute position under left padding);
+ *  - an empty set of surviving tokens gives an all-zero output row;
+ *  - antiquant dequantises x as (x + offset) * scale; entry 0 of the leading
+ *    axis of scale/offset is for key, entry 1 for value;
+ *  - kvPaddingSize is int64 with 1 (broadcast) or B entries.
+ *
+ * Calling model (mirrors the two-phase API of the aclnnIncreFlashAttentionV2
+ * page): ifa_create validates the static problem description and returns a
+ * plan plus the workspace size; ifa_run validates the per-call data and
+ * enqueues the computation on the caller's stream (asynchronous); the caller
+ * owns every tensor, the workspace and the stream.  Results are deterministic:
+ * the same inputs give bitwise-identical outputs.
+ *
+ * Errors: no exception or abort crosses this ABI.  Return codes follow the
+ * aclnnIncreFlashAttentionV2 page's Return Value table.
+ */
+#ifndef IFA_H
+#define IFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ifa_status;
+#define IFA_OK 0
+#define IFA_ERR_PARAM_NULLPTR 161001 /* a required pointer is NULL */
+#define IFA_ERR_PARAM_INVALID 161002 /* dtype/layout/shape/value outside the supported range */
+#define IFA_ERR_RUNTIME 361001       /* a CUDA runtime call failed */
+
+/* Layout of query / attentionOut (and of a contiguous key/value cache). */
+typedef enum { IFA_LAYOUT_BSH = 0, IFA_LAYOUT_BSND = 1, IFA_LAYOUT_BNSD = 2 } ifa_layout;
+
+/* Key/value storage.  CONTIG: (B,S,H) / (B,S,KV_N,D) / (B,KV_N,S,D) per
+ * inputLayout.  PAGED_NBSD: (blockNum, KV_N, blockSize, D), only with a BNSD
+ * query.  PAGED_BSH: (blockNum, blockSize, KV_N*D), any query layout.
+ * ("IncreFlashAttention" README, page attention constraints.) */
+typedef enum { IFA_KV_CONTIG = 0, IFA_KV_PAGED_NBSD = 1, IFA_KV_PAGED_BSH = 2 } ifa_kv_format;
+
+typedef enum { IFA_F16 = 0, IFA_BF16 = 1, IFA_I8 = 2, IFA_U8 = 3, IFA_BOOL = 4 } ifa_dtype;
+
+typedef enum {
+    IFA_ANTIQUANT_NONE = 0,
+    IFA_ANTIQUANT_PER_CHANNEL = 1, /* scale/offset memory (2, KV_N, D): (2,N,1,D), (2,N,D) or (2,H) */
+    IFA_ANTIQUANT_PER_TENSOR = 2   /* scale/offset of shape (2) */
+} ifa_antiquant;
+
+/*
+ * Static description of one decode-attention problem (sizes and options).
+ * All int32 fields hold the enum values above.
+ */
+typedef struct ifa_params {
+    int64_t B;                /* batch, 0..65536 */
+    int64_t numHeads;         /* query heads N, 1..256 */
+    int64_t numKeyValueHeads; /* key/value heads; 0 means numHeads; numHeads % it == 0 */
+    int64_t headDim;          /* D, 1..512; a multiple of 8 (fp16/bf16 key/value) or 16 (int8) */
+    int64_t maxSeqLen;        /* CONTIG: the key/value S extent (Smax); ignored when paged */
+    int32_t q_dtype;          /* IFA_F16 | IFA_BF16; attentionOut has this dtype */
+    int32_t kv_dtype;         /* = q_dtype, or IFA_I8 (requires antiquant) */
+    int32_t inputLayout;      /* ifa_layout */
+    int32_t kvFormat;         /* ifa_kv_format */
+    int64_t blockSize;        /* paged: tokens per block, <= 512, multiple of 16 (32 for int8) */
+    int64_t blockNum;         /* paged: physical blocks in the cache */
+    int64_t blockTableCols;   /* paged: second dimension of blockTable */
+    int32_t has_mask;         /* 1 if attenMask is passed */
+    int32_t mask_dtype;       /* IFA_BOOL | IFA_I8 | IFA_U8 (values 0 or 1; nonzero excludes) */
+    int64_t maskB;            /* attenMask shape (maskB, maskN, 1, maskS): maskB in {1, B} */
+    int64_t maskN;            /* maskN in {1, numHeads} (query heads) */
+    int64_t maskS;            /* >= every valid window end */
+    int32_t antiquant;        /* ifa_antiquant; not NONE exactly when kv_dtype is IFA_I8 */
+    int32_t has_kv_padding;   /* 1 if kvPaddingSize is passed (left padding; contiguous only) */
+    double scaleValue;        /* the scale applied to q . k (typically 1/sqrt(D)) */
+    int64_t splitTiles;       /* 0: automatic split plan; > 0: at most this many 64-token tiles per
+                                 CTA (testing split invariance); negative is invalid */
+} ifa_params;
+
+typedef struct ifa_plan ifa_plan;
+
+/*
+ * Phase 1: validate `params` and build a plan for the current CUDA device.
+ *   plan            out: owned by the library, free with ifa_destroy
+ *   workspace_bytes out: device workspace every ifa_run on this plan needs
+ * Returns IFA_ERR_PARAM_NULLPTR for NULL arguments, IFA_ERR_PARAM_INVALID for a
+ * description outside the supported range, IFA_ERR_RUNTIME if the device
+ * cannot be queried.  Allocates the plan and a 4-byte device error word.
+ */
+ifa_status ifa_create(const ifa_params* params, ifa_plan** plan, size_t* workspace_bytes);
+
+/*
+ * Phase 2: enqueue one decode-attention call on `stream` (a cudaStream_t,
+ * NULL for the legacy default stream).  Asynchronous; host arrays are read
+ * before the call returns.
+ *
+ * Device pointers (16-byte aligned unless noted):
+ *   query            (B,N,1,D) / (B,1,N,D) / (B,1,H) of q_dtype
+ *   key, value       key/value cache per kvFormat (may alias each other)
+ *   attenMask        nullable unless has_mask; 1 byte per element, any alignment
+ *   blockTable       int32 (B, blockTableCols), 4-byte aligned; required when paged;
+ *                    entries of blocks a batch does not reach are never read
+ *   antiquantScale   per-channel (2, KV_N, D) or per-tensor (2), of q_dtype, 2-byte aligned
+ *   antiquantOffset  same shape and dtype
+ *   attentionOut     same shape and dtype as query
+ *   workspace        >= workspace_bytes from ifa_create (nullable when that is 0)
+ * Host pointers:
+ *   actualSeqLengths int64 (B); NULL means every batch uses maxSeqLen (contiguous only);
+ *                    required when paged or left padded.  Values in [0, maxSeqLen]
+ *                    (contiguous right padding) or [0, blockTableCols*blockSize] (paged).
+ *   kvPaddingSize    int64, 1 or B entries (`n_kv_padding`), nullable; negative values
+ *                    count as 0; window [maxSeqLen-pad-len, maxSeqLen-pad), all-zero output
+ *                    when its start or end is negative.  Without actualSeqLengths the
+ *                    call uses right padding.
+ * Device-side data errors (a needed blockTable entry outside [0, blockNum)) leave the
+ * affected tokens out and set a flag readable with ifa_get_device_errors.
+ */
+ifa_status ifa_run(ifa_plan* plan, const void* query, const void* key, const void* value,
+                   const void* attenMask, const int64_t* actualSeqLengths,
+                   const int64_t* kvPaddingSize, int64_t n_kv_padding, const int32_t* blockTable,
+                   const void* antiquantScale, const void* antiquantOffset, void* attentionOut,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Release a plan (NULL is accepted). Waits for nothing; do not free while a run is in flight. */
+ifa_status ifa_destroy(ifa_plan* plan);
+
+/*
+ * Synchronise `stream`, return in *flags the device error bits accumulated by this
+ * plan's runs since the last call (1: blockTable entry out of range, 2: a pipeline
+ * wait timed out), and clear them.
+ */
+ifa_status ifa_get_device_errors(ifa_plan* plan, void* stream, int64_t* flags);
+
+/*
+ * Number of CUDA kernels the most recent ifa_run on `plan` enqueued (1: the split-KV
+ * partial kernel alone; 2: plus the log-sum-exp combine kernel); 0 before any run or
+ * for a NULL plan.  Lets callers count launches, e.g. when capturing CUDA graphs.
+ */
+int64_t ifa_last_launch_count(const ifa_plan* plan);
+
+/* Static text for a status code. */
+const char* ifa_status_string(ifa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* IFA_H */

@@ -1,0 +1,204 @@
+"""Python binding of ``libifa.so`` (C ABI declared in ``include/ifa.h``).
+
+The functions below carry the C names and only marshal arguments: every step
+of the computation runs in the library's CUDA kernels.  torch supplies device
+memory and streams.  Loading fails loudly if the library has not been built;
+there is no fallback implementation.
+
+``IncreFlashAttention`` wraps a plan: construct it with the static problem
+description, then call it with device tensors and host length arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libifa.so")
+
+IFA_OK = 0
+IFA_ERR_PARAM_NULLPTR = 161001
+IFA_ERR_PARAM_INVALID = 161002
+IFA_ERR_RUNTIME = 361001
+
+LAYOUTS = {"BSH": 0, "BSND": 1, "BNSD": 2}
+KV_FORMATS = {"contig": 0, "paged_nbsd": 1, "paged_bsh": 2}
+DTYPES = {"fp16": 0, "bf16": 1, "int8": 2, "uint8": 3, "bool": 4}
+ANTIQUANT = {"none": 0, "per_channel": 1, "per_tensor": 2}
+
+# Every symbol include/ifa.h declares.
+EXPORTED = ("ifa_create", "ifa_run", "ifa_destroy", "ifa_get_device_errors", "ifa_last_launch_count",
+            "ifa_status_string")
+
+
+class IfaParams(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int64), ("numHeads", ctypes.c_int64), ("numKeyValueHeads", ctypes.c_int64),
+        ("headDim", ctypes.c_int64), ("maxSeqLen", ctypes.c_int64),
+        ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+        ("inputLayout", ctypes.c_int32), ("kvFormat", ctypes.c_int32),
+        ("blockSize", ctypes.c_int64), ("blockNum", ctypes.c_int64), ("blockTableCols", ctypes.c_int64),
+        ("has_mask", ctypes.c_int32), ("mask_dtype", ctypes.c_int32),
+        ("maskB", ctypes.c_int64), ("maskN", ctypes.c_int64), ("maskS", ctypes.c_int64),
+        ("antiquant", ctypes.c_int32), ("has_kv_padding", ctypes.c_int32),
+        ("scaleValue", ctypes.c_double), ("splitTiles", ctypes.c_int64),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+class IfaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+        self.status = status
+
+
+def load_library():
+    """Open libifa.so (built by ``kv_cache_incremental_split_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: run kv_cache_incremental_split_gb300.build first")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, sz, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64
+            lib.ifa_create.restype = ctypes.c_int32
+            lib.ifa_create.argtypes = [ctypes.POINTER(IfaParams), ctypes.POINTER(vp), ctypes.POINTER(sz)]
+            lib.ifa_run.restype = ctypes.c_int32
+            lib.ifa_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]
+            lib.ifa_destroy.restype = ctypes.c_int32
+            lib.ifa_destroy.argtypes = [vp]
+            lib.ifa_get_device_errors.restype = ctypes.c_int32
+            lib.ifa_get_device_errors.argtypes = [vp, vp, ctypes.POINTER(i64)]
+            lib.ifa_last_launch_count.restype = ctypes.c_int64
+            lib.ifa_last_launch_count.argtypes = [vp]
+            lib.ifa_status_string.restype = ctypes.c_char_p
+            lib.ifa_status_string.argtypes = [ctypes.c_int32]
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().ifa_status_string(int(status)).decode()
+
+
+def ifa_create(params: IfaParams):
+    """Returns (status, plan handle or None, workspace bytes)."""
+    lib = load_library()
+    plan = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = lib.ifa_create(ctypes.byref(params), ctypes.byref(plan), ctypes.byref(ws))
+    return st, (plan.value if st == IFA_OK else None), ws.value
+
+
+def ifa_run(plan, query, key, value, atten_mask, actual_seq_lengths, kv_padding_size, n_kv_padding,
+            block_table, antiquant_scale, antiquant_offset, attention_out, workspace, workspace_bytes,
+            stream) -> int:
+    """All pointer arguments are integers (device addresses, or host addresses for
+    ``actual_seq_lengths`` / ``kv_padding_size``) or None."""
+    return load_library().ifa_run(plan, query, key, value, atten_mask, actual_seq_lengths, kv_padding_size,
+                                   n_kv_padding, block_table, antiquant_scale, antiquant_offset, attention_out,
+                                   workspace, workspace_bytes, stream)
+
+
+def ifa_destroy(plan) -> int:
+    return load_library().ifa_destroy(plan)
+
+
+def ifa_get_device_errors(plan, stream) -> int:
+    flags = ctypes.c_int64()
+    st = load_library().ifa_get_device_errors(plan, stream, ctypes.byref(flags))
+    if st != IFA_OK:
+        raise IfaError(st, "ifa_get_device_errors")
+    return flags.value
+
+
+def _ptr(t):
+    return None if t is None else int(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+class IncreFlashAttention:
+    """A plan for one decode-attention problem shape (see ``include/ifa.h``).
+
+    Construction validates the description (``ifa_create``) and allocates the
+    device workspace with torch.  Calling the object enqueues ``ifa_run`` on
+    the current (or given) torch stream and returns the output tensor.
+    """
+
+    def __init__(self, *, batch: int, num_heads: int, num_kv_heads: int = 0, head_dim: int,
+                 max_seq_len: int = 0, dtype: str = "bf16", kv_dtype: Optional[str] = None,
+                 layout: str = "BSH", kv_format: str = "contig", block_size: int = 0,
+                 block_num: int = 0, block_table_cols: int = 0,
+                 mask_shape: Optional[Sequence[int]] = None, mask_dtype: str = "bool",
+                 antiquant: str = "none", kv_padding: bool = False,
+                 scale: Optional[float] = None, split_tiles: int = 0, device=None):
+        import torch
+        p = IfaParams()
+        p.B, p.numHeads, p.numKeyValueHeads, p.headDim = batch, num_heads, num_kv_heads, head_dim
+        p.maxSeqLen = max_seq_len
+        p.q_dtype = DTYPES[dtype]
+        p.kv_dtype = DTYPES[kv_dtype or dtype]
+        p.inputLayout = LAYOUTS[layout]
+        p.kvFormat = KV_FORMATS[kv_format]
+        p.blockSize, p.blockNum, p.blockTableCols = block_size, block_num, block_table_cols
+        if mask_shape is not None:
+            p.has_mask = 1
+            p.mask_dtype = DTYPES[mask_dtype]
+            p.maskB, p.maskN, p.maskS = int(mask_shape[0]), int(mask_shape[1]), int(mask_shape[-1])
+        p.antiquant = ANTIQUANT[antiquant]
+        p.has_kv_padding = int(bool(kv_padding))
+        p.scaleValue = (1.0 / math.sqrt(head_dim)) if scale is None else float(scale)
+        p.splitTiles = split_tiles
+        self.params = p
+        self.batch, self.num_heads, self.head_dim = batch, num_heads, head_dim
+        self.dtype = dtype
+        st, plan, ws = ifa_create(p)
+        if st != IFA_OK:
+            raise IfaError(st, "ifa_create")
+        self.plan = plan
+        self.workspace_bytes = ws
+        dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+
+    def __del__(self):
+        plan = getattr(self, "plan", None)
+        if plan is not None and _lib is not None:
+            _lib.ifa_destroy(plan)
+            self.plan = None
+
+    def __call__(self, query, key, value, *, atten_mask=None, actual_seq_lengths=None,
+                 kv_padding_size=None, block_table=None, antiquant_scale=None, antiquant_offset=None,
+                 out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty_like(query)
+        lens = None if actual_seq_lengths is None else np.ascontiguousarray(actual_seq_lengths, dtype=np.int64)
+        pads = None if kv_padding_size is None else np.ascontiguousarray(kv_padding_size, dtype=np.int64).reshape(-1)
+        st = ifa_run(self.plan, _ptr(query), _ptr(key), _ptr(value), _ptr(atten_mask),
+                     None if lens is None else lens.ctypes.data,
+                     None if pads is None else pads.ctypes.data, 0 if pads is None else pads.size,
+                     _ptr(block_table), _ptr(antiquant_scale), _ptr(antiquant_offset), _ptr(out),
+                     _ptr(self.workspace), self.workspace.numel(), _stream_handle(stream))
+        if st != IFA_OK:
+            raise IfaError(st, "ifa_run")
+        return out
+
+    def last_launch_count(self) -> int:
+        return int(load_library().ifa_last_launch_count(self.plan))
+
+    def device_errors(self, stream=None) -> int:
+        return ifa_get_device_errors(self.plan, _stream_handle(stream))

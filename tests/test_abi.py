@@ -1,0 +1,136 @@
+"""CPU-only checks of the C-ABI library: it builds, loads, exports every symbol
+include/ifa.h declares, lays ifa_params out like the header, and rejects
+invalid problem descriptions with the documented status codes."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from kv_cache_incremental_split_gb300 import build as libbuild
+from kv_cache_incremental_split_gb300 import ifa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ifa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return ifa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(\w+)\s*\([^;{]*\)\s*;", text)) - {"if", "while"})
+
+
+def test_header_declares_what_the_binding_exports():
+    assert sorted(ifa.EXPORTED) == declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_params_struct_layout_matches_header(tmp_path):
+    src = tmp_path / "layout.c"
+    fields = [f for f, _ in ifa.IfaParams._fields_]
+    body = "\n".join(f'  printf("%zu\\n", offsetof(ifa_params, {f}));' for f in fields)
+    src.write_text(f'#include <stdio.h>\n#include <stddef.h>\n#include "ifa.h"\nint main(void) {{\n'
+                   f'  printf("%zu\\n", sizeof(ifa_params));\n{body}\n  return 0;\n}}\n')
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = [int(x) for x in subprocess.check_output([str(exe)]).split()]
+    assert got[0] == ctypes.sizeof(ifa.IfaParams)
+    for (name, _), off in zip(ifa.IfaParams._fields_, got[1:]):
+        assert getattr(ifa.IfaParams, name).offset == off, name
+
+
+def test_status_strings(lib):
+    assert "161001" in ifa.status_string(ifa.IFA_ERR_PARAM_NULLPTR)
+    assert "161002" in ifa.status_string(ifa.IFA_ERR_PARAM_INVALID)
+    assert "361001" in ifa.status_string(ifa.IFA_ERR_RUNTIME)
+    assert ifa.status_string(ifa.IFA_OK) == "success"
+
+
+def base_params(**kw):
+    p = ifa.IfaParams()
+    p.B, p.numHeads, p.numKeyValueHeads, p.headDim, p.maxSeqLen = 4, 8, 2, 128, 1024
+    p.q_dtype = p.kv_dtype = ifa.DTYPES["bf16"]
+    p.inputLayout = ifa.LAYOUTS["BSH"]
+    p.kvFormat = ifa.KV_FORMATS["contig"]
+    p.scaleValue = 0.088
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def create_status(lib, p):
+    plan = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = lib.ifa_create(ctypes.byref(p), ctypes.byref(plan), ctypes.byref(ws))
+    if st == ifa.IFA_OK:
+        lib.ifa_destroy(plan)
+    return st
+
+
+def test_null_arguments(lib):
+    plan = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    assert lib.ifa_create(None, ctypes.byref(plan), ctypes.byref(ws)) == ifa.IFA_ERR_PARAM_NULLPTR
+    p = base_params()
+    assert lib.ifa_create(ctypes.byref(p), None, ctypes.byref(ws)) == ifa.IFA_ERR_PARAM_NULLPTR
+    assert lib.ifa_run(None, 0, 0, 0, None, None, None, 0, None, None, None, 0, None, 0, None) == \
+        ifa.IFA_ERR_PARAM_NULLPTR
+    assert lib.ifa_destroy(None) == ifa.IFA_OK
+    flags = ctypes.c_int64()
+    assert lib.ifa_get_device_errors(None, None, ctypes.byref(flags)) == ifa.IFA_ERR_PARAM_NULLPTR
+
+
+INVALID = [
+    dict(B=-1), dict(B=65537), dict(numHeads=0), dict(numHeads=257), dict(numKeyValueHeads=3),
+    dict(headDim=0), dict(headDim=520), dict(headDim=100),  # not a multiple of 8
+    dict(q_dtype=2), dict(kv_dtype=0),  # bf16 query with fp16 cache
+    dict(kv_dtype=2),  # int8 cache without antiquant
+    dict(antiquant=1),  # antiquant without an int8 cache
+    dict(inputLayout=3), dict(kvFormat=3), dict(maxSeqLen=0),
+    dict(kvFormat=1, blockSize=128, blockNum=10, blockTableCols=4),  # NBSD cache needs a BNSD query
+    dict(kvFormat=2, blockSize=0, blockNum=10, blockTableCols=4),
+    dict(kvFormat=2, blockSize=520, blockNum=10, blockTableCols=4),
+    dict(kvFormat=2, blockSize=24, blockNum=10, blockTableCols=4),  # not 16-aligned
+    dict(kvFormat=2, blockSize=128, blockNum=0, blockTableCols=4),
+    dict(kvFormat=2, blockSize=128, blockNum=10, blockTableCols=4, has_kv_padding=1),
+    dict(has_mask=1, mask_dtype=0, maskB=1, maskN=1, maskS=1024),  # fp16 mask
+    dict(has_mask=1, mask_dtype=4, maskB=2, maskN=1, maskS=1024),  # maskB not in {1, B}
+    dict(has_mask=1, mask_dtype=4, maskB=4, maskN=2, maskS=1024),  # maskN not in {1, N}
+    dict(has_mask=1, mask_dtype=4, maskB=4, maskN=8, maskS=0),
+    dict(scaleValue=float("nan")), dict(splitTiles=-1),
+]
+
+
+@pytest.mark.parametrize("kw", INVALID)
+def test_invalid_descriptions_are_rejected(lib, kw):
+    assert create_status(lib, base_params(**kw)) == ifa.IFA_ERR_PARAM_INVALID
+
+
+def test_int8_cache_needs_16_aligned_head_dim(lib):
+    p = base_params(kv_dtype=2, antiquant=1, headDim=72, q_dtype=0)
+    assert create_status(lib, p) == ifa.IFA_ERR_PARAM_INVALID
+
+
+VALID = [
+    dict(), dict(numKeyValueHeads=0), dict(inputLayout=2, kvFormat=1, blockSize=128, blockNum=10, blockTableCols=4),
+    dict(kvFormat=2, blockSize=16, blockNum=10, blockTableCols=4),
+    dict(q_dtype=0, kv_dtype=2, antiquant=2, kvFormat=0, has_kv_padding=1),
+    dict(has_mask=1, mask_dtype=4, maskB=1, maskN=8, maskS=1024), dict(headDim=16), dict(headDim=256),
+]
+
+
+@pytest.mark.parametrize("kw", VALID)
+def test_valid_descriptions_pass_validation(lib, kw):
+    # Without a GPU the device query fails after validation (IFA_ERR_RUNTIME); with one the plan is created.
+    assert create_status(lib, base_params(**kw)) in (ifa.IFA_OK, ifa.IFA_ERR_RUNTIME)

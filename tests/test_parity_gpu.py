@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA decode kernels (through the C ABI) against the float64
+CPU oracle on the same seeded inputs, element by element.
+
+Tolerances: max abs error <= 2e-3 for fp16 outputs and <= 1.5e-2 for bf16
+outputs; int8 key/value paths are compared with the oracle evaluated on the
+same dequantised values (the oracle applies (x + offset) * scale itself).
+"""
+import math
+
+import numpy as np
+import pytest
+
+from kv_cache_incremental_split_gb300 import inputs as gen
+from harness import TOL, DeviceCase, gpu_ifa, make_op, max_abs_err, oracle_ifa, out_to_f64
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from kv_cache_incremental_split_gb300 import build
+    build.build()
+
+
+def check(case, split_tiles=0, batches=None, tol=None):
+    got = gpu_ifa(case, split_tiles)
+    ref = oracle_ifa(case, batches)
+    if batches is not None:
+        got = got[np.asarray(batches)]
+    err = max_abs_err(got, ref)
+    t = tol if tol is not None else TOL[case.q_dtype]
+    assert np.all(np.isfinite(got))
+    assert err <= t, f"max abs err {err} > {t}"
+    return got, ref
+
+
+# ---------------------------------------------------------------- the five workloads, small and full
+
+def test_worked_example_all_ones():
+    """aclnnIncreFlashAttentionV2 page, Example: all-ones fp16 inputs give all-ones outputs."""
+    q = np.ones((1, 2, 1, 16), dtype=np.float16)
+    k = np.ones((1, 2, 16, 16), dtype=np.float16)
+    case = gen.IfaCase("example", q, k, k.copy(), num_heads=2, num_kv_heads=2, scale=0.25, layout="BNSD",
+                       q_dtype="fp16", kv_dtype="fp16", max_seq_len=16,
+                       atten_mask=np.zeros((1, 1, 1, 16), dtype=np.int8),
+                       actual_seq_lengths=np.array([16], dtype=np.int64))
+    got = gpu_ifa(case)
+    assert np.array_equal(got, np.ones_like(got))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_mha_full_size(seed):
+    check(gen.tiny_mha(seed))
+
+
+@pytest.mark.parametrize("layout", ["BSH", "BSND", "BNSD"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_gqa_padded_small(layout, dtype):
+    check(gen.gqa_padded(3, B=5, N=32, KV_N=8, D=128, Smax=700, layout=layout, dtype=dtype))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_gqa_padded_full_size(seed):
+    check(gen.gqa_padded(seed))
+
+
+@pytest.mark.parametrize("kv_format", ["paged_nbsd", "paged_bsh"])
+@pytest.mark.parametrize("block_size", [128, 16, 48])
+def test_paged_small(kv_format, block_size):
+    check(gen.paged_gqa(4, B=6, N=32, KV_N=8, D=128, block_size=block_size, len_lo=1, len_hi=1500,
+                        kv_format=kv_format))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_paged_full_size_sampled(seed):
+    case = gen.paged_gqa(seed)
+    rng = np.random.default_rng(100 + seed)
+    batches = np.sort(rng.choice(case.B, size=4, replace=False))
+    check(case, batches=batches)
+
+
+@pytest.mark.parametrize("per_tensor", [False, True])
+def test_int8_leftpad_small(per_tensor):
+    check(gen.int8_leftpad(5, B=6, N=64, KV_N=8, D=128, Smax=600, len_lo=1, len_hi=600, pad_extra=64,
+                           per_tensor=per_tensor))
+
+
+def test_int8_bf16_query():
+    check(gen.int8_leftpad(6, B=3, N=16, KV_N=4, D=128, Smax=300, len_lo=1, len_hi=300, q_dtype="bf16"))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_int8_leftpad_full_size_sampled(seed):
+    case = gen.int8_leftpad(seed)
+    rng = np.random.default_rng(200 + seed)
+    check(case, batches=np.sort(rng.choice(case.B, size=4, replace=False)))
+
+
+# ---------------------------------------------------------------- split plan, determinism
+
+@pytest.mark.parametrize("split_tiles", [1, 2, 3, 7])
+def test_forced_splits_match_oracle(split_tiles):
+    case = gen.gqa_padded(7, B=4, N=16, KV_N=4, D=128, Smax=1000, layout="BNSD", dtype="bf16")
+    check(case, split_tiles=split_tiles)
+
+
+def test_split_invariance_and_run_to_run_determinism():
+    case = gen.paged_gqa(8, B=5, N=32, KV_N=8, D=128, block_size=128, len_lo=100, len_hi=3000)
+    dc = DeviceCase(case)
+    outs = {}
+    for st in (0, 1, 5):
+        op = make_op(case, st)
+        a = out_to_f64(dc.run(op))
+        b = out_to_f64(dc.run(op))
+        assert np.array_equal(a, b), "run-to-run results differ"
+        outs[st] = a
+    assert max_abs_err(outs[0], outs[1]) <= TOL["bf16"]
+    assert max_abs_err(outs[0], outs[5]) <= TOL["bf16"]
+
+
+# ---------------------------------------------------------------- edge cases
+
+def test_head_groupings():
+    for N, KV_N in ((8, 8), (16, 1), (32, 1), (12, 4), (48, 2)):
+        check(gen.gqa_padded(9, B=2, N=N, KV_N=KV_N, D=64, Smax=300, layout="BNSD", dtype="fp16"))
+
+
+@pytest.mark.parametrize("D", [16, 80, 256])
+def test_head_dims(D):
+    check(gen.gqa_padded(10, B=2, N=8, KV_N=2, D=D, Smax=200, layout="BSND", dtype="bf16"))
+
+
+def test_lengths_zero_one_and_ragged():
+    case = gen.gqa_padded(11, B=6, N=8, KV_N=2, D=128, Smax=300, layout="BSH", dtype="fp16", mask=False)
+    case.actual_seq_lengths = np.array([0, 1, 63, 64, 65, 300], dtype=np.int64)
+    got, _ = check(case)
+    assert np.all(got[0] == 0)
+
+
+def test_all_lengths_zero():
+    case = gen.gqa_padded(12, B=3, N=8, KV_N=2, D=64, Smax=50, layout="BNSD", dtype="bf16", mask=False)
+    case.actual_seq_lengths = np.zeros(3, dtype=np.int64)
+    got = gpu_ifa(case)
+    assert np.all(got == 0)
+
+
+def test_batch_above_inline_limit():
+    case = gen.gqa_padded(13, B=300, N=4, KV_N=2, D=64, Smax=80, layout="BNSD", dtype="fp16", mask=False,
+                          len_lo=0)
+    check(case)
+
+
+def test_fully_masked_rows_and_per_head_mask():
+    case = gen.gqa_padded(14, B=3, N=8, KV_N=2, D=128, Smax=200, layout="BNSD", dtype="bf16", mask=False)
+    m = (np.random.default_rng(1).random((3, 8, 1, 200)) < 0.5)
+    m[1, 3] = True  # batch 1, head 3: nothing survives
+    case.atten_mask = m
+    got, _ = check(case)
+    assert np.all(got[1, 3] == 0)
+
+
+def test_broadcast_mask_1N1S():
+    case = gen.gqa_padded(15, B=3, N=8, KV_N=2, D=64, Smax=150, layout="BSH", dtype="fp16", mask=False)
+    case.atten_mask = (np.random.default_rng(2).random((1, 8, 1, 150)) < 0.3).astype(np.uint8)
+    check(case)
+
+
+def test_left_pad_edge_windows():
+    case = gen.int8_leftpad(16, B=4, N=8, KV_N=2, D=128, Smax=256, len_lo=1, len_hi=256)
+    case.actual_seq_lengths = np.array([200, 10, 256, 100], dtype=np.int64)
+    case.kv_padding_size = np.array([100, -7, 0, 156], dtype=np.int64)  # b0 out of range -> zeros
+    got, _ = check(case)
+    assert np.all(got[0] == 0)
+
+
+def test_nan_beyond_the_window_does_not_leak():
+    case = gen.gqa_padded(17, B=2, N=8, KV_N=2, D=128, Smax=256, layout="BNSD", dtype="fp16", mask=False)
+    case.actual_seq_lengths = np.array([70, 129], dtype=np.int64)
+    for b, L in enumerate(case.actual_seq_lengths):
+        case.key[b, :, L:] = np.float16(np.nan)
+        case.value[b, :, L:] = np.float16(np.nan)
+    check(case)
+
+
+def test_bad_block_table_entry_sets_error_flag():
+    case = gen.paged_gqa(18, B=2, N=8, KV_N=2, D=64, block_size=64, len_lo=300, len_hi=400, dtype="bf16")
+    case.block_table = case.block_table.copy()
+    case.block_table[1, 2] = case.key.shape[0] + 5  # out of range: those tokens are left out
+    dc = DeviceCase(case)
+    op = make_op(case)
+    out = out_to_f64(dc.run(op)).reshape(2, 8, 64)
+    torch.cuda.synchronize()
+    assert op.device_errors() & 1
+    ref = oracle_ifa(case)  # the oracle leaves the same tokens out
+    assert max_abs_err(out, ref) <= TOL["bf16"]
+    assert op.device_errors() == 0  # cleared by the previous read
