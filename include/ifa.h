@@ -154,6 +154,42 @@ ifa_status ifa_destroy(ifa_plan* plan);
 ifa_status ifa_get_device_errors(ifa_plan* plan, void* stream, int64_t* flags);
 
 /*
+ * ifa_run_noalloc -- the same computation as ifa_create + ifa_run + ifa_destroy in
+ * one call that allocates nothing.  (The pages have no counterpart: their API
+ * always asks the caller for a workspace.)
+ *
+ * For callers that cannot allocate device memory: code that runs inside a
+ * memory pool or allocator it does not own, serving runtimes that forbid any
+ * allocation on the request path, or processes whose device footprint must not
+ * grow after start-up.  Neither this function nor anything it calls uses
+ * cudaMalloc, cudaFree or any other allocating routine; host-side state lives on
+ * the stack.
+ *
+ * Scratch: the split-KV partials live in one fixed array of
+ * IFA_NOALLOC_SCRATCH_BYTES in the library's device memory.  Every GPU that loads
+ * the library holds that array until the process exits, and every call on a
+ * device shares it and finds the previous call's contents there (nothing in it
+ * needs to start at zero).  Calls whose kernels overlap on the GPU (for
+ * example on two streams) race on the array: serialise them.  The first call on
+ * each device looks the array's address up (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.
+ *
+ * Limits: params->B <= IFA_NOALLOC_MAX_BATCH (a larger B returns
+ * IFA_ERR_PARAM_INVALID: the per-batch windows travel in the launch parameters),
+ * and the grid is capped so that its partials fit the array.  Other arguments,
+ * validation and results are those of ifa_run, except that `deviceErrorFlags`
+ * (device int32, nullable) receives the device error bits (OR-ed in, never
+ * cleared here) instead of a plan's error word.  Asynchronous on `stream`.
+ */
+#define IFA_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define IFA_NOALLOC_MAX_BATCH 256
+ifa_status ifa_run_noalloc(const ifa_params* params, const void* query, const void* key, const void* value,
+                           const void* attenMask, const int64_t* actualSeqLengths,
+                           const int64_t* kvPaddingSize, int64_t n_kv_padding, const int32_t* blockTable,
+                           const void* antiquantScale, const void* antiquantOffset, void* attentionOut,
+                           int32_t* deviceErrorFlags, void* stream);
+
+/*
  * Number of CUDA kernels the most recent ifa_run on `plan` enqueued (1: the split-KV
  * partial kernel alone; 2: plus the log-sum-exp combine kernel); 0 before any run or
  * for a NULL plan.  Lets callers count launches, e.g. when capturing CUDA graphs.

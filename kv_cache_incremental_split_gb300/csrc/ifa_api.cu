@@ -462,3 +462,12 @@ extern "C" ifa_status ifa_run(ifa_plan* pl, const void* query, const void* key, 
     }
     return IFA_OK;
 }
+
+// Shared with the fixed-scratch entry point (ifa_noalloc.cu).
+namespace ifa {
+bool params_are_valid(const ifa_params& p) { return valid_params(p); }
+bool decode_cfg(int kv, int dpad, int nt, int* slot_floats, int* smem) {
+    return cfg_lookup(kv, dpad, nt, slot_floats, smem);
+}
+void* tensor_map_encoder() { return reinterpret_cast<void*>(get_encode_fn()); }
+}  // namespace ifa

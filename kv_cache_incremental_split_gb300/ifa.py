@@ -33,7 +33,11 @@ ANTIQUANT = {"none": 0, "per_channel": 1, "per_tensor": 2}
 
 # Every symbol include/ifa.h declares.
 EXPORTED = ("ifa_create", "ifa_run", "ifa_destroy", "ifa_get_device_errors", "ifa_last_launch_count",
-            "ifa_status_string")
+            "ifa_run_noalloc", "ifa_status_string")
+
+# Fixed scratch of ifa_run_noalloc (include/ifa.h).
+IFA_NOALLOC_SCRATCH_BYTES = 4 << 20
+IFA_NOALLOC_MAX_BATCH = 256
 
 
 class IfaParams(ctypes.Structure):
@@ -79,6 +83,9 @@ def load_library():
             lib.ifa_get_device_errors.argtypes = [vp, vp, ctypes.POINTER(i64)]
             lib.ifa_last_launch_count.restype = ctypes.c_int64
             lib.ifa_last_launch_count.argtypes = [vp]
+            lib.ifa_run_noalloc.restype = ctypes.c_int32
+            lib.ifa_run_noalloc.argtypes = [ctypes.POINTER(IfaParams), vp, vp, vp, vp, vp, vp, i64, vp, vp, vp,
+                                            vp, vp, vp]
             lib.ifa_status_string.restype = ctypes.c_char_p
             lib.ifa_status_string.argtypes = [ctypes.c_int32]
             _lib = lib
@@ -106,6 +113,17 @@ def ifa_run(plan, query, key, value, atten_mask, actual_seq_lengths, kv_padding_
     return load_library().ifa_run(plan, query, key, value, atten_mask, actual_seq_lengths, kv_padding_size,
                                    n_kv_padding, block_table, antiquant_scale, antiquant_offset, attention_out,
                                    workspace, workspace_bytes, stream)
+
+
+def ifa_run_noalloc(params: IfaParams, query, key, value, atten_mask, actual_seq_lengths, kv_padding_size,
+                    n_kv_padding, block_table, antiquant_scale, antiquant_offset, attention_out,
+                    device_error_flags, stream) -> int:
+    """Plan-less, allocation-free call (include/ifa.h): for callers that cannot
+    allocate device memory.  Pointer arguments are integers or None."""
+    return load_library().ifa_run_noalloc(ctypes.byref(params), query, key, value, atten_mask,
+                                          actual_seq_lengths, kv_padding_size, n_kv_padding, block_table,
+                                          antiquant_scale, antiquant_offset, attention_out,
+                                          device_error_flags, stream)
 
 
 def ifa_destroy(plan) -> int:
