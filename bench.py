@@ -45,10 +45,14 @@ WORKLOADS = {
                   "random block table, lengths U{512..32768}"),
     "int8_leftpad": ("int8 KV antiquant + left padding: B=32 N=64 KV_N=8 D=128 fp16 query, BNSD int8 K/V, "
                      "per-channel scale/offset, Smax=8192, lengths U{256..8192}, pad Smax-len-U{0..64}"),
+    "paged_gqa_small": ("paged GQA decode, profiling size: B=64 N=32 KV_N=8 D=128 bf16, blockSize 128, "
+                        "random block table, lengths U{512..4096}"),
 }
 
 
 def make_case(name: str, seed: int) -> gen.IfaCase:
+    if name == "paged_gqa_small":
+        return gen.paged_gqa(seed, len_hi=4096)
     return {"gqa_padded": gen.gqa_padded, "tiny_mha": gen.tiny_mha, "paged_gqa": gen.paged_gqa,
             "int8_leftpad": gen.int8_leftpad}[name](seed)
 

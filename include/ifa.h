@@ -136,6 +136,9 @@ ifa_status ifa_create(const ifa_params* params, ifa_plan** plan, size_t* workspa
  *                    call uses right padding.
  * Device-side data errors (a needed blockTable entry outside [0, blockNum)) leave the
  * affected tokens out and set a flag readable with ifa_get_device_errors.
+ * Runs of one plan must not overlap on the GPU (they share the plan's per-sequence
+ * arrival counters): use one plan per stream.  The call is one kernel launch and can be
+ * captured in a CUDA graph; a captured call replays with the lengths it was captured with.
  */
 ifa_status ifa_run(ifa_plan* plan, const void* query, const void* key, const void* value,
                    const void* attenMask, const int64_t* actualSeqLengths,
@@ -165,11 +168,12 @@ ifa_status ifa_get_device_errors(ifa_plan* plan, void* stream, int64_t* flags);
  * cudaMalloc, cudaFree or any other allocating routine; host-side state lives on
  * the stack.
  *
- * Scratch: the split-KV partials live in one fixed array of
- * IFA_NOALLOC_SCRATCH_BYTES in the library's device memory.  Every GPU that loads
- * the library holds that array until the process exits, and every call on a
- * device shares it and finds the previous call's contents there (nothing in it
- * needs to start at zero).  Calls whose kernels overlap on the GPU (for
+ * Scratch: the split-KV partials and the per-sequence arrival counters live in one
+ * fixed array of IFA_NOALLOC_SCRATCH_BYTES in the library's device memory.  Every GPU
+ * that loads the library holds that array until the process exits, and every call on
+ * a device shares it and finds the previous call's contents there.  Nothing in it
+ * needs to start at zero: the counters carry a per-call tag, so a value left by an
+ * earlier (even aborted) call is ignored.  Calls whose kernels overlap on the GPU (for
  * example on two streams) race on the array: serialise them.  The first call on
  * each device looks the array's address up (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.
@@ -190,9 +194,10 @@ ifa_status ifa_run_noalloc(const ifa_params* params, const void* query, const vo
                            int32_t* deviceErrorFlags, void* stream);
 
 /*
- * Number of CUDA kernels the most recent ifa_run on `plan` enqueued (1: the split-KV
- * partial kernel alone; 2: plus the log-sum-exp combine kernel); 0 before any run or
- * for a NULL plan.  Lets callers count launches, e.g. when capturing CUDA graphs.
+ * Number of CUDA kernels the most recent ifa_run on `plan` enqueued: 1 (the split-KV
+ * kernel, which also merges the sequence pieces it cut), or 0 before any run, after a
+ * run with B = 0, or for a NULL plan.  Lets callers count launches, e.g. when capturing
+ * CUDA graphs.
  */
 int64_t ifa_last_launch_count(const ifa_plan* plan);
 
