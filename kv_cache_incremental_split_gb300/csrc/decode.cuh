@@ -26,8 +26,10 @@ enum KvKind : int { KV_BF16 = 0, KV_F16 = 1, KV_I8 = 2 };
 //   len : valid tokens (0 = all-zero output row)
 //   pre : exclusive prefix over batches of (tiles of b) x (sequences of b)
 struct alignas(128) DecodeParams {
-    CUtensorMap tmK;  // 4-D map (x=d, y=token, z=kv head, w=batch or block)
+    CUtensorMap tmK;   // 4-D map (x=d, y=token, z=kv head, w=batch or block), box_rows-row boxes
     CUtensorMap tmV;
+    CUtensorMap tmKt;  // the same tensors with tail_rows-row boxes, for the last tile of a window
+    CUtensorMap tmVt;
     const void* q;
     void* out;
     const uint8_t* mask;
@@ -43,7 +45,7 @@ struct alignas(128) DecodeParams {
     int B, N, KV_N, D, G, GT, NGS;
     int q_bf16;
     int paged;
-    int block_size, bt_cols, block_num, box_rows;
+    int block_size, bt_cols, block_num, box_rows, tail_rows;
     long long mask_bstride, mask_nstride;
     int has_mask;
     int aq_per_channel;
@@ -89,7 +91,8 @@ struct KernelChoice {
     int KV_N, G, GT, NT, NGS;
     int kv_kind, es, dpad;
     int T;          // tokens per tile
-    int box_rows;   // rows per TMA sub-box
+    int box_rows;   // rows per TMA box of a full tile (a whole tile, or one cache block)
+    int tail_rows;  // rows per TMA box of a window's last, partial tile
     int slot_floats, smem, threads;
     DecodeLaunchFn launch;
 };
@@ -105,7 +108,9 @@ ifa_status check_run_pointers(const ifa_params& p, const void* query, const void
                               const void* attenMask, const int64_t* actualSeqLengths, const int64_t* kvPaddingSize,
                               int64_t n_kv_padding, const int32_t* blockTable, const void* antiquantScale,
                               const void* antiquantOffset, const void* attentionOut);
-bool encode_kv_map(const ifa_params& p, const KernelChoice& kc, const void* base, CUtensorMap* map);
+bool encode_kv_map(const ifa_params& p, const KernelChoice& kc, const void* base, int box_rows, CUtensorMap* map);
+// The four maps a call needs (key/value x full/tail boxes).
+bool encode_kv_maps(const ifa_params& p, const KernelChoice& kc, const void* key, const void* value, DecodeParams& dp);
 // Everything but the tensor maps, the scratch pointers and the window table.
 void fill_decode_params(DecodeParams& dp, const ifa_params& p, const KernelChoice& kc, const void* query,
                         const void* attenMask, const int32_t* blockTable, const void* antiquantScale,

@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     int* info = reinterpret_cast<int*>(empty + C::STAGES);
     volatile int* abort_flag = info + C::STAGES;
     volatile int* last_flag = abort_flag + 1;
+    volatile int* blkbuf = last_flag + 1;  // [8] block ids of the current tile's full boxes (producer)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -201,12 +202,14 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         if (lane == 0) {
             prefetch_tensormap(&p.tmK);
             prefetch_tensormap(&p.tmV);
+            prefetch_tensormap(&p.tmKt);
+            prefetch_tensormap(&p.tmVt);
         }
         const uint64_t pol = policy_evict_first();
         const int br = p.box_rows;
-        const int nsub = T / br;  // 1..8
+        const int tr = p.tail_rows;
+        const int nsub = T / br;  // full boxes per tile: 1..8
         const int batch_tiles = 32 / nsub;
-        const uint32_t sub_bytes = 2u * C::NCG * 128u * (uint32_t)br;
         TileCursor cur;
         cursor_init<T>(cur, bd, B, lo);
         int my_blk = 0;
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         for (long long g = lo; g < hi; ++g, ++it) {
             const int kk = (int)((g - lo) % batch_tiles);
             if (p.paged && kk == 0) {
-                // Block ids of the next batch_tiles tiles: lane l reads sub-box (l % nsub) of tile (l / nsub).
+                // Block ids of the next batch_tiles tiles: lane l reads full box (l % nsub) of tile (l / nsub).
                 TileCursor c2 = cur;
                 const int adv = lane / nsub;
                 const bool live = (g + adv) < hi;
@@ -242,32 +245,33 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
             const int gs = cur.r % p.NGS;
             const int valid = min(T, bd[B + b] - cur.i * T);
             uint8_t* sb = stages + stage * C::STAGE_BYTES;
-            int blks[8];
-#pragma unroll
-            for (int s = 0; s < 8; ++s) blks[s] = 0;
             if (p.paged) {
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    if (s < nsub) blks[s] = __shfl_sync(0xffffffffu, my_blk, kk * nsub + s);
+                const int v = __shfl_sync(0xffffffffu, my_blk, (kk * nsub + lane) & 31);
+                if (lane < nsub) blkbuf[lane] = v;
             }
+            __syncwarp();
             if (lane == 0) {
                 const bool first = (cur.i == 0) || (g == lo);
+                // A full tile moves in nsub boxes of br rows; a window's last tile in boxes of tr rows
+                // that stop at the first one past the window end.
+                const bool tail = valid < T;
+                const int rows_per = tail ? tr : br;
+                const int nbox = tail ? (valid + tr - 1) / tr : nsub;
+                const uint32_t box_bytes = 2u * C::NCG * 128u * (uint32_t)rows_per;
                 uint32_t bytes = 0;
-                int badmask = 0, loadmask = 0, rows = 0;
+                int badmask = 0, rows = 0;
                 if (first) {
                     rows = min(p.GT, p.G - gs * p.GT);
                     bytes += (uint32_t)rows * (uint32_t)p.D * 2u;
                 }
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    if (s >= nsub || s * br >= valid) continue;  // past the window end: not fetched
-                    if (!p.paged || (blks[s] >= 0 && blks[s] < p.block_num)) {
-                        loadmask |= 1 << s;
-                        bytes += sub_bytes;
-                    } else {
-                        badmask |= 1 << s;
+                if (p.paged) {
+                    for (int s = 0; s < nsub; ++s) {
+                        const int blk = blkbuf[s];
+                        if (s * br < valid && !(blk >= 0 && blk < p.block_num)) badmask |= 1 << s;
                     }
                 }
+                for (int k = 0; k < nbox; ++k)
+                    if (!((badmask >> ((k * rows_per) / br)) & 1)) bytes += box_bytes;
                 if (badmask) record_error(p, kErrBadBlock);
                 info[stage] = badmask;
                 mbar_arrive_expect_tx(&full[stage], bytes);
@@ -279,22 +283,25 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                         bulk_g2s(qdst + row * C::QROW, qsrc + (long long)row * p.D * 2, (uint32_t)p.D * 2u, &full[stage]);
                 }
                 const int st = bd[b];
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    if (!((loadmask >> s) & 1)) continue;
+                const CUtensorMap* mk = tail ? &p.tmKt : &p.tmK;
+                const CUtensorMap* mv = tail ? &p.tmVt : &p.tmV;
+                for (int k = 0; k < nbox; ++k) {
+                    const int r0 = k * rows_per;  // first row of the box within the tile
+                    const int s = r0 / br;
+                    if ((badmask >> s) & 1) continue;
                     int y, w;
                     if (p.paged) {
-                        y = (cur.i * T + s * br) % p.block_size;
-                        w = blks[s];
+                        y = (cur.i * T + r0) % p.block_size;
+                        w = blkbuf[s];
                     } else {
-                        y = st + cur.i * T + s * br;
+                        y = st + cur.i * T + r0;
                         w = b;
                     }
 #pragma unroll
                     for (int cg = 0; cg < C::NCG; ++cg) {
-                        const int off = cg * (T * 128) + s * br * 128;
-                        tma_load_4d(sb + off, &p.tmK, &full[stage], cg * C::CG_ELEMS, y, h, w, pol);
-                        tma_load_4d(sb + C::KT_BYTES + off, &p.tmV, &full[stage], cg * C::CG_ELEMS, y, h, w, pol);
+                        const int off = cg * (T * 128) + r0 * 128;
+                        tma_load_4d(sb + off, mk, &full[stage], cg * C::CG_ELEMS, y, h, w, pol);
+                        tma_load_4d(sb + C::KT_BYTES + off, mv, &full[stage], cg * C::CG_ELEMS, y, h, w, pol);
                     }
                 }
             }

@@ -138,12 +138,10 @@ extern "C" ifa_status ifa_run(ifa_plan* pl, const void* query, const void* key, 
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     DecodeParams& dp = *pl->dp;
-    if (key != pl->last_k) {
-        if (!encode_kv_map(p, pl->kc, key, &dp.tmK)) return IFA_ERR_RUNTIME;
+    if (key != pl->last_k || value != pl->last_v) {
+        pl->last_k = pl->last_v = nullptr;
+        if (!encode_kv_maps(p, pl->kc, key, value, dp)) return IFA_ERR_RUNTIME;
         pl->last_k = key;
-    }
-    if (value != pl->last_v) {
-        if (!encode_kv_map(p, pl->kc, value, &dp.tmV)) return IFA_ERR_RUNTIME;
         pl->last_v = value;
     }
     fill_decode_params(dp, p, pl->kc, query, attenMask, blockTable, antiquantScale, antiquantOffset, attentionOut, W,

@@ -112,9 +112,11 @@ ifa_status choose_kernel(const ifa_params& p, KernelChoice* kc) {
     kc->launch = decode_launcher(kc->kv_kind, kc->dpad, kc->NT);
     if (!kc->launch || !decode_cfg(kc->kv_kind, kc->dpad, kc->NT, &kc->slot_floats, &kc->smem, &kc->T, &kc->threads))
         return IFA_ERR_PARAM_INVALID;
-    // 32-row TMA sub-boxes (smaller when a cache block is smaller): rows past a window end are not fetched.
-    kc->box_rows = (int)gcd64(kc->T, 32);
-    if (p.kvFormat != IFA_KV_CONTIG) kc->box_rows = (int)gcd64(kc->box_rows, p.blockSize);
+    // Full tiles move in boxes as large as the tile (or the cache block); a window's last
+    // tile moves in boxes of at most 32 rows, so rows past the window end are not fetched.
+    kc->box_rows = kc->T;
+    if (p.kvFormat != IFA_KV_CONTIG) kc->box_rows = (int)gcd64(kc->T, p.blockSize);
+    kc->tail_rows = std::min(kc->box_rows, 32);
     return IFA_OK;
 }
 
@@ -205,7 +207,7 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-bool encode_kv_map(const ifa_params& p, const KernelChoice& kc, const void* base, CUtensorMap* map) {
+bool encode_kv_map(const ifa_params& p, const KernelChoice& kc, const void* base, int box_rows, CUtensorMap* map) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const uint64_t E = (uint64_t)kc.es, D = (uint64_t)p.headDim, KVN = (uint64_t)kc.KV_N;
@@ -223,7 +225,7 @@ bool encode_kv_map(const ifa_params& p, const KernelChoice& kc, const void* base
         strides[1] = D * E;
         strides[2] = S * KVN * D * E;
     }
-    cuuint32_t box[4] = {(cuuint32_t)(128 / kc.es), (cuuint32_t)kc.box_rows, 1, 1};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / kc.es), (cuuint32_t)box_rows, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUtensorMapDataType dt = kc.kv_kind == KV_I8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : (kc.kv_kind == KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -231,6 +233,11 @@ bool encode_kv_map(const ifa_params& p, const KernelChoice& kc, const void* base
     return enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_kv_maps(const ifa_params& p, const KernelChoice& kc, const void* key, const void* value, DecodeParams& dp) {
+    return encode_kv_map(p, kc, key, kc.box_rows, &dp.tmK) && encode_kv_map(p, kc, value, kc.box_rows, &dp.tmV) &&
+           encode_kv_map(p, kc, key, kc.tail_rows, &dp.tmKt) && encode_kv_map(p, kc, value, kc.tail_rows, &dp.tmVt);
 }
 
 void fill_decode_params(DecodeParams& dp, const ifa_params& p, const KernelChoice& kc, const void* query,
@@ -257,6 +264,7 @@ void fill_decode_params(DecodeParams& dp, const ifa_params& p, const KernelChoic
     dp.bt_cols = (int)p.blockTableCols;
     dp.block_num = (int)p.blockNum;
     dp.box_rows = kc.box_rows;
+    dp.tail_rows = kc.tail_rows;
     dp.has_mask = p.has_mask != 0;
     dp.mask_bstride = (p.has_mask && p.maskB > 1) ? p.maskN * p.maskS : 0;
     dp.mask_nstride = (p.has_mask && p.maskN > 1) ? p.maskS : 0;
