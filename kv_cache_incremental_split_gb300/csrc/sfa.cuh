@@ -1,0 +1,51 @@
+// Sparse-index MLA-absorb decode ("SparseFlashAttention" README): launch
+// parameters and fixed sizes of the tcgen05 kernel (sfa_kernel.cu).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ifa.h"
+
+namespace ifa {
+
+constexpr int kSfaTile = 64;        // sparse positions per tile (the N of S = Q K^T)
+constexpr int kSfaD = 512;          // head dim of query, key and value
+constexpr int kSfaDr = 64;          // rope dim
+constexpr int kSfaHalf = 256;       // value channels per CTA sequence (one half of D)
+constexpr int kSfaQBlocks = 9;      // 64-column blocks of [q | q_rope]
+constexpr int kSfaVBlocks = 4;      // 64-column blocks of one value half
+constexpr int kSfaStages = 8;       // 8 KB ring stages (64 rows x 128 B)
+constexpr int kSfaStageBytes = kSfaTile * 128;
+constexpr int kSfaQBytes = kSfaQBlocks * 128 * 128;
+constexpr int kSfaThreads = 6 * 32;  // producer, MMA issuer, four softmax warps
+constexpr int kSfaSlotFloats = 128 * kSfaHalf + 2 * 128;  // partial O of one piece + m + l
+constexpr int kSfaSmem = 1024 + kSfaQBytes + kSfaStages * kSfaStageBytes + 512;
+constexpr size_t kSfaPartialOffset = 4096;  // workspace: [0,256) error word, [256, ..) counters, partials
+constexpr float kSfaRescaleSlack = 8.0f;    // log2 units the running max may trail before O is rescaled
+
+struct alignas(128) SfaParams {
+    CUtensorMap tmQ;    // 3-D (d, head, batch) over query, 64 x 128 x 1 boxes
+    CUtensorMap tmQr;   // same over query_rope
+    CUtensorMap tmK;    // 2-D (d, cache row) over key, 64 x 1 boxes (row gathers)
+    CUtensorMap tmKr;   // over key_rope
+    CUtensorMap tmV;    // over value
+    const int32_t* indices;
+    const int32_t* block_table;
+    const int32_t* lens;
+    void* out;
+    float* partials;
+    unsigned long long* counters;
+    int* err;
+    long long W;        // tiles: 2 * B * tiles_per_seq
+    int P;
+    int B, QN, S_sp, tiles_per_seq;
+    int block_size, bt_cols, block_num, total_rows;
+    int is_bf16;
+    float scale_log2;
+    unsigned int gen;
+};
+
+cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream);
+
+}  // namespace ifa

@@ -33,7 +33,7 @@ ANTIQUANT = {"none": 0, "per_channel": 1, "per_tensor": 2}
 
 # Every symbol include/ifa.h declares.
 EXPORTED = ("ifa_create", "ifa_run", "ifa_destroy", "ifa_get_device_errors", "ifa_last_launch_count",
-            "ifa_run_noalloc", "ifa_status_string")
+            "ifa_run_noalloc", "sfa_workspace_size", "sfa_run", "ifa_status_string")
 
 # Fixed scratch of ifa_run_noalloc (include/ifa.h).
 IFA_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -51,6 +51,16 @@ class IfaParams(ctypes.Structure):
         ("maskB", ctypes.c_int64), ("maskN", ctypes.c_int64), ("maskS", ctypes.c_int64),
         ("antiquant", ctypes.c_int32), ("has_kv_padding", ctypes.c_int32),
         ("scaleValue", ctypes.c_double), ("splitTiles", ctypes.c_int64),
+    ]
+
+
+class SfaParams(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int64), ("Q_N", ctypes.c_int64), ("KV_N", ctypes.c_int64), ("D", ctypes.c_int64),
+        ("Dr", ctypes.c_int64), ("block_size", ctypes.c_int64), ("block_num", ctypes.c_int64),
+        ("block_table_cols", ctypes.c_int64), ("sparse_size", ctypes.c_int64),
+        ("sparse_block_size", ctypes.c_int64), ("dtype", ctypes.c_int32), ("sparse_mode", ctypes.c_int32),
+        ("scale_value", ctypes.c_double),
     ]
 
 
@@ -86,6 +96,10 @@ def load_library():
             lib.ifa_run_noalloc.restype = ctypes.c_int32
             lib.ifa_run_noalloc.argtypes = [ctypes.POINTER(IfaParams), vp, vp, vp, vp, vp, vp, i64, vp, vp, vp,
                                             vp, vp, vp]
+            lib.sfa_workspace_size.restype = ctypes.c_int32
+            lib.sfa_workspace_size.argtypes = [ctypes.POINTER(SfaParams), ctypes.POINTER(sz)]
+            lib.sfa_run.restype = ctypes.c_int32
+            lib.sfa_run.argtypes = [ctypes.POINTER(SfaParams), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
             lib.ifa_status_string.restype = ctypes.c_char_p
             lib.ifa_status_string.argtypes = [ctypes.c_int32]
             _lib = lib
@@ -220,3 +234,66 @@ class IncreFlashAttention:
 
     def device_errors(self, stream=None) -> int:
         return ifa_get_device_errors(self.plan, _stream_handle(stream))
+
+
+def sfa_workspace_size(params: SfaParams):
+    """Returns (status, workspace bytes)."""
+    ws = ctypes.c_size_t()
+    st = load_library().sfa_workspace_size(ctypes.byref(params), ctypes.byref(ws))
+    return st, ws.value
+
+
+def sfa_run(params: SfaParams, query, query_rope, key, key_rope, value, sparse_indices, block_table,
+            actual_seq_lengths_kv, attention_out, workspace, workspace_bytes, device_error_flags, stream) -> int:
+    """Pointer arguments are integers (device addresses) or None."""
+    return load_library().sfa_run(ctypes.byref(params), query, query_rope, key, key_rope, value, sparse_indices,
+                                  block_table, actual_seq_lengths_kv, attention_out, workspace, workspace_bytes,
+                                  device_error_flags, stream)
+
+
+class SparseFlashAttention:
+    """Sparse-index MLA-absorb decode (``sfa_run`` in ``include/ifa.h``).
+
+    Construction validates the static description and allocates the workspace
+    with torch; calling the object enqueues ``sfa_run`` on the current (or given)
+    torch stream and returns the output tensor (B, 1, Q_N, 512).
+    """
+
+    def __init__(self, *, batch: int, num_heads: int, block_size: int, block_num: int, block_table_cols: int,
+                 sparse_size: int, dtype: str = "bf16", scale: Optional[float] = None, sparse_mode: int = 0,
+                 device=None):
+        import torch
+        p = SfaParams()
+        p.B, p.Q_N, p.KV_N, p.D, p.Dr = batch, num_heads, 1, 512, 64
+        p.block_size, p.block_num, p.block_table_cols = block_size, block_num, block_table_cols
+        p.sparse_size, p.sparse_block_size = sparse_size, 1
+        p.dtype = DTYPES[dtype]
+        p.sparse_mode = sparse_mode
+        p.scale_value = (1.0 / math.sqrt(576)) if scale is None else float(scale)
+        self.params = p
+        st, ws = sfa_workspace_size(p)
+        if st != IFA_OK:
+            raise IfaError(st, "sfa_workspace_size")
+        dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.errors = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def __call__(self, query, query_rope, key, key_rope, value, sparse_indices, block_table, actual_seq_lengths_kv,
+                 *, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty_like(query)
+        st = sfa_run(self.params, _ptr(query), _ptr(query_rope), _ptr(key), _ptr(key_rope), _ptr(value),
+                     _ptr(sparse_indices), _ptr(block_table), _ptr(actual_seq_lengths_kv), _ptr(out),
+                     _ptr(self.workspace), self.workspace.numel(), _ptr(self.errors), _stream_handle(stream))
+        if st != IFA_OK:
+            raise IfaError(st, "sfa_run")
+        return out
+
+    def device_errors(self, clear: bool = True) -> int:
+        import torch
+        torch.cuda.synchronize()
+        v = int(self.errors.item())
+        if clear:
+            self.errors.zero_()
+        return v

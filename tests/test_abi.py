@@ -135,3 +135,52 @@ VALID = [
 def test_valid_descriptions_pass_validation(lib, kw):
     # Without a GPU the device query fails after validation (IFA_ERR_RUNTIME); with one the plan is created.
     assert create_status(lib, base_params(**kw)) in (ifa.IFA_OK, ifa.IFA_ERR_RUNTIME)
+
+
+def test_sfa_params_struct_layout_matches_header(tmp_path):
+    src = tmp_path / "sfa_layout.c"
+    body = "\n".join(f'  printf("%zu\\n", offsetof(sfa_params, {f}));' for f, _ in ifa.SfaParams._fields_)
+    src.write_text(f'#include <stdio.h>\n#include <stddef.h>\n#include "ifa.h"\nint main(void) {{\n'
+                   f'  printf("%zu\\n", sizeof(sfa_params));\n{body}\n  return 0;\n}}\n')
+    exe = tmp_path / "sfa_layout"
+    subprocess.check_call(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = [int(x) for x in subprocess.check_output([str(exe)]).split()]
+    assert got[0] == ctypes.sizeof(ifa.SfaParams)
+    for (name, _), off in zip(ifa.SfaParams._fields_, got[1:]):
+        assert getattr(ifa.SfaParams, name).offset == off, name
+
+
+def sfa_params(**kw):
+    p = ifa.SfaParams()
+    p.B, p.Q_N, p.KV_N, p.D, p.Dr = 4, 128, 1, 512, 64
+    p.block_size, p.block_num, p.block_table_cols, p.sparse_size, p.sparse_block_size = 64, 100, 20, 2048, 1
+    p.dtype = ifa.DTYPES["bf16"]
+    p.sparse_mode = 0
+    p.scale_value = 1 / 24
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+SFA_INVALID = [dict(KV_N=2), dict(D=256), dict(Dr=32), dict(Q_N=0), dict(Q_N=129), dict(block_size=24),
+               dict(block_size=2048), dict(sparse_block_size=2), dict(sparse_mode=1), dict(dtype=2),
+               dict(sparse_size=0), dict(block_num=0), dict(B=-1), dict(scale_value=float("inf"))]
+
+
+@pytest.mark.parametrize("kw", SFA_INVALID)
+def test_sfa_invalid_descriptions_are_rejected(lib, kw):
+    st, _ = ifa.sfa_workspace_size(sfa_params(**kw))
+    assert st == ifa.IFA_ERR_PARAM_INVALID
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(Q_N=16), dict(sparse_mode=3), dict(dtype=0), dict(block_size=16)])
+def test_sfa_valid_descriptions_pass_validation(lib, kw):
+    st, ws = ifa.sfa_workspace_size(sfa_params(**kw))
+    assert st in (ifa.IFA_OK, ifa.IFA_ERR_RUNTIME)
+    if st == ifa.IFA_OK:
+        assert ws > 0
+
+
+def test_sfa_run_null_arguments(lib):
+    assert ifa.sfa_run(sfa_params(), None, None, None, None, None, None, None, None, None, None, 0, None, None) in \
+        (ifa.IFA_ERR_PARAM_NULLPTR,)

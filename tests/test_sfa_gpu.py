@@ -1,0 +1,142 @@
+"""GPU parity of the sparse-index MLA-absorb decode kernel (tcgen05) against the
+float64 CPU oracle on the same seeded inputs.  Tolerances: max abs error <=
+1.5e-2 (bf16 outputs) and <= 2e-3 (fp16 outputs); the selected-set check is
+bit-exact."""
+import numpy as np
+import pytest
+
+import oracle
+from kv_cache_incremental_split_gb300 import inputs as gen
+from harness import TOL, max_abs_err, out_to_f64, to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from kv_cache_incremental_split_gb300 import build
+    build.build()
+
+
+def run_gpu(c, sparse_mode=0):
+    from kv_cache_incremental_split_gb300.ifa import SparseFlashAttention
+    op = SparseFlashAttention(batch=c.B, num_heads=c.query.shape[2], block_size=c.key.shape[1],
+                              block_num=c.key.shape[0], block_table_cols=c.block_table.shape[1],
+                              sparse_size=c.sparse_indices.shape[-1], dtype=c.dtype, scale=c.scale,
+                              sparse_mode=sparse_mode)
+    t = [to_device(a) for a in (c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices,
+                                c.block_table, c.actual_seq_lengths_kv)]
+    out = op(*t)
+    torch.cuda.synchronize()
+    return out_to_f64(out).reshape(c.B, c.query.shape[2], 512), op
+
+
+def run_ref(c, batches=None):
+    cc = c
+    if batches is not None:
+        import copy
+        cc = copy.copy(c)
+        bs = np.asarray(batches)
+        cc.query, cc.query_rope = c.query[bs], c.query_rope[bs]
+        cc.sparse_indices, cc.block_table = c.sparse_indices[bs], c.block_table[bs]
+        cc.actual_seq_lengths_kv = c.actual_seq_lengths_kv[bs]
+    return oracle.sfa_ref(cc.query, cc.query_rope, cc.key, cc.key_rope, cc.value, cc.sparse_indices,
+                          cc.block_table, cc.actual_seq_lengths_kv, scale=cc.scale)
+
+
+def check(c, batches=None, sparse_mode=0):
+    got, op = run_gpu(c, sparse_mode)
+    ref = run_ref(c, batches)
+    if batches is not None:
+        got = got[np.asarray(batches)]
+    assert np.all(np.isfinite(got))
+    err = max_abs_err(got, ref)
+    assert err <= TOL[c.dtype], err
+    return got, op
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_sfa_small(seed):
+    check(gen.sfa_mla(seed, B=3, Q_N=128, block_size=64, kv_len=1000, sparse_size=300, nvalid_lo=1,
+                      nvalid_hi=300))
+
+
+@pytest.mark.parametrize("Q_N,block_size", [(16, 16), (64, 48), (1, 1024), (100, 128)])
+def test_sfa_heads_and_block_sizes(Q_N, block_size):
+    check(gen.sfa_mla(2, B=2, Q_N=Q_N, block_size=block_size, kv_len=3000, sparse_size=200, nvalid_lo=50,
+                      nvalid_hi=200))
+
+
+def test_sfa_fp16_and_sparse_mode_3():
+    c = gen.sfa_mla(3, B=2, Q_N=128, block_size=64, kv_len=800, sparse_size=130, nvalid_lo=60, nvalid_hi=130,
+                    dtype="fp16")
+    check(c)
+    check(c, sparse_mode=3)
+
+
+def test_sfa_long_rows_are_split_and_merged():
+    # few batches, long index rows: sequences are cut into several pieces across CTAs
+    check(gen.sfa_mla(4, B=1, Q_N=128, block_size=64, kv_len=32768, sparse_size=2048, nvalid_lo=2048,
+                      nvalid_hi=2048))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_sfa_full_size_sampled(seed):
+    c = gen.sfa_mla(seed)
+    rng = np.random.default_rng(300 + seed)
+    check(c, batches=np.sort(rng.choice(c.B, size=3, replace=False)))
+
+
+def test_sfa_edge_rows():
+    c = gen.sfa_mla(5, B=4, Q_N=32, block_size=64, kv_len=512, sparse_size=100, nvalid_lo=10, nvalid_hi=100)
+    c.sparse_indices[0] = -1                      # nothing selected: zeros
+    c.sparse_indices[1] = -1
+    c.sparse_indices[1, 0, 0, 0] = 77             # one index: that value row
+    c.sparse_indices[2, 0, 0, 5] = 600            # beyond the length, in the middle: skipped
+    c.sparse_indices[3, 0, 0, :4] = [9, 9, 9, 3]  # duplicates count once per occurrence
+    got, _ = check(c)
+    assert np.all(got[0] == 0)
+
+
+def test_sfa_selected_set_bit_exact():
+    """Q = 0 and value row = code of its token: the output is exactly the mean of the
+    codes of the valid selected tokens (powers-of-two counts make the mean exact)."""
+    c = gen.sfa_mla(6, B=2, Q_N=128, block_size=64, kv_len=4096, sparse_size=256, nvalid_lo=256, nvalid_hi=256)
+    c.query[:] = 0
+    c.query_rope[:] = 0
+    codes = np.zeros(c.value.shape, dtype=np.float32)
+    bs = 64
+    for b in range(2):
+        for blk_i, blk in enumerate(c.block_table[b]):
+            codes[blk, :, 0, :] = (np.arange(bs) + blk_i * bs)[:, None] % 128
+    c.value = gen.to_storage(codes, "bf16")
+    idx = np.full((2, 1, 1, 256), -1, dtype=np.int32)
+    rng = np.random.default_rng(7)
+    idx[0, 0, 0, :128] = rng.choice(4096, size=128, replace=False)
+    idx[1, 0, 0, :64] = rng.choice(4096, size=64, replace=False)
+    c.sparse_indices = idx
+    got, _ = run_gpu(c)
+    ref = run_ref(c)  # exact means (power-of-two counts), representable in float32
+    ref_bf16 = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(ref.astype(np.float32))).astype(np.float64)
+    assert np.array_equal(got, ref_bf16)
+
+
+def test_sfa_bad_block_entry_sets_error_flag():
+    c = gen.sfa_mla(8, B=2, Q_N=16, block_size=64, kv_len=640, sparse_size=64, nvalid_lo=64, nvalid_hi=64)
+    c.block_table[1, :] = c.key.shape[0] + 3  # every entry of batch 1 out of range: its tokens are left out
+    got, op = run_gpu(c)
+    assert op.device_errors() & 1
+    ref = run_ref(c)
+    assert max_abs_err(got, ref) <= TOL["bf16"]
+    assert np.all(got[1] == 0)
+
+
+def test_sfa_deterministic():
+    c = gen.sfa_mla(9, B=2, Q_N=128, block_size=64, kv_len=8192, sparse_size=2048, nvalid_lo=1500,
+                    nvalid_hi=2048)
+    a, _ = run_gpu(c)
+    b, _ = run_gpu(c)
+    assert np.array_equal(a, b)
