@@ -1,17 +1,18 @@
 #!/usr/bin/env python3
 """Decode-attention benchmark: KV-cache GB/s read and decode-attention calls/s.
 
-One step = one ifa_run call (split-KV partial kernel + combine kernel) over one
-batch of the workload.  Default workload: GQA decode against a padded cache,
-B=16, N=32, KV_N=8, D=128, BSH bf16, Smax=4096, lengths ~ U{1..4096}, bool mask
-(B,1,1,S) true past each length.
+One step = one library call (ifa_run, or sfa_run for the sparse workload) over
+one batch of the workload.  Default workload: GQA decode against a padded
+cache, B=16, N=32, KV_N=8, D=128, BSH bf16, Smax=4096, lengths ~ U{1..4096},
+bool mask (B,1,1,S) true past each length.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
-Prints one JSON line on rank 0.  ``value`` is algorithmic bytes (valid-token K
-and V, query, output, mask over the valid windows, block-table entries used,
-antiquant parameters) per step divided by the device time per step, summed over
-ranks (weak scaling: every rank runs its own copy of the workload).
+Prints one JSON line on rank 0.  ``value`` is algorithmic bytes per step
+(key/value rows of the valid tokens, query, output, mask over the valid
+windows, block-table entries and sparse indices used, antiquant parameters)
+divided by the device time per step, summed over ranks (weak scaling: every
+rank runs its own rank-seeded copy of the workload).
 """
 from __future__ import annotations
 
@@ -47,12 +48,20 @@ WORKLOADS = {
                      "per-channel scale/offset, Smax=8192, lengths U{256..8192}, pad Smax-len-U{0..64}"),
     "paged_gqa_small": ("paged GQA decode, profiling size: B=64 N=32 KV_N=8 D=128 bf16, blockSize 128, "
                         "random block table, lengths U{512..4096}"),
+    "sfa_mla": ("sparse MLA-absorb decode: B=32 Q_N=128 KV_N=1 D=512+rope 64 bf16, PA_BSND block 64, "
+                "KV length 32768, sparse_indices (B,1,1,2048) with U{1024..2048} valid then -1, scale 1/sqrt(576)"),
+    "sfa_mla_small": ("sparse MLA-absorb decode, profiling size: B=8 Q_N=128 D=512+64 bf16, block 64, "
+                      "KV length 8192, 2048 indices with U{1024..2048} valid"),
 }
 
 
-def make_case(name: str, seed: int) -> gen.IfaCase:
+def make_case(name: str, seed: int):
     if name == "paged_gqa_small":
         return gen.paged_gqa(seed, len_hi=4096)
+    if name == "sfa_mla":
+        return gen.sfa_mla(seed)
+    if name == "sfa_mla_small":
+        return gen.sfa_mla(seed, B=8, kv_len=8192)
     return {"gqa_padded": gen.gqa_padded, "tiny_mha": gen.tiny_mha, "paged_gqa": gen.paged_gqa,
             "int8_leftpad": gen.int8_leftpad}[name](seed)
 
@@ -76,7 +85,21 @@ def windows(case: gen.IfaCase):
     return out
 
 
-def algorithmic_bytes(case: gen.IfaCase) -> int:
+def sfa_valid_counts(case: gen.SfaCase):
+    idx = case.sparse_indices.reshape(case.B, -1)
+    lens = case.actual_seq_lengths_kv.reshape(-1, 1)
+    return ((idx >= 0) & (idx < lens)).sum(axis=1)
+
+
+def algorithmic_bytes(case) -> int:
+    if isinstance(case, gen.SfaCase):
+        n = int(sfa_valid_counts(case).sum())
+        QN = case.query.shape[2]
+        total = n * (512 + 64 + 512) * 2                       # key, key_rope and value rows of selected tokens
+        total += case.B * QN * (512 + 64) * 2                  # query and query_rope
+        total += case.B * QN * 512 * 2                         # output
+        total += case.sparse_indices.nbytes + n * 4            # indices and block-table entries used
+        return int(total)
     kv_es = 1 if case.kv_dtype == "int8" else 2
     kvn = case.num_kv_heads or case.num_heads
     toks = sum(L for _, L in windows(case))
@@ -100,10 +123,11 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 
 
 class ClockSampler:
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.t0 = self.t1 = None
+        self.lines = []
 
     def __enter__(self):
         try:
@@ -123,7 +147,6 @@ class ClockSampler:
         self.t1 = time.time()
 
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             time.sleep(0.15)
             self.proc.terminate()
@@ -171,9 +194,9 @@ def kernel_sources_digest() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the partial kernel from a committed ncu summary,
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary,
     valid only while the kernel sources are unchanged since the capture."""
-    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.txt")
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -222,35 +245,50 @@ def aggregate(local_elapsed_ms: float, local_bytes: float, world: int):
 
 # ------------------------------------------------------------------------ CPU oracle baseline
 
-def oracle_sample(case: gen.IfaCase, budget_s: float, start_batch: int = 0):
+def _batch_subset(case, b):
+    """The same problem restricted to batch b (shared paged caches stay whole)."""
+    from copy import copy
+    c = copy(case)
+    sel = np.array([b])
+    if isinstance(case, gen.SfaCase):
+        c.query, c.query_rope = case.query[sel], case.query_rope[sel]
+        c.sparse_indices, c.block_table = case.sparse_indices[sel], case.block_table[sel]
+        c.actual_seq_lengths_kv = case.actual_seq_lengths_kv[sel]
+        return c
+    c.query = case.query[sel]
+    if case.kv_format == "contig":
+        c.key, c.value = case.key[sel], case.value[sel]
+    if case.block_table is not None:
+        c.block_table = case.block_table[sel]
+    if case.atten_mask is not None and case.atten_mask.shape[0] > 1:
+        c.atten_mask = case.atten_mask[sel]
+    if case.actual_seq_lengths is not None:
+        c.actual_seq_lengths = case.actual_seq_lengths[sel]
+    if case.kv_padding_size is not None and case.kv_padding_size.size > 1:
+        c.kv_padding_size = case.kv_padding_size[sel]
+    return c
+
+
+def oracle_sample(case, budget_s: float, start_batch: int = 0):
     """Time the CPU oracle, batch by batch, for about `budget_s` seconds."""
     import oracle  # test infrastructure: only the CPU-baseline leg of the benchmark uses it
-    from copy import copy
     fmt = {"contig": oracle.CONTIG, "paged_nbsd": oracle.PAGED_NBSD, "paged_bsh": oracle.PAGED_BSH}
     aq = {"none": oracle.AQ_NONE, "per_channel": oracle.AQ_PER_CHANNEL, "per_tensor": oracle.AQ_PER_TENSOR}
     done, nbytes, t_used = [], 0, 0.0
     b = start_batch % case.B
     while True:
-        c = copy(case)
-        sel = np.array([b])
-        c.query = case.query[sel]
-        if case.kv_format == "contig":
-            c.key, c.value = case.key[sel], case.value[sel]
-        if case.block_table is not None:
-            c.block_table = case.block_table[sel]
-        if case.atten_mask is not None and case.atten_mask.shape[0] > 1:
-            c.atten_mask = case.atten_mask[sel]
-        if case.actual_seq_lengths is not None:
-            c.actual_seq_lengths = case.actual_seq_lengths[sel]
-        if case.kv_padding_size is not None and case.kv_padding_size.size > 1:
-            c.kv_padding_size = case.kv_padding_size[sel]
+        c = _batch_subset(case, b)
         t = time.perf_counter()
-        oracle.ifa_ref(c.query, c.key, c.value, num_heads=c.num_heads, num_kv_heads=c.num_kv_heads,
-                       scale=c.scale, layout=c.layout, kv_format=fmt[c.kv_format], block_size=c.block_size,
-                       block_table=c.block_table, atten_mask=c.atten_mask,
-                       actual_seq_lengths=c.actual_seq_lengths, kv_padding_size=c.kv_padding_size,
-                       antiquant=aq[c.antiquant], antiquant_scale=c.antiquant_scale,
-                       antiquant_offset=c.antiquant_offset)
+        if isinstance(c, gen.SfaCase):
+            oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
+                           c.actual_seq_lengths_kv, scale=c.scale)
+        else:
+            oracle.ifa_ref(c.query, c.key, c.value, num_heads=c.num_heads, num_kv_heads=c.num_kv_heads,
+                           scale=c.scale, layout=c.layout, kv_format=fmt[c.kv_format], block_size=c.block_size,
+                           block_table=c.block_table, atten_mask=c.atten_mask,
+                           actual_seq_lengths=c.actual_seq_lengths, kv_padding_size=c.kv_padding_size,
+                           antiquant=aq[c.antiquant], antiquant_scale=c.antiquant_scale,
+                           antiquant_offset=c.antiquant_offset)
         t_used += time.perf_counter() - t
         nbytes += algorithmic_bytes(c)
         done.append(b)
@@ -289,6 +327,100 @@ def run_reference(args):
 
 # ------------------------------------------------------------------------ GPU arm
 
+def _to_dev(a, dev):
+    import torch
+    if a is None:
+        return None
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return (t.view(torch.bfloat16) if a.dtype == np.uint16 else t).to(dev)
+
+
+class IfaWorkload:
+    """One incremental-attention problem on the device, with rotating key/value copies."""
+
+    def __init__(self, case: gen.IfaCase, dev, copies_for):
+        from kv_cache_incremental_split_gb300.ifa import IncreFlashAttention
+        self.case, self.dev = case, dev
+        m = case.atten_mask
+        self.op = IncreFlashAttention(
+            batch=case.B, num_heads=case.num_heads, num_kv_heads=case.num_kv_heads, head_dim=case.D,
+            max_seq_len=case.max_seq_len, dtype=case.q_dtype, kv_dtype=case.kv_dtype, layout=case.layout,
+            kv_format=case.kv_format, block_size=case.block_size,
+            block_num=case.key.shape[0] if case.kv_format != "contig" else 0,
+            block_table_cols=case.block_table.shape[1] if case.block_table is not None else 0,
+            mask_shape=None if m is None else m.shape, mask_dtype="bool", antiquant=case.antiquant,
+            kv_padding=case.kv_padding_size is not None, scale=case.scale, device=dev)
+        self.q = _to_dev(case.query, dev)
+        k, v = _to_dev(case.key, dev), _to_dev(case.value, dev)
+        self.mask, self.bt = _to_dev(case.atten_mask, dev), _to_dev(case.block_table, dev)
+        self.sc, self.of = _to_dev(case.antiquant_scale, dev), _to_dev(case.antiquant_offset, dev)
+        self.copies = copies_for
+        self.rotating_bytes = k.numel() * k.element_size() + v.numel() * v.element_size()
+        self.ks = [k] + [k.clone() for _ in range(self.copies - 1)]
+        self.vs = [v] + [v.clone() for _ in range(self.copies - 1)]
+        self.outs = [self.q.new_empty(self.q.shape) for _ in range(self.copies)]
+        self.dtype = case.q_dtype if case.kv_dtype != "int8" else "int8-kv/" + case.q_dtype
+        self.call_name = "ifa_run"
+
+    def call(self, i, stream):
+        c = self.case
+        return self.op(self.q, self.ks[i], self.vs[i], atten_mask=self.mask, actual_seq_lengths=c.actual_seq_lengths,
+                       kv_padding_size=c.kv_padding_size, block_table=self.bt, antiquant_scale=self.sc,
+                       antiquant_offset=self.of, out=self.outs[i], stream=stream)
+
+    def launches_per_call(self):
+        return self.op.last_launch_count()
+
+    def host_inputs(self):
+        c = self.case
+        return {n: a for n, a in (("q", c.query), ("k", c.key), ("v", c.value), ("mask", c.atten_mask),
+                                  ("bt", c.block_table), ("sc", c.antiquant_scale), ("of", c.antiquant_offset))
+                if a is not None}
+
+    def call_on(self, d, stream):
+        c = self.case
+        return self.op(d["q"], d["k"], d["v"], atten_mask=d.get("mask"), actual_seq_lengths=c.actual_seq_lengths,
+                       kv_padding_size=c.kv_padding_size, block_table=d.get("bt"), antiquant_scale=d.get("sc"),
+                       antiquant_offset=d.get("of"), stream=stream)
+
+
+class SfaWorkload:
+    """One sparse MLA-absorb problem on the device, with rotating cache copies."""
+
+    def __init__(self, case: gen.SfaCase, dev, copies_for):
+        from kv_cache_incremental_split_gb300.ifa import SparseFlashAttention
+        self.case, self.dev = case, dev
+        self.op = SparseFlashAttention(batch=case.B, num_heads=case.query.shape[2], block_size=case.key.shape[1],
+                                       block_num=case.key.shape[0], block_table_cols=case.block_table.shape[1],
+                                       sparse_size=case.sparse_indices.shape[-1], dtype=case.dtype,
+                                       scale=case.scale, device=dev)
+        self.q, self.qr = _to_dev(case.query, dev), _to_dev(case.query_rope, dev)
+        self.idx, self.bt = _to_dev(case.sparse_indices, dev), _to_dev(case.block_table, dev)
+        self.lens = _to_dev(case.actual_seq_lengths_kv, dev)
+        k, kr, v = _to_dev(case.key, dev), _to_dev(case.key_rope, dev), _to_dev(case.value, dev)
+        self.copies = copies_for
+        self.rotating_bytes = sum(t.numel() * t.element_size() for t in (k, kr, v))
+        self.caches = [(k, kr, v)] + [(k.clone(), kr.clone(), v.clone()) for _ in range(self.copies - 1)]
+        self.outs = [self.q.new_empty(self.q.shape) for _ in range(self.copies)]
+        self.dtype = case.dtype
+        self.call_name = "sfa_run"
+
+    def call(self, i, stream):
+        k, kr, v = self.caches[i]
+        return self.op(self.q, self.qr, k, kr, v, self.idx, self.bt, self.lens, out=self.outs[i], stream=stream)
+
+    def launches_per_call(self):
+        return 1
+
+    def host_inputs(self):
+        c = self.case
+        return {"q": c.query, "qr": c.query_rope, "k": c.key, "kr": c.key_rope, "v": c.value,
+                "idx": c.sparse_indices, "bt": c.block_table, "lens": c.actual_seq_lengths_kv}
+
+    def call_on(self, d, stream):
+        return self.op(d["q"], d["qr"], d["k"], d["kr"], d["v"], d["idx"], d["bt"], d["lens"], stream=stream)
+
+
 def run_gpu(args):
     import torch
 
@@ -303,54 +435,25 @@ def run_gpu(args):
 
     from kv_cache_incremental_split_gb300 import build as libbuild
     libbuild.build()
-    from kv_cache_incremental_split_gb300.ifa import IncreFlashAttention
 
     case = make_case(args.workload, args.seed + rank)
     alg = algorithmic_bytes(case)
-
-    def dev_t(a):
-        if a is None:
-            return None
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        return (t.view(torch.bfloat16) if a.dtype == np.uint16 else t).to(dev)
-
-    m = case.atten_mask
-    op = IncreFlashAttention(
-        batch=case.B, num_heads=case.num_heads, num_kv_heads=case.num_kv_heads, head_dim=case.D,
-        max_seq_len=case.max_seq_len, dtype=case.q_dtype, kv_dtype=case.kv_dtype, layout=case.layout,
-        kv_format=case.kv_format, block_size=case.block_size,
-        block_num=case.key.shape[0] if case.kv_format != "contig" else 0,
-        block_table_cols=case.block_table.shape[1] if case.block_table is not None else 0,
-        mask_shape=None if m is None else m.shape, mask_dtype="bool", antiquant=case.antiquant,
-        kv_padding=case.kv_padding_size is not None, scale=case.scale, device=dev)
-
-    q, k, v = dev_t(case.query), dev_t(case.key), dev_t(case.value)
-    mask, bt = dev_t(case.atten_mask), dev_t(case.block_table)
-    sc, of = dev_t(case.antiquant_scale), dev_t(case.antiquant_offset)
-    kv_bytes = k.numel() * k.element_size() + v.numel() * v.element_size()
-    # Rotate through enough key/value copies that the valid bytes streamed between two
-    # uses of one copy exceed L2 several times (inputs larger than L2: no flush needed).
+    # Rotate through enough input copies that the bytes streamed between two uses of one
+    # copy exceed L2 several times (inputs larger than L2: no flush between steps).
     copies = max(1, min(8, math.ceil(6 * L2_BYTES / max(1, alg))))
-    ks = [k] + [k.clone() for _ in range(copies - 1)]
-    vs = [v] + [v.clone() for _ in range(copies - 1)]
-    outs = [torch.empty_like(q) for _ in range(copies)]
+    wl = SfaWorkload(case, dev, copies) if isinstance(case, gen.SfaCase) else IfaWorkload(case, dev, copies)
     stream = torch.cuda.Stream(device=dev)
-
-    def call(i):
-        return op(q, ks[i], vs[i], atten_mask=mask, actual_seq_lengths=case.actual_seq_lengths,
-                  kv_padding_size=case.kv_padding_size, block_table=bt, antiquant_scale=sc,
-                  antiquant_offset=of, out=outs[i], stream=stream)
 
     with torch.cuda.stream(stream):
         for w in range(max(args.warmup, 3)):
-            call(w % copies)
+            wl.call(w % copies, stream)
         stream.synchronize()
-        launches_per_call = op.last_launch_count()
+        launches_per_call = wl.launches_per_call()
         graphs = []
         for i in range(copies):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                call(i)
+                wl.call(i, stream)
             graphs.append(g)
         for i in range(copies):
             graphs[i].replay()
@@ -363,7 +466,7 @@ def run_gpu(args):
         stream.synchronize()
         e0.record(stream)
         for i in range(n_eager):
-            call(i % copies)
+            wl.call(i % copies, stream)
         e1.record(stream)
         e1.synchronize()
         eager_ms = e0.elapsed_time(e1) / n_eager
@@ -395,30 +498,20 @@ def run_gpu(args):
     value = total_bytes / (max_elapsed * 1e-3) / 1e9
     local_gbs = alg / (elapsed / args.steps * 1e-3) / 1e9
 
-    # ---- end to end through the public API: pinned host inputs -> device -> ifa_run -> host output
-    host = {n: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-            for n, a in (("q", case.query), ("k", case.key), ("v", case.value), ("mask", case.atten_mask),
-                         ("bt", case.block_table), ("sc", case.antiquant_scale), ("of", case.antiquant_offset))
-            if a is not None}
+    # ---- end to end through the public API: pinned host inputs -> device -> call -> host output
+    host = {n: torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for n, a in wl.host_inputs().items()}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d_in = {n: torch.empty(t.shape, dtype=t.dtype, device=dev) for n, t in host.items()}
-    out_host = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    bf_names = {n for n, a in wl.host_inputs().items() if a.dtype == np.uint16}
+    d_raw = {n: torch.empty(t.shape, dtype=t.dtype, device=dev) for n, t in host.items()}
+    d_in = {n: (t.view(torch.bfloat16) if n in bf_names else t) for n, t in d_raw.items()}
+    out_host = torch.empty(wl.q.shape, dtype=wl.q.dtype).pin_memory()
     d2h = out_host.numel() * out_host.element_size()
     n_e2e = max(3, min(args.steps, 20))
 
     def e2e_step():
         for n, t in host.items():
-            d_in[n].copy_(t, non_blocking=True)
-        qq = d_in["q"].view(torch.bfloat16) if case.query.dtype == np.uint16 else d_in["q"]
-        kk = d_in["k"].view(torch.bfloat16) if case.key.dtype == np.uint16 else d_in["k"]
-        vv = d_in["v"].view(torch.bfloat16) if case.value.dtype == np.uint16 else d_in["v"]
-        sc_ = d_in.get("sc")
-        of_ = d_in.get("of")
-        if sc_ is not None and case.antiquant_scale.dtype == np.uint16:
-            sc_, of_ = sc_.view(torch.bfloat16), of_.view(torch.bfloat16)
-        o = op(qq, kk, vv, atten_mask=d_in.get("mask"), actual_seq_lengths=case.actual_seq_lengths,
-               kv_padding_size=case.kv_padding_size, block_table=d_in.get("bt"), antiquant_scale=sc_,
-               antiquant_offset=of_, stream=stream)
+            d_raw[n].copy_(t, non_blocking=True)
+        o = wl.call_on(d_in, stream)
         out_host.copy_(o, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -448,20 +541,19 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": case.q_dtype if case.kv_dtype != "int8" else "int8-kv/" + case.q_dtype,
-            "data": "synthetic",
+            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "config": {"workload": WORKLOADS[args.workload], "seed": args.seed,
                        "algorithmic_bytes_per_step": alg,
-                       "l2": f"inputs larger than L2: {copies} rotating key/value copies "
-                             f"({copies * kv_bytes / 1e6:.0f} MB) ",
-                       "launch": "CUDA graph replay of one ifa_run call per step",
+                       "l2": f"inputs larger than L2: {copies} rotating cache copies "
+                             f"({copies * wl.rotating_bytes / 1e6:.0f} MB)",
+                       "launch": f"CUDA graph replay of one {wl.call_name} call per step",
                        "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
             "calls_per_sec": world * 1e3 / ms_per_step,
             "calls_per_sec_eager": 1e3 / eager_ms,
             "pct_of_hbm_peak": 100.0 * local_gbs / peak,
             "roofline": {"bound": "hbm", "achieved": local_gbs, "peak": peak, "unit": "GB/s",
                          "frac": local_gbs / peak, "peak_kind": peak_kind,
-                         "timed": "ifa_run (split-KV partial kernel + combine kernel) per step, CUDA events",
+                         "timed": f"{wl.call_name} per step (one kernel launch), CUDA events on its stream",
                          "traffic": recorded_traffic(args.workload)},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
