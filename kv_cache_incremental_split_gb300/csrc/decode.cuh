@@ -30,6 +30,7 @@ struct alignas(128) DecodeParams {
     CUtensorMap tmV;
     CUtensorMap tmKt;  // the same tensors with tail_rows-row boxes, for the last tile of a window
     CUtensorMap tmVt;
+    CUtensorMap tmM;   // 2-D (mask position, mask row) over a per-batch mask, used when mask_tma
     const void* q;
     void* out;
     const uint8_t* mask;
@@ -48,6 +49,7 @@ struct alignas(128) DecodeParams {
     int block_size, bt_cols, block_num, box_rows, tail_rows;
     long long mask_bstride, mask_nstride;
     int has_mask;
+    int mask_tma;              // the producer stages each tile's mask bytes (per-batch masks)
     int aq_per_channel;
     float scale_log2;          // scaleValue * log2(e)
     int slot_floats;
@@ -70,7 +72,9 @@ struct DecodeCfg {
     static constexpr int GT_PAD = 8 * NT;                      // query heads per CTA, padded
     static constexpr int QROW = DPAD * 2 + 16;                 // padded query row in shared memory
     static constexpr int Q_BYTES = GT_PAD * QROW;
-    static constexpr int STAGE_BYTES = round_up_c(2 * KT_BYTES + Q_BYTES, 1024);
+    static constexpr int MASK_BYTES = 256;                     // one tile's mask bytes (T + 16 <= 256)
+    static constexpr int MASK_OFF = 2 * KT_BYTES + Q_BYTES;    // within a stage
+    static constexpr int STAGE_BYTES = round_up_c(2 * KT_BYTES + Q_BYTES + MASK_BYTES, 1024);
     static constexpr int MW = NWC < 4 ? NWC : 4;               // warps the merge buffer holds at once
     static constexpr int MERGE_BYTES = MW * GT_PAD * (DPAD + 2) * 4;
     static constexpr int BAR_BYTES = 256;
@@ -80,6 +84,7 @@ struct DecodeCfg {
     static constexpr int SLOT_FLOATS = GT_PAD * DPAD + 2 * GT_PAD;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(T % 32 == 0, "tiles are whole 32-row sub-boxes");
+    static_assert(MASK_OFF % 128 == 0 && T + 16 <= MASK_BYTES, "mask staging area");
 };
 
 typedef cudaError_t (*DecodeLaunchFn)(const DecodeParams&, int grid, cudaStream_t);
@@ -111,6 +116,9 @@ ifa_status check_run_pointers(const ifa_params& p, const void* query, const void
 bool encode_kv_map(const ifa_params& p, const KernelChoice& kc, const void* base, int box_rows, CUtensorMap* map);
 // The four maps a call needs (key/value x full/tail boxes).
 bool encode_kv_maps(const ifa_params& p, const KernelChoice& kc, const void* key, const void* value, DecodeParams& dp);
+// Stages per-tile mask bytes by TMA when the mask is per batch and 16-byte aligned: sets
+// dp.mask_tma and dp.tmM.  Returns false only when encoding fails.
+bool encode_mask_map(const ifa_params& p, const KernelChoice& kc, const void* mask, DecodeParams& dp);
 // Everything but the tensor maps, the scratch pointers and the window table.
 void fill_decode_params(DecodeParams& dp, const ifa_params& p, const KernelChoice& kc, const void* query,
                         const void* attenMask, const int32_t* blockTable, const void* antiquantScale,

@@ -204,6 +204,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
             prefetch_tensormap(&p.tmV);
             prefetch_tensormap(&p.tmKt);
             prefetch_tensormap(&p.tmVt);
+            if (p.mask_tma) prefetch_tensormap(&p.tmM);
         }
         const uint64_t pol = policy_evict_first();
         const int br = p.box_rows;
@@ -272,6 +273,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                 }
                 for (int k = 0; k < nbox; ++k)
                     if (!((badmask >> ((k * rows_per) / br)) & 1)) bytes += box_bytes;
+                if (p.mask_tma) bytes += (uint32_t)(T + 16);
                 if (badmask) record_error(p, kErrBadBlock);
                 info[stage] = badmask;
                 mbar_arrive_expect_tx(&full[stage], bytes);
@@ -283,6 +285,11 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                         bulk_g2s(qdst + row * C::QROW, qsrc + (long long)row * p.D * 2, (uint32_t)p.D * 2u, &full[stage]);
                 }
                 const int st = bd[b];
+                if (p.mask_tma) {
+                    // this tile's mask bytes, from the 16-byte boundary at or below its first position
+                    const int x0 = st + cur.i * T;
+                    tma_load_2d(sb + C::MASK_OFF, &p.tmM, &full[stage], x0 & ~15, p.mask_bstride ? b : 0);
+                }
                 const CUtensorMap* mk = tail ? &p.tmKt : &p.tmK;
                 const CUtensorMap* mv = tail ? &p.tmVt : &p.tmV;
                 for (int k = 0; k < nbox; ++k) {
@@ -329,14 +336,15 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
 
     TileCursor cur;
     cursor_init<T>(cur, bd, B, lo);
-    uint32_t mask_next = p.has_mask ? load_mask_bits<NT, T>(p, cur, bd, row0, r, q4) : 0u;
+    const bool mask_regs = p.has_mask && !p.mask_tma;  // masks without staging: loaded one tile ahead
+    uint32_t mask_next = mask_regs ? load_mask_bits<NT, T>(p, cur, bd, row0, r, q4) : 0u;
     long long it = 0;
     for (long long g = lo; g < hi; ++g, ++it) {
         const TileCursor tc = cur;
-        const uint32_t mbits = mask_next;
+        uint32_t mbits = mask_next;
         if (g + 1 < hi) {
             cursor_next<T>(cur, bd, B, RS);
-            if (p.has_mask) mask_next = load_mask_bits<NT, T>(p, cur, bd, row0, r, q4);  // one tile ahead
+            if (mask_regs) mask_next = load_mask_bits<NT, T>(p, cur, bd, row0, r, q4);  // one tile ahead
         }
         const int stage = (int)(it % C::STAGES);
         const uint32_t round = (uint32_t)(it / C::STAGES);
@@ -407,6 +415,14 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
 
         const int valid = min(T, len - i * T);
         const int badmask = info[stage];
+        if (p.mask_tma) {
+            const uint8_t* ms = sb + C::MASK_OFF + ((bd[b] + i * T) & 15);
+            const int tl = row0 + r, th = row0 + r + 8;
+            const uint32_t pat = ((tl < valid && ms[tl]) ? 0x3u : 0u) | ((th < valid && ms[th]) ? 0xCu : 0u);
+            mbits = 0;
+#pragma unroll
+            for (int j = 0; j < NT; ++j) mbits |= pat << (4 * j);
+        }
         // Rows past the window end (or in a skipped block) may hold anything, NaN
         // included: clear this warp's invalid value rows so 0 * garbage stays 0.
         if constexpr (KV != KV_I8) {

@@ -24,6 +24,7 @@ struct ifa_plan {
     unsigned int gen;
     const void* last_k;
     const void* last_v;
+    const void* last_mask;
     DecodeParams* dp;
     int64_t last_launches;
     std::vector<int32_t> bdata;
@@ -76,7 +77,7 @@ extern "C" ifa_status ifa_create(const ifa_params* params, ifa_plan** plan, size
         delete pl;
         return IFA_ERR_RUNTIME;
     }
-    pl->last_k = pl->last_v = nullptr;
+    pl->last_k = pl->last_v = pl->last_mask = nullptr;
     pl->last_launches = 0;
     pl->gen = 0;
     *plan = pl;
@@ -143,6 +144,11 @@ extern "C" ifa_status ifa_run(ifa_plan* pl, const void* query, const void* key, 
         if (!encode_kv_maps(p, pl->kc, key, value, dp)) return IFA_ERR_RUNTIME;
         pl->last_k = key;
         pl->last_v = value;
+    }
+    if (attenMask != pl->last_mask || !p.has_mask) {
+        pl->last_mask = nullptr;
+        if (!encode_mask_map(p, pl->kc, attenMask, dp)) return IFA_ERR_RUNTIME;
+        pl->last_mask = attenMask;
     }
     fill_decode_params(dp, p, pl->kc, query, attenMask, blockTable, antiquantScale, antiquantOffset, attentionOut, W,
                        P);

@@ -95,7 +95,7 @@ extern "C" ifa_status ifa_run_noalloc(const ifa_params* params, const void* quer
     st = build_windows(p, kc, actualSeqLengths, kvPaddingSize, n_kv_padding, dp.bdata_inline, &W, &max_seq_tiles);
     if (st != IFA_OK) return st;
     const int P = choose_grid(p, W, max_seq_tiles, P_max);
-    if (!encode_kv_maps(p, kc, key, value, dp)) return IFA_ERR_RUNTIME;
+    if (!encode_kv_maps(p, kc, key, value, dp) || !encode_mask_map(p, kc, attenMask, dp)) return IFA_ERR_RUNTIME;
     fill_decode_params(dp, p, kc, query, attenMask, blockTable, antiquantScale, antiquantOffset, attentionOut, W, P);
     dp.partials = reinterpret_cast<float*>(scratch + kPartialOffset);
     dp.counters = reinterpret_cast<unsigned long long*>(scratch + kCounterOffset);

@@ -197,3 +197,18 @@ def test_bad_block_table_entry_sets_error_flag():
     ref = oracle_ifa(case)  # the oracle leaves the same tokens out
     assert max_abs_err(out, ref) <= TOL["bf16"]
     assert op.device_errors() == 0  # cleared by the previous read
+
+
+@pytest.mark.parametrize("left_pad", [False, True])
+def test_mask_staged_by_the_producer(left_pad):
+    """Per-batch masks whose row length is a multiple of 16 bytes are staged per tile by
+    TMA; windows then start anywhere (left padding), not only on 16-byte boundaries."""
+    rng = np.random.default_rng(31)
+    case = gen.gqa_padded(31, B=5, N=16, KV_N=4, D=128, Smax=640, layout="BNSD", dtype="fp16", mask=False)
+    case.atten_mask = rng.random((5, 1, 1, 640)) < 0.3
+    if left_pad:
+        case.actual_seq_lengths = np.array([100, 333, 640, 17, 500], dtype=np.int64)
+        case.kv_padding_size = np.array([3, 300, 0, 611, 77], dtype=np.int64)
+    check(case)
+    case.atten_mask = case.atten_mask[:1]  # (1,1,1,S): one row for every batch
+    check(case)
