@@ -13,6 +13,7 @@ constexpr int kWarpTokens = 16;      // tokens of a stage owned by one consumer 
 constexpr int kInlineB = 256;        // per-batch windows travel in the launch parameters up to this B
 constexpr int kMaxCtas = 256;        // upper bound on the grid
 constexpr int kMinPieceTiles = 4;    // do not cut sequences into pieces shorter than this (tiles)
+constexpr int kPieceCostBytes = 96 * 1024;  // fixed work of a sequence piece, in key/value bytes
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded spin-waits: 2 s
 
 // Device error word bits (OR-ed into the error word).
@@ -38,7 +39,7 @@ struct alignas(128) DecodeParams {
     const void* aq_scale;
     const void* aq_offset;
     float* partials;           // 2 slots per CTA
-    unsigned long long* counters;  // arrival counters, one per CTA: (generation << 32) | arrivals
+    unsigned int* counters;    // arrival counters [2][kMaxCtas]; a call uses set gen & 1
     int* err;
     const int32_t* ext_bdata;  // per-batch windows in global memory when B > kInlineB
     long long W;               // total tiles
@@ -53,8 +54,9 @@ struct alignas(128) DecodeParams {
     int aq_per_channel;
     float scale_log2;          // scaleValue * log2(e)
     int slot_floats;
-    unsigned int gen;          // nonzero tag of this call for the arrival counters
+    unsigned int gen;          // call number: picks the counter set, and the set the call clears
     int bdata_inline[3 * kInlineB + 1];
+    int bounds[kMaxCtas + 1];  // CTA c takes the tiles [bounds[c], bounds[c+1]), strictly increasing
 };
 
 __host__ __device__ constexpr int round_up_c(int x, int m) { return (x + m - 1) / m * m; }
@@ -76,11 +78,19 @@ struct DecodeCfg {
     static constexpr int MASK_OFF = 2 * KT_BYTES + Q_BYTES;    // within a stage
     static constexpr int STAGE_BYTES = round_up_c(2 * KT_BYTES + Q_BYTES + MASK_BYTES, 1024);
     static constexpr int MW = NWC < 4 ? NWC : 4;               // warps the merge buffer holds at once
-    static constexpr int MERGE_BYTES = MW * GT_PAD * (DPAD + 2) * 4;
+    static constexpr int FRAG4 = (DPAD / 16) * NT;             // float4 accumulator groups per lane
+    // merge buffer: MW warps' accumulator fragments, lane-contiguous float4; also holds the
+    // (M, L) of up to kMaxCtas pieces when the last piece merges a sequence
+    static constexpr int MERGE_BYTES = MW * FRAG4 * 32 * 16 > 2 * kMaxCtas * GT_PAD * 4 ? MW * FRAG4 * 32 * 16
+                                                                                          : 2 * kMaxCtas * GT_PAD * 4;
+    static constexpr int ML_BYTES = 2 * NWC * GT_PAD * 4;      // per-warp running max and sum of each head
+    static constexpr int BD_BYTES = round_up_c((3 * kInlineB + 1 + kMaxCtas + 1) * 4, 128);  // windows, bounds
+    static constexpr int INFO_BYTES = 8 * 32;                  // TileInfo of each stage
     static constexpr int BAR_BYTES = 256;
+    static constexpr int AUX_BYTES = MERGE_BYTES + ML_BYTES + BD_BYTES + INFO_BYTES + BAR_BYTES;
     static constexpr int BUDGET = 225 * 1024;
-    static constexpr int STAGES = clamp_c((BUDGET - MERGE_BYTES - 1024 - BAR_BYTES) / STAGE_BYTES, 2, 8);
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + MERGE_BYTES + BAR_BYTES;
+    static constexpr int STAGES = clamp_c((BUDGET - AUX_BYTES - 1024) / STAGE_BYTES, 2, 8);
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + AUX_BYTES;
     static constexpr int SLOT_FLOATS = GT_PAD * DPAD + 2 * GT_PAD;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(T % 32 == 0, "tiles are whole 32-row sub-boxes");
@@ -98,6 +108,7 @@ struct KernelChoice {
     int T;          // tokens per tile
     int box_rows;   // rows per TMA box of a full tile (a whole tile, or one cache block)
     int tail_rows;  // rows per TMA box of a window's last, partial tile
+    int piece_cost; // fixed work of a sequence piece, in tiles (weights the CTA split)
     int slot_floats, smem, threads;
     DecodeLaunchFn launch;
 };
@@ -108,6 +119,8 @@ ifa_status choose_kernel(const ifa_params& p, KernelChoice* kc);
 ifa_status build_windows(const ifa_params& p, const KernelChoice& kc, const int64_t* lens, const int64_t* pads,
                          int64_t n_pads, int32_t* bd, int64_t* W, int* max_seq_tiles);
 int choose_grid(const ifa_params& p, int64_t W, int max_seq_tiles, int P_max);
+// Tile ranges of the P CTAs (bounds[0..P]), from the windows build_windows wrote.
+void build_bounds(const ifa_params& p, const KernelChoice& kc, const int32_t* bd, int64_t W, int P, int32_t* bounds);
 // Checks of the per-call pointers shared by both run entry points.
 ifa_status check_run_pointers(const ifa_params& p, const void* query, const void* key, const void* value,
                               const void* attenMask, const int64_t* actualSeqLengths, const int64_t* kvPaddingSize,

@@ -3,19 +3,26 @@
 // sequences (stream-K style: variable lengths are balanced to +-1 tile).
 //
 // Warp NWC is the producer: TMA loads (128-byte swizzle, L2 evict-first) of
-// the key and value tiles in 32-row sub-boxes (sub-boxes past the window end
-// are not fetched), per-row bulk copies of the query rows at each sequence
-// piece start, block-table prefetch for the next tiles, bounded waits.
+// the key and value tiles (whole-tile boxes, or one box per cache block when
+// paged; a window's last tile in 32-row boxes that stop past the window end),
+// per-row bulk copies of the query rows at each sequence piece start, the
+// tile's mask bytes when the mask is per batch, block-table prefetch for the
+// next tiles, and a TileInfo record per stage that tells the consumers which
+// tile they hold.  Every wait is bounded.
 // Warps 0..NWC-1 each own 16 tokens of every stage and run
 //   S^T = K . Q^T      mma.sync m16n8k16, tokens on M, query heads on N
 //   mask, online softmax in the exp2 domain (fp32), rescale skipped while the
 //   running maxima do not move
 //   O^T += V^T . P^T   ldmatrix.trans for V^T, movmatrix for P^T
-// A sequence piece that starts and ends inside the CTA is normalised and
-// written to the output.  A piece cut by a CTA boundary writes (O, m, l) to
-// the CTA's partial slot and bumps the sequence's arrival counter; the CTA
+// At the end of a sequence piece the warps exchange (m, l) and their
+// accumulator fragments through shared memory as lane-contiguous float4
+// (no bank conflicts) and sum the fragments normalised by the piece's L.  A
+// piece that starts and ends inside the CTA is written to the output.  A
+// piece cut by a CTA boundary writes its normalised O with (M, L) per head to
+// the CTA's partial slot and bumps the sequence's arrival counter; the piece
 // that arrives last merges all pieces in piece order (deterministic, no float
-// atomics) and resets the counter, so one launch finishes the call.
+// atomics), so one launch finishes the call.  Counters come in two sets: a
+// call counts in set gen & 1 and clears the other set for the next call.
 //
 // int8 key/value (antiquant): the per-channel key scale is folded into the
 // query (q'[d] = q[d] * scale_K[d]) and the key offset is dropped, because it
@@ -34,15 +41,26 @@ namespace ifa {
 struct TileCursor {
     int b;      // batch
     int r;      // sequence within the batch: kv_head * NGS + slice
+    int h, gs;  // kv head and query-head slice of r
     int i;      // tile within the sequence
     int tiles;  // tiles of each sequence of batch b
 };
+
+// What the producer tells the consumer warps about the tile in a stage.
+struct TileInfo {
+    int b, h, gs, i;  // batch, kv head, query-head slice, tile within the sequence
+    int tiles;        // tiles of the sequence
+    int valid;        // rows of the tile inside the window
+    int badmask;      // full-tile boxes skipped for an out-of-range block id
+    int mask_shift;   // first mask byte of the tile within the staged mask bytes
+};
+static_assert(sizeof(TileInfo) == 32, "two int4 per stage");
 
 template <int T>
 __device__ __forceinline__ int tiles_of(int len) { return (len + T - 1) / T; }
 
 template <int T>
-__device__ __forceinline__ void cursor_init(TileCursor& c, const int* bd, int B, long long g) {
+__device__ __forceinline__ void cursor_init(TileCursor& c, const int* bd, int B, int NGS, long long g) {
     const int* pre = bd + 2 * B;
     int lo = 0, hi = B;  // invariant: pre[lo] <= g < pre[hi] (pre[B] = W > g)
     while (hi - lo > 1) {
@@ -55,23 +73,35 @@ __device__ __forceinline__ void cursor_init(TileCursor& c, const int* bd, int B,
     const long long off = g - pre[lo];
     c.r = (int)(off / c.tiles);
     c.i = (int)(off % c.tiles);
+    c.h = c.r / NGS;
+    c.gs = c.r - c.h * NGS;
 }
 
 template <int T>
-__device__ __forceinline__ void cursor_next(TileCursor& c, const int* bd, int B, int RS) {
+__device__ __forceinline__ void cursor_next(TileCursor& c, const int* bd, int B, int RS, int NGS) {
     if (++c.i < c.tiles) return;
     c.i = 0;
+    if (++c.gs == NGS) {
+        c.gs = 0;
+        ++c.h;
+    }
     if (++c.r < RS) return;
-    c.r = 0;
+    c.r = c.h = c.gs = 0;
     do {
         ++c.b;
     } while (c.b < B && bd[B + c.b] == 0);
     c.tiles = c.b < B ? tiles_of<T>(bd[B + c.b]) : 1;
 }
 
-// CTA whose tile range [floor(c W / P), floor((c+1) W / P)) holds global tile t.
-__device__ __forceinline__ int cta_of(long long t, long long W, int P) {
-    return (int)(((t + 1) * (long long)P - 1) / W);
+// CTA whose tile range [bounds[c], bounds[c+1]) holds global tile t (bounds strictly increasing).
+__device__ __forceinline__ int cta_of(long long t, const int* bounds, int P) {
+    int lo = 0, hi = P;  // invariant: bounds[lo] <= t < bounds[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if ((long long)bounds[mid] <= t) lo = mid;
+        else hi = mid;
+    }
+    return lo;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -111,7 +141,7 @@ __device__ __forceinline__ uint32_t load_mask_bits(const DecodeParams& p, const 
     const int B = p.B;
     const int len = bd[B + c.b];
     const int valid = min(T, len - c.i * T);
-    const int h = c.r / p.NGS, gs = c.r % p.NGS;
+    const int h = c.h, gs = c.gs;
     const int GTv = min(p.GT, p.G - gs * p.GT);
     const uint8_t* base = p.mask + (long long)c.b * p.mask_bstride + (long long)bd[c.b] + (long long)c.i * T;
     const int tl = row0 + r, th = row0 + r + 8;
@@ -149,28 +179,47 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     constexpr int KSTEPS = DPAD / 16;
     constexpr int MT = DPAD / 16;
     constexpr int MW = C::MW;
-    static_assert(C::MERGE_BYTES >= (kMaxCtas + 1) * C::GT_PAD * 4, "merge buffer holds the piece factors");
+    constexpr int FRAG4 = C::FRAG4;
+    constexpr int GT_PAD = C::GT_PAD;
+    constexpr int NPOS = (FRAG4 * 32 + CONSUMERS - 1) / CONSUMERS;  // fragment positions a thread combines
+    constexpr int DSTEP = (KV == KV_I8) ? 1 : 8;  // channel distance between the two halves of a fragment
+    static_assert(C::BAR_BYTES >= 16 * C::STAGES + 48, "barrier area");
+    static_assert(C::STAGES * 32 <= C::INFO_BYTES, "tile info area");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
-    float* mrg_o = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES);
-    float* mrg_m = mrg_o + MW * C::GT_PAD * DPAD;
-    float* mrg_l = mrg_m + MW * C::GT_PAD;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::MERGE_BYTES);
+    uint8_t* aux = smem + C::STAGES * C::STAGE_BYTES;
+    float4* mrg = reinterpret_cast<float4*>(aux);  // [MW][FRAG4][32 lanes] accumulator fragments
+    float* mlm = reinterpret_cast<float*>(aux + C::MERGE_BYTES);  // [NWC][GT_PAD] running max of each warp
+    float* mll = mlm + NWC * GT_PAD;                               // [NWC][GT_PAD] row sums of each warp
+    int* sbd = reinterpret_cast<int*>(aux + C::MERGE_BYTES + C::ML_BYTES);  // window table copy
+    int4* tinfo = reinterpret_cast<int4*>(aux + C::MERGE_BYTES + C::ML_BYTES + C::BD_BYTES);  // TileInfo per stage
+    uint64_t* full = reinterpret_cast<uint64_t*>(aux + C::MERGE_BYTES + C::ML_BYTES + C::BD_BYTES + C::INFO_BYTES);
     uint64_t* empty = full + C::STAGES;
-    int* info = reinterpret_cast<int*>(empty + C::STAGES);
-    volatile int* abort_flag = info + C::STAGES;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::STAGES);
     volatile int* last_flag = abort_flag + 1;
     volatile int* blkbuf = last_flag + 1;  // [8] block ids of the current tile's full boxes (producer)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int* bd = p.ext_bdata ? p.ext_bdata : p.bdata_inline;
     const int B = p.B;
     const int RS = p.KV_N * p.NGS;
-    const long long lo = (long long)blockIdx.x * p.W / p.P;
-    const long long hi = (long long)(blockIdx.x + 1) * p.W / p.P;
+    const long long lo = p.bounds[blockIdx.x];
+    const long long hi = p.bounds[blockIdx.x + 1];
+    // The window table is read every tile: keep it in shared memory when it came inline.
+    const int* bd = p.ext_bdata ? p.ext_bdata : sbd;
+    if (!p.ext_bdata)
+        for (int x = threadIdx.x; x < 3 * B + 1; x += C::THREADS) sbd[x] = p.bdata_inline[x];
+    int* sbounds = sbd + 3 * kInlineB + 1;
+    for (int x = threadIdx.x; x <= p.P; x += C::THREADS) sbounds[x] = p.bounds[x];
+    // The next call counts its arrivals in the other counter set: clear that set now
+    // (entry c by CTA c mod P), so no call depends on how an earlier one ended.
+    {
+        unsigned int* next_set = p.counters + ((p.gen + 1u) & 1u) * kMaxCtas;
+        for (long long c = blockIdx.x + (long long)threadIdx.x * p.P; c < kMaxCtas; c += (long long)C::THREADS * p.P)
+            next_set[c] = 0u;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -212,7 +261,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         const int nsub = T / br;  // full boxes per tile: 1..8
         const int batch_tiles = 32 / nsub;
         TileCursor cur;
-        cursor_init<T>(cur, bd, B, lo);
+        cursor_init<T>(cur, bd, B, p.NGS, lo);
         int my_blk = 0;
         long long it = 0;
         for (long long g = lo; g < hi; ++g, ++it) {
@@ -223,7 +272,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                 const int adv = lane / nsub;
                 const bool live = (g + adv) < hi;
                 if (live)
-                    for (int a = 0; a < adv; ++a) cursor_next<T>(c2, bd, B, RS);
+                    for (int a = 0; a < adv; ++a) cursor_next<T>(c2, bd, B, RS, p.NGS);
                 my_blk = -2;
                 if (live) {
                     const int t0 = c2.i * T + (lane % nsub) * br;
@@ -242,8 +291,8 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
             __syncwarp();
             if (*abort_flag) break;
             const int b = cur.b;
-            const int h = cur.r / p.NGS;
-            const int gs = cur.r % p.NGS;
+            const int h = cur.h;
+            const int gs = cur.gs;
             const int valid = min(T, bd[B + b] - cur.i * T);
             uint8_t* sb = stages + stage * C::STAGE_BYTES;
             if (p.paged) {
@@ -275,7 +324,9 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                     if (!((badmask >> ((k * rows_per) / br)) & 1)) bytes += box_bytes;
                 if (p.mask_tma) bytes += (uint32_t)(T + 16);
                 if (badmask) record_error(p, kErrBadBlock);
-                info[stage] = badmask;
+                const int st = bd[b];
+                tinfo[2 * stage] = make_int4(b, h, gs, cur.i);
+                tinfo[2 * stage + 1] = make_int4(cur.tiles, valid, badmask, (st + cur.i * T) & 15);
                 mbar_arrive_expect_tx(&full[stage], bytes);
                 if (first) {
                     const char* qsrc = reinterpret_cast<const char*>(p.q) +
@@ -284,7 +335,6 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                     for (int row = 0; row < rows; ++row)
                         bulk_g2s(qdst + row * C::QROW, qsrc + (long long)row * p.D * 2, (uint32_t)p.D * 2u, &full[stage]);
                 }
-                const int st = bd[b];
                 if (p.mask_tma) {
                     // this tile's mask bytes, from the 16-byte boundary at or below its first position
                     const int x0 = st + cur.i * T;
@@ -313,7 +363,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                 }
             }
             __syncwarp();
-            cursor_next<T>(cur, bd, B, RS);
+            cursor_next<T>(cur, bd, B, RS, p.NGS);
         }
         // On abort, let every issued copy land before the CTA's shared memory is released.
         if (*abort_flag && lane == 0) {
@@ -334,17 +384,20 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     float acc[MT][NT][4];
     float m_run[NT][2], l_run[NT][2];
 
-    TileCursor cur;
-    cursor_init<T>(cur, bd, B, lo);
-    const bool mask_regs = p.has_mask && !p.mask_tma;  // masks without staging: loaded one tile ahead
-    uint32_t mask_next = mask_regs ? load_mask_bits<NT, T>(p, cur, bd, row0, r, q4) : 0u;
+    // Masks the producer does not stage are read by the consumers, one tile ahead.
+    const bool mask_regs = p.has_mask && !p.mask_tma;
+    TileCursor mcur;
+    uint32_t mask_next = 0;
+    if (mask_regs) {
+        cursor_init<T>(mcur, bd, B, p.NGS, lo);
+        mask_next = load_mask_bits<NT, T>(p, mcur, bd, row0, r, q4);
+    }
     long long it = 0;
     for (long long g = lo; g < hi; ++g, ++it) {
-        const TileCursor tc = cur;
         uint32_t mbits = mask_next;
-        if (g + 1 < hi) {
-            cursor_next<T>(cur, bd, B, RS);
-            if (mask_regs) mask_next = load_mask_bits<NT, T>(p, cur, bd, row0, r, q4);  // one tile ahead
+        if (mask_regs && g + 1 < hi) {
+            cursor_next<T>(mcur, bd, B, RS, p.NGS);
+            mask_next = load_mask_bits<NT, T>(p, mcur, bd, row0, r, q4);
         }
         const int stage = (int)(it % C::STAGES);
         const uint32_t round = (uint32_t)(it / C::STAGES);
@@ -355,13 +408,12 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         __syncwarp();
         if (*abort_flag) break;
 
-        const int b = tc.b;
-        const int h = tc.r / p.NGS;
-        const int gs = tc.r % p.NGS;
-        const int i = tc.i;
-        const int len = bd[B + b];
+        const int4 ia = tinfo[2 * stage];
+        const int4 ib = tinfo[2 * stage + 1];
+        const int b = ia.x, h = ia.y, gs = ia.z, i = ia.w;
+        const int tiles = ib.x, valid = ib.y, badmask = ib.z;
         const bool first = (i == 0) || (g == lo);
-        const bool last = (i == tc.tiles - 1) || (g == hi - 1);
+        const bool last = (i == tiles - 1) || (g == hi - 1);
         const int GTv = min(p.GT, p.G - gs * p.GT);
         uint8_t* sb = stages + stage * C::STAGE_BYTES;
         const uint32_t kbase = smem_u32(sb);
@@ -413,10 +465,8 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
             }
         }
 
-        const int valid = min(T, len - i * T);
-        const int badmask = info[stage];
         if (p.mask_tma) {
-            const uint8_t* ms = sb + C::MASK_OFF + ((bd[b] + i * T) & 15);
+            const uint8_t* ms = sb + C::MASK_OFF + ib.w;
             const int tl = row0 + r, th = row0 + r + 8;
             const uint32_t pat = ((tl < valid && ms[tl]) ? 0x3u : 0u) | ((th < valid && ms[th]) ? 0xCu : 0u);
             mbits = 0;
@@ -487,8 +537,11 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
 
         // ---------------------------------------------------------- mask, online softmax
         const int t_lo = row0 + r, t_hi = row0 + r + 8;
-        const bool ok_lo = t_lo < valid && !((badmask >> (t_lo / p.box_rows)) & 1);
-        const bool ok_hi = t_hi < valid && !((badmask >> (t_hi / p.box_rows)) & 1);
+        bool ok_lo = t_lo < valid, ok_hi = t_hi < valid;
+        if (badmask) {
+            ok_lo = ok_lo && !((badmask >> (t_lo / p.box_rows)) & 1);
+            ok_hi = ok_hi && !((badmask >> (t_hi / p.box_rows)) & 1);
+        }
         uint32_t pb[NT][2];
         float x[NT][4];
         bool moved = false;
@@ -583,6 +636,56 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
 
         if (!last) continue;
         // ============================================================ piece epilogue
+        // Accumulator element e of (md, j) in lane (r, q4) is query head gg = 8j + 2q4 + (e & 1)
+        // and channel d = 16md + r + 8(e >> 1) (int8: 16md + 2r + (e >> 1)).  Fragments travel
+        // between warps as lane-contiguous float4 ("position" k = (md * NT + j) * 32 + lane),
+        // and the thread that combines position k sits in lane k % 32, so it owns the same heads.
+        const long long seq_first = g - i;
+        const bool complete = seq_first >= lo && seq_first + tiles <= hi;
+        const long long obase = ((long long)b * p.N + (long long)h * p.G + (long long)gs * p.GT) * p.D;
+
+        // value antiquant factors of the channels this thread writes, loaded ahead of use
+        float vsc[NPOS][2], vof[NPOS][2];
+#pragma unroll
+        for (int n = 0; n < NPOS; ++n)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) vsc[n][hh] = vof[n][hh] = 0.f;
+        if constexpr (KV == KV_I8) {
+#pragma unroll
+            for (int n = 0; n < NPOS; ++n) {
+                const int k = tid + n * CONSUMERS;
+                if (k < FRAG4 * 32) {
+                    const int d0 = 16 * ((k >> 5) / NT) + 2 * ((k & 31) >> 2);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int d = d0 + hh;
+                        if (d < p.D) {
+                            const long long si = p.aq_per_channel ? (long long)(p.KV_N + h) * p.D + d : 1;
+                            vsc[n][hh] = ld_half_as_float(p.aq_scale, si, p.q_bf16);
+                            vof[n][hh] = ld_half_as_float(p.aq_offset, si, p.q_bf16);
+                        }
+                    }
+                }
+            }
+        }
+        // writes one combined fragment position to the output
+        auto put = [&](const float4& o, int k, bool live0, bool live1, int n) {
+            const int gg0 = 8 * ((k >> 5) % NT) + 2 * (k & 3);
+            const int d0 = (KV == KV_I8) ? 16 * ((k >> 5) / NT) + 2 * ((k & 31) >> 2) : 16 * ((k >> 5) / NT) + ((k & 31) >> 2);
+            const float v[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int gg = gg0 + (e & 1);
+                const int d = d0 + (e >> 1) * DSTEP;
+                if (gg < GTv && d < p.D) {
+                    float y = v[e];
+                    if constexpr (KV == KV_I8) y = ((e & 1) ? live1 : live0) ? (y + vof[n][e >> 1]) * vsc[n][e >> 1] : 0.f;
+                    st_out(p.out, obase + (long long)gg * p.D + d, y, p.q_bf16);
+                }
+            }
+        };
+
+        // (1) row sums of this warp; every warp publishes (m, l), warps MW.. their fragments
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -593,171 +696,173 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                 v += __shfl_xor_sync(0xffffffffu, v, 16);
                 l_run[j][u] = v;
             }
-        // publish (m, l, O) of warp w into merge slot `slot`
-        auto publish = [&](int slot) {
-            if (r == 0) {
+        if (r == 0) {
 #pragma unroll
-                for (int j = 0; j < NT; ++j)
+            for (int j = 0; j < NT; ++j)
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int gg = 8 * j + 2 * q4 + u;
-                        mrg_m[slot * C::GT_PAD + gg] = m_run[j][u];
-                        mrg_l[slot * C::GT_PAD + gg] = l_run[j][u];
-                    }
-            }
+                for (int u = 0; u < 2; ++u) {
+                    mlm[warp * GT_PAD + 8 * j + 2 * q4 + u] = m_run[j][u];
+                    mll[warp * GT_PAD + 8 * j + 2 * q4 + u] = l_run[j][u];
+                }
+        }
+        if (warp >= MW) {
 #pragma unroll
             for (int md = 0; md < MT; ++md)
 #pragma unroll
                 for (int j = 0; j < NT; ++j)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int gg = 8 * j + 2 * q4 + (e & 1);
-                        const int d = (KV == KV_I8) ? 16 * md + 2 * r + (e >> 1) : 16 * md + r + 8 * (e >> 1);
-                        mrg_o[(slot * C::GT_PAD + gg) * DPAD + d] = acc[md][j][e];
-                    }
-        };
-        if constexpr (NWC > MW) {
-            // first fold warps MW.. into warps 0..MW-1, in registers
-            if (warp >= MW) publish(warp - MW);
-            named_bar_sync(1, CONSUMERS);
-            if (warp < MW) {
-#pragma unroll
-                for (int j = 0; j < NT; ++j)
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int gg = 8 * j + 2 * q4 + u;
-                        const float mp = mrg_m[warp * C::GT_PAD + gg];
-                        const float lp = mrg_l[warp * C::GT_PAD + gg];
-                        const float M = fmaxf(m_run[j][u], mp);
-                        const float f1 = m_run[j][u] == -INFINITY ? 0.f : ex2(m_run[j][u] - M);
-                        const float f2 = mp == -INFINITY ? 0.f : ex2(mp - M);
-                        l_run[j][u] = l_run[j][u] * f1 + lp * f2;
-                        m_run[j][u] = M;
-#pragma unroll
-                        for (int md = 0; md < MT; ++md)
-#pragma unroll
-                            for (int hh = 0; hh < 2; ++hh) {
-                                const int e = u + 2 * hh;
-                                const int d = (KV == KV_I8) ? 16 * md + 2 * r + hh : 16 * md + r + 8 * hh;
-                                acc[md][j][e] = acc[md][j][e] * f1 + mrg_o[(warp * C::GT_PAD + gg) * DPAD + d] * f2;
-                            }
-                    }
-            }
-            named_bar_sync(1, CONSUMERS);
+                    mrg[((warp - MW) * FRAG4 + md * NT + j) * 32 + lane] =
+                        make_float4(acc[md][j][0], acc[md][j][1], acc[md][j][2], acc[md][j][3]);
         }
-        if (warp < MW) publish(warp);
         named_bar_sync(1, CONSUMERS);
 
-        const long long seq_first = g - i;
-        const bool complete = seq_first >= lo && seq_first + tc.tiles <= hi;
-        const int slot = 2 * (int)blockIdx.x + (seq_first <= lo ? 0 : 1);
-        float* sp = p.partials + (long long)slot * p.slot_floats;
-        const long long obase = ((long long)b * p.N + (long long)h * p.G + (long long)gs * p.GT) * p.D;
-        for (int idx = tid; idx < GTv * p.D; idx += CONSUMERS) {
-            const int gg = idx / p.D;
-            const int d = idx - gg * p.D;
-            float M = -INFINITY;
+        // (2) per head: M = max over warps, L = sum of l ex2(m - M), and the weight
+        //     ex2(m_w - M) / L of each warp w; lane r of a column takes warp r.  Warps
+        //     0..MW-1 then fold in warp w + MW, both sides weighted.
+        float Mh[NT][2], Lh[NT][2], fs[NT][2], fo[NT][2];
 #pragma unroll
-            for (int w = 0; w < MW; ++w) M = fmaxf(M, mrg_m[w * C::GT_PAD + gg]);
-            float L = 0.f, O = 0.f;
-            if (M != -INFINITY) {
+        for (int j = 0; j < NT; ++j)
 #pragma unroll
-                for (int w = 0; w < MW; ++w) {
-                    const float f = ex2(mrg_m[w * C::GT_PAD + gg] - M);
-                    L += mrg_l[w * C::GT_PAD + gg] * f;
-                    O += mrg_o[(w * C::GT_PAD + gg) * DPAD + d] * f;
-                }
+            for (int u = 0; u < 2; ++u) {
+                const int gg = 8 * j + 2 * q4 + u;
+                const int wr = r % NWC;
+                const float mw = mlm[wr * GT_PAD + gg];
+                float M = mw;
+                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 8));
+                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
+                const float e = mw == -INFINITY ? 0.f : ex2(mw - M);
+                float L = r < NWC ? mll[wr * GT_PAD + gg] * e : 0.f;
+                L += __shfl_xor_sync(0xffffffffu, L, 4);
+                L += __shfl_xor_sync(0xffffffffu, L, 8);
+                L += __shfl_xor_sync(0xffffffffu, L, 16);
+                const float wgt = L > 0.f ? e / L : 0.f;
+                Mh[j][u] = M;
+                Lh[j][u] = L;
+                fs[j][u] = __shfl_sync(0xffffffffu, wgt, ((warp % NWC) << 2) | q4);
+                fo[j][u] = __shfl_sync(0xffffffffu, wgt, (((warp + MW) % NWC) << 2) | q4);
             }
-            if (complete) {
-                float v = 0.f;
-                if (L > 0.f) {
-                    v = O / L;
-                    if constexpr (KV == KV_I8) {
-                        const long long si = p.aq_per_channel ? (long long)(p.KV_N + h) * p.D + d : 1;
-                        v = (v + ld_half_as_float(p.aq_offset, si, p.q_bf16)) * ld_half_as_float(p.aq_scale, si, p.q_bf16);
+        if (warp < MW) {
+#pragma unroll
+            for (int md = 0; md < MT; ++md)
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    float4* slot = mrg + (warp * FRAG4 + md * NT + j) * 32 + lane;
+                    if constexpr (NWC > MW) {
+                        const float4 o = *slot;
+                        *slot = make_float4(acc[md][j][0] * fs[j][0] + o.x * fo[j][0], acc[md][j][1] * fs[j][1] + o.y * fo[j][1],
+                                            acc[md][j][2] * fs[j][0] + o.z * fo[j][0], acc[md][j][3] * fs[j][1] + o.w * fo[j][1]);
+                    } else {
+                        *slot = make_float4(acc[md][j][0] * fs[j][0], acc[md][j][1] * fs[j][1], acc[md][j][2] * fs[j][0],
+                                            acc[md][j][3] * fs[j][1]);
                     }
                 }
-                st_out(p.out, obase + idx, v, p.q_bf16);
-            } else {
-                sp[gg * DPAD + d] = O;
-                if (d == 0) {
-                    sp[C::GT_PAD * DPAD + gg] = M;
-                    sp[C::GT_PAD * DPAD + C::GT_PAD + gg] = L;
+        }
+        named_bar_sync(1, CONSUMERS);
+
+        // (3) sum the MW normalised fragments: the output of a whole sequence, or this
+        //     piece's partial (normalised O, with M and L per head) for the merge
+        const int slot = 2 * (int)blockIdx.x + (seq_first <= lo ? 0 : 1);
+        float* sp = p.partials + (long long)slot * p.slot_floats;
+#pragma unroll
+        for (int n = 0; n < NPOS; ++n) {
+            const int k = tid + n * CONSUMERS;
+            if (k < FRAG4 * 32) {
+                float4 o = mrg[k];
+#pragma unroll
+                for (int w = 1; w < MW; ++w) {
+                    const float4 v = mrg[w * FRAG4 * 32 + k];
+                    o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w;
+                }
+                if (complete) {
+                    const int j = (k >> 5) % NT;
+                    float l0 = Lh[0][0], l1 = Lh[0][1];
+#pragma unroll
+                    for (int jj = 1; jj < NT; ++jj)
+                        if (j == jj) l0 = Lh[jj][0], l1 = Lh[jj][1];
+                    put(o, k, l0 > 0.f, l1 > 0.f, n);
+                } else {
+                    reinterpret_cast<float4*>(sp)[k] = o;
                 }
             }
         }
         if (!complete) {
-            // Arrive on the sequence's counter; the last piece to arrive merges all pieces.
-            const int c_first = cta_of(seq_first, p.W, p.P);
-            const int c_last = cta_of(seq_first + tc.tiles - 1, p.W, p.P);
-            __threadfence();
+            if (warp == 0 && r == 0) {
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        sp[GT_PAD * DPAD + 8 * j + 2 * q4 + u] = Mh[j][u];
+                        sp[GT_PAD * DPAD + GT_PAD + 8 * j + 2 * q4 + u] = Lh[j][u];
+                    }
+            }
+            // (4) arrive on the sequence's counter; the piece that arrives last merges all pieces
+            const int c_first = cta_of(seq_first, sbounds, p.P);
+            const int c_last = cta_of(seq_first + tiles - 1, sbounds, p.P);
+            const int npieces = c_last - c_first + 1;
             named_bar_sync(1, CONSUMERS);
             if (tid == 0) {
-                // Counter word: (generation << 32) | arrivals.  A word carrying another call's tag
-                // (left by an aborted call) counts as empty, so no call depends on a zeroed start.
-                unsigned long long* ctr = p.counters + c_first;
-                const unsigned long long tag = (unsigned long long)p.gen << 32;
-                unsigned long long cur = atomicAdd(ctr, 0ull);
-                unsigned long long mine = 0;
-                for (int tries = 0; tries < (1 << 16); ++tries) {
-                    const unsigned long long want = ((cur & 0xffffffff00000000ull) == tag) ? cur + 1 : tag + 1;
-                    const unsigned long long prev = atomicCAS(ctr, cur, want);
-                    if (prev == cur) {
-                        mine = want;
-                        break;
-                    }
-                    cur = prev;
-                }
-                if (mine == 0) record_error(p, kErrTimeout);
-                const int is_last = mine != 0 && (int)(mine & 0xffffffffull) == c_last - c_first + 1;
-                if (is_last) *ctr = 0ull;  // every piece has arrived
-                *last_flag = is_last;
+                __threadfence();  // this CTA's partial, ordered before the arrival (cumulative over the barrier)
+                const unsigned int n = atomicAdd(p.counters + (p.gen & 1u) * kMaxCtas + c_first, 1u) + 1u;
+                __threadfence();
+                *last_flag = n == (unsigned int)npieces;
             }
             named_bar_sync(1, CONSUMERS);
             if (*last_flag) {
-                __threadfence();
-                const int npieces = c_last - c_first + 1;
-                const long long lo_first = (long long)c_first * p.W / p.P;
+                const long long lo_first = sbounds[c_first];
                 const int slot0 = 2 * c_first + (seq_first <= lo_first ? 0 : 1);
-                float* fac = mrg_o;                       // [npieces][GT_PAD] merge factors
-                float* live = mrg_o + npieces * C::GT_PAD;  // [GT_PAD]
-                for (int gg = tid; gg < GTv; gg += CONSUMERS) {
-                    float M = -INFINITY;
-                    for (int k = 0; k < npieces; ++k) {
-                        const int sl = k == 0 ? slot0 : 2 * (c_first + k);
-                        M = fmaxf(M, __ldcg(p.partials + (long long)sl * p.slot_floats + C::GT_PAD * DPAD + gg));
-                    }
-                    float L = 0.f;
-                    for (int k = 0; k < npieces; ++k) {
-                        const int sl = k == 0 ? slot0 : 2 * (c_first + k);
-                        const float* pp = p.partials + (long long)sl * p.slot_floats;
-                        const float f = M == -INFINITY ? 0.f : ex2(__ldcg(pp + C::GT_PAD * DPAD + gg) - M);
-                        fac[k * C::GT_PAD + gg] = f;
-                        L += __ldcg(pp + C::GT_PAD * DPAD + C::GT_PAD + gg) * f;
-                    }
-                    const float inv = L > 0.f ? 1.f / L : 0.f;
-                    for (int k = 0; k < npieces; ++k) fac[k * C::GT_PAD + gg] *= inv;
-                    live[gg] = L > 0.f ? 1.f : 0.f;
+                float* pm = reinterpret_cast<float*>(mrg);  // [npieces][GT_PAD] M, then the head's total
+                float* pw = pm + npieces * GT_PAD;            // [npieces][GT_PAD] L, then the piece weights
+                for (int x2 = tid; x2 < npieces * GT_PAD; x2 += CONSUMERS) {
+                    const int k = x2 / GT_PAD, gg = x2 % GT_PAD;
+                    const int sl = k == 0 ? slot0 : 2 * (c_first + k);
+                    const float* pp = p.partials + (long long)sl * p.slot_floats + GT_PAD * DPAD;
+                    pm[x2] = __ldcg(pp + gg);
+                    pw[x2] = __ldcg(pp + GT_PAD + gg);
                 }
                 named_bar_sync(1, CONSUMERS);
-                for (int idx = tid; idx < GTv * p.D; idx += CONSUMERS) {
-                    const int gg = idx / p.D;
-                    const int d = idx - gg * p.D;
-                    float o = 0.f;
+                if (tid < GT_PAD) {
+                    float M = -INFINITY;
+                    for (int k = 0; k < npieces; ++k) M = fmaxf(M, pm[k * GT_PAD + tid]);
+                    float S = 0.f;
                     for (int k = 0; k < npieces; ++k) {
-                        const int sl = k == 0 ? slot0 : 2 * (c_first + k);
-                        o += fac[k * C::GT_PAD + gg] * __ldcg(p.partials + (long long)sl * p.slot_floats + gg * DPAD + d);
+                        const float mk = pm[k * GT_PAD + tid];
+                        const float wk = mk == -INFINITY ? 0.f : pw[k * GT_PAD + tid] * ex2(mk - M);
+                        pw[k * GT_PAD + tid] = wk;
+                        S += wk;
                     }
-                    if constexpr (KV == KV_I8) {
-                        if (live[gg] != 0.f) {
-                            const long long si = p.aq_per_channel ? (long long)(p.KV_N + h) * p.D + d : 1;
-                            o = (o + ld_half_as_float(p.aq_offset, si, p.q_bf16)) *
-                                ld_half_as_float(p.aq_scale, si, p.q_bf16);
-                        } else {
-                            o = 0.f;
+                    const float inv = S > 0.f ? 1.f / S : 0.f;
+                    for (int k = 0; k < npieces; ++k) pw[k * GT_PAD + tid] *= inv;
+                    pm[tid] = S;  // column tid is this thread's alone
+                }
+                named_bar_sync(1, CONSUMERS);
+#pragma unroll
+                for (int n = 0; n < NPOS; ++n) {
+                    const int k = tid + n * CONSUMERS;
+                    if (k < FRAG4 * 32) {
+                        const int gg0 = 8 * ((k >> 5) % NT) + 2 * (k & 3);
+                        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                        int pc = 0;
+                        for (; pc + 4 <= npieces; pc += 4) {
+                            float4 v[4];
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const int sl = pc + t == 0 ? slot0 : 2 * (c_first + pc + t);
+                                v[t] = __ldcg(reinterpret_cast<const float4*>(p.partials + (long long)sl * p.slot_floats) + k);
+                            }
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const float w0 = pw[(pc + t) * GT_PAD + gg0], w1 = pw[(pc + t) * GT_PAD + gg0 + 1];
+                                o.x += w0 * v[t].x; o.y += w1 * v[t].y; o.z += w0 * v[t].z; o.w += w1 * v[t].w;
+                            }
                         }
+                        for (; pc < npieces; ++pc) {
+                            const int sl = pc == 0 ? slot0 : 2 * (c_first + pc);
+                            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.partials + (long long)sl * p.slot_floats) + k);
+                            const float w0 = pw[pc * GT_PAD + gg0], w1 = pw[pc * GT_PAD + gg0 + 1];
+                            o.x += w0 * v.x; o.y += w1 * v.y; o.z += w0 * v.z; o.w += w1 * v.w;
+                        }
+                        put(o, k, pm[gg0] > 0.f, pm[gg0 + 1] > 0.f, n);
                     }
-                    st_out(p.out, obase + idx, o, p.q_bf16);
                 }
             }
         }

@@ -20,7 +20,7 @@ struct ifa_plan {
     KernelChoice kc;
     int num_sms, P_max, device;
     size_t partial_bytes, ws_bytes;
-    int* d_state;  // [0]: device error word; 8-byte words from byte 8 on: arrival counters
+    int* d_state;  // [0]: device error word; from byte 8 on: two sets of kMaxCtas arrival counters
     unsigned int gen;
     const void* last_k;
     const void* last_v;
@@ -64,7 +64,7 @@ extern "C" ifa_status ifa_create(const ifa_params* params, ifa_plan** plan, size
     pl->partial_bytes = align_up((size_t)2 * pl->P_max * kc.slot_floats * sizeof(float), 256);
     pl->ws_bytes = pl->partial_bytes;
     if (params->B > kInlineB) pl->ws_bytes += align_up((size_t)(3 * params->B + 1) * sizeof(int32_t), 256);
-    const size_t state_bytes = 8 + (size_t)kMaxCtas * sizeof(unsigned long long);
+    const size_t state_bytes = 8 + (size_t)2 * kMaxCtas * sizeof(unsigned int);
     if (cudaMalloc(&pl->d_state, state_bytes) != cudaSuccess ||
         cudaMemset(pl->d_state, 0, state_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -152,11 +152,11 @@ extern "C" ifa_status ifa_run(ifa_plan* pl, const void* query, const void* key, 
     }
     fill_decode_params(dp, p, pl->kc, query, attenMask, blockTable, antiquantScale, antiquantOffset, attentionOut, W,
                        P);
+    build_bounds(p, pl->kc, bd.data(), W, P, dp.bounds);
     dp.partials = reinterpret_cast<float*>(workspace);
     dp.err = pl->d_state;
-    dp.counters = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(pl->d_state) + 8);
-    if (++pl->gen == 0) pl->gen = 1;
-    dp.gen = pl->gen;
+    dp.counters = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(pl->d_state) + 8);
+    dp.gen = ++pl->gen;  // wraps: consecutive calls alternate the counter set
     if (B <= kInlineB) {
         std::memcpy(dp.bdata_inline, bd.data(), bd.size() * sizeof(int32_t));
         dp.ext_bdata = nullptr;

@@ -22,12 +22,13 @@ using namespace ifa;
 namespace {
 
 constexpr size_t kScratchBytes = IFA_NOALLOC_SCRATCH_BYTES;
-// Layout of the scratch: [0, 256) device error word; [256, 256 + 8*kMaxCtas) arrival
-// counters, tagged with each call's generation so that whatever an earlier call left
-// there is ignored; from kPartialOffset on, the partial slots.
+// Layout of the scratch: [0, 256) device error word; [256, 256 + 8*kMaxCtas) two sets of
+// arrival counters (a call counts in set gen & 1 and clears the other set for the next
+// call, so whatever an aborted call left behind is gone two calls later); from
+// kPartialOffset on, the partial slots.
 constexpr size_t kCounterOffset = 256;
 constexpr size_t kPartialOffset = 4096;
-static_assert(kCounterOffset + sizeof(unsigned long long) * kMaxCtas <= kPartialOffset, "scratch layout");
+static_assert(kCounterOffset + 2 * sizeof(unsigned int) * kMaxCtas <= kPartialOffset, "scratch layout");
 constexpr int kMaxDevices = 64;
 
 // The scratch every ifa_run_noalloc call on a device shares.  In host code this
@@ -97,12 +98,11 @@ extern "C" ifa_status ifa_run_noalloc(const ifa_params* params, const void* quer
     const int P = choose_grid(p, W, max_seq_tiles, P_max);
     if (!encode_kv_maps(p, kc, key, value, dp) || !encode_mask_map(p, kc, attenMask, dp)) return IFA_ERR_RUNTIME;
     fill_decode_params(dp, p, kc, query, attenMask, blockTable, antiquantScale, antiquantOffset, attentionOut, W, P);
+    build_bounds(p, kc, dp.bdata_inline, W, P, dp.bounds);
     dp.partials = reinterpret_cast<float*>(scratch + kPartialOffset);
-    dp.counters = reinterpret_cast<unsigned long long*>(scratch + kCounterOffset);
+    dp.counters = reinterpret_cast<unsigned int*>(scratch + kCounterOffset);
     static std::atomic<unsigned int> generation{0};
-    unsigned int gen = ++generation;
-    if (gen == 0) gen = ++generation;
-    dp.gen = gen;
+    dp.gen = ++generation;  // wraps: consecutive calls alternate the counter set
     dp.err = deviceErrorFlags ? deviceErrorFlags : reinterpret_cast<int*>(scratch);
     dp.ext_bdata = nullptr;
     if (kc.launch(dp, P, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {

@@ -117,6 +117,8 @@ ifa_status choose_kernel(const ifa_params& p, KernelChoice* kc) {
     kc->box_rows = kc->T;
     if (p.kvFormat != IFA_KV_CONTIG) kc->box_rows = (int)gcd64(kc->T, p.blockSize);
     kc->tail_rows = std::min(kc->box_rows, 32);
+    const int tile_bytes = 2 * kc->T * kc->dpad * kc->es;
+    kc->piece_cost = std::max(1, kPieceCostBytes / tile_bytes);
     return IFA_OK;
 }
 
@@ -164,6 +166,50 @@ int choose_grid(const ifa_params& p, int64_t W, int max_seq_tiles, int P_max) {
     int64_t min_share = p.splitTiles > 0 ? p.splitTiles : std::min<int64_t>(max_seq_tiles, kMinPieceTiles);
     min_share = std::max<int64_t>(min_share, 1);
     return (int)std::max<int64_t>(1, std::min<int64_t>(P_max, (W + min_share - 1) / min_share));
+}
+
+// Without splitTiles, a sequence costs its tiles plus piece_cost tiles of fixed work (the
+// query load and the epilogue), and CTA c starts at the first tile whose cost prefix reaches
+// c * total / P.  A boundary that lands in a sequence's fixed cost moves to that sequence's
+// start, so it does not cut it.  With splitTiles the shares are equal (c W / P).  Every CTA
+// gets at least one tile (P <= W), so the CTAs a sequence spans each hold one of its pieces.
+void build_bounds(const ifa_params& p, const KernelChoice& kc, const int32_t* bd, int64_t W, int P, int32_t* bounds) {
+    const int B = (int)p.B;
+    bounds[0] = 0;
+    bounds[P] = (int32_t)W;
+    if (p.splitTiles > 0 || P == 1) {
+        for (int c = 1; c < P; ++c) bounds[c] = (int32_t)((int64_t)c * W / P);
+        return;
+    }
+    const int64_t RS = (int64_t)kc.KV_N * kc.NGS;
+    const int64_t E = kc.piece_cost;
+    auto tiles_of = [&](int b) { return ((int64_t)bd[B + b] + kc.T - 1) / kc.T; };
+    int64_t total = W;
+    for (int b = 0; b < B; ++b)
+        if (bd[B + b] > 0) total += E * RS;
+    int b = 0;
+    int64_t C0 = 0, G0 = 0;  // cost and tiles of the batches before b
+    for (int c = 1; c < P; ++c) {
+        const int64_t X = (int64_t)c * total / P;
+        while (b < B) {
+            const int64_t t = tiles_of(b);
+            const int64_t cb = t > 0 ? RS * (t + E) : 0;
+            if (C0 + cb > X) break;
+            C0 += cb;
+            G0 += t * RS;
+            ++b;
+        }
+        int64_t g = W;
+        if (b < B) {
+            const int64_t t = tiles_of(b);
+            const int64_t off = X - C0;
+            const int64_t k = off / (t + E), rem = off - k * (t + E);
+            g = G0 + k * t + (rem <= E ? 0 : rem - E);
+        }
+        bounds[c] = (int32_t)g;
+    }
+    for (int c = 1; c < P; ++c) bounds[c] = std::max(bounds[c], bounds[c - 1] + 1);
+    for (int c = P - 1; c >= 1; --c) bounds[c] = std::min(bounds[c], bounds[c + 1] - 1);
 }
 
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
