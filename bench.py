@@ -410,7 +410,7 @@ class SfaWorkload:
         return self.op(self.q, self.qr, k, kr, v, self.idx, self.bt, self.lens, out=self.outs[i], stream=stream)
 
     def launches_per_call(self):
-        return 1
+        return 2  # decode kernel + combine kernel
 
     def host_inputs(self):
         c = self.case

@@ -246,6 +246,8 @@ ifa_status sfa_workspace_size(const sfa_params* params, size_t* workspace_bytes)
  *   sfa_workspace_size bytes; deviceErrorFlags (int32, nullable) receives device error
  *   bits (1: a needed block_table entry outside [0, block_num); 2: a wait timed out).
  * `value` may alias `key`.  Calls that share a workspace must not overlap on the GPU.
+ * The call enqueues two kernels: the decode kernel, and a combine kernel that merges
+ * the pieces of the (batch, value-half) sequences the decode kernel split across CTAs.
  */
 ifa_status sfa_run(const sfa_params* params, const void* query, const void* query_rope, const void* key,
                    const void* key_rope, const void* value, const int32_t* sparse_indices,

@@ -1,5 +1,6 @@
 // Sparse-index MLA-absorb decode ("SparseFlashAttention" README): launch
-// parameters and fixed sizes of the tcgen05 kernel (sfa_kernel.cu).
+// parameters and fixed sizes of the tcgen05 kernel and its combine kernel
+// (sfa_kernel.cu).
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -18,11 +19,15 @@ constexpr int kSfaVBlocks = 4;      // 64-column blocks of one value half
 constexpr int kSfaStages = 8;       // 8 KB ring stages (64 rows x 128 B)
 constexpr int kSfaStageBytes = kSfaTile * 128;
 constexpr int kSfaQBytes = kSfaQBlocks * 128 * 128;
-constexpr int kSfaThreads = 6 * 32;  // producer, MMA issuer, four softmax warps
-constexpr int kSfaSlotFloats = 128 * kSfaHalf + 2 * 128;  // partial O of one piece + m + l
-constexpr int kSfaSmem = 1024 + kSfaQBytes + kSfaStages * kSfaStageBytes + 512;
-constexpr size_t kSfaPartialOffset = 4096;  // workspace: [0,256) error word, [256, ..) counters, partials
+constexpr int kSfaRSlots = 8;       // resolved tiles the resolver warp may run ahead
+constexpr int kSfaRSlotBytes = 288; // rows[64], valid mask, flag (16-byte aligned)
+constexpr int kSfaThreads = 7 * 32;  // producer, MMA issuer, four softmax warps, resolver
+constexpr int kSfaSlotFloats = 128 * kSfaHalf + 2 * 128;  // normalised O of one piece + M + L
+constexpr int kSfaBarBytes = 512;
+constexpr int kSfaSmem = 1024 + kSfaQBytes + kSfaStages * kSfaStageBytes + kSfaRSlots * kSfaRSlotBytes + kSfaBarBytes;
+constexpr size_t kSfaPartialOffset = 4096;  // workspace: [0,256) error word, partial slots from here
 constexpr float kSfaRescaleSlack = 8.0f;    // log2 units the running max may trail before O is rescaled
+constexpr int kSfaCombineRows = 16;         // query heads per combine CTA
 
 struct alignas(128) SfaParams {
     CUtensorMap tmQ;    // 3-D (d, head, batch) over query, 64 x 128 x 1 boxes
@@ -35,7 +40,6 @@ struct alignas(128) SfaParams {
     const int32_t* lens;
     void* out;
     float* partials;
-    unsigned long long* counters;
     int* err;
     long long W;        // tiles: 2 * B * tiles_per_seq
     int P;
@@ -43,9 +47,9 @@ struct alignas(128) SfaParams {
     int block_size, bt_cols, block_num, total_rows;
     int is_bf16;
     float scale_log2;
-    unsigned int gen;
 };
 
+// Enqueues the decode kernel and the combine kernel (two launches).
 cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream);
 
 }  // namespace ifa

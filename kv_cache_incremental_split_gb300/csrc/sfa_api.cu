@@ -6,7 +6,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -138,16 +137,12 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
     const long long min_share = std::max(1, std::min(tps, kMinPieceTiles));
     const int P = (int)std::max<long long>(1, std::min<long long>(P_max, (W + min_share - 1) / min_share));
 
-    static std::atomic<unsigned int> generation{0};
-    unsigned int gen = ++generation;
-    if (gen == 0) gen = ++generation;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     sp.indices = sparse_indices;
     sp.block_table = block_table;
     sp.lens = actual_seq_lengths_kv;
     sp.out = attention_out;
     sp.partials = reinterpret_cast<float*>(ws + kSfaPartialOffset);
-    sp.counters = reinterpret_cast<unsigned long long*>(ws + 256);
     sp.err = deviceErrorFlags ? deviceErrorFlags : reinterpret_cast<int*>(ws);
     sp.W = W;
     sp.P = P;
@@ -161,7 +156,6 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
     sp.total_rows = (int)rows;
     sp.is_bf16 = bf;
     sp.scale_log2 = (float)(p.scale_value * 1.4426950408889634);
-    sp.gen = gen;
     if (launch_sfa(sp, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return IFA_ERR_RUNTIME;
