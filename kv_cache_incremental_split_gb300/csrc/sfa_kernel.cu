@@ -14,14 +14,17 @@
 //
 // Per CTA:
 //  * resolver (warp 6): for each tile, the cache row of every position (index ->
-//    block table, one tile of indices prefetched ahead) and the valid mask, into
-//    a ring of kSfaRSlots resolved tiles.  A tile with no valid position is
-//    skipped by every role below.
-//  * producer (warp 0): Q of batch b (9 column blocks of [q | q_rope], 128 rows,
-//    147 KB, resident while b does not change) by 3-D TMA tiles; per tile, the 64
-//    key rows (9 column blocks incl. rope) and, one tile later, the 64 value rows
-//    of half h (4 blocks) by TMA tile::gather4 into a ring of 8 KB stages.
-//    Invalid positions gather an out-of-range row (zero fill, no memory traffic).
+//    block table, software-pipelined over three tiles) and the valid mask, into a
+//    ring of kSfaRSlots resolved tiles.  A tile with no valid position is skipped
+//    by every role below.
+//  * producer (warp 0) and gatherers (warps 7-9): warp 0 loads Q of batch b (9
+//    column blocks of [q | q_rope], 128 rows, 147 KB, resident while b does not
+//    change) by 3-D TMA tiles; per tile, the 64 key rows (9 column blocks incl.
+//    rope) and, one tile later, the 64 value rows of half h (4 blocks) go by TMA
+//    tile::gather4 into a ring of 8 KB stages.  The four warps take four of each
+//    stage's 16 groups of 4 rows each (one warp alone cannot issue gathers fast
+//    enough).  Invalid positions gather an out-of-range row (zero fill, no memory
+//    traffic).
 //  * MMA issuer (warp 1): S_n[128 x 64] = Q K_n^T into one of two TMEM score
 //    buffers (36 MMAs, M=128 N=64 K=16), then O += P_{n-1} V_{n-1} with P from
 //    TMEM and V (MN-major) from shared memory, so the scores of tile n are
@@ -46,23 +49,6 @@ __device__ __forceinline__ float ex2f_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// Cache row of index `idx` of batch b, or total_rows when idx is outside [0, len) or
-// its block-table entry is bad (then *bad is set).
-__device__ __forceinline__ int row_of(const SfaParams& p, int b, int idx, int len, bool* bad) {
-    *bad = false;
-    if (idx < 0 || idx >= len) return p.total_rows;
-    if (idx / p.block_size >= p.bt_cols) {  // a length beyond the block table: treated as a bad entry
-        *bad = true;
-        return p.total_rows;
-    }
-    const int blk = __ldg(p.block_table + (long long)b * p.bt_cols + idx / p.block_size);
-    if (blk < 0 || blk >= p.block_num) {
-        *bad = true;
-        return p.total_rows;
-    }
-    return blk * p.block_size + idx % p.block_size;
 }
 
 // CTA whose tile range [floor(c W / P), floor((c+1) W / P)) holds global tile t.
@@ -118,12 +104,12 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSfaStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], kSfaIssuers);
             mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < kSfaRSlots; ++s) {
             mbar_init(&r_full[s], 1);
-            mbar_init(&r_empty[s], 6);  // producer, MMA issuer, four softmax warps
+            mbar_init(&r_empty[s], kSfaIssuers + 5);  // gatherers, MMA issuer, four softmax warps
         }
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
@@ -151,28 +137,57 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
 
     if (warp == 6 && lo < hi) {
         // ================================================================ resolver
+        // Three tiles in flight: the indices of tile g+2, the block-table entries and
+        // length of tile g+1, and the rows of tile g.
         auto load_idx = [&](long long g, int& i_lo, int& i_hi) {
+            i_lo = i_hi = -1;
+            if (g >= hi) return;
             const int seq = (int)(g / tps), t = (int)(g % tps);
             const int b = seq >> 1;
             const int pos = t * kSfaTile + lane;
             const int32_t* row = p.indices + (long long)b * p.S_sp;
-            i_lo = pos < p.S_sp ? __ldg(row + pos) : -1;
-            i_hi = pos + 32 < p.S_sp ? __ldg(row + pos + 32) : -1;
+            if (pos < p.S_sp) i_lo = __ldg(row + pos);
+            if (pos + 32 < p.S_sp) i_hi = __ldg(row + pos + 32);
         };
-        int ilo, ihi;
-        load_idx(lo, ilo, ihi);
+        // block-table entry of index idx (read only when it lies inside the table), -1 otherwise
+        auto load_blk = [&](int b, int idx) -> int {
+            if (idx < 0 || idx / p.block_size >= p.bt_cols) return -1;
+            return __ldg(p.block_table + (long long)b * p.bt_cols + idx / p.block_size);
+        };
+        int i0lo, i0hi, i1lo, i1hi;
+        load_idx(lo, i0lo, i0hi);
+        load_idx(lo + 1, i1lo, i1hi);
+        int b0 = (int)(lo / tps) >> 1;
+        int len0 = __ldg(p.lens + b0);
+        int bt0lo = load_blk(b0, i0lo), bt0hi = load_blk(b0, i0hi);
         long long k = 0;
         for (long long g = lo; g < hi; ++g, ++k) {
-            int nlo = -1, nhi = -1;
-            if (g + 1 < hi) load_idx(g + 1, nlo, nhi);  // one tile of indices ahead
-            const int b = (int)(g / tps) >> 1;
-            const int len = __ldg(p.lens + b);
-            bool bad_lo, bad_hi;
-            const int row_lo = row_of(p, b, ilo, len, &bad_lo);
-            const int row_hi = row_of(p, b, ihi, len, &bad_hi);
-            if (__any_sync(0xffffffffu, bad_lo || bad_hi) && lane == 0) atomicOr(p.err, kErrBadBlock);
-            const uint32_t m_lo = __ballot_sync(0xffffffffu, row_lo != p.total_rows);
-            const uint32_t m_hi = __ballot_sync(0xffffffffu, row_hi != p.total_rows);
+            int i2lo, i2hi;
+            load_idx(g + 2, i2lo, i2hi);
+            int b1 = 0, len1 = 0, bt1lo = -1, bt1hi = -1;
+            if (g + 1 < hi) {
+                b1 = (int)((g + 1) / tps) >> 1;
+                len1 = __ldg(p.lens + b1);
+                bt1lo = load_blk(b1, i1lo);
+                bt1hi = load_blk(b1, i1hi);
+            }
+            // rows of tile g: invalid (total_rows) outside [0, len); bad block-table entries are flagged
+            int rows2[2];
+            bool bad = false;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int idx = u ? i0hi : i0lo;
+                const int blk = u ? bt0hi : bt0lo;
+                int r = p.total_rows;
+                if (idx >= 0 && idx < len0) {
+                    if (blk < 0 || blk >= p.block_num) bad = true;  // includes a length beyond the block table
+                    else r = blk * p.block_size + idx % p.block_size;
+                }
+                rows2[u] = r;
+            }
+            if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, kErrBadBlock);
+            const uint32_t m_lo = __ballot_sync(0xffffffffu, rows2[0] != p.total_rows);
+            const uint32_t m_hi = __ballot_sync(0xffffffffu, rows2[1] != p.total_rows);
             const int slot = (int)(k % kSfaRSlots);
             const uint32_t round = (uint32_t)(k / kSfaRSlots);
             if (round > 0 && !mbar_wait_bounded(&r_empty[slot], (round - 1) & 1, kWaitLimitNs)) {
@@ -181,8 +196,8 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 break;
             }
             RSlot* rs = slot_of(k);
-            rs->rows[lane] = row_lo;
-            rs->rows[lane + 32] = row_hi;
+            rs->rows[lane] = rows2[0];
+            rs->rows[lane + 32] = rows2[1];
             if (lane == 0) {
                 rs->vmask[0] = m_lo;
                 rs->vmask[1] = m_hi;
@@ -190,13 +205,20 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&r_full[slot]);
-            ilo = nlo;
-            ihi = nhi;
+            i0lo = i1lo;
+            i0hi = i1hi;
+            i1lo = i2lo;
+            i1hi = i2hi;
+            b0 = b1;
+            len0 = len1;
+            bt0lo = bt1lo;
+            bt0hi = bt1hi;
             if (*abort_flag) break;
         }
-    } else if (warp == 0 && lo < hi) {
-        // ================================================================ producer
-        if (lane == 0) {
+    } else if ((warp == 0 || warp >= 7) && lo < hi) {
+        // ================================================================ producer and gatherers
+        const int gi = warp == 0 ? 0 : warp - 6;  // this warp's quarter of each stage's row groups
+        if (lane == 0 && gi == 0) {
             prefetch_tensormap(&p.tmQ);
             prefetch_tensormap(&p.tmQr);
             prefetch_tensormap(&p.tmK);
@@ -210,8 +232,10 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         bool ok = true;
         // Gathers column blocks [blk0, blk0 + nblk) of the rows of resolved tile `rs`
         // (blocks 0..7: key, 8: key rope, 9..12: value half h).
+        constexpr int kGroups = 16 / kSfaIssuers;  // gather4 row groups per warp and stage
         auto gather = [&](const RSlot* rs, int blk0, int nblk, int h) {
-            const int4 r4 = lane < 16 ? reinterpret_cast<const int4*>(rs->rows)[lane] : make_int4(0, 0, 0, 0);
+            const int grp = gi * kGroups + lane;
+            const int4 r4 = lane < kGroups ? reinterpret_cast<const int4*>(rs->rows)[grp] : make_int4(0, 0, 0, 0);
             for (int blk = blk0; blk < blk0 + nblk; ++blk, ++it) {
                 const int stage = (int)(it % kSfaStages);
                 const uint32_t round = (uint32_t)(it / kSfaStages);
@@ -221,9 +245,9 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                     ok = false;
                     return;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(&full[stage], kSfaStageBytes);
+                if (lane == 0) mbar_arrive_expect_tx(&full[stage], kSfaStageBytes / kSfaIssuers);
                 __syncwarp();
-                if (lane < 16) {
+                if (lane < kGroups) {
                     const CUtensorMap* map;
                     int x;
                     if (blk < 8) {
@@ -236,7 +260,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                         map = &p.tmV;
                         x = h * kSfaHalf + (blk - kSfaQBlocks) * 64;
                     }
-                    tma_gather4(ring + stage * kSfaStageBytes + lane * 512, map, &full[stage], x, r4.x, r4.y, r4.z,
+                    tma_gather4(ring + stage * kSfaStageBytes + grp * 512, map, &full[stage], x, r4.x, r4.y, r4.z,
                                 r4.w, pol);
                 }
                 __syncwarp();
@@ -268,7 +292,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 if (lane == 0) mbar_arrive(&r_empty[slot]);
                 continue;
             }
-            if (b != prev_b) {  // new query batch: wait until the MMAs using the old one are done
+            if (b != prev_b && gi == 0) {  // new query batch: wait until the MMAs using the old one are done
                 if (epoch > 0 && !mbar_wait_bounded(q_empty, (epoch - 1) & 1, kWaitLimitNs)) {
                     if (lane == 0) atomicOr(p.err, kErrTimeout);
                     *abort_flag = 1;
@@ -280,8 +304,8 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                     tma_load_3d(sq + 8 * 16384, &p.tmQr, q_full, 0, 0, b);
                 }
                 ++epoch;
-                prev_b = b;
             }
+            prev_b = b;
             gather(rs, 0, kSfaQBlocks, h);
             if (!ok) break;
             flush();
