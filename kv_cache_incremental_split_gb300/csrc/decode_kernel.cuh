@@ -28,7 +28,12 @@
 // query (q'[d] = q[d] * scale_K[d]) and the key offset is dropped, because it
 // adds the same constant to every score of a row; the value scale and offset
 // are applied once to the normalised output: out = scale_V * (o + offset_V).
-// int8 bytes become exact fp16 values with a byte permute and one subtract.
+// int8 bytes become the exact fp16 values x + 1152 with one byte permute, and
+// the bias is never subtracted per element: on the key side it adds
+// 1152 * sum_d q'[d] to every score of a head, which the softmax ignores; on
+// the value side the normalised output comes out as o + 1152 exactly, because
+// the row sums l add up the same fp16-rounded probabilities the P.V MMAs use,
+// so -1152 joins offset_V.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -508,10 +513,10 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                     uint32_t r0, r1, r2, r3;
                     ldsm_x4(addr, r0, r1, r2, r3);
                     r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
-                    const uint32_t a0 = i8x2_to_f16x2(r0, 0x4140), a2 = i8x2_to_f16x2(r0, 0x4342);
-                    const uint32_t a1 = i8x2_to_f16x2(r1, 0x4140), a3 = i8x2_to_f16x2(r1, 0x4342);
-                    const uint32_t c0 = i8x2_to_f16x2(r2, 0x4140), c2 = i8x2_to_f16x2(r2, 0x4342);
-                    const uint32_t c1 = i8x2_to_f16x2(r3, 0x4140), c3 = i8x2_to_f16x2(r3, 0x4342);
+                    const uint32_t a0 = i8x2_to_f16x2_biased(r0, 0x4140), a2 = i8x2_to_f16x2_biased(r0, 0x4342);
+                    const uint32_t a1 = i8x2_to_f16x2_biased(r1, 0x4140), a3 = i8x2_to_f16x2_biased(r1, 0x4342);
+                    const uint32_t c0 = i8x2_to_f16x2_biased(r2, 0x4140), c2 = i8x2_to_f16x2_biased(r2, 0x4342);
+                    const uint32_t c1 = i8x2_to_f16x2_biased(r3, 0x4140), c3 = i8x2_to_f16x2_biased(r3, 0x4342);
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
                         mma_16816<false>(s[j], a0, a1, a2, a3, qf[ks][j][0], qf[ks][j][1]);
@@ -586,10 +591,20 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                 const float m_use = m_run[j][u] == -INFINITY ? 0.f : m_run[j][u];
                 pr[u] = ex2(x[j][u] - m_use);
                 pr[u + 2] = ex2(x[j][u + 2] - m_use);
-                l_run[j][u] += pr[u] + pr[u + 2];
             }
-            pb[j][0] = movmatrix_t(pack2<MMA_BF16>(pr[0], pr[1]));
-            pb[j][1] = movmatrix_t(pack2<MMA_BF16>(pr[2], pr[3]));
+            const uint32_t h0 = pack2<MMA_BF16>(pr[0], pr[1]), h1 = pack2<MMA_BF16>(pr[2], pr[3]);
+            if constexpr (KV == KV_I8) {
+                // row sums of the fp16-rounded probabilities the P.V MMAs see (keeps the value bias exact)
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+                l_run[j][0] += f0.x + f1.x;
+                l_run[j][1] += f0.y + f1.y;
+            } else {
+                l_run[j][0] += pr[0] + pr[2];
+                l_run[j][1] += pr[1] + pr[3];
+            }
+            pb[j][0] = movmatrix_t(h0);
+            pb[j][1] = movmatrix_t(h1);
         }
 
         // ---------------------------------------------------------- O^T += V^T . P^T
@@ -605,10 +620,10 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                     uint32_t r0, r1, r2, r3;
                     ldsm_x4_t(addr, r0, r1, r2, r3);
                     r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
-                    const uint32_t a0 = i8x2_to_f16x2(r0, 0x4240), a1 = i8x2_to_f16x2(r0, 0x4341);
-                    const uint32_t a2 = i8x2_to_f16x2(r1, 0x4240), a3 = i8x2_to_f16x2(r1, 0x4341);
-                    const uint32_t e0 = i8x2_to_f16x2(r2, 0x4240), e1 = i8x2_to_f16x2(r2, 0x4341);
-                    const uint32_t e2 = i8x2_to_f16x2(r3, 0x4240), e3 = i8x2_to_f16x2(r3, 0x4341);
+                    const uint32_t a0 = i8x2_to_f16x2_biased(r0, 0x4240), a1 = i8x2_to_f16x2_biased(r0, 0x4341);
+                    const uint32_t a2 = i8x2_to_f16x2_biased(r1, 0x4240), a3 = i8x2_to_f16x2_biased(r1, 0x4341);
+                    const uint32_t e0 = i8x2_to_f16x2_biased(r2, 0x4240), e1 = i8x2_to_f16x2_biased(r2, 0x4341);
+                    const uint32_t e2 = i8x2_to_f16x2_biased(r3, 0x4240), e3 = i8x2_to_f16x2_biased(r3, 0x4341);
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
                         mma_16816<false>(acc[c][j], a0, a1, a2, a3, pb[j][0], pb[j][1]);
@@ -662,7 +677,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                         if (d < p.D) {
                             const long long si = p.aq_per_channel ? (long long)(p.KV_N + h) * p.D + d : 1;
                             vsc[n][hh] = ld_half_as_float(p.aq_scale, si, p.q_bf16);
-                            vof[n][hh] = ld_half_as_float(p.aq_offset, si, p.q_bf16);
+                            vof[n][hh] = ld_half_as_float(p.aq_offset, si, p.q_bf16) - kI8Bias;  // values carry +1152
                         }
                     }
                 }

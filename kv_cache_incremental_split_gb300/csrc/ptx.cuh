@@ -142,15 +142,14 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
-// Two signed int8 bytes of `w` (selected by `sel`) -> two exact fp16 values.
-// Flipping the sign bit maps x to x + 128 in [0, 255]; placing that byte as the
-// low mantissa byte under exponent bits 0x64 gives the fp16 number 1024 + x + 128
-// exactly (fp16 has unit spacing on [1024, 2048)), and subtracting 1152 returns x.
-__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t w_flipped, uint32_t sel) {
-    uint32_t h = prmt(w_flipped, 0x64646464u, sel);
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
-    return r;
+// Two signed int8 bytes of `w` (selected by `sel`), sign bits flipped -> two exact
+// fp16 values x + kI8Bias.  Flipping the sign bit maps x to x + 128 in [0, 255];
+// placing that byte as the low mantissa byte under exponent bits 0x64 gives the
+// fp16 number 1024 + x + 128 exactly (fp16 has unit spacing on [1024, 2048)).
+// The bias is left in: callers remove it where it is cheapest.
+constexpr float kI8Bias = 1152.f;
+__device__ __forceinline__ uint32_t i8x2_to_f16x2_biased(uint32_t w_flipped, uint32_t sel) {
+    return prmt(w_flipped, 0x64646464u, sel);
 }
 
 }  // namespace ifa
