@@ -68,7 +68,13 @@ struct DecodeCfg {
     static constexpr int CG_ELEMS = 128 / ES;                  // elements per 128-byte column group
     static constexpr int NCG = DPAD * ES / 128;                // column groups per row
     static constexpr int NWC = DPAD <= 128 ? 8 : 4;            // consumer warps
-    static constexpr int THREADS = (NWC + 1) * 32;             // + one producer warp
+    // Eight consumer warps plus a producer would leave 168 registers a thread (three warps
+    // on one SM sub-partition); with twelve warps the producer's warpgroup gives registers
+    // back (setmaxnreg) so the two consumer warpgroups get CONSUMER_REGS each.
+    static constexpr bool SPLIT_REGS = NWC == 8;
+    static constexpr int THREADS = SPLIT_REGS ? 12 * 32 : (NWC + 1) * 32;  // consumers + producer (+ 3 idle)
+    static constexpr int CONSUMER_REGS = 200, PRODUCER_REGS = 56;
+    static constexpr int REG_POOL_NEEDED = NWC * 32 * CONSUMER_REGS + 4 * 32 * PRODUCER_REGS;
     static constexpr int T = kWarpTokens * NWC;                // tokens per stage (one tile)
     static constexpr int KT_BYTES = NCG * T * 128;             // one K (or V) tile
     static constexpr int GT_PAD = 8 * NT;                      // query heads per CTA, padded

@@ -251,8 +251,10 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     }
     if (lo >= hi) return;
 
-    if (warp == NWC) {
+    if (warp >= NWC) {
         // ================================================================ producer warp
+        if constexpr (C::SPLIT_REGS) setmaxnreg_dec<C::PRODUCER_REGS>();
+        if (warp > NWC) return;  // the rest of the producer's warpgroup only gives its registers back
         if (lane == 0) {
             prefetch_tensormap(&p.tmK);
             prefetch_tensormap(&p.tmV);
@@ -379,6 +381,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     }
 
     // ==================================================================== consumer warps
+    if constexpr (C::SPLIT_REGS) setmaxnreg_inc<C::CONSUMER_REGS>();
     const int r = lane >> 2;
     const int q4 = lane & 3;
     const int row0 = warp * kWarpTokens;
@@ -893,6 +896,14 @@ cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) 
         cudaError_t e = cudaFuncSetAttribute(decode_kernel<KV, DPAD, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM);
         if (e != cudaSuccess) return e;
+        if constexpr (C::SPLIT_REGS) {
+            // setmaxnreg.inc draws on the registers the block was launched with: refuse to launch
+            // a build whose register count cannot cover the split (the increase would never return).
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, decode_kernel<KV, DPAD, NT>);
+            if (e != cudaSuccess) return e;
+            if ((long long)fa.numRegs * C::THREADS < C::REG_POOL_NEEDED) return cudaErrorInvalidConfiguration;
+        }
         configured = true;
     }
     decode_kernel<KV, DPAD, NT><<<grid, C::THREADS, C::SMEM, stream>>>(p);
