@@ -75,9 +75,9 @@ __device__ __forceinline__ void cursor_init(TileCursor& c, const int* bd, int B,
     }
     c.b = lo;
     c.tiles = tiles_of<T>(bd[B + lo]);
-    const long long off = g - pre[lo];
-    c.r = (int)(off / c.tiles);
-    c.i = (int)(off % c.tiles);
+    const int off = (int)(g - pre[lo]);  // W < 2^31
+    c.r = off / c.tiles;
+    c.i = off - c.r * c.tiles;
     c.h = c.r / NGS;
     c.gs = c.r - c.h * NGS;
 }
@@ -208,22 +208,31 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if (threadIdx.x == NWC * 32) {  // the descriptor fetches overlap the rest of the prologue
+        prefetch_tensormap(&p.tmK);
+        prefetch_tensormap(&p.tmV);
+        prefetch_tensormap(&p.tmKt);
+        prefetch_tensormap(&p.tmVt);
+        if (p.mask_tma) prefetch_tensormap(&p.tmM);
+    }
+    // Programmatic dependent launch: the next kernel on the stream may start its own prologue on
+    // SMs this grid leaves; everything before pdl_wait_primary() below touches only launch
+    // parameters and shared memory.
+    pdl_launch_dependents();
     const int B = p.B;
     const int RS = p.KV_N * p.NGS;
     const long long lo = p.bounds[blockIdx.x];
     const long long hi = p.bounds[blockIdx.x + 1];
     // The window table is read every tile: keep it in shared memory when it came inline.
+    // Both launch-parameter arrays are copied by one loop, so their reads overlap.
     const int* bd = p.ext_bdata ? p.ext_bdata : sbd;
-    if (!p.ext_bdata)
-        for (int x = threadIdx.x; x < 3 * B + 1; x += C::THREADS) sbd[x] = p.bdata_inline[x];
     int* sbounds = sbd + 3 * kInlineB + 1;
-    for (int x = threadIdx.x; x <= p.P; x += C::THREADS) sbounds[x] = p.bounds[x];
-    // The next call counts its arrivals in the other counter set: clear that set now
-    // (entry c by CTA c mod P), so no call depends on how an earlier one ended.
     {
-        unsigned int* next_set = p.counters + ((p.gen + 1u) & 1u) * kMaxCtas;
-        for (long long c = blockIdx.x + (long long)threadIdx.x * p.P; c < kMaxCtas; c += (long long)C::THREADS * p.P)
-            next_set[c] = 0u;
+        const int nbd = p.ext_bdata ? 0 : 3 * B + 1;
+        for (int x = threadIdx.x; x < nbd + p.P + 1; x += C::THREADS) {
+            if (x < nbd) sbd[x] = p.bdata_inline[x];
+            else sbounds[x - nbd] = p.bounds[x - nbd];
+        }
     }
 
     if (threadIdx.x == 0) {
@@ -242,6 +251,17 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     }
     fence_proxy_async_smem();
     __syncthreads();
+    // Inputs, outputs and the workspace may belong to the previous kernel on the stream until it
+    // has completed.
+    pdl_wait_primary();
+
+    // The next call counts its arrivals in the other counter set: clear that set now
+    // (entry c by CTA c mod P), so no call depends on how an earlier one ended.
+    {
+        unsigned int* next_set = p.counters + ((p.gen + 1u) & 1u) * kMaxCtas;
+        for (long long c = blockIdx.x + (long long)threadIdx.x * p.P; c < kMaxCtas; c += (long long)C::THREADS * p.P)
+            next_set[c] = 0u;
+    }
 
     // Batches with no valid token produce all-zero rows; CTA c takes b = c, c+P, ...
     for (int b = blockIdx.x; b < B; b += p.P) {
@@ -255,13 +275,6 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         // ================================================================ producer warp
         if constexpr (C::SPLIT_REGS) setmaxnreg_dec<C::PRODUCER_REGS>();
         if (warp > NWC) return;  // the rest of the producer's warpgroup only gives its registers back
-        if (lane == 0) {
-            prefetch_tensormap(&p.tmK);
-            prefetch_tensormap(&p.tmV);
-            prefetch_tensormap(&p.tmKt);
-            prefetch_tensormap(&p.tmVt);
-            if (p.mask_tma) prefetch_tensormap(&p.tmM);
-        }
         const uint64_t pol = policy_evict_first();
         const int br = p.box_rows;
         const int tr = p.tail_rows;
@@ -270,9 +283,9 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         TileCursor cur;
         cursor_init<T>(cur, bd, B, p.NGS, lo);
         int my_blk = 0;
-        long long it = 0;
+        int it = 0;  // tiles of this CTA so far (< 2^31)
         for (long long g = lo; g < hi; ++g, ++it) {
-            const int kk = (int)((g - lo) % batch_tiles);
+            const int kk = it % batch_tiles;
             if (p.paged && kk == 0) {
                 // Block ids of the next batch_tiles tiles: lane l reads full box (l % nsub) of tile (l / nsub).
                 TileCursor c2 = cur;
@@ -287,7 +300,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                         my_blk = __ldg(&p.block_table[(long long)c2.b * p.bt_cols + t0 / p.block_size]);
                 }
             }
-            const int stage = (int)(it % C::STAGES);
+            const int stage = it % C::STAGES;
             const uint32_t round = (uint32_t)(it / C::STAGES);
             if (round > 0) {
                 if (!mbar_wait_bounded(&empty[stage], (round - 1) & 1, kWaitLimitNs)) {
@@ -400,14 +413,14 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         cursor_init<T>(mcur, bd, B, p.NGS, lo);
         mask_next = load_mask_bits<NT, T>(p, mcur, bd, row0, r, q4);
     }
-    long long it = 0;
+    int it = 0;
     for (long long g = lo; g < hi; ++g, ++it) {
         uint32_t mbits = mask_next;
         if (mask_regs && g + 1 < hi) {
             cursor_next<T>(mcur, bd, B, RS, p.NGS);
             mask_next = load_mask_bits<NT, T>(p, mcur, bd, row0, r, q4);
         }
-        const int stage = (int)(it % C::STAGES);
+        const int stage = it % C::STAGES;
         const uint32_t round = (uint32_t)(it / C::STAGES);
         if (!mbar_wait_bounded(&full[stage], round & 1, kWaitLimitNs)) {
             if (lane == 0) record_error(p, kErrTimeout);
@@ -906,8 +919,17 @@ cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) 
         }
         configured = true;
     }
-    decode_kernel<KV, DPAD, NT><<<grid, C::THREADS, C::SMEM, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<KV, DPAD, NT>, p);
 }
 
 }  // namespace ifa
