@@ -9,7 +9,8 @@
 
 namespace ifa {
 
-constexpr int kWarpTokens = 16;      // tokens of a stage owned by one consumer warp (the mma M)
+constexpr int kMaskBox = 128;        // bytes per mask TMA box; a tile's boxes land back to back on 128-byte
+                                     // boundaries (a tensor copy's shared-memory destination must be)
 constexpr int kInlineB = 256;        // per-batch windows travel in the launch parameters up to this B
 constexpr int kMaxCtas = 256;        // upper bound on the grid
 constexpr int kMinPieceTiles = 4;    // do not cut sequences into pieces shorter than this (tiles)
@@ -75,12 +76,17 @@ struct DecodeCfg {
     static constexpr int THREADS = SPLIT_REGS ? 12 * 32 : (NWC + 1) * 32;  // consumers + producer (+ 3 idle)
     static constexpr int CONSUMER_REGS = 200, PRODUCER_REGS = 56;
     static constexpr int REG_POOL_NEEDED = NWC * 32 * CONSUMER_REGS + 4 * 32 * PRODUCER_REGS;
-    static constexpr int T = kWarpTokens * NWC;                // tokens per stage (one tile)
+    // int8 tiles are half the bytes of 16-bit ones: each consumer warp takes two 16-token
+    // mma M tiles, so a stage holds as many bytes and the per-tile work is shared by 32 tokens.
+    static constexpr int KWT = (KV == KV_I8 && DPAD <= 128) ? 32 : 16;  // tokens of a stage per consumer warp
+    static constexpr int MTW = KWT / 16;                        // 16-token mma M tiles per consumer warp
+    static constexpr int T = KWT * NWC;                         // tokens per stage (one tile)
     static constexpr int KT_BYTES = NCG * T * 128;             // one K (or V) tile
     static constexpr int GT_PAD = 8 * NT;                      // query heads per CTA, padded
     static constexpr int QROW = DPAD * 2 + 16;                 // padded query row in shared memory
     static constexpr int Q_BYTES = GT_PAD * QROW;
-    static constexpr int MASK_BYTES = 256;                     // one tile's mask bytes (T + 16 <= 256)
+    static constexpr int MASK_LOADS = (T + 16 + kMaskBox - 1) / kMaskBox;  // mask boxes per tile
+    static constexpr int MASK_BYTES = MASK_LOADS * kMaskBox;  // one tile's mask bytes, contiguous
     static constexpr int MASK_OFF = 2 * KT_BYTES + Q_BYTES;    // within a stage
     static constexpr int STAGE_BYTES = round_up_c(2 * KT_BYTES + Q_BYTES + MASK_BYTES, 1024);
     static constexpr int MW = NWC < 4 ? NWC : 4;               // warps the merge buffer holds at once
@@ -100,7 +106,8 @@ struct DecodeCfg {
     static constexpr int SLOT_FLOATS = GT_PAD * DPAD + 2 * GT_PAD;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(T % 32 == 0, "tiles are whole 32-row sub-boxes");
-    static_assert(MASK_OFF % 128 == 0 && T + 16 <= MASK_BYTES, "mask staging area");
+    static_assert(MASK_OFF % 128 == 0 && kMaskBox % 128 == 0 && T + 16 <= MASK_BYTES, "mask staging area");
+    static_assert(T <= 256, "TMA boxes hold at most 256 rows");
 };
 
 typedef cudaError_t (*DecodeLaunchFn)(const DecodeParams&, int grid, cudaStream_t);

@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                 }
                 for (int k = 0; k < nbox; ++k)
                     if (!((badmask >> ((k * rows_per) / br)) & 1)) bytes += box_bytes;
-                if (p.mask_tma) bytes += (uint32_t)(T + 16);
+                if (p.mask_tma) bytes += (uint32_t)(C::MASK_LOADS * kMaskBox);
                 if (badmask) record_error(p, kErrBadBlock);
                 const int st = bd[b];
                 tinfo[2 * stage] = make_int4(b, h, gs, cur.i);
@@ -358,7 +358,10 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                 if (p.mask_tma) {
                     // this tile's mask bytes, from the 16-byte boundary at or below its first position
                     const int x0 = st + cur.i * T;
-                    tma_load_2d(sb + C::MASK_OFF, &p.tmM, &full[stage], x0 & ~15, p.mask_bstride ? b : 0);
+#pragma unroll
+                    for (int ml = 0; ml < C::MASK_LOADS; ++ml)
+                        tma_load_2d(sb + C::MASK_OFF + ml * kMaskBox, &p.tmM, &full[stage], (x0 & ~15) + ml * kMaskBox,
+                                    p.mask_bstride ? b : 0);
                 }
                 const CUtensorMap* mk = tail ? &p.tmKt : &p.tmK;
                 const CUtensorMap* mv = tail ? &p.tmVt : &p.tmV;
@@ -397,7 +400,8 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     if constexpr (C::SPLIT_REGS) setmaxnreg_inc<C::CONSUMER_REGS>();
     const int r = lane >> 2;
     const int q4 = lane & 3;
-    const int row0 = warp * kWarpTokens;
+    constexpr int MTW = C::MTW;
+    const int row0 = warp * C::KWT;
     const float sl2 = p.scale_log2;
     const int tid = threadIdx.x;  // 0 .. CONSUMERS-1
 
@@ -408,17 +412,24 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     // Masks the producer does not stage are read by the consumers, one tile ahead.
     const bool mask_regs = p.has_mask && !p.mask_tma;
     TileCursor mcur;
-    uint32_t mask_next = 0;
+    uint32_t mask_next[MTW];
+#pragma unroll
+    for (int mt = 0; mt < MTW; ++mt) mask_next[mt] = 0u;
     if (mask_regs) {
         cursor_init<T>(mcur, bd, B, p.NGS, lo);
-        mask_next = load_mask_bits<NT, T>(p, mcur, bd, row0, r, q4);
+#pragma unroll
+        for (int mt = 0; mt < MTW; ++mt) mask_next[mt] = load_mask_bits<NT, T>(p, mcur, bd, row0 + 16 * mt, r, q4);
     }
     int it = 0;
     for (long long g = lo; g < hi; ++g, ++it) {
-        uint32_t mbits = mask_next;
+        uint32_t mbits[MTW];
+#pragma unroll
+        for (int mt = 0; mt < MTW; ++mt) mbits[mt] = mask_next[mt];
         if (mask_regs && g + 1 < hi) {
             cursor_next<T>(mcur, bd, B, RS, p.NGS);
-            mask_next = load_mask_bits<NT, T>(p, mcur, bd, row0, r, q4);
+#pragma unroll
+            for (int mt = 0; mt < MTW; ++mt)  // one tile ahead
+                mask_next[mt] = load_mask_bits<NT, T>(p, mcur, bd, row0 + 16 * mt, r, q4);
         }
         const int stage = it % C::STAGES;
         const uint32_t round = (uint32_t)(it / C::STAGES);
@@ -488,17 +499,20 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
 
         if (p.mask_tma) {
             const uint8_t* ms = sb + C::MASK_OFF + ib.w;
-            const int tl = row0 + r, th = row0 + r + 8;
-            const uint32_t pat = ((tl < valid && ms[tl]) ? 0x3u : 0u) | ((th < valid && ms[th]) ? 0xCu : 0u);
-            mbits = 0;
 #pragma unroll
-            for (int j = 0; j < NT; ++j) mbits |= pat << (4 * j);
+            for (int mt = 0; mt < MTW; ++mt) {
+                const int tl = row0 + 16 * mt + r, th = tl + 8;
+                const uint32_t pat = ((tl < valid && ms[tl]) ? 0x3u : 0u) | ((th < valid && ms[th]) ? 0xCu : 0u);
+                mbits[mt] = 0;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) mbits[mt] |= pat << (4 * j);
+            }
         }
         // Rows past the window end (or in a skipped block) may hold anything, NaN
         // included: clear this warp's invalid value rows so 0 * garbage stays 0.
         if constexpr (KV != KV_I8) {
-            if (valid < row0 + kWarpTokens || badmask) {
-                for (int idx = lane; idx < kWarpTokens * C::NCG * 8; idx += 32) {
+            if (valid < row0 + C::KWT || badmask) {
+                for (int idx = lane; idx < C::KWT * C::NCG * 8; idx += 32) {
                     const int rr = idx / (C::NCG * 8);
                     const int c16 = idx % (C::NCG * 8);
                     const int row = row0 + rr;
@@ -512,20 +526,21 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         }
 
         // ---------------------------------------------------------- S^T = K . Q^T (two accumulator chains)
-        float s[NT][4], s2[NT][4];
+        float s[MTW][NT][4], s2[MTW][NT][4];
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
+        for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) s[j][e] = s2[j][e] = 0.f;
-        {
-            const int lrow = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-            const uint32_t rbase = kbase + lrow * 128;
-            const int sw = lrow & 7;
-            if constexpr (KV == KV_I8) {
+            for (int j = 0; j < NT; ++j)
 #pragma unroll
-                for (int ks = 0; ks < KSTEPS; ks += 2) {
+                for (int e = 0; e < 4; ++e) s[mt][j][e] = s2[mt][j][e] = 0.f;
+        if constexpr (KV == KV_I8) {
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ks += 2) {
+#pragma unroll
+                for (int mt = 0; mt < MTW; ++mt) {
+                    const int lrow = row0 + 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
                     const int ch = ks + (lane >> 4);  // 16-byte chunk = 16 channels
-                    const uint32_t addr = rbase + (ch >> 3) * (T * 128) + (((ch & 7) ^ sw) << 4);
+                    const uint32_t addr = kbase + lrow * 128 + (ch >> 3) * (T * 128) + (((ch & 7) ^ (lrow & 7)) << 4);
                     uint32_t r0, r1, r2, r3;
                     ldsm_x4(addr, r0, r1, r2, r3);
                     r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
@@ -535,55 +550,65 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                     const uint32_t c1 = i8x2_to_f16x2_biased(r3, 0x4140), c3 = i8x2_to_f16x2_biased(r3, 0x4342);
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
-                        mma_16816<false>(s[j], a0, a1, a2, a3, qf[ks][j][0], qf[ks][j][1]);
-                        mma_16816<false>(s2[j], c0, c1, c2, c3, qf[ks + 1][j][0], qf[ks + 1][j][1]);
+                        mma_16816<false>(s[mt][j], a0, a1, a2, a3, qf[ks][j][0], qf[ks][j][1]);
+                        mma_16816<false>(s2[mt][j], c0, c1, c2, c3, qf[ks + 1][j][0], qf[ks + 1][j][1]);
                     }
                 }
-            } else {
+            }
+        } else {
 #pragma unroll
-                for (int ks = 0; ks < KSTEPS; ++ks) {
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+#pragma unroll
+                for (int mt = 0; mt < MTW; ++mt) {
+                    const int lrow = row0 + 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
                     const int ch = 2 * ks + (lane >> 4);  // 16-byte chunk = 8 channels
-                    const uint32_t addr = rbase + (ch >> 3) * (T * 128) + (((ch & 7) ^ sw) << 4);
+                    const uint32_t addr = kbase + lrow * 128 + (ch >> 3) * (T * 128) + (((ch & 7) ^ (lrow & 7)) << 4);
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4(addr, a0, a1, a2, a3);
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
                         // one n-tile: alternate two accumulators to halve the dependent chain
-                        if (NT == 1 && (ks & 1)) mma_16816<MMA_BF16>(s2[j], a0, a1, a2, a3, qf[ks][j][0], qf[ks][j][1]);
-                        else mma_16816<MMA_BF16>(s[j], a0, a1, a2, a3, qf[ks][j][0], qf[ks][j][1]);
+                        if (NT == 1 && (ks & 1)) mma_16816<MMA_BF16>(s2[mt][j], a0, a1, a2, a3, qf[ks][j][0], qf[ks][j][1]);
+                        else mma_16816<MMA_BF16>(s[mt][j], a0, a1, a2, a3, qf[ks][j][0], qf[ks][j][1]);
                     }
                 }
             }
         }
 
         // ---------------------------------------------------------- mask, online softmax
-        const int t_lo = row0 + r, t_hi = row0 + r + 8;
-        bool ok_lo = t_lo < valid, ok_hi = t_hi < valid;
-        if (badmask) {
-            ok_lo = ok_lo && !((badmask >> (t_lo / p.box_rows)) & 1);
-            ok_hi = ok_hi && !((badmask >> (t_hi / p.box_rows)) & 1);
+        uint32_t pb[MTW][NT][2];
+        float x[MTW][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < MTW; ++mt) {
+            const int t_lo = row0 + 16 * mt + r, t_hi = t_lo + 8;
+            bool ok_lo = t_lo < valid, ok_hi = t_hi < valid;
+            if (badmask) {
+                ok_lo = ok_lo && !((badmask >> (t_lo / p.box_rows)) & 1);
+                ok_hi = ok_hi && !((badmask >> (t_hi / p.box_rows)) & 1);
+            }
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool ok = ((e >> 1) ? ok_hi : ok_lo) && !((mbits[mt] >> (4 * j + e)) & 1u);
+                    x[mt][j][e] = ok ? (s[mt][j][e] + s2[mt][j][e]) * sl2 : -INFINITY;
+                }
         }
-        uint32_t pb[NT][2];
-        float x[NT][4];
         bool moved = false;
         float mnew[NT][2];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const bool ok = ((e >> 1) ? ok_hi : ok_lo) && !((mbits >> (4 * j + e)) & 1u);
-                x[j][e] = ok ? (s[j][e] + s2[j][e]) * sl2 : -INFINITY;
-            }
+        for (int j = 0; j < NT; ++j)
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                float mx = fmaxf(x[j][u], x[j][u + 2]);
+                float mx = fmaxf(x[0][j][u], x[0][j][u + 2]);
+#pragma unroll
+                for (int mt = 1; mt < MTW; ++mt) mx = fmaxf(mx, fmaxf(x[mt][j][u], x[mt][j][u + 2]));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 mnew[j][u] = fmaxf(m_run[j][u], mx);
                 moved |= mnew[j][u] != m_run[j][u];
             }
-        }
         if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
             for (int j = 0; j < NT; ++j)
@@ -600,39 +625,40 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                 }
         }
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            float pr[4];
+        for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const float m_use = m_run[j][u] == -INFINITY ? 0.f : m_run[j][u];
-                pr[u] = ex2(x[j][u] - m_use);
-                pr[u + 2] = ex2(x[j][u + 2] - m_use);
+            for (int j = 0; j < NT; ++j) {
+                float pr[4];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const float m_use = m_run[j][u] == -INFINITY ? 0.f : m_run[j][u];
+                    pr[u] = ex2(x[mt][j][u] - m_use);
+                    pr[u + 2] = ex2(x[mt][j][u + 2] - m_use);
+                }
+                const uint32_t h0 = pack2<MMA_BF16>(pr[0], pr[1]), h1 = pack2<MMA_BF16>(pr[2], pr[3]);
+                if constexpr (KV == KV_I8) {
+                    // row sums of the fp16-rounded probabilities the P.V MMAs see (keeps the value bias exact)
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+                    l_run[j][0] += f0.x + f1.x;
+                    l_run[j][1] += f0.y + f1.y;
+                } else {
+                    l_run[j][0] += pr[0] + pr[2];
+                    l_run[j][1] += pr[1] + pr[3];
+                }
+                pb[mt][j][0] = movmatrix_t(h0);
+                pb[mt][j][1] = movmatrix_t(h1);
             }
-            const uint32_t h0 = pack2<MMA_BF16>(pr[0], pr[1]), h1 = pack2<MMA_BF16>(pr[2], pr[3]);
-            if constexpr (KV == KV_I8) {
-                // row sums of the fp16-rounded probabilities the P.V MMAs see (keeps the value bias exact)
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
-                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
-                l_run[j][0] += f0.x + f1.x;
-                l_run[j][1] += f0.y + f1.y;
-            } else {
-                l_run[j][0] += pr[0] + pr[2];
-                l_run[j][1] += pr[1] + pr[3];
-            }
-            pb[j][0] = movmatrix_t(h0);
-            pb[j][1] = movmatrix_t(h1);
-        }
 
         // ---------------------------------------------------------- O^T += V^T . P^T
-        {
-            if constexpr (KV == KV_I8) {
-                const int lrow = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const uint32_t rbase = vbase + lrow * 128;
-                const int sw = lrow & 7;
+        if constexpr (KV == KV_I8) {
 #pragma unroll
-                for (int c = 0; c < MT; c += 2) {
+            for (int c = 0; c < MT; c += 2) {
+#pragma unroll
+                for (int mt = 0; mt < MTW; ++mt) {
+                    const int lrow = row0 + 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
                     const int ch = c + (lane >> 4);
-                    const uint32_t addr = rbase + (ch >> 3) * (T * 128) + (((ch & 7) ^ sw) << 4);
+                    const uint32_t addr = vbase + lrow * 128 + (ch >> 3) * (T * 128) + (((ch & 7) ^ (lrow & 7)) << 4);
                     uint32_t r0, r1, r2, r3;
                     ldsm_x4_t(addr, r0, r1, r2, r3);
                     r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
@@ -642,23 +668,25 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                     const uint32_t e2 = i8x2_to_f16x2_biased(r3, 0x4240), e3 = i8x2_to_f16x2_biased(r3, 0x4341);
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
-                        mma_16816<false>(acc[c][j], a0, a1, a2, a3, pb[j][0], pb[j][1]);
-                        mma_16816<false>(acc[c + 1][j], e0, e1, e2, e3, pb[j][0], pb[j][1]);
+                        mma_16816<false>(acc[c][j], a0, a1, a2, a3, pb[mt][j][0], pb[mt][j][1]);
+                        mma_16816<false>(acc[c + 1][j], e0, e1, e2, e3, pb[mt][j][0], pb[mt][j][1]);
                     }
                 }
-            } else {
-                const int mi = lane >> 3;
-                const int lrow = row0 + (lane & 7) + (mi >> 1) * 8;
-                const uint32_t rbase = vbase + lrow * 128;
-                const int sw = lrow & 7;
+            }
+        } else {
+            const int mi = lane >> 3;
 #pragma unroll
-                for (int md = 0; md < MT; ++md) {
+            for (int md = 0; md < MT; ++md) {
+#pragma unroll
+                for (int mt = 0; mt < MTW; ++mt) {
+                    const int lrow = row0 + 16 * mt + (lane & 7) + (mi >> 1) * 8;
                     const int ch = 2 * md + (mi & 1);
-                    const uint32_t addr = rbase + (ch >> 3) * (T * 128) + (((ch & 7) ^ sw) << 4);
+                    const uint32_t addr = vbase + lrow * 128 + (ch >> 3) * (T * 128) + (((ch & 7) ^ (lrow & 7)) << 4);
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4_t(addr, a0, a1, a2, a3);
 #pragma unroll
-                    for (int j = 0; j < NT; ++j) mma_16816<MMA_BF16>(acc[md][j], a0, a1, a2, a3, pb[j][0], pb[j][1]);
+                    for (int j = 0; j < NT; ++j)
+                        mma_16816<MMA_BF16>(acc[md][j], a0, a1, a2, a3, pb[mt][j][0], pb[mt][j][1]);
                 }
             }
         }

@@ -291,10 +291,11 @@ bool encode_mask_map(const ifa_params& p, const KernelChoice& kc, const void* ma
     if (!p.has_mask || p.maskN != 1 || p.maskS % 16 != 0 || (reinterpret_cast<uintptr_t>(mask) % 16) != 0) return true;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    // Box: the tile plus the up-to-15-byte lead from rounding its start down to 16 bytes.
+    // A tile's mask bytes plus the up-to-15-byte lead from rounding its start down to 16 bytes
+    // come in one to three kMaskBox-byte boxes.
     cuuint64_t dims[2] = {(cuuint64_t)p.maskS, (cuuint64_t)p.maskB};
     cuuint64_t strides[1] = {(cuuint64_t)p.maskS};
-    cuuint32_t box[2] = {(cuuint32_t)(kc.T + 16), 1};
+    cuuint32_t box[2] = {(cuuint32_t)kMaskBox, 1};
     cuuint32_t estr[2] = {1, 1};
     if (enc(&dp.tmM, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(mask), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,

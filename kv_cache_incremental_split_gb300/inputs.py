@@ -240,6 +240,24 @@ def paged_gqa(seed: int = 0, B=64, N=32, KV_N=8, D=128, block_size=128, len_lo=5
                    block_table=bt, actual_seq_lengths=lens, meta={"blocknum": blocknum})
 
 
+def int8_paged(seed: int = 0, B=4, N=16, KV_N=4, D=128, block_size=64, len_lo=1, len_hi=1024,
+               kv_format="paged_nbsd", q_dtype="fp16") -> IfaCase:
+    """int8 key/value in a paged cache (per-channel antiquant), blocks a random permutation."""
+    rng = np.random.default_rng(seed)
+    lens = _lengths(rng, B, len_lo, len_hi)
+    cols = (len_hi + block_size - 1) // block_size
+    bt, blocknum = _block_table(rng, lens, block_size, cols)
+    shape = (blocknum, KV_N, block_size, D) if kv_format == "paged_nbsd" else (blocknum, block_size, KV_N * D)
+    scale = to_storage(rng.uniform(0.005, 0.02, size=(2, KV_N, 1, D)).astype(np.float32), q_dtype)
+    offset = to_storage(rng.uniform(-4.0, 4.0, size=(2, KV_N, 1, D)).astype(np.float32), q_dtype)
+    return IfaCase("int8_paged", random_storage(seed, 1, (B, N, 1, D), q_dtype),
+                   uniform_int8(seed, 2, shape), uniform_int8(seed, 3, shape),
+                   num_heads=N, num_kv_heads=KV_N, scale=1.0 / math.sqrt(D), layout="BNSD",
+                   kv_format=kv_format, q_dtype=q_dtype, kv_dtype="int8", block_size=block_size,
+                   block_table=bt, actual_seq_lengths=lens, antiquant="per_channel",
+                   antiquant_scale=scale, antiquant_offset=offset, meta={"blocknum": blocknum})
+
+
 def int8_leftpad(seed: int = 0, B=32, N=64, KV_N=8, D=128, Smax=8192, len_lo=256, len_hi=8192,
                  pad_extra=64, per_tensor=False, q_dtype="fp16") -> IfaCase:
     rng = np.random.default_rng(seed)

@@ -212,3 +212,37 @@ def test_mask_staged_by_the_producer(left_pad):
     check(case)
     case.atten_mask = case.atten_mask[:1]  # (1,1,1,S): one row for every batch
     check(case)
+
+
+# ---- int8 key/value with two 16-token mma tiles per consumer warp (256-token tiles)
+
+
+@pytest.mark.parametrize("block_size,kv_format", [(32, "paged_nbsd"), (96, "paged_nbsd"), (256, "paged_bsh")])
+def test_int8_paged(block_size, kv_format):
+    """Paged int8 caches: a 256-token tile spans 8, 8 or 1 cache blocks (box rows gcd(256, block))."""
+    check(gen.int8_paged(41, B=5, N=16, KV_N=4, D=128, block_size=block_size, len_lo=1, len_hi=900,
+                         kv_format=kv_format))
+
+
+@pytest.mark.parametrize("left_pad", [False, True])
+def test_int8_mask_staged_in_two_boxes(left_pad):
+    """A 256-token tile's mask bytes come in two TMA boxes; windows start anywhere."""
+    rng = np.random.default_rng(42)
+    case = gen.int8_leftpad(42, B=5, N=16, KV_N=4, D=128, Smax=640, len_lo=1, len_hi=640)
+    if not left_pad:
+        case.kv_padding_size = None
+    case.atten_mask = rng.random((5, 1, 1, 640)) < 0.3
+    check(case)
+
+
+def test_int8_per_head_mask():
+    """Per-head masks are read by the consumer warps, one tile ahead, for both 16-token tiles."""
+    rng = np.random.default_rng(43)
+    case = gen.int8_leftpad(43, B=3, N=16, KV_N=4, D=128, Smax=600, len_lo=1, len_hi=600)
+    case.atten_mask = rng.random((3, 16, 1, 600)) < 0.4
+    check(case)
+
+
+@pytest.mark.parametrize("split_tiles", [1, 2, 3])
+def test_int8_forced_splits(split_tiles):
+    check(gen.int8_leftpad(44, B=4, N=32, KV_N=4, D=128, Smax=2000, len_lo=300, len_hi=2000), split_tiles=split_tiles)
