@@ -14,7 +14,11 @@ constexpr int kMaskBox = 128;        // bytes per mask TMA box; a tile's boxes l
 constexpr int kInlineB = 256;        // per-batch windows travel in the launch parameters up to this B
 constexpr int kMaxCtas = 256;        // upper bound on the grid
 constexpr int kMinPieceTiles = 4;    // do not cut sequences into pieces shorter than this (tiles)
-constexpr int kPieceCostBytes = 96 * 1024;  // fixed work of a sequence piece, in key/value bytes
+// Fixed work of a sequence piece (query load, epilogue, arrival), in key/value bytes of tile
+// time; int8 pieces also fetch their antiquant scale rows.  Tuned on the GQA, paged and int8
+// workloads (piece-heavy CTAs otherwise finish last).
+constexpr int kPieceCostBytes = 160 * 1024;
+constexpr int kPieceCostBytesI8 = 320 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded spin-waits: 2 s
 
 // Device error word bits (OR-ed into the error word).

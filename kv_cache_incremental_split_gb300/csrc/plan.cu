@@ -118,7 +118,7 @@ ifa_status choose_kernel(const ifa_params& p, KernelChoice* kc) {
     if (p.kvFormat != IFA_KV_CONTIG) kc->box_rows = (int)gcd64(kc->T, p.blockSize);
     kc->tail_rows = std::min(kc->box_rows, 32);
     const int tile_bytes = 2 * kc->T * kc->dpad * kc->es;
-    kc->piece_cost = std::max(1, kPieceCostBytes / tile_bytes);
+    kc->piece_cost = std::max(1, (kc->kv_kind == KV_I8 ? kPieceCostBytesI8 : kPieceCostBytes) / tile_bytes);
     return IFA_OK;
 }
 
