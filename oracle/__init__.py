@@ -62,7 +62,7 @@ def _load():
                                            vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, vp, ip,
                                            vp, vp, dp, vp]
             lib.sfa_oracle_run.restype = ctypes.c_int
-            lib.sfa_oracle_run.argtypes = [i64, i64, i64, i64, ip, i64, i64, i64, i64,
+            lib.sfa_oracle_run.argtypes = [i64, i64, i64, i64, ip, i64, i64, i64, i64, i64,
                                            vp, vp, vp, vp, vp, vp, vp, vp, dp, vp]
             _lib = lib
     return _lib
@@ -146,8 +146,10 @@ def ifa_ref(query, key, value, *, num_heads, num_kv_heads=0, scale, layout="BNSD
 
 
 def sfa_ref(query, query_rope, key, key_rope, value, sparse_indices, block_table,
-            actual_seq_lengths_kv, *, scale):
+            actual_seq_lengths_kv, *, scale, sparse_block_size=1):
     """Reference sparse MLA-absorb decode output, float64 (B, Q_N, D).
+
+    sparse_block_size > 1: each index selects that many consecutive tokens (block-wise).
 
     query (B,1,Q_N,D), query_rope (B,1,Q_N,Dr), key/value (block_num, block_size, 1, D),
     key_rope (block_num, block_size, 1, Dr), sparse_indices (B,1,1,sparse_size) int32,
@@ -167,7 +169,7 @@ def sfa_ref(query, query_rope, key, key_rope, value, sparse_indices, block_table
     block_num, block_size = k.shape[0], k.shape[1]
     out = np.zeros((B, Q_N, D), dtype=np.float64)
     rc = lib.sfa_oracle_run(B, Q_N, D, Dr, _dtype_code(q), block_size, block_num, bt.shape[1],
-                            idx.shape[-1], _ptr(q), _ptr(qr), _ptr(k), _ptr(kr), _ptr(v),
+                            idx.shape[-1], int(sparse_block_size), _ptr(q), _ptr(qr), _ptr(k), _ptr(kr), _ptr(v),
                             _ptr(idx), _ptr(bt), _ptr(lens), float(scale), _ptr(out))
     if rc < 0:
         raise ValueError("oracle rejected its arguments")

@@ -259,17 +259,23 @@ int ifa_oracle_run(int64_t B, int64_t N, int64_t KV_N, int64_t D, int q_dtype, i
  *   value (block_num, block_size, 1, D)   query (B, 1, Q_N, D), query_rope (B, 1, Q_N, Dr)
  *   sparse_indices (B, 1, 1, sparse_size), block_table (B, bt_cols)
  * s_j = scale * (q . k[idx_j] + q_rope . k_rope[idx_j]);  out = softmax(s) . v[idx_j].
+ * sparse_block_size (README "sparse_block_size", 1 = token-wise): entry j of a row selects
+ * the tokens idx_j * sparse_block_size + o, o = 0 .. sparse_block_size - 1 (block-wise:
+ * the tokens of a block share the selection); a token at or past actual_seq_lengths_kv[b],
+ * or any token of a negative entry, is skipped.
  * Returns the number of skipped out-of-range block-table entries, -1 on bad arguments.
  */
 int sfa_oracle_run(int64_t B, int64_t Q_N, int64_t D, int64_t Dr, int dtype, int64_t block_size,
-                   int64_t block_num, int64_t bt_cols, int64_t sparse_size, const void* q,
-                   const void* q_rope, const void* k, const void* k_rope, const void* v,
+                   int64_t block_num, int64_t bt_cols, int64_t sparse_size, int64_t sparse_block_size,
+                   const void* q, const void* q_rope, const void* k, const void* k_rope, const void* v,
                    const int32_t* sparse_indices, const int32_t* block_table,
                    const int32_t* lens_kv, double scale, double* out) {
-    if (B < 0 || Q_N <= 0 || D <= 0 || Dr < 0 || block_size <= 0 || sparse_size <= 0) return -1;
+    if (B < 0 || Q_N <= 0 || D <= 0 || Dr < 0 || block_size <= 0 || sparse_size <= 0 || sparse_block_size <= 0)
+        return -1;
     int bad = 0;
-    double* s = (double*)malloc((size_t)sparse_size * sizeof(double));
-    int64_t* row = (int64_t*)malloc((size_t)sparse_size * sizeof(int64_t));
+    const int64_t npos = sparse_size * sparse_block_size; /* selected token positions per row */
+    double* s = (double*)malloc((size_t)npos * sizeof(double));
+    int64_t* row = (int64_t*)malloc((size_t)npos * sizeof(int64_t));
     if (!s || !row) {
         free(s);
         free(row);
@@ -277,23 +283,25 @@ int sfa_oracle_run(int64_t B, int64_t Q_N, int64_t D, int64_t Dr, int dtype, int
     }
     for (int64_t b = 0; b < B; b++) {
         /* resolve the selected rows once per batch: physical row = blk * block_size + slot */
-        for (int64_t j = 0; j < sparse_size; j++) {
-            int64_t idx = sparse_indices[b * sparse_size + j];
+        for (int64_t j = 0; j < npos; j++) {
+            int64_t idx = sparse_indices[b * sparse_size + j / sparse_block_size];
             row[j] = -1;
-            if (idx < 0 || idx >= lens_kv[b]) continue;
-            int64_t blk = block_table[b * bt_cols + idx / block_size];
+            if (idx < 0) continue;
+            int64_t tok = idx * sparse_block_size + j % sparse_block_size;
+            if (tok >= lens_kv[b]) continue;
+            int64_t blk = block_table[b * bt_cols + tok / block_size];
             if (blk < 0 || blk >= block_num) {
                 bad++;
                 continue;
             }
-            row[j] = blk * block_size + idx % block_size;
+            row[j] = blk * block_size + tok % block_size;
         }
         for (int64_t n = 0; n < Q_N; n++) {
             double* o = out + (b * Q_N + n) * D;
             for (int64_t d = 0; d < D; d++) o[d] = 0.0;
             double smax = -INFINITY;
             int any = 0;
-            for (int64_t j = 0; j < sparse_size; j++) {
+            for (int64_t j = 0; j < npos; j++) {
                 if (row[j] < 0) continue;
                 double dot = 0.0;
                 for (int64_t d = 0; d < D; d++)
@@ -307,7 +315,7 @@ int sfa_oracle_run(int64_t B, int64_t Q_N, int64_t D, int64_t Dr, int dtype, int
             }
             if (!any) continue;
             double denom = 0.0;
-            for (int64_t j = 0; j < sparse_size; j++) {
+            for (int64_t j = 0; j < npos; j++) {
                 if (row[j] < 0) continue;
                 double w = exp(s[j] - smax);
                 denom += w;

@@ -475,3 +475,56 @@ def test_sfa_index_order_is_irrelevant_and_duplicates_count_twice():
             ref = torch_attention(np.concatenate([q[b, n], qr[b, n]]),
                                   np.concatenate([k[rows], kr[rows]], axis=1), v[rows], c.scale)
             np.testing.assert_allclose(got[b, n], ref, rtol=1e-12, atol=1e-13)
+
+
+def sref_block(c, sbs, **over):
+    a = dict(sparse_indices=c.sparse_indices, actual_seq_lengths_kv=c.actual_seq_lengths_kv)
+    a.update(over)
+    return oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, a["sparse_indices"], c.block_table,
+                          a["actual_seq_lengths_kv"], scale=c.scale, sparse_block_size=sbs)
+
+
+@pytest.mark.parametrize("sbs", [2, 4, 16])
+def test_sfa_blockwise_selected_set_exact_mean(sbs):
+    """Block-wise sparsity (SparseFlashAttention README, sparse_block_size): with Q = 0 and each
+    value row holding its token index, the output is the exact mean of the indices of the valid
+    tokens of the selected blocks: tokens idx*sbs .. idx*sbs+sbs-1 below the length, nothing for
+    a negative entry, duplicates counted twice."""
+    c = _sfa(34)
+    c.query[:] = 0
+    c.query_rope[:] = 0
+    bs = 16
+    codes = np.zeros(c.value.shape, dtype=np.float32)
+    for b in range(2):
+        for t in range(64):
+            codes[c.block_table[b, t // bs], t % bs, 0, :] = t
+    c.value = gen.to_storage(codes, "bf16")
+    nblk = 64 // sbs
+    idx = np.full((2, 1, 1, 16), -1, dtype=np.int32)
+    sel0 = [nblk - 1, 0, -1, 2 % nblk, 0]          # last block, a duplicate, an invalid entry
+    idx[0, 0, 0, :len(sel0)] = sel0
+    idx[1, 0, 0, :2] = [1, nblk - 1]
+    lens = np.array([64, 64 - sbs // 2 - 1], dtype=np.int32)  # batch 1: last block partly past the length
+    out = sref_block(c, sbs, sparse_indices=idx, actual_seq_lengths_kv=lens)
+    for b, sel in ((0, sel0), (1, [1, nblk - 1])):
+        toks = [i * sbs + o for i in sel if i >= 0 for o in range(sbs) if i * sbs + o < lens[b]]
+        assert np.all(out[b] == np.mean(toks)), (b, sbs)
+
+
+@pytest.mark.parametrize("sbs", [2, 8])
+def test_sfa_blockwise_equals_tokenwise_on_expanded_indices(sbs):
+    c = _sfa(35, kv_len=64, sparse_size=8, nvalid_lo=3, nvalid_hi=8)
+    rng = np.random.default_rng(35)
+    nblk = 64 // sbs
+    blk = np.full((2, 1, 1, 8), -1, dtype=np.int32)
+    for b in range(2):
+        blk[b, 0, 0, :5] = rng.choice(nblk, size=5, replace=False)
+    lens = np.array([64, 50], dtype=np.int32)
+    tok = np.full((2, 1, 1, 8 * sbs), -1, dtype=np.int32)
+    for b in range(2):
+        for j in range(8):
+            if blk[b, 0, 0, j] >= 0:
+                tok[b, 0, 0, j * sbs:(j + 1) * sbs] = blk[b, 0, 0, j] * sbs + np.arange(sbs)
+    got = sref_block(c, sbs, sparse_indices=blk, actual_seq_lengths_kv=lens)
+    want = sref_block(c, 1, sparse_indices=tok, actual_seq_lengths_kv=lens)
+    assert np.array_equal(got, want)
