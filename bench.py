@@ -52,6 +52,8 @@ WORKLOADS = {
                 "KV length 32768, sparse_indices (B,1,1,2048) with U{1024..2048} valid then -1, scale 1/sqrt(576)"),
     "sfa_mla_small": ("sparse MLA-absorb decode, profiling size: B=8 Q_N=128 D=512+64 bf16, block 64, "
                       "KV length 8192, 2048 indices with U{1024..2048} valid"),
+    "sfa_mla_blockwise": ("sparse MLA-absorb decode, block-wise: B=32 Q_N=128 D=512+64 bf16, PA_BSND block 64, "
+                          "KV length 32768, sparse_block_size 16, 128 block indices with U{64..128} valid then -1"),
 }
 
 
@@ -62,6 +64,8 @@ def make_case(name: str, seed: int):
         return gen.sfa_mla(seed)
     if name == "sfa_mla_small":
         return gen.sfa_mla(seed, B=8, kv_len=8192)
+    if name == "sfa_mla_blockwise":
+        return gen.sfa_mla(seed, sparse_size=128, nvalid_lo=64, nvalid_hi=128, sparse_block_size=16)
     return {"gqa_padded": gen.gqa_padded, "tiny_mha": gen.tiny_mha, "paged_gqa": gen.paged_gqa,
             "int8_leftpad": gen.int8_leftpad}[name](seed)
 
@@ -86,9 +90,12 @@ def windows(case: gen.IfaCase):
 
 
 def sfa_valid_counts(case: gen.SfaCase):
-    idx = case.sparse_indices.reshape(case.B, -1)
-    lens = case.actual_seq_lengths_kv.reshape(-1, 1)
-    return ((idx >= 0) & (idx < lens)).sum(axis=1)
+    """Selected tokens per batch row: each index covers sparse_block_size tokens, those below the length count."""
+    sbs = case.sparse_block_size
+    idx = case.sparse_indices.reshape(case.B, -1).astype(np.int64)
+    lens = case.actual_seq_lengths_kv.reshape(-1, 1, 1).astype(np.int64)
+    tok = idx[:, :, None] * sbs + np.arange(sbs)[None, None, :]
+    return ((idx[:, :, None] >= 0) & (tok < lens)).reshape(case.B, -1).sum(axis=1)
 
 
 def algorithmic_bytes(case) -> int:
@@ -281,7 +288,7 @@ def oracle_sample(case, budget_s: float, start_batch: int = 0):
         t = time.perf_counter()
         if isinstance(c, gen.SfaCase):
             oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
-                           c.actual_seq_lengths_kv, scale=c.scale)
+                           c.actual_seq_lengths_kv, scale=c.scale, sparse_block_size=c.sparse_block_size)
         else:
             oracle.ifa_ref(c.query, c.key, c.value, num_heads=c.num_heads, num_kv_heads=c.num_kv_heads,
                            scale=c.scale, layout=c.layout, kv_format=fmt[c.kv_format], block_size=c.block_size,
@@ -394,7 +401,7 @@ class SfaWorkload:
         self.op = SparseFlashAttention(batch=case.B, num_heads=case.query.shape[2], block_size=case.key.shape[1],
                                        block_num=case.key.shape[0], block_table_cols=case.block_table.shape[1],
                                        sparse_size=case.sparse_indices.shape[-1], dtype=case.dtype,
-                                       scale=case.scale, device=dev)
+                                       scale=case.scale, sparse_block_size=case.sparse_block_size, device=dev)
         self.q, self.qr = _to_dev(case.query, dev), _to_dev(case.query_rope, dev)
         self.idx, self.bt = _to_dev(case.sparse_indices, dev), _to_dev(case.block_table, dev)
         self.lens = _to_dev(case.actual_seq_lengths_kv, dev)

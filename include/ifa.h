@@ -207,14 +207,16 @@ int64_t ifa_last_launch_count(const ifa_plan* plan);
  *
  *     out[b, n, :] = softmax_j( scale_value * (q[b,n] . k[i_j] + q_rope[b,n] . k_rope[i_j]) ) . v[i_j]
  *
- * over the selected tokens i_j = sparse_indices[b, 0, 0, j] with 0 <= i_j <
- * actual_seq_lengths_kv[b] (entries outside that range, e.g. the -1 tail, are skipped
- * wherever they sit; duplicates count once per occurrence; an empty selection gives an
- * all-zero row).  Token i lives in block block_table[b][i / block_size], slot
+ * over the selected tokens i_j with 0 <= i_j < actual_seq_lengths_kv[b] (tokens outside that
+ * range, e.g. from the -1 tail, are skipped wherever they sit; duplicates count once per
+ * occurrence; an empty selection gives an all-zero row).  Token-wise (sparse_block_size 1):
+ * i_j = sparse_indices[b, 0, 0, j].  Block-wise (sparse_block_size = s > 1, README
+ * "sparse_block_size"): entry j selects the s tokens sparse_indices[b, 0, 0, j] * s + o,
+ * o = 0 .. s - 1.  Token i lives in block block_table[b][i / block_size], slot
  * i % block_size of the PA_BSND caches.  Only the layouts and modes the README lists for
  * this decode case are accepted: query layout BSND with Q_S = 1, key/value layout PA_BSND,
- * KV_N = 1, D = 512, Dr = 64, attention_mode 2 (MLA-absorb), sparse_block_size 1
- * (token-wise), sparse_mode 0 or 3 (identical for Q_S = 1), Q_N in 1..128.
+ * KV_N = 1, D = 512, Dr = 64, attention_mode 2 (MLA-absorb), sparse_mode 0 or 3 (identical
+ * for Q_S = 1), Q_N in 1..128.
  */
 typedef struct sfa_params {
     int64_t B;               /* batch, 1..65536 */
@@ -226,7 +228,7 @@ typedef struct sfa_params {
     int64_t block_num;       /* blocks in the caches */
     int64_t block_table_cols;/* second dimension of block_table */
     int64_t sparse_size;     /* indices per batch row, >= 1 */
-    int64_t sparse_block_size; /* must be 1 */
+    int64_t sparse_block_size; /* 1 (token-wise) or a power of two <= 128 dividing block_size */
     int32_t dtype;           /* IFA_BF16 or IFA_F16, shared by every tensor and the output */
     int32_t sparse_mode;     /* 0 or 3 */
     double scale_value;      /* scale applied to the scores (typically 1/sqrt(D + Dr)) */

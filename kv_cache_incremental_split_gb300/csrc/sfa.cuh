@@ -44,7 +44,8 @@ struct alignas(128) SfaParams {
     int* err;
     long long W;        // tiles: 2 * B * tiles_per_seq
     int P;
-    int B, QN, S_sp, tiles_per_seq;
+    int B, QN, S_sp, tiles_per_seq;  // S_sp: indices per row; tiles cover S_sp << sbs_log2 positions
+    int sbs_log2;                    // log2(sparse_block_size): position p reads index p >> sbs_log2
     int block_size, bt_cols, block_num, total_rows;
     int is_bf16;
     float scale_log2;

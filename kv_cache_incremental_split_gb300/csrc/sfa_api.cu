@@ -1,7 +1,8 @@
 // C ABI of the sparse MLA-absorb decode (sfa_workspace_size, sfa_run).  The
 // checks follow the "SparseFlashAttention" README's 参数说明 and 约束说明 for
 // the decode case this library implements (Q_S = 1, BSND query, PA_BSND
-// key/value, KV_N = 1, D = 512, Dr = 64, token-wise sparsity, MLA-absorb).
+// key/value, KV_N = 1, D = 512, Dr = 64, token-wise or block-wise sparsity,
+// MLA-absorb).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -26,7 +27,11 @@ bool sfa_valid(const sfa_params& p) {
     if (p.block_num < 1 || p.block_table_cols < 1 || p.sparse_size < 1) return false;
     if (p.block_num * p.block_size >= INT32_MAX) return false;
     if (p.sparse_size > INT32_MAX / 2 || p.block_table_cols > INT32_MAX / 2) return false;
-    if (p.sparse_block_size != 1) return false;
+    // token-wise (1) or block-wise: a power of two up to 128 that divides block_size
+    if (p.sparse_block_size < 1 || p.sparse_block_size > 128 || (p.sparse_block_size & (p.sparse_block_size - 1)) != 0)
+        return false;
+    if (p.block_size % p.sparse_block_size != 0) return false;
+    if (p.sparse_size * p.sparse_block_size > INT32_MAX / 2) return false;
     if (p.sparse_mode != 0 && p.sparse_mode != 3) return false;
     if (p.dtype != IFA_BF16 && p.dtype != IFA_F16) return false;
     if (!std::isfinite(p.scale_value)) return false;
@@ -130,7 +135,7 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
             !encode(&sp.tmV, bf, value, 2, dk, sk, bg))
             return IFA_ERR_RUNTIME;
     }
-    const int tps = (int)((p.sparse_size + kSfaTile - 1) / kSfaTile);
+    const int tps = (int)((p.sparse_size * p.sparse_block_size + kSfaTile - 1) / kSfaTile);
     const long long W = 2LL * p.B * tps;
     if (W > INT32_MAX) return IFA_ERR_PARAM_INVALID;
     // equal contiguous shares of at least min(tiles per sequence, 4) tiles
@@ -149,6 +154,8 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
     sp.B = (int)p.B;
     sp.QN = (int)p.Q_N;
     sp.S_sp = (int)p.sparse_size;
+    sp.sbs_log2 = 0;
+    while ((1LL << sp.sbs_log2) < p.sparse_block_size) ++sp.sbs_log2;
     sp.tiles_per_seq = tps;
     sp.block_size = (int)p.block_size;
     sp.bt_cols = (int)p.block_table_cols;

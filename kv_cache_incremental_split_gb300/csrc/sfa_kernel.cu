@@ -139,17 +139,28 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         // ================================================================ resolver
         // Three tiles in flight: the indices of tile g+2, the block-table entries and
         // length of tile g+1, and the rows of tile g.
+        // token of position pos (-1 when its index is negative): index pos >> sbs_log2 selects
+        // the tokens index << sbs_log2 .. + (1 << sbs_log2) - 1 (token-wise when sbs_log2 = 0)
+        const int npos = p.S_sp << p.sbs_log2;
+        const int smask = (1 << p.sbs_log2) - 1;
         auto load_idx = [&](long long g, int& i_lo, int& i_hi) {
             i_lo = i_hi = -1;
             if (g >= hi) return;
             const int seq = (int)(g / tps), t = (int)(g % tps);
             const int b = seq >> 1;
-            const int pos = t * kSfaTile + lane;
             const int32_t* row = p.indices + (long long)b * p.S_sp;
-            if (pos < p.S_sp) i_lo = __ldg(row + pos);
-            if (pos + 32 < p.S_sp) i_hi = __ldg(row + pos + 32);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int pos = t * kSfaTile + lane + 32 * u;
+                int tok = -1;
+                if (pos < npos) {
+                    const int idx = __ldg(row + (pos >> p.sbs_log2));
+                    if (idx >= 0 && idx <= (INT32_MAX >> p.sbs_log2)) tok = (idx << p.sbs_log2) + (pos & smask);
+                }
+                (u ? i_hi : i_lo) = tok;
+            }
         };
-        // block-table entry of index idx (read only when it lies inside the table), -1 otherwise
+        // block-table entry of token idx (read only when it lies inside the table), -1 otherwise
         auto load_blk = [&](int b, int idx) -> int {
             if (idx < 0 || idx / p.block_size >= p.bt_cols) return -1;
             return __ldg(p.block_table + (long long)b * p.bt_cols + idx / p.block_size);

@@ -261,12 +261,12 @@ class SparseFlashAttention:
 
     def __init__(self, *, batch: int, num_heads: int, block_size: int, block_num: int, block_table_cols: int,
                  sparse_size: int, dtype: str = "bf16", scale: Optional[float] = None, sparse_mode: int = 0,
-                 device=None):
+                 sparse_block_size: int = 1, device=None):
         import torch
         p = SfaParams()
         p.B, p.Q_N, p.KV_N, p.D, p.Dr = batch, num_heads, 1, 512, 64
         p.block_size, p.block_num, p.block_table_cols = block_size, block_num, block_table_cols
-        p.sparse_size, p.sparse_block_size = sparse_size, 1
+        p.sparse_size, p.sparse_block_size = sparse_size, sparse_block_size
         p.dtype = DTYPES[dtype]
         p.sparse_mode = sparse_mode
         p.scale_value = (1.0 / math.sqrt(576)) if scale is None else float(scale)

@@ -163,7 +163,9 @@ def sfa_params(**kw):
 
 
 SFA_INVALID = [dict(KV_N=2), dict(D=256), dict(Dr=32), dict(Q_N=0), dict(Q_N=129), dict(block_size=24),
-               dict(block_size=2048), dict(sparse_block_size=2), dict(sparse_mode=1), dict(dtype=2),
+               dict(block_size=2048), dict(sparse_block_size=0), dict(sparse_block_size=3),
+               dict(sparse_block_size=256), dict(sparse_block_size=128),  # 128 does not divide block_size 64
+               dict(sparse_size=2**30, sparse_block_size=64), dict(sparse_mode=1), dict(dtype=2),
                dict(sparse_size=0), dict(block_num=0), dict(B=-1), dict(scale_value=float("inf"))]
 
 
@@ -173,7 +175,9 @@ def test_sfa_invalid_descriptions_are_rejected(lib, kw):
     assert st == ifa.IFA_ERR_PARAM_INVALID
 
 
-@pytest.mark.parametrize("kw", [dict(), dict(Q_N=16), dict(sparse_mode=3), dict(dtype=0), dict(block_size=16)])
+@pytest.mark.parametrize("kw", [dict(), dict(Q_N=16), dict(sparse_mode=3), dict(dtype=0), dict(block_size=16),
+                                dict(sparse_block_size=2), dict(sparse_block_size=64),
+                                dict(block_size=128, sparse_block_size=128)])
 def test_sfa_valid_descriptions_pass_validation(lib, kw):
     st, ws = ifa.sfa_workspace_size(sfa_params(**kw))
     assert st in (ifa.IFA_OK, ifa.IFA_ERR_RUNTIME)

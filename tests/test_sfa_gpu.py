@@ -26,7 +26,7 @@ def run_gpu(c, sparse_mode=0):
     op = SparseFlashAttention(batch=c.B, num_heads=c.query.shape[2], block_size=c.key.shape[1],
                               block_num=c.key.shape[0], block_table_cols=c.block_table.shape[1],
                               sparse_size=c.sparse_indices.shape[-1], dtype=c.dtype, scale=c.scale,
-                              sparse_mode=sparse_mode)
+                              sparse_mode=sparse_mode, sparse_block_size=c.sparse_block_size)
     t = [to_device(a) for a in (c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices,
                                 c.block_table, c.actual_seq_lengths_kv)]
     out = op(*t)
@@ -44,7 +44,8 @@ def run_ref(c, batches=None):
         cc.sparse_indices, cc.block_table = c.sparse_indices[bs], c.block_table[bs]
         cc.actual_seq_lengths_kv = c.actual_seq_lengths_kv[bs]
     return oracle.sfa_ref(cc.query, cc.query_rope, cc.key, cc.key_rope, cc.value, cc.sparse_indices,
-                          cc.block_table, cc.actual_seq_lengths_kv, scale=cc.scale)
+                          cc.block_table, cc.actual_seq_lengths_kv, scale=cc.scale,
+                          sparse_block_size=cc.sparse_block_size)
 
 
 def check(c, batches=None, sparse_mode=0):
@@ -140,3 +141,25 @@ def test_sfa_deterministic():
     a, _ = run_gpu(c)
     b, _ = run_gpu(c)
     assert np.array_equal(a, b)
+
+
+# ---- block-wise sparsity (sparse_block_size > 1)
+
+
+@pytest.mark.parametrize("sbs,block_size,sparse_size,nvalid_hi", [(2, 64, 97, 60), (16, 64, 47, 40), (64, 64, 13, 13),
+                                                                   (128, 128, 7, 7)])
+def test_sfa_blockwise_matches_oracle(sbs, block_size, sparse_size, nvalid_hi):
+    """Each index selects sbs consecutive tokens; positions span several tiles and end ragged."""
+    c = gen.sfa_mla(60 + sbs, B=3, Q_N=128, block_size=block_size, kv_len=4096, sparse_size=sparse_size,
+                    nvalid_lo=3, nvalid_hi=nvalid_hi, sparse_block_size=sbs)
+    c.actual_seq_lengths_kv[1] = 4096 - 37  # selected blocks of batch 1 may end past its length
+    check(c)
+
+
+def test_sfa_blockwise_invalid_entries_and_short_rows():
+    c = gen.sfa_mla(70, B=4, Q_N=64, block_size=64, kv_len=2048, sparse_size=40, nvalid_lo=1, nvalid_hi=40,
+                    sparse_block_size=8)
+    c.sparse_indices[2, 0, 0, :] = -1  # nothing selected: zeros
+    c.sparse_indices[3, 0, 0, ::3] = -1  # -1 entries scattered through the row
+    got, _ = check(c)
+    assert np.all(got[2] == 0)
