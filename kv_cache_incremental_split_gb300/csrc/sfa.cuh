@@ -36,6 +36,9 @@ struct alignas(128) SfaParams {
     CUtensorMap tmK;    // 2-D (d, cache row) over key, 64 x 1 boxes (row gathers)
     CUtensorMap tmKr;   // over key_rope
     CUtensorMap tmV;    // over value
+    CUtensorMap tmKb;   // block-wise runs (sparse_block_size >= 8): the same tensors with
+    CUtensorMap tmKrb;  //   64 x min(sparse_block_size, 64) boxes of consecutive rows
+    CUtensorMap tmVb;
     const int32_t* indices;
     const int32_t* block_table;
     const int32_t* lens;

@@ -134,6 +134,13 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
             !encode(&sp.tmK, bf, key, 2, dk, sk, bg) || !encode(&sp.tmKr, bf, key_rope, 2, dkr, skr, bg) ||
             !encode(&sp.tmV, bf, value, 2, dk, sk, bg))
             return IFA_ERR_RUNTIME;
+        if (p.sparse_block_size >= 8) {
+            // a selected block is sparse_block_size consecutive rows of one cache block
+            cuuint32_t bb[2] = {64, (cuuint32_t)std::min<int64_t>(p.sparse_block_size, kSfaTile)};
+            if (!encode(&sp.tmKb, bf, key, 2, dk, sk, bb) || !encode(&sp.tmKrb, bf, key_rope, 2, dkr, skr, bb) ||
+                !encode(&sp.tmVb, bf, value, 2, dk, sk, bb))
+                return IFA_ERR_RUNTIME;
+        }
     }
     const int tps = (int)((p.sparse_size * p.sparse_block_size + kSfaTile - 1) / kSfaTile);
     const long long W = 2LL * p.B * tps;

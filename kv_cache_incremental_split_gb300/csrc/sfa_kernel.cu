@@ -235,6 +235,11 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             prefetch_tensormap(&p.tmK);
             prefetch_tensormap(&p.tmKr);
             prefetch_tensormap(&p.tmV);
+            if (p.sbs_log2 >= 3) {
+                prefetch_tensormap(&p.tmKb);
+                prefetch_tensormap(&p.tmKrb);
+                prefetch_tensormap(&p.tmVb);
+            }
         }
         const uint64_t pol = policy_evict_first();
         long long it = 0;
@@ -244,6 +249,13 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         // Gathers column blocks [blk0, blk0 + nblk) of the rows of resolved tile `rs`
         // (blocks 0..7: key, 8: key rope, 9..12: value half h).
         constexpr int kGroups = 16 / kSfaIssuers;  // gather4 row groups per warp and stage
+        // Block-wise selections of 8 or more tokens are runs of consecutive cache rows: one tiled
+        // box of run_rows rows per run (or per 64-row half of a 128-token run) instead of gathers.
+        const bool runs = p.sbs_log2 >= 3;
+        const int run_rows = runs ? min(1 << p.sbs_log2, kSfaTile) : 0;
+        const int nruns = runs ? kSfaTile / run_rows : 0;  // boxes per stage: 8, 4, 2 or 1
+        int my_runs = 0;                                    // this warp takes runs gi, gi + 4, ...
+        for (int k = gi; k < nruns; k += kSfaIssuers) ++my_runs;
         auto gather = [&](const RSlot* rs, int blk0, int nblk, int h) {
             const int grp = gi * kGroups + lane;
             const int4 r4 = lane < kGroups ? reinterpret_cast<const int4*>(rs->rows)[grp] : make_int4(0, 0, 0, 0);
@@ -255,6 +267,30 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                     *abort_flag = 1;
                     ok = false;
                     return;
+                }
+                if (runs) {
+                    if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)(my_runs * run_rows * 128));
+                    __syncwarp();
+                    const int k = gi + kSfaIssuers * lane;  // run this lane loads
+                    if (lane < my_runs) {
+                        const CUtensorMap* map;
+                        int x;
+                        if (blk < 8) {
+                            map = &p.tmKb;
+                            x = blk * 64;
+                        } else if (blk == 8) {
+                            map = &p.tmKrb;
+                            x = 0;
+                        } else {
+                            map = &p.tmVb;
+                            x = h * kSfaHalf + (blk - kSfaQBlocks) * 64;
+                        }
+                        // the run's first row; an invalid run starts past the last row (zero fill)
+                        tma_load_2d(ring + stage * kSfaStageBytes + k * run_rows * 128, map, &full[stage], x,
+                                    rs->rows[k * run_rows]);
+                    }
+                    __syncwarp();
+                    continue;
                 }
                 if (lane == 0) mbar_arrive_expect_tx(&full[stage], kSfaStageBytes / kSfaIssuers);
                 __syncwarp();

@@ -146,10 +146,11 @@ def test_sfa_deterministic():
 # ---- block-wise sparsity (sparse_block_size > 1)
 
 
-@pytest.mark.parametrize("sbs,block_size,sparse_size,nvalid_hi", [(2, 64, 97, 60), (16, 64, 47, 40), (64, 64, 13, 13),
-                                                                   (128, 128, 7, 7)])
+@pytest.mark.parametrize("sbs,block_size,sparse_size,nvalid_hi", [(2, 64, 97, 60), (8, 64, 61, 50), (16, 64, 47, 40),
+                                                                   (32, 64, 21, 21), (64, 64, 13, 13), (128, 128, 7, 7)])
 def test_sfa_blockwise_matches_oracle(sbs, block_size, sparse_size, nvalid_hi):
-    """Each index selects sbs consecutive tokens; positions span several tiles and end ragged."""
+    """Each index selects sbs consecutive tokens; positions span several tiles and end ragged.  From 8
+    tokens on, runs move as tiled boxes of consecutive rows (8, 4, 2 or 1 per stage), else by gathers."""
     c = gen.sfa_mla(60 + sbs, B=3, Q_N=128, block_size=block_size, kv_len=4096, sparse_size=sparse_size,
                     nvalid_lo=3, nvalid_hi=nvalid_hi, sparse_block_size=sbs)
     c.actual_seq_lengths_kv[1] = 4096 - 37  # selected blocks of batch 1 may end past its length
