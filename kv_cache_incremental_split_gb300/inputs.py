@@ -149,17 +149,19 @@ class IfaCase:
 @dataclass
 class SfaCase:
     name: str
-    query: np.ndarray           # (B, 1, Q_N, D)
-    query_rope: np.ndarray      # (B, 1, Q_N, Dr)
+    query: np.ndarray           # (B, Q_S, Q_N, D)
+    query_rope: np.ndarray      # (B, Q_S, Q_N, Dr)
     key: np.ndarray             # (block_num, block_size, 1, D)
     key_rope: np.ndarray        # (block_num, block_size, 1, Dr)
     value: np.ndarray           # (block_num, block_size, 1, D)
-    sparse_indices: np.ndarray  # (B, 1, 1, sparse_size) int32
+    sparse_indices: np.ndarray  # (B, Q_S, 1, sparse_size) int32
     block_table: np.ndarray     # (B, cols) int32
     actual_seq_lengths_kv: np.ndarray  # (B,) int32
     scale: float
     dtype: str = "bf16"
     sparse_block_size: int = 1  # > 1: each index selects that many consecutive tokens
+    sparse_mode: int = 0        # 3: right-down causal over the Q_S query tokens
+    actual_seq_lengths_query: Optional[np.ndarray] = None  # (B,) int32, None: every query token valid
     meta: Dict[str, Any] = field(default_factory=dict)
 
     @property
@@ -278,23 +280,27 @@ def int8_leftpad(seed: int = 0, B=32, N=64, KV_N=8, D=128, Smax=8192, len_lo=256
 
 
 def sfa_mla(seed: int = 0, B=32, Q_N=128, D=512, Dr=64, block_size=64, kv_len=32768,
-            sparse_size=2048, nvalid_lo=1024, nvalid_hi=2048, dtype="bf16", sparse_block_size=1) -> SfaCase:
-    """Indices are distinct and valid first, then -1; with sparse_block_size > 1 they are
-    block indices below kv_len / sparse_block_size."""
+            sparse_size=2048, nvalid_lo=1024, nvalid_hi=2048, dtype="bf16", sparse_block_size=1, Q_S=1,
+            sparse_mode=0, q_lens=None) -> SfaCase:
+    """Indices of each (batch, query token) row are distinct and valid first, then -1; with
+    sparse_block_size > 1 they are block indices below kv_len / sparse_block_size.  Q_S query
+    tokens per batch (multi-token prediction); q_lens: valid query tokens per batch, or None."""
     rng = np.random.default_rng(seed)
     cols = (kv_len + block_size - 1) // block_size
     block_num = B * cols
     bt = rng.permutation(block_num).astype(np.int32).reshape(B, cols)
-    idx = np.full((B, 1, 1, sparse_size), -1, dtype=np.int32)
+    idx = np.full((B, Q_S, 1, sparse_size), -1, dtype=np.int32)
     n_units = kv_len // sparse_block_size
     for b in range(B):
-        nv = int(rng.integers(nvalid_lo, nvalid_hi + 1))
-        idx[b, 0, 0, :nv] = rng.choice(n_units, size=nv, replace=False).astype(np.int32)
+        for s in range(Q_S):
+            nv = int(rng.integers(nvalid_lo, nvalid_hi + 1))
+            idx[b, s, 0, :nv] = rng.choice(n_units, size=nv, replace=False).astype(np.int32)
     lens = np.full(B, kv_len, dtype=np.int32)
-    return SfaCase("sfa_mla", random_storage(seed, 1, (B, 1, Q_N, D), dtype),
-                   random_storage(seed, 4, (B, 1, Q_N, Dr), dtype),
+    lq = None if q_lens is None else np.asarray(q_lens, dtype=np.int32).reshape(B)
+    return SfaCase("sfa_mla", random_storage(seed, 1, (B, Q_S, Q_N, D), dtype),
+                   random_storage(seed, 4, (B, Q_S, Q_N, Dr), dtype),
                    random_storage(seed, 2, (block_num, block_size, 1, D), dtype),
                    random_storage(seed, 5, (block_num, block_size, 1, Dr), dtype),
                    random_storage(seed, 3, (block_num, block_size, 1, D), dtype),
                    idx, bt, lens, scale=1.0 / math.sqrt(D + Dr), dtype=dtype,
-                   sparse_block_size=sparse_block_size)
+                   sparse_block_size=sparse_block_size, sparse_mode=sparse_mode, actual_seq_lengths_query=lq)

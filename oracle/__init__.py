@@ -62,8 +62,8 @@ def _load():
                                            vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, vp, ip,
                                            vp, vp, dp, vp]
             lib.sfa_oracle_run.restype = ctypes.c_int
-            lib.sfa_oracle_run.argtypes = [i64, i64, i64, i64, ip, i64, i64, i64, i64, i64,
-                                           vp, vp, vp, vp, vp, vp, vp, vp, dp, vp]
+            lib.sfa_oracle_run.argtypes = [i64, i64, i64, i64, i64, ip, i64, i64, i64, i64, i64, i64,
+                                           vp, vp, vp, vp, vp, vp, vp, vp, vp, dp, vp]
             _lib = lib
     return _lib
 
@@ -146,14 +146,14 @@ def ifa_ref(query, key, value, *, num_heads, num_kv_heads=0, scale, layout="BNSD
 
 
 def sfa_ref(query, query_rope, key, key_rope, value, sparse_indices, block_table,
-            actual_seq_lengths_kv, *, scale, sparse_block_size=1):
-    """Reference sparse MLA-absorb decode output, float64 (B, Q_N, D).
+            actual_seq_lengths_kv, *, scale, sparse_block_size=1, sparse_mode=0, actual_seq_lengths_query=None):
+    """Reference sparse MLA-absorb decode output, float64 (B, Q_S, Q_N, D); (B, Q_N, D) when Q_S = 1.
 
-    sparse_block_size > 1: each index selects that many consecutive tokens (block-wise).
-
-    query (B,1,Q_N,D), query_rope (B,1,Q_N,Dr), key/value (block_num, block_size, 1, D),
-    key_rope (block_num, block_size, 1, Dr), sparse_indices (B,1,1,sparse_size) int32,
-    block_table (B, cols) int32, actual_seq_lengths_kv (B,) int32.
+    query (B,Q_S,Q_N,D), query_rope (B,Q_S,Q_N,Dr), key/value (block_num, block_size, 1, D),
+    key_rope (block_num, block_size, 1, Dr), sparse_indices (B,Q_S,1,sparse_size) int32,
+    block_table (B, cols) int32, actual_seq_lengths_kv (B,) int32; sparse_block_size > 1: each
+    index selects that many consecutive tokens (block-wise); sparse_mode 3: right-down causal
+    over the Q_S query tokens; actual_seq_lengths_query (B,) int32 or None.
     """
     lib = _load()
     q = _c(query)
@@ -164,13 +164,15 @@ def sfa_ref(query, query_rope, key, key_rope, value, sparse_indices, block_table
     idx = _c(sparse_indices, np.int32)
     bt = _c(block_table, np.int32)
     lens = _c(actual_seq_lengths_kv, np.int32)
-    B, Q_N, D = q.shape[0], q.shape[2], q.shape[3]
+    lq = None if actual_seq_lengths_query is None else _c(actual_seq_lengths_query, np.int32)
+    B, Q_S, Q_N, D = q.shape[0], q.shape[1], q.shape[2], q.shape[3]
     Dr = qr.shape[3]
     block_num, block_size = k.shape[0], k.shape[1]
-    out = np.zeros((B, Q_N, D), dtype=np.float64)
-    rc = lib.sfa_oracle_run(B, Q_N, D, Dr, _dtype_code(q), block_size, block_num, bt.shape[1],
-                            idx.shape[-1], int(sparse_block_size), _ptr(q), _ptr(qr), _ptr(k), _ptr(kr), _ptr(v),
-                            _ptr(idx), _ptr(bt), _ptr(lens), float(scale), _ptr(out))
+    out = np.zeros((B, Q_S, Q_N, D), dtype=np.float64)
+    rc = lib.sfa_oracle_run(B, Q_S, Q_N, D, Dr, _dtype_code(q), block_size, block_num, bt.shape[1],
+                            idx.shape[-1], int(sparse_block_size), int(sparse_mode), _ptr(q), _ptr(qr), _ptr(k),
+                            _ptr(kr), _ptr(v), _ptr(idx), _ptr(bt), _ptr(lens),
+                            None if lq is None else _ptr(lq), float(scale), _ptr(out))
     if rc < 0:
         raise ValueError("oracle rejected its arguments")
-    return out
+    return out[:, 0] if Q_S == 1 else out

@@ -263,14 +263,21 @@ int ifa_oracle_run(int64_t B, int64_t N, int64_t KV_N, int64_t D, int q_dtype, i
  * the tokens idx_j * sparse_block_size + o, o = 0 .. sparse_block_size - 1 (block-wise:
  * the tokens of a block share the selection); a token at or past actual_seq_lengths_kv[b],
  * or any token of a negative entry, is skipped.
+ * Q_S query tokens per batch (query (B, Q_S, Q_N, D), sparse_indices (B, Q_S, 1, sparse_size),
+ * out (B, Q_S, Q_N, D)): each (b, s) row is its own problem over its own index row.
+ * lens_q (nullable: every row valid) gives the valid query tokens of each batch; rows s at or
+ * past it are all zero.  sparse_mode 3 (README "sparse_mode", rightDownCausal): query token s
+ * sits at key position lens_kv[b] - lens_q[b] + s and selected tokens past it are skipped;
+ * sparse_mode 0 masks nothing.
  * Returns the number of skipped out-of-range block-table entries, -1 on bad arguments.
  */
-int sfa_oracle_run(int64_t B, int64_t Q_N, int64_t D, int64_t Dr, int dtype, int64_t block_size,
+int sfa_oracle_run(int64_t B, int64_t Q_S, int64_t Q_N, int64_t D, int64_t Dr, int dtype, int64_t block_size,
                    int64_t block_num, int64_t bt_cols, int64_t sparse_size, int64_t sparse_block_size,
-                   const void* q, const void* q_rope, const void* k, const void* k_rope, const void* v,
-                   const int32_t* sparse_indices, const int32_t* block_table,
-                   const int32_t* lens_kv, double scale, double* out) {
-    if (B < 0 || Q_N <= 0 || D <= 0 || Dr < 0 || block_size <= 0 || sparse_size <= 0 || sparse_block_size <= 0)
+                   int64_t sparse_mode, const void* q, const void* q_rope, const void* k, const void* k_rope,
+                   const void* v, const int32_t* sparse_indices, const int32_t* block_table,
+                   const int32_t* lens_kv, const int32_t* lens_q, double scale, double* out) {
+    if (B < 0 || Q_S <= 0 || Q_N <= 0 || D <= 0 || Dr < 0 || block_size <= 0 || sparse_size <= 0 ||
+        sparse_block_size <= 0 || (sparse_mode != 0 && sparse_mode != 3))
         return -1;
     int bad = 0;
     const int64_t npos = sparse_size * sparse_block_size; /* selected token positions per row */
@@ -281,14 +288,20 @@ int sfa_oracle_run(int64_t B, int64_t Q_N, int64_t D, int64_t Dr, int dtype, int
         free(row);
         return -1;
     }
-    for (int64_t b = 0; b < B; b++) {
-        /* resolve the selected rows once per batch: physical row = blk * block_size + slot */
+    for (int64_t bs_row = 0; bs_row < B * Q_S; bs_row++) {
+        const int64_t b = bs_row / Q_S, sq = bs_row % Q_S;
+        const int64_t qlen = lens_q ? lens_q[b] : Q_S;
+        /* keys this query row may use: [0, limit) */
+        int64_t limit = lens_kv[b];
+        if (sq >= qlen) limit = 0;
+        else if (sparse_mode == 3) limit = lens_kv[b] - qlen + sq + 1;
+        /* resolve the selected rows once per query row: physical row = blk * block_size + slot */
         for (int64_t j = 0; j < npos; j++) {
-            int64_t idx = sparse_indices[b * sparse_size + j / sparse_block_size];
+            int64_t idx = sparse_indices[bs_row * sparse_size + j / sparse_block_size];
             row[j] = -1;
             if (idx < 0) continue;
             int64_t tok = idx * sparse_block_size + j % sparse_block_size;
-            if (tok >= lens_kv[b]) continue;
+            if (tok >= lens_kv[b] || tok >= limit) continue;
             int64_t blk = block_table[b * bt_cols + tok / block_size];
             if (blk < 0 || blk >= block_num) {
                 bad++;
@@ -297,7 +310,7 @@ int sfa_oracle_run(int64_t B, int64_t Q_N, int64_t D, int64_t Dr, int dtype, int
             row[j] = blk * block_size + tok % block_size;
         }
         for (int64_t n = 0; n < Q_N; n++) {
-            double* o = out + (b * Q_N + n) * D;
+            double* o = out + (bs_row * Q_N + n) * D;
             for (int64_t d = 0; d < D; d++) o[d] = 0.0;
             double smax = -INFINITY;
             int any = 0;
@@ -305,9 +318,9 @@ int sfa_oracle_run(int64_t B, int64_t Q_N, int64_t D, int64_t Dr, int dtype, int
                 if (row[j] < 0) continue;
                 double dot = 0.0;
                 for (int64_t d = 0; d < D; d++)
-                    dot += load_value(q, (b * Q_N + n) * D + d, dtype) * load_value(k, row[j] * D + d, dtype);
+                    dot += load_value(q, (bs_row * Q_N + n) * D + d, dtype) * load_value(k, row[j] * D + d, dtype);
                 for (int64_t d = 0; d < Dr; d++)
-                    dot += load_value(q_rope, (b * Q_N + n) * Dr + d, dtype) *
+                    dot += load_value(q_rope, (bs_row * Q_N + n) * Dr + d, dtype) *
                            load_value(k_rope, row[j] * Dr + d, dtype);
                 s[j] = scale * dot;
                 if (s[j] > smax) smax = s[j];

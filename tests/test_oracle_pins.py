@@ -528,3 +528,98 @@ def test_sfa_blockwise_equals_tokenwise_on_expanded_indices(sbs):
     got = sref_block(c, sbs, sparse_indices=blk, actual_seq_lengths_kv=lens)
     want = sref_block(c, 1, sparse_indices=tok, actual_seq_lengths_kv=lens)
     assert np.array_equal(got, want)
+
+
+# ------------------------------------------- multi-token queries and the right-down causal mode
+
+def _sfa_mtp(seed, Q_S, **kw):
+    base = dict(B=2, Q_N=4, D=32, Dr=8, block_size=16, kv_len=64, sparse_size=16, nvalid_lo=4,
+                nvalid_hi=16, Q_S=Q_S)
+    base.update(kw)
+    return gen.sfa_mla(seed, **base)
+
+
+def _token_codes(c, kv_len=64, bs=16):
+    codes = np.zeros(c.value.shape, dtype=np.float32)
+    for b in range(c.B):
+        for t in range(kv_len):
+            codes[c.block_table[b, t // bs], t % bs, 0, :] = t
+    return gen.to_storage(codes, "bf16")
+
+
+def test_sfa_multi_token_rows_match_torch_mla_per_row():
+    """Q_S = 3, sparse_mode 0: query token s of batch b attends over its own index row
+    (b, s) with its own query; each row is checked against the dense library attention."""
+    c = _sfa_mtp(40, 3)
+    out = oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
+                         c.actual_seq_lengths_kv, scale=c.scale)
+    assert out.shape == (2, 3, 4, 32)
+    q = as_f64(c.query, "bf16")
+    qr = as_f64(c.query_rope, "bf16")
+    k = as_f64(c.key, "bf16").reshape(-1, 32)
+    kr = as_f64(c.key_rope, "bf16").reshape(-1, 8)
+    v = as_f64(c.value, "bf16").reshape(-1, 32)
+    for b in range(2):
+        for s in range(3):
+            sel = [i for i in c.sparse_indices[b, s, 0] if i >= 0]
+            rows = _rows(c, b, sel)
+            for n in range(4):
+                ref = torch_attention(np.concatenate([q[b, s, n], qr[b, s, n]]),
+                                      np.concatenate([k[rows], kr[rows]], axis=1), v[rows], c.scale)
+                np.testing.assert_allclose(out[b, s, n], ref, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("sbs", [1, 4])
+def test_sfa_right_down_causal_exact_means(sbs):
+    """sparse_mode 3 (rightDownCausal) with Q = 0, value row = token index and every token
+    selected: with len keys and qlen valid query tokens, query token s < qlen averages tokens
+    0 .. len - qlen + s exactly, i.e. (len - qlen + s) / 2; tokens s >= qlen give zero rows;
+    sparse_mode 0 averages every token below len for each valid row."""
+    Q_S = 4
+    c = _sfa_mtp(41, Q_S)
+    c.query[:] = 0
+    c.query_rope[:] = 0
+    c.value = _token_codes(c)
+    idx = np.full((2, Q_S, 1, 64), -1, dtype=np.int32)
+    idx[:, :, 0, :64 // sbs] = np.arange(64 // sbs, dtype=np.int32)
+    lens = np.array([64, 50], dtype=np.int32)
+    for lq in (None, np.array([4, 2], dtype=np.int32), np.array([0, 1], dtype=np.int32)):
+        qlen = np.full(2, Q_S) if lq is None else lq
+        for mode in (0, 3):
+            out = oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, idx, c.block_table, lens,
+                                 scale=c.scale, sparse_block_size=sbs, sparse_mode=mode,
+                                 actual_seq_lengths_query=lq)
+            for b in range(2):
+                for s in range(Q_S):
+                    if s >= qlen[b]:
+                        assert np.all(out[b, s] == 0.0), (b, s, mode)
+                        continue
+                    last = lens[b] - qlen[b] + s if mode == 3 else lens[b] - 1
+                    assert np.all(out[b, s] == last / 2.0), (b, s, mode, lq)
+
+
+def test_sfa_causal_mode_equals_explicit_index_pruning():
+    """Under sparse_mode 3 a selected token past a query token's causal position counts for
+    nothing: the output equals sparse_mode 0 on indices with those entries set to -1."""
+    Q_S = 3
+    c = _sfa_mtp(42, Q_S, nvalid_lo=16, nvalid_hi=16)
+    lens = np.array([60, 64], dtype=np.int32)
+    lq = np.array([3, 2], dtype=np.int32)
+    # make sure the last tokens are selected somewhere in every row
+    c.sparse_indices[:, :, 0, :3] = np.array([lens.min() - 1, lens.min() - 2, lens.min() - 3])[None, None]
+    c.sparse_indices[1, :, 0, 3:6] = np.array([63, 62, 61])
+    causal = oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
+                            lens, scale=c.scale, sparse_mode=3, actual_seq_lengths_query=lq)
+    pruned = c.sparse_indices.copy()
+    for b in range(2):
+        for s in range(Q_S):
+            row = pruned[b, s, 0]
+            row[row > lens[b] - lq[b] + s] = -1
+    plain = oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, pruned, c.block_table, lens,
+                           scale=c.scale, sparse_mode=0, actual_seq_lengths_query=lq)
+    assert np.array_equal(causal, plain)
+    assert np.all(causal[1, 2] == 0.0)
+    # something was pruned, so the modes differ on at least one valid row
+    full = oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
+                          lens, scale=c.scale, sparse_mode=0, actual_seq_lengths_query=lq)
+    assert not np.array_equal(full[0, 0], causal[0, 0])
