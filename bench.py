@@ -54,6 +54,9 @@ WORKLOADS = {
                       "KV length 8192, 2048 indices with U{1024..2048} valid"),
     "sfa_mla_blockwise": ("sparse MLA-absorb decode, block-wise: B=32 Q_N=128 D=512+64 bf16, PA_BSND block 64, "
                           "KV length 32768, sparse_block_size 16, 128 block indices with U{64..128} valid then -1"),
+    "sfa_mla_mtp": ("sparse MLA-absorb decode, two query tokens (multi-token prediction): B=32 Q_S=2 Q_N=128 "
+                    "D=512+64 bf16, PA_BSND block 64, KV length 32768, sparse_mode 3 (right-down causal), "
+                    "sparse_indices (B,2,1,2048) with U{1024..2048} valid per row then -1"),
 }
 
 
@@ -66,6 +69,8 @@ def make_case(name: str, seed: int):
         return gen.sfa_mla(seed, B=8, kv_len=8192)
     if name == "sfa_mla_blockwise":
         return gen.sfa_mla(seed, sparse_size=128, nvalid_lo=64, nvalid_hi=128, sparse_block_size=16)
+    if name == "sfa_mla_mtp":
+        return gen.sfa_mla(seed, Q_S=2, sparse_mode=3)
     return {"gqa_padded": gen.gqa_padded, "tiny_mha": gen.tiny_mha, "paged_gqa": gen.paged_gqa,
             "int8_leftpad": gen.int8_leftpad}[name](seed)
 
@@ -90,12 +95,21 @@ def windows(case: gen.IfaCase):
 
 
 def sfa_valid_counts(case: gen.SfaCase):
-    """Selected tokens per batch row: each index covers sparse_block_size tokens, those below the length count."""
+    """Selected tokens per (batch, query token) row, shape (B * Q_S,): each index covers
+    sparse_block_size tokens; those below the row's key limit count (the length, cut to
+    len - qlen + s + 1 under sparse_mode 3, none for query tokens at or past qlen)."""
     sbs = case.sparse_block_size
-    idx = case.sparse_indices.reshape(case.B, -1).astype(np.int64)
-    lens = case.actual_seq_lengths_kv.reshape(-1, 1, 1).astype(np.int64)
-    tok = idx[:, :, None] * sbs + np.arange(sbs)[None, None, :]
-    return ((idx[:, :, None] >= 0) & (tok < lens)).reshape(case.B, -1).sum(axis=1)
+    B, Q_S = case.query.shape[0], case.query.shape[1]
+    idx = case.sparse_indices.reshape(B, Q_S, -1).astype(np.int64)
+    lens = case.actual_seq_lengths_kv.astype(np.int64).reshape(B, 1)
+    qlen = (np.full((B, 1), Q_S, dtype=np.int64) if case.actual_seq_lengths_query is None
+            else case.actual_seq_lengths_query.astype(np.int64).reshape(B, 1))
+    s = np.arange(Q_S, dtype=np.int64)[None, :]
+    limit = lens - qlen + s + 1 if case.sparse_mode == 3 else np.broadcast_to(lens, (B, Q_S))
+    limit = np.where(s < qlen, limit, 0)
+    tok = idx[..., None] * sbs + np.arange(sbs)
+    ok = (idx[..., None] >= 0) & (tok < limit[:, :, None, None])
+    return ok.reshape(B * Q_S, -1).sum(axis=1)
 
 
 def algorithmic_bytes(case) -> int:
@@ -103,8 +117,9 @@ def algorithmic_bytes(case) -> int:
         n = int(sfa_valid_counts(case).sum())
         QN = case.query.shape[2]
         total = n * (512 + 64 + 512) * 2                       # key, key_rope and value rows of selected tokens
-        total += case.B * QN * (512 + 64) * 2                  # query and query_rope
-        total += case.B * QN * 512 * 2                         # output
+        rows = case.B * case.query.shape[1]                    # (batch, query token) rows
+        total += rows * QN * (512 + 64) * 2                    # query and query_rope
+        total += rows * QN * 512 * 2                           # output
         total += case.sparse_indices.nbytes + n * 4            # indices and block-table entries used
         return int(total)
     kv_es = 1 if case.kv_dtype == "int8" else 2
@@ -261,6 +276,8 @@ def _batch_subset(case, b):
         c.query, c.query_rope = case.query[sel], case.query_rope[sel]
         c.sparse_indices, c.block_table = case.sparse_indices[sel], case.block_table[sel]
         c.actual_seq_lengths_kv = case.actual_seq_lengths_kv[sel]
+        if case.actual_seq_lengths_query is not None:
+            c.actual_seq_lengths_query = case.actual_seq_lengths_query[sel]
         return c
     c.query = case.query[sel]
     if case.kv_format == "contig":
@@ -288,7 +305,8 @@ def oracle_sample(case, budget_s: float, start_batch: int = 0):
         t = time.perf_counter()
         if isinstance(c, gen.SfaCase):
             oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
-                           c.actual_seq_lengths_kv, scale=c.scale, sparse_block_size=c.sparse_block_size)
+                           c.actual_seq_lengths_kv, scale=c.scale, sparse_block_size=c.sparse_block_size,
+                           sparse_mode=c.sparse_mode, actual_seq_lengths_query=c.actual_seq_lengths_query)
         else:
             oracle.ifa_ref(c.query, c.key, c.value, num_heads=c.num_heads, num_kv_heads=c.num_kv_heads,
                            scale=c.scale, layout=c.layout, kv_format=fmt[c.kv_format], block_size=c.block_size,
@@ -401,10 +419,12 @@ class SfaWorkload:
         self.op = SparseFlashAttention(batch=case.B, num_heads=case.query.shape[2], block_size=case.key.shape[1],
                                        block_num=case.key.shape[0], block_table_cols=case.block_table.shape[1],
                                        sparse_size=case.sparse_indices.shape[-1], dtype=case.dtype,
-                                       scale=case.scale, sparse_block_size=case.sparse_block_size, device=dev)
+                                       scale=case.scale, sparse_block_size=case.sparse_block_size,
+                                       sparse_mode=case.sparse_mode, q_seq_len=case.query.shape[1], device=dev)
         self.q, self.qr = _to_dev(case.query, dev), _to_dev(case.query_rope, dev)
         self.idx, self.bt = _to_dev(case.sparse_indices, dev), _to_dev(case.block_table, dev)
         self.lens = _to_dev(case.actual_seq_lengths_kv, dev)
+        self.lq = None if case.actual_seq_lengths_query is None else _to_dev(case.actual_seq_lengths_query, dev)
         k, kr, v = _to_dev(case.key, dev), _to_dev(case.key_rope, dev), _to_dev(case.value, dev)
         self.copies = copies_for
         self.rotating_bytes = sum(t.numel() * t.element_size() for t in (k, kr, v))
@@ -416,7 +436,8 @@ class SfaWorkload:
 
     def call(self, i, stream):
         k, kr, v = self.caches[i]
-        return self.op(self.q, self.qr, k, kr, v, self.idx, self.bt, self.lens, out=self.outs[i], stream=stream)
+        return self.op(self.q, self.qr, k, kr, v, self.idx, self.bt, self.lens, actual_seq_lengths_query=self.lq,
+                       out=self.outs[i], stream=stream)
 
     def launches_per_call(self):
         return 2  # decode kernel + combine kernel
@@ -424,10 +445,12 @@ class SfaWorkload:
     def host_inputs(self):
         c = self.case
         return {"q": c.query, "qr": c.query_rope, "k": c.key, "kr": c.key_rope, "v": c.value,
-                "idx": c.sparse_indices, "bt": c.block_table, "lens": c.actual_seq_lengths_kv}
+                "idx": c.sparse_indices, "bt": c.block_table, "lens": c.actual_seq_lengths_kv,
+                **({} if c.actual_seq_lengths_query is None else {"lq": c.actual_seq_lengths_query})}
 
     def call_on(self, d, stream):
-        return self.op(d["q"], d["qr"], d["k"], d["kr"], d["v"], d["idx"], d["bt"], d["lens"], stream=stream)
+        return self.op(d["q"], d["qr"], d["k"], d["kr"], d["v"], d["idx"], d["bt"], d["lens"],
+                       actual_seq_lengths_query=d.get("lq"), stream=stream)
 
 
 def run_gpu(args):

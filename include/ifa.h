@@ -207,19 +207,24 @@ int64_t ifa_last_launch_count(const ifa_plan* plan);
  *
  *     out[b, n, :] = softmax_j( scale_value * (q[b,n] . k[i_j] + q_rope[b,n] . k_rope[i_j]) ) . v[i_j]
  *
- * over the selected tokens i_j with 0 <= i_j < actual_seq_lengths_kv[b] (tokens outside that
+ * for every query token s of batch b (the line holds with q[b,s,n], i_j from row (b, s) and
+ * out[b,s,n]), over the selected tokens i_j with 0 <= i_j < limit(b, s) (tokens outside that
  * range, e.g. from the -1 tail, are skipped wherever they sit; duplicates count once per
  * occurrence; an empty selection gives an all-zero row).  Token-wise (sparse_block_size 1):
- * i_j = sparse_indices[b, 0, 0, j].  Block-wise (sparse_block_size = s > 1, README
- * "sparse_block_size"): entry j selects the s tokens sparse_indices[b, 0, 0, j] * s + o,
- * o = 0 .. s - 1.  Token i lives in block block_table[b][i / block_size], slot
- * i % block_size of the PA_BSND caches.  Only the layouts and modes the README lists for
- * this decode case are accepted: query layout BSND with Q_S = 1, key/value layout PA_BSND,
- * KV_N = 1, D = 512, Dr = 64, attention_mode 2 (MLA-absorb), sparse_mode 0 or 3 (identical
- * for Q_S = 1), Q_N in 1..128.
+ * i_j = sparse_indices[b, s, 0, j].  Block-wise (sparse_block_size = t > 1, README
+ * "sparse_block_size"): entry j selects the t tokens sparse_indices[b, s, 0, j] * t + o,
+ * o = 0 .. t - 1.  Token i lives in block block_table[b][i / block_size], slot
+ * i % block_size of the PA_BSND caches.  With len = actual_seq_lengths_kv[b] and
+ * qlen = actual_seq_lengths_query[b] (Q_S when that array is NULL; README: 0 <= qlen <= Q_S):
+ * limit(b, s) = 0 for s >= qlen (an all-zero row); otherwise len under sparse_mode 0, and
+ * len - qlen + s + 1 under sparse_mode 3 (rightDownCausal: the last valid query token is
+ * aligned with the last key).  Only the layouts and modes the README lists for this case are
+ * accepted: query layout BSND, key/value layout PA_BSND, KV_N = 1, D = 512, Dr = 64,
+ * attention_mode 2 (MLA-absorb), sparse_mode 0 or 3, Q_N in 1..128.
  */
 typedef struct sfa_params {
     int64_t B;               /* batch, 1..65536 */
+    int64_t Q_S;             /* query tokens per batch, 1..1024, B * Q_S <= 2^20 */
     int64_t Q_N;             /* query heads, 1..128 */
     int64_t KV_N;            /* must be 1 */
     int64_t D;               /* 512: head dim of query, key and value */
@@ -227,7 +232,7 @@ typedef struct sfa_params {
     int64_t block_size;      /* tokens per cache block: a multiple of 16, <= 1024 */
     int64_t block_num;       /* blocks in the caches */
     int64_t block_table_cols;/* second dimension of block_table */
-    int64_t sparse_size;     /* indices per batch row, >= 1 */
+    int64_t sparse_size;     /* indices per query row, >= 1 */
     int64_t sparse_block_size; /* 1 (token-wise) or a power of two <= 128 dividing block_size */
     int32_t dtype;           /* IFA_BF16 or IFA_F16, shared by every tensor and the output */
     int32_t sparse_mode;     /* 0 or 3 */
@@ -241,10 +246,11 @@ ifa_status sfa_workspace_size(const sfa_params* params, size_t* workspace_bytes)
 /*
  * Enqueue one sparse decode call on `stream` (cudaStream_t, NULL = legacy default).
  * Device pointers, 16-byte aligned unless noted:
- *   query (B,1,Q_N,D), query_rope (B,1,Q_N,Dr), key and value (block_num, block_size, 1, D),
- *   key_rope (block_num, block_size, 1, Dr), attention_out (B,1,Q_N,D), all of `dtype`;
- *   sparse_indices int32 (B,1,1,sparse_size), block_table int32 (B, block_table_cols),
- *   actual_seq_lengths_kv int32 (B) (4-byte aligned); workspace of at least
+ *   query (B,Q_S,Q_N,D), query_rope (B,Q_S,Q_N,Dr), key and value (block_num, block_size, 1, D),
+ *   key_rope (block_num, block_size, 1, Dr), attention_out (B,Q_S,Q_N,D), all of `dtype`;
+ *   sparse_indices int32 (B,Q_S,1,sparse_size), block_table int32 (B, block_table_cols),
+ *   actual_seq_lengths_kv int32 (B) and actual_seq_lengths_query int32 (B, nullable)
+ *   (4-byte aligned); workspace of at least
  *   sfa_workspace_size bytes; deviceErrorFlags (int32, nullable) receives device error
  *   bits (1: a needed block_table entry outside [0, block_num); 2: a wait timed out).
  * `value` may alias `key`.  Calls that share a workspace must not overlap on the GPU.
@@ -253,8 +259,9 @@ ifa_status sfa_workspace_size(const sfa_params* params, size_t* workspace_bytes)
  */
 ifa_status sfa_run(const sfa_params* params, const void* query, const void* query_rope, const void* key,
                    const void* key_rope, const void* value, const int32_t* sparse_indices,
-                   const int32_t* block_table, const int32_t* actual_seq_lengths_kv, void* attention_out,
-                   void* workspace, size_t workspace_bytes, int32_t* deviceErrorFlags, void* stream);
+                   const int32_t* block_table, const int32_t* actual_seq_lengths_kv,
+                   const int32_t* actual_seq_lengths_query, void* attention_out, void* workspace,
+                   size_t workspace_bytes, int32_t* deviceErrorFlags, void* stream);
 
 /* Static text for a status code. */
 const char* ifa_status_string(ifa_status status);

@@ -31,7 +31,7 @@ constexpr float kSfaRescaleSlack = 8.0f;    // log2 units the running max may tr
 constexpr int kSfaCombineRows = 16;         // query heads per combine CTA
 
 struct alignas(128) SfaParams {
-    CUtensorMap tmQ;    // 3-D (d, head, batch) over query, 64 x 128 x 1 boxes
+    CUtensorMap tmQ;    // 3-D (d, head, query row) over query, 64 x 128 x 1 boxes
     CUtensorMap tmQr;   // same over query_rope
     CUtensorMap tmK;    // 2-D (d, cache row) over key, 64 x 1 boxes (row gathers)
     CUtensorMap tmKr;   // over key_rope
@@ -42,12 +42,15 @@ struct alignas(128) SfaParams {
     const int32_t* indices;
     const int32_t* block_table;
     const int32_t* lens;
+    const int32_t* lens_q;  // valid query tokens per batch (nullable: all Q_S)
     void* out;
     float* partials;
     int* err;
-    long long W;        // tiles: 2 * B * tiles_per_seq
+    long long W;        // tiles: 2 * R * tiles_per_seq
     int P;
-    int B, QN, S_sp, tiles_per_seq;  // S_sp: indices per row; tiles cover S_sp << sbs_log2 positions
+    int R, QS, QN, S_sp, tiles_per_seq;  // R = B * QS query rows (row r: batch r / QS, query token r % QS);
+                                         // S_sp: indices per row; tiles cover S_sp << sbs_log2 positions
+    int causal;                      // sparse_mode 3: query token s of a batch sees keys up to len - qlen + s
     int sbs_log2;                    // log2(sparse_block_size): position p reads index p >> sbs_log2
     int block_size, bt_cols, block_num, total_rows;
     int is_bf16;

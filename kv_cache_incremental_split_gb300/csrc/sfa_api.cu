@@ -1,8 +1,8 @@
 // C ABI of the sparse MLA-absorb decode (sfa_workspace_size, sfa_run).  The
 // checks follow the "SparseFlashAttention" README's 参数说明 and 约束说明 for
-// the decode case this library implements (Q_S = 1, BSND query, PA_BSND
-// key/value, KV_N = 1, D = 512, Dr = 64, token-wise or block-wise sparsity,
-// MLA-absorb).
+// the decode case this library implements (BSND query with Q_S query tokens,
+// PA_BSND key/value, KV_N = 1, D = 512, Dr = 64, token-wise or block-wise
+// sparsity, sparse_mode 0 or 3, MLA-absorb).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -21,6 +21,7 @@ namespace {
 
 bool sfa_valid(const sfa_params& p) {
     if (p.B < 0 || p.B > 65536) return false;
+    if (p.Q_S < 1 || p.Q_S > 1024 || p.B * p.Q_S > (1 << 20)) return false;
     if (p.Q_N < 1 || p.Q_N > 128) return false;
     if (p.KV_N != 1 || p.D != kSfaD || p.Dr != kSfaDr) return false;
     if (p.block_size < 16 || p.block_size > 1024 || p.block_size % 16 != 0) return false;
@@ -93,8 +94,9 @@ extern "C" ifa_status sfa_workspace_size(const sfa_params* params, size_t* works
 
 extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const void* query_rope, const void* key,
                               const void* key_rope, const void* value, const int32_t* sparse_indices,
-                              const int32_t* block_table, const int32_t* actual_seq_lengths_kv, void* attention_out,
-                              void* workspace, size_t workspace_bytes, int32_t* deviceErrorFlags, void* stream) {
+                              const int32_t* block_table, const int32_t* actual_seq_lengths_kv,
+                              const int32_t* actual_seq_lengths_query, void* attention_out, void* workspace,
+                              size_t workspace_bytes, int32_t* deviceErrorFlags, void* stream) {
     if (!params) return IFA_ERR_PARAM_NULLPTR;
     const sfa_params& p = *params;
     if (!sfa_valid(p)) return IFA_ERR_PARAM_INVALID;
@@ -105,6 +107,7 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
         !aligned(value, 16) || !aligned(attention_out, 16) || !aligned(workspace, 16) ||
         !aligned(sparse_indices, 4) || !aligned(block_table, 4) || !aligned(actual_seq_lengths_kv, 4))
         return IFA_ERR_PARAM_INVALID;
+    if (actual_seq_lengths_query && !aligned(actual_seq_lengths_query, 4)) return IFA_ERR_PARAM_INVALID;
     if (deviceErrorFlags && !aligned(deviceErrorFlags, 4)) return IFA_ERR_PARAM_INVALID;
     size_t need = 0;
     const ifa_status st = sfa_workspace_size(&p, &need);
@@ -118,12 +121,13 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
     std::memset(&sp, 0, sizeof(sp));
     const bool bf = p.dtype == IFA_BF16;
     const uint64_t es = 2;
+    const int64_t R = p.B * p.Q_S;  // query rows: (batch, query token) pairs, each its own problem
     const uint64_t rows = (uint64_t)(p.block_num * p.block_size);
     {
-        cuuint64_t dq[3] = {(cuuint64_t)kSfaD, (cuuint64_t)p.Q_N, (cuuint64_t)p.B};
+        cuuint64_t dq[3] = {(cuuint64_t)kSfaD, (cuuint64_t)p.Q_N, (cuuint64_t)R};
         cuuint64_t sq[2] = {kSfaD * es, (cuuint64_t)p.Q_N * kSfaD * es};
         cuuint32_t bq[3] = {64, 128, 1};
-        cuuint64_t dr[3] = {(cuuint64_t)kSfaDr, (cuuint64_t)p.Q_N, (cuuint64_t)p.B};
+        cuuint64_t dr[3] = {(cuuint64_t)kSfaDr, (cuuint64_t)p.Q_N, (cuuint64_t)R};
         cuuint64_t sr[2] = {kSfaDr * es, (cuuint64_t)p.Q_N * kSfaDr * es};
         cuuint64_t dk[2] = {(cuuint64_t)kSfaD, rows};
         cuuint64_t sk[1] = {kSfaD * es};
@@ -143,7 +147,7 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
         }
     }
     const int tps = (int)((p.sparse_size * p.sparse_block_size + kSfaTile - 1) / kSfaTile);
-    const long long W = 2LL * p.B * tps;
+    const long long W = 2LL * R * tps;
     if (W > INT32_MAX) return IFA_ERR_PARAM_INVALID;
     // equal contiguous shares of at least min(tiles per sequence, 4) tiles
     const long long min_share = std::max(1, std::min(tps, kMinPieceTiles));
@@ -153,12 +157,15 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
     sp.indices = sparse_indices;
     sp.block_table = block_table;
     sp.lens = actual_seq_lengths_kv;
+    sp.lens_q = actual_seq_lengths_query;
     sp.out = attention_out;
     sp.partials = reinterpret_cast<float*>(ws + kSfaPartialOffset);
     sp.err = deviceErrorFlags ? deviceErrorFlags : reinterpret_cast<int*>(ws);
     sp.W = W;
     sp.P = P;
-    sp.B = (int)p.B;
+    sp.R = (int)R;
+    sp.QS = (int)p.Q_S;
+    sp.causal = p.sparse_mode == 3;
     sp.QN = (int)p.Q_N;
     sp.S_sp = (int)p.sparse_size;
     sp.sbs_log2 = 0;

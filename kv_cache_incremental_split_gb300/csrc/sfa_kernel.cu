@@ -160,16 +160,29 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 (u ? i_hi : i_lo) = tok;
             }
         };
-        // block-table entry of token idx (read only when it lies inside the table), -1 otherwise
+        // block-table entry of token idx of batch b (read only when it lies inside the table), -1 otherwise
         auto load_blk = [&](int b, int idx) -> int {
             if (idx < 0 || idx / p.block_size >= p.bt_cols) return -1;
             return __ldg(p.block_table + (long long)b * p.bt_cols + idx / p.block_size);
         };
+        // keys query row r may use: [0, limit).  Rows past the batch's valid query tokens use
+        // none; under the right-down causal mode token s sits at key len - qlen + s.
+        auto row_limit = [&](int b, int r) -> int {
+            const int len = __ldg(p.lens + b);
+            if (p.QS == 1 && !p.lens_q) return len;
+            const int s = r - b * p.QS;
+            const int qlen = p.lens_q ? __ldg(p.lens_q + b) : p.QS;
+            if (s >= qlen) return 0;
+            if (!p.causal) return len;
+            const long long lim = (long long)len - qlen + s + 1;  // <= len since s < qlen
+            return lim < 0 ? 0 : (int)lim;
+        };
         int i0lo, i0hi, i1lo, i1hi;
         load_idx(lo, i0lo, i0hi);
         load_idx(lo + 1, i1lo, i1hi);
-        int b0 = (int)(lo / tps) >> 1;
-        int len0 = __ldg(p.lens + b0);
+        int r0 = (int)(lo / tps) >> 1;
+        int b0 = r0 / p.QS;
+        int len0 = row_limit(b0, r0);
         int bt0lo = load_blk(b0, i0lo), bt0hi = load_blk(b0, i0hi);
         long long k = 0;
         for (long long g = lo; g < hi; ++g, ++k) {
@@ -177,12 +190,13 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             load_idx(g + 2, i2lo, i2hi);
             int b1 = 0, len1 = 0, bt1lo = -1, bt1hi = -1;
             if (g + 1 < hi) {
-                b1 = (int)((g + 1) / tps) >> 1;
-                len1 = __ldg(p.lens + b1);
+                const int r1 = (int)((g + 1) / tps) >> 1;
+                b1 = r1 / p.QS;
+                len1 = row_limit(b1, r1);
                 bt1lo = load_blk(b1, i1lo);
                 bt1hi = load_blk(b1, i1hi);
             }
-            // rows of tile g: invalid (total_rows) outside [0, len); bad block-table entries are flagged
+            // rows of tile g: invalid (total_rows) outside [0, limit); bad block-table entries are flagged
             int rows2[2];
             bool bad = false;
 #pragma unroll
@@ -624,7 +638,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
     if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-// Merges the pieces of every sequence that CTA boundaries cut: grid (2B sequences,
+// Merges the pieces of every sequence that CTA boundaries cut: grid (2R sequences,
 // 128 / kSfaCombineRows), 128 threads; thread = (head row, 32 channels).  Piece k
 // weighs L_k 2^(M_k - M) / sum_j L_j 2^(M_j - M) with M the largest M_k.
 __global__ void __launch_bounds__(128) sfa_combine(const __grid_constant__ SfaParams p) {
@@ -690,7 +704,7 @@ cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream) {
     sfa_kernel<<<p.P, kSfaThreads, kSfaSmem, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    sfa_combine<<<dim3(2 * p.B, 128 / kSfaCombineRows), 128, 0, stream>>>(p);
+    sfa_combine<<<dim3(2 * p.R, 128 / kSfaCombineRows), 128, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

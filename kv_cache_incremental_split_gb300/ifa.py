@@ -56,7 +56,7 @@ class IfaParams(ctypes.Structure):
 
 class SfaParams(ctypes.Structure):
     _fields_ = [
-        ("B", ctypes.c_int64), ("Q_N", ctypes.c_int64), ("KV_N", ctypes.c_int64), ("D", ctypes.c_int64),
+        ("B", ctypes.c_int64), ("Q_S", ctypes.c_int64), ("Q_N", ctypes.c_int64), ("KV_N", ctypes.c_int64), ("D", ctypes.c_int64),
         ("Dr", ctypes.c_int64), ("block_size", ctypes.c_int64), ("block_num", ctypes.c_int64),
         ("block_table_cols", ctypes.c_int64), ("sparse_size", ctypes.c_int64),
         ("sparse_block_size", ctypes.c_int64), ("dtype", ctypes.c_int32), ("sparse_mode", ctypes.c_int32),
@@ -99,7 +99,8 @@ def load_library():
             lib.sfa_workspace_size.restype = ctypes.c_int32
             lib.sfa_workspace_size.argtypes = [ctypes.POINTER(SfaParams), ctypes.POINTER(sz)]
             lib.sfa_run.restype = ctypes.c_int32
-            lib.sfa_run.argtypes = [ctypes.POINTER(SfaParams), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+            lib.sfa_run.argtypes = [ctypes.POINTER(SfaParams), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp,
+                                    vp]
             lib.ifa_status_string.restype = ctypes.c_char_p
             lib.ifa_status_string.argtypes = [ctypes.c_int32]
             _lib = lib
@@ -244,11 +245,12 @@ def sfa_workspace_size(params: SfaParams):
 
 
 def sfa_run(params: SfaParams, query, query_rope, key, key_rope, value, sparse_indices, block_table,
-            actual_seq_lengths_kv, attention_out, workspace, workspace_bytes, device_error_flags, stream) -> int:
+            actual_seq_lengths_kv, actual_seq_lengths_query, attention_out, workspace, workspace_bytes,
+            device_error_flags, stream) -> int:
     """Pointer arguments are integers (device addresses) or None."""
     return load_library().sfa_run(ctypes.byref(params), query, query_rope, key, key_rope, value, sparse_indices,
-                                  block_table, actual_seq_lengths_kv, attention_out, workspace, workspace_bytes,
-                                  device_error_flags, stream)
+                                  block_table, actual_seq_lengths_kv, actual_seq_lengths_query, attention_out,
+                                  workspace, workspace_bytes, device_error_flags, stream)
 
 
 class SparseFlashAttention:
@@ -256,15 +258,17 @@ class SparseFlashAttention:
 
     Construction validates the static description and allocates the workspace
     with torch; calling the object enqueues ``sfa_run`` on the current (or given)
-    torch stream and returns the output tensor (B, 1, Q_N, 512).
+    torch stream and returns the output tensor (B, Q_S, Q_N, 512).  ``q_seq_len`` is Q_S,
+    the query tokens per batch (several for multi-token prediction); ``sparse_mode`` 3
+    masks each of them right-down causally.
     """
 
     def __init__(self, *, batch: int, num_heads: int, block_size: int, block_num: int, block_table_cols: int,
                  sparse_size: int, dtype: str = "bf16", scale: Optional[float] = None, sparse_mode: int = 0,
-                 sparse_block_size: int = 1, device=None):
+                 sparse_block_size: int = 1, q_seq_len: int = 1, device=None):
         import torch
         p = SfaParams()
-        p.B, p.Q_N, p.KV_N, p.D, p.Dr = batch, num_heads, 1, 512, 64
+        p.B, p.Q_S, p.Q_N, p.KV_N, p.D, p.Dr = batch, q_seq_len, num_heads, 1, 512, 64
         p.block_size, p.block_num, p.block_table_cols = block_size, block_num, block_table_cols
         p.sparse_size, p.sparse_block_size = sparse_size, sparse_block_size
         p.dtype = DTYPES[dtype]
@@ -279,12 +283,13 @@ class SparseFlashAttention:
         self.errors = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def __call__(self, query, query_rope, key, key_rope, value, sparse_indices, block_table, actual_seq_lengths_kv,
-                 *, out=None, stream=None):
+                 *, actual_seq_lengths_query=None, out=None, stream=None):
         import torch
         if out is None:
             out = torch.empty_like(query)
         st = sfa_run(self.params, _ptr(query), _ptr(query_rope), _ptr(key), _ptr(key_rope), _ptr(value),
-                     _ptr(sparse_indices), _ptr(block_table), _ptr(actual_seq_lengths_kv), _ptr(out),
+                     _ptr(sparse_indices), _ptr(block_table), _ptr(actual_seq_lengths_kv),
+                     _ptr(actual_seq_lengths_query), _ptr(out),
                      _ptr(self.workspace), self.workspace.numel(), _ptr(self.errors), _stream_handle(stream))
         if st != IFA_OK:
             raise IfaError(st, "sfa_run")

@@ -152,7 +152,7 @@ def test_sfa_params_struct_layout_matches_header(tmp_path):
 
 def sfa_params(**kw):
     p = ifa.SfaParams()
-    p.B, p.Q_N, p.KV_N, p.D, p.Dr = 4, 128, 1, 512, 64
+    p.B, p.Q_S, p.Q_N, p.KV_N, p.D, p.Dr = 4, 1, 128, 1, 512, 64
     p.block_size, p.block_num, p.block_table_cols, p.sparse_size, p.sparse_block_size = 64, 100, 20, 2048, 1
     p.dtype = ifa.DTYPES["bf16"]
     p.sparse_mode = 0
@@ -166,7 +166,8 @@ SFA_INVALID = [dict(KV_N=2), dict(D=256), dict(Dr=32), dict(Q_N=0), dict(Q_N=129
                dict(block_size=2048), dict(sparse_block_size=0), dict(sparse_block_size=3),
                dict(sparse_block_size=256), dict(sparse_block_size=128),  # 128 does not divide block_size 64
                dict(sparse_size=2**30, sparse_block_size=64), dict(sparse_mode=1), dict(dtype=2),
-               dict(sparse_size=0), dict(block_num=0), dict(B=-1), dict(scale_value=float("inf"))]
+               dict(sparse_size=0), dict(block_num=0), dict(B=-1), dict(scale_value=float("inf")),
+               dict(Q_S=0), dict(Q_S=1025), dict(B=2048, Q_S=1024)]
 
 
 @pytest.mark.parametrize("kw", SFA_INVALID)
@@ -177,7 +178,8 @@ def test_sfa_invalid_descriptions_are_rejected(lib, kw):
 
 @pytest.mark.parametrize("kw", [dict(), dict(Q_N=16), dict(sparse_mode=3), dict(dtype=0), dict(block_size=16),
                                 dict(sparse_block_size=2), dict(sparse_block_size=64),
-                                dict(block_size=128, sparse_block_size=128)])
+                                dict(block_size=128, sparse_block_size=128), dict(Q_S=2, sparse_mode=3),
+                                dict(Q_S=4, sparse_mode=0)])
 def test_sfa_valid_descriptions_pass_validation(lib, kw):
     st, ws = ifa.sfa_workspace_size(sfa_params(**kw))
     assert st in (ifa.IFA_OK, ifa.IFA_ERR_RUNTIME)
@@ -186,5 +188,6 @@ def test_sfa_valid_descriptions_pass_validation(lib, kw):
 
 
 def test_sfa_run_null_arguments(lib):
-    assert ifa.sfa_run(sfa_params(), None, None, None, None, None, None, None, None, None, None, 0, None, None) in \
+    assert ifa.sfa_run(sfa_params(), None, None, None, None, None, None, None, None, None, None, None, 0, None,
+                       None) in \
         (ifa.IFA_ERR_PARAM_NULLPTR,)

@@ -21,20 +21,24 @@ def _built():
     build.build()
 
 
-def run_gpu(c, sparse_mode=0):
+def run_gpu(c, sparse_mode=None):
     from kv_cache_incremental_split_gb300.ifa import SparseFlashAttention
+    Q_S = c.query.shape[1]
     op = SparseFlashAttention(batch=c.B, num_heads=c.query.shape[2], block_size=c.key.shape[1],
                               block_num=c.key.shape[0], block_table_cols=c.block_table.shape[1],
                               sparse_size=c.sparse_indices.shape[-1], dtype=c.dtype, scale=c.scale,
-                              sparse_mode=sparse_mode, sparse_block_size=c.sparse_block_size)
+                              sparse_mode=c.sparse_mode if sparse_mode is None else sparse_mode,
+                              sparse_block_size=c.sparse_block_size, q_seq_len=Q_S)
     t = [to_device(a) for a in (c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices,
                                 c.block_table, c.actual_seq_lengths_kv)]
-    out = op(*t)
+    lq = None if c.actual_seq_lengths_query is None else to_device(c.actual_seq_lengths_query)
+    out = op(*t, actual_seq_lengths_query=lq)
     torch.cuda.synchronize()
-    return out_to_f64(out).reshape(c.B, c.query.shape[2], 512), op
+    shape = (c.B, c.query.shape[2], 512) if Q_S == 1 else (c.B, Q_S, c.query.shape[2], 512)
+    return out_to_f64(out).reshape(shape), op
 
 
-def run_ref(c, batches=None):
+def run_ref(c, batches=None, sparse_mode=None):
     cc = c
     if batches is not None:
         import copy
@@ -43,14 +47,18 @@ def run_ref(c, batches=None):
         cc.query, cc.query_rope = c.query[bs], c.query_rope[bs]
         cc.sparse_indices, cc.block_table = c.sparse_indices[bs], c.block_table[bs]
         cc.actual_seq_lengths_kv = c.actual_seq_lengths_kv[bs]
+        if c.actual_seq_lengths_query is not None:
+            cc.actual_seq_lengths_query = c.actual_seq_lengths_query[bs]
     return oracle.sfa_ref(cc.query, cc.query_rope, cc.key, cc.key_rope, cc.value, cc.sparse_indices,
                           cc.block_table, cc.actual_seq_lengths_kv, scale=cc.scale,
-                          sparse_block_size=cc.sparse_block_size)
+                          sparse_block_size=cc.sparse_block_size,
+                          sparse_mode=cc.sparse_mode if sparse_mode is None else sparse_mode,
+                          actual_seq_lengths_query=cc.actual_seq_lengths_query)
 
 
-def check(c, batches=None, sparse_mode=0):
+def check(c, batches=None, sparse_mode=None):
     got, op = run_gpu(c, sparse_mode)
-    ref = run_ref(c, batches)
+    ref = run_ref(c, batches, sparse_mode)
     if batches is not None:
         got = got[np.asarray(batches)]
     assert np.all(np.isfinite(got))
@@ -89,6 +97,13 @@ def test_sfa_full_size_sampled(seed):
     c = gen.sfa_mla(seed)
     rng = np.random.default_rng(300 + seed)
     check(c, batches=np.sort(rng.choice(c.B, size=3, replace=False)))
+
+
+def test_sfa_mtp_full_size_sampled():
+    # the multi-token workload at full size (B=32, Q_S=2, 2048 indices per row, causal), sampled batches
+    c = gen.sfa_mla(0, Q_S=2, sparse_mode=3)
+    c.sparse_indices[:, :, 0, 0] = 32767  # the last key: visible to query token 1 only
+    check(c, batches=np.array([0, 17, 31]))
 
 
 def test_sfa_edge_rows():
@@ -164,3 +179,40 @@ def test_sfa_blockwise_invalid_entries_and_short_rows():
     c.sparse_indices[3, 0, 0, ::3] = -1  # -1 entries scattered through the row
     got, _ = check(c)
     assert np.all(got[2] == 0)
+
+
+# ------------------------------------------- multi-token queries and the right-down causal mode
+
+@pytest.mark.parametrize("Q_S,mode", [(2, 3), (4, 0), (3, 3)])
+def test_sfa_multi_token_matches_oracle(Q_S, mode):
+    c = gen.sfa_mla(20 + Q_S, B=3, Q_N=64, block_size=64, kv_len=700, sparse_size=260, nvalid_lo=100,
+                    nvalid_hi=260, Q_S=Q_S, sparse_mode=mode)
+    # every row selects the last keys, so the causal boundary falls inside the selection
+    c.sparse_indices[:, :, 0, :4] = np.array([699, 698, 697, 696], dtype=np.int32)
+    check(c)
+
+
+def test_sfa_multi_token_query_lengths_and_zero_rows():
+    c = gen.sfa_mla(24, B=4, Q_N=128, block_size=64, kv_len=500, sparse_size=200, nvalid_lo=150,
+                    nvalid_hi=200, Q_S=4, sparse_mode=3, q_lens=[4, 2, 0, 1])
+    c.actual_seq_lengths_kv = np.array([500, 300, 500, 3], dtype=np.int32)
+    c.sparse_indices[:, :, 0, :3] = np.array([2, 1, 0], dtype=np.int32)
+    got, _ = check(c)
+    assert np.all(got[1, 2:] == 0.0) and np.all(got[2] == 0.0) and np.all(got[3, 1:] == 0.0)
+
+
+def test_sfa_multi_token_long_rows_split_across_ctas():
+    # 2 x 2 x 2 sequences of 32 tiles: several CTAs per sequence, merged by the combine kernel
+    c = gen.sfa_mla(25, B=2, Q_N=128, block_size=64, kv_len=8192, sparse_size=2048, nvalid_lo=1800,
+                    nvalid_hi=2048, Q_S=2, sparse_mode=3)
+    c.sparse_indices[:, :, 0, :2] = np.array([8191, 8190], dtype=np.int32)
+    check(c)
+
+
+@pytest.mark.parametrize("sbs", [4, 16])
+def test_sfa_multi_token_blockwise_causal(sbs):
+    c = gen.sfa_mla(26, B=2, Q_N=32, block_size=64, kv_len=1024, sparse_size=40, nvalid_lo=20, nvalid_hi=40,
+                    Q_S=3, sparse_mode=3, sparse_block_size=sbs, q_lens=[3, 2])
+    c.actual_seq_lengths_kv = np.array([1024 - sbs // 2, 1000], dtype=np.int32)
+    c.sparse_indices[:, :, 0, 0] = 1024 // sbs - 1  # the last block: partly past length and causal limit
+    check(c)
