@@ -204,20 +204,31 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------ helpers
 
-def kernel_sources_digest() -> str:
+def kernel_sources_digest(family: str) -> str:
+    """Digest of the sources that decide one kernel family's DRAM traffic: "decode" (the
+    split-KV decode kernel, its planner and API) or "sfa" (the sparse decode and combine
+    kernels, their API, and the shared constants and PTX helpers)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kv_cache_incremental_split_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
+        if not f.endswith((".cu", ".cuh")):
+            continue
+        sfa_file = f.startswith("sfa")
+        shared = f in ("decode.cuh", "ptx.cuh")
+        if (family == "sfa" and (sfa_file or shared)) or (family == "decode" and not sfa_file):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode())
                 h.update(fh.read())
     return h.hexdigest()[:16]
 
 
+def kernel_family(workload: str) -> str:
+    return "sfa" if workload.startswith("sfa") else "decode"
+
+
 def recorded_traffic(workload: str):
     """DRAM bytes per launch of the dominant kernel from a committed ncu summary,
-    valid only while the kernel sources are unchanged since the capture."""
+    valid only while that kernel family's sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
     if not os.path.exists(path):
         return None
@@ -227,7 +238,7 @@ def recorded_traffic(workload: str):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-    if vals.get("kernel_sources_digest") != kernel_sources_digest():
+    if vals.get("kernel_sources_digest") != kernel_sources_digest(kernel_family(workload)):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])

@@ -14,11 +14,14 @@ constexpr int kMaskBox = 128;        // bytes per mask TMA box; a tile's boxes l
 constexpr int kInlineB = 256;        // per-batch windows travel in the launch parameters up to this B
 constexpr int kMaxCtas = 256;        // upper bound on the grid
 constexpr int kMinPieceTiles = 4;    // do not cut sequences into pieces shorter than this (tiles)
-// Fixed work of a sequence piece (query load, epilogue, arrival), in key/value bytes of tile
-// time; int8 pieces also fetch their antiquant scale rows.  Tuned on the GQA, paged and int8
-// workloads (piece-heavy CTAs otherwise finish last).
-constexpr int kPieceCostBytes = 160 * 1024;
-constexpr int kPieceCostBytesI8 = 320 * 1024;
+// Fixed work of a sequence piece, in key/value bytes of tile time, weighing the CTA split: a
+// whole sequence pays its epilogue (kPieceCostBytes); each piece of a sequence that CTA
+// boundaries cut pays the partial write, the arrival and its share of the merge, which sit
+// on the latency path at the end of a CTA's range (kCutCostBytes).
+constexpr int kPieceCostBytes = 64 * 1024;
+constexpr int kCutCostBytes = 160 * 1024;
+constexpr int kPieceCostBytesI8 = 192 * 1024;
+constexpr int kCutCostBytesI8 = 320 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded spin-waits: 2 s
 
 // Device error word bits (OR-ed into the error word).
@@ -57,6 +60,7 @@ struct alignas(128) DecodeParams {
     int has_mask;
     int mask_tma;              // the producer stages each tile's mask bytes (per-batch masks)
     int aq_per_channel;
+    int aq_stage;              // per-channel key scales reach shared memory with each piece's query
     float scale_log2;          // scaleValue * log2(e)
     int slot_floats;
     unsigned int gen;          // call number: picks the counter set, and the set the call clears
@@ -92,7 +96,9 @@ struct DecodeCfg {
     static constexpr int MASK_LOADS = (T + 16 + kMaskBox - 1) / kMaskBox;  // mask boxes per tile
     static constexpr int MASK_BYTES = MASK_LOADS * kMaskBox;  // one tile's mask bytes, contiguous
     static constexpr int MASK_OFF = 2 * KT_BYTES + Q_BYTES;    // within a stage
-    static constexpr int STAGE_BYTES = round_up_c(2 * KT_BYTES + Q_BYTES + MASK_BYTES, 1024);
+    static constexpr int AQ_OFF = MASK_OFF + MASK_BYTES;       // int8: the key scale row of a piece's kv head
+    static constexpr int AQ_BYTES = KV == KV_I8 ? DPAD * 2 : 0;
+    static constexpr int STAGE_BYTES = round_up_c(2 * KT_BYTES + Q_BYTES + MASK_BYTES + AQ_BYTES, 1024);
     static constexpr int MW = NWC < 4 ? NWC : 4;               // warps the merge buffer holds at once
     static constexpr int FRAG4 = (DPAD / 16) * NT;             // float4 accumulator groups per lane
     // merge buffer: MW warps' accumulator fragments, lane-contiguous float4; also holds the
@@ -106,6 +112,7 @@ struct DecodeCfg {
     static constexpr int AUX_BYTES = MERGE_BYTES + ML_BYTES + BD_BYTES + INFO_BYTES + BAR_BYTES;
     static constexpr int BUDGET = 225 * 1024;
     static constexpr int STAGES = clamp_c((BUDGET - AUX_BYTES - 1024) / STAGE_BYTES, 2, 8);
+    static constexpr int PREFETCH_TILES = STAGES;  // tiles pulled into L2 before the previous kernel ends
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + AUX_BYTES;
     static constexpr int SLOT_FLOATS = GT_PAD * DPAD + 2 * GT_PAD;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -125,7 +132,8 @@ struct KernelChoice {
     int T;          // tokens per tile
     int box_rows;   // rows per TMA box of a full tile (a whole tile, or one cache block)
     int tail_rows;  // rows per TMA box of a window's last, partial tile
-    int piece_cost; // fixed work of a sequence piece, in tiles (weights the CTA split)
+    int piece_cost; // fixed work of a whole sequence, in 1/16 tiles (weights the CTA split)
+    int cut_cost;   // fixed work of each piece of a cut sequence, in 1/16 tiles
     int slot_floats, smem, threads;
     DecodeLaunchFn launch;
 };

@@ -251,6 +251,30 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     }
     fence_proxy_async_smem();
     __syncthreads();
+    if (threadIdx.x == NWC * 32 && !p.paged && !p.ext_bdata && lo < hi) {
+        // While the previous kernel on the stream finishes, pull this CTA's first tiles of a
+        // contiguous cache into L2 (a paged cache would need the block table, which may still
+        // be written).  The loads after the wait below then start from L2.
+        TileCursor pc;
+        cursor_init<T>(pc, bd, B, p.NGS, lo);
+        for (long long g = lo; g < hi && g < lo + C::PREFETCH_TILES; ++g) {
+            const int valid = min(T, bd[B + pc.b] - pc.i * T);
+            const bool tail = valid < T;
+            const int rows_per = tail ? p.tail_rows : p.box_rows;
+            const int nbox = tail ? (valid + rows_per - 1) / rows_per : T / p.box_rows;
+            const CUtensorMap* mk = tail ? &p.tmKt : &p.tmK;
+            const CUtensorMap* mv = tail ? &p.tmVt : &p.tmV;
+            for (int k = 0; k < nbox; ++k) {
+                const int y = bd[pc.b] + pc.i * T + k * rows_per;
+#pragma unroll
+                for (int cg = 0; cg < C::NCG; ++cg) {
+                    tma_prefetch_4d(mk, cg * C::CG_ELEMS, y, pc.h, pc.b);
+                    tma_prefetch_4d(mv, cg * C::CG_ELEMS, y, pc.h, pc.b);
+                }
+            }
+            cursor_next<T>(pc, bd, B, RS, p.NGS);
+        }
+    }
     // Inputs, outputs and the workspace may belong to the previous kernel on the stream until it
     // has completed.
     pdl_wait_primary();
@@ -333,6 +357,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                 if (first) {
                     rows = min(p.GT, p.G - gs * p.GT);
                     bytes += (uint32_t)rows * (uint32_t)p.D * 2u;
+                    if (KV == KV_I8 && p.aq_stage) bytes += (uint32_t)p.D * 2u;
                 }
                 if (p.paged) {
                     for (int s = 0; s < nsub; ++s) {
@@ -354,6 +379,9 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                     uint8_t* qdst = sb + 2 * C::KT_BYTES;
                     for (int row = 0; row < rows; ++row)
                         bulk_g2s(qdst + row * C::QROW, qsrc + (long long)row * p.D * 2, (uint32_t)p.D * 2u, &full[stage]);
+                    if (KV == KV_I8 && p.aq_stage)  // the key scales of kv head h (entry 0 of the leading axis)
+                        bulk_g2s(sb + C::AQ_OFF, reinterpret_cast<const char*>(p.aq_scale) + (long long)h * p.D * 2,
+                                 (uint32_t)p.D * 2u, &full[stage]);
                 }
                 if (p.mask_tma) {
                     // this tile's mask bytes, from the 16-byte boundary at or below its first position
@@ -408,6 +436,13 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     uint32_t qf[KSTEPS][NT][2];
     float acc[MT][NT][4];
     float m_run[NT][2], l_run[NT][2];
+    // int8: value antiquant factors of the channels this thread writes in a piece's epilogue,
+    // loaded at the piece's first tile so their latency hides behind its tiles
+    float vsc[NPOS][2], vof[NPOS][2];
+#pragma unroll
+    for (int n = 0; n < NPOS; ++n)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) vsc[n][hh] = vof[n][hh] = 0.f;
 
     // Masks the producer does not stage are read by the consumers, one tile ahead.
     const bool mask_regs = p.has_mask && !p.mask_tma;
@@ -471,8 +506,13 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                                 const unsigned short u = *reinterpret_cast<const unsigned short*>(qrow + d * 2);
                                 x = p.q_bf16 ? __bfloat162float(__ushort_as_bfloat16(u))
                                              : __half2float(__ushort_as_half(u));
-                                const long long si = p.aq_per_channel ? (long long)h * p.D + d : 0;
-                                x *= ld_half_as_float(p.aq_scale, si, p.q_bf16);
+                                if (p.aq_stage) {
+                                    const unsigned short us = *reinterpret_cast<const unsigned short*>(sb + C::AQ_OFF + d * 2);
+                                    x *= p.q_bf16 ? __bfloat162float(__ushort_as_bfloat16(us)) : __half2float(__ushort_as_half(us));
+                                } else {
+                                    const long long si = p.aq_per_channel ? (long long)h * p.D + d : 0;
+                                    x *= ld_half_as_float(p.aq_scale, si, p.q_bf16);
+                                }
                             }
                             qv[e] = x;
                         }
@@ -494,6 +534,24 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
             for (int j = 0; j < NT; ++j) {
                 m_run[j][0] = m_run[j][1] = -INFINITY;
                 l_run[j][0] = l_run[j][1] = 0.f;
+            }
+            if constexpr (KV == KV_I8) {
+#pragma unroll
+                for (int n = 0; n < NPOS; ++n) {
+                    const int k = tid + n * CONSUMERS;
+                    if (k < FRAG4 * 32) {
+                        const int d0 = 16 * ((k >> 5) / NT) + 2 * ((k & 31) >> 2);
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int d = d0 + hh;
+                            if (d < p.D) {
+                                const long long si = p.aq_per_channel ? (long long)(p.KV_N + h) * p.D + d : 1;
+                                vsc[n][hh] = ld_half_as_float(p.aq_scale, si, p.q_bf16);
+                                vof[n][hh] = ld_half_as_float(p.aq_offset, si, p.q_bf16) - kI8Bias;  // values carry +1152
+                            }
+                        }
+                    }
+                }
             }
         }
 
@@ -703,30 +761,6 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         const bool complete = seq_first >= lo && seq_first + tiles <= hi;
         const long long obase = ((long long)b * p.N + (long long)h * p.G + (long long)gs * p.GT) * p.D;
 
-        // value antiquant factors of the channels this thread writes, loaded ahead of use
-        float vsc[NPOS][2], vof[NPOS][2];
-#pragma unroll
-        for (int n = 0; n < NPOS; ++n)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) vsc[n][hh] = vof[n][hh] = 0.f;
-        if constexpr (KV == KV_I8) {
-#pragma unroll
-            for (int n = 0; n < NPOS; ++n) {
-                const int k = tid + n * CONSUMERS;
-                if (k < FRAG4 * 32) {
-                    const int d0 = 16 * ((k >> 5) / NT) + 2 * ((k & 31) >> 2);
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int d = d0 + hh;
-                        if (d < p.D) {
-                            const long long si = p.aq_per_channel ? (long long)(p.KV_N + h) * p.D + d : 1;
-                            vsc[n][hh] = ld_half_as_float(p.aq_scale, si, p.q_bf16);
-                            vof[n][hh] = ld_half_as_float(p.aq_offset, si, p.q_bf16) - kI8Bias;  // values carry +1152
-                        }
-                    }
-                }
-            }
-        }
         // writes one combined fragment position to the output
         auto put = [&](const float4& o, int k, bool live0, bool live1, int n) {
             const int gg0 = 8 * ((k >> 5) % NT) + 2 * (k & 3);
@@ -860,15 +894,30 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
             const int npieces = c_last - c_first + 1;
             named_bar_sync(1, CONSUMERS);
             if (tid == 0) {
-                __threadfence();  // this CTA's partial, ordered before the arrival (cumulative over the barrier)
-                const unsigned int n = atomicAdd(p.counters + (p.gen & 1u) * kMaxCtas + c_first, 1u) + 1u;
-                __threadfence();
+                // release: this CTA's partial (written by every consumer thread before the barrier)
+                // is visible before the arrival; acquire: so are the partials of earlier arrivals
+                const unsigned int n =
+                    atom_add_acq_rel_gpu(p.counters + (p.gen & 1u) * kMaxCtas + c_first, 1u) + 1u;
                 *last_flag = n == (unsigned int)npieces;
             }
             named_bar_sync(1, CONSUMERS);
             if (*last_flag) {
                 const long long lo_first = sbounds[c_first];
                 const int slot0 = 2 * c_first + (seq_first <= lo_first ? 0 : 1);
+                // the first two pieces' partial fragments do not depend on the weights: load them now
+                float4 pre[NPOS][2];
+#pragma unroll
+                for (int n = 0; n < NPOS; ++n) {
+                    const int k = tid + n * CONSUMERS;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        pre[n][t] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (k < FRAG4 * 32 && t < npieces) {
+                            const int sl = t == 0 ? slot0 : 2 * (c_first + t);
+                            pre[n][t] = __ldcg(reinterpret_cast<const float4*>(p.partials + (long long)sl * p.slot_floats) + k);
+                        }
+                    }
+                }
                 float* pm = reinterpret_cast<float*>(mrg);  // [npieces][GT_PAD] M, then the head's total
                 float* pw = pm + npieces * GT_PAD;            // [npieces][GT_PAD] L, then the piece weights
                 for (int x2 = tid; x2 < npieces * GT_PAD; x2 += CONSUMERS) {
@@ -900,7 +949,14 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                     if (k < FRAG4 * 32) {
                         const int gg0 = 8 * ((k >> 5) % NT) + 2 * (k & 3);
                         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-                        int pc = 0;
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            if (t < npieces) {
+                                const float w0 = pw[t * GT_PAD + gg0], w1 = pw[t * GT_PAD + gg0 + 1];
+                                o.x += w0 * pre[n][t].x; o.y += w1 * pre[n][t].y; o.z += w0 * pre[n][t].z; o.w += w1 * pre[n][t].w;
+                            }
+                        }
+                        int pc = 2;
                         for (; pc + 4 <= npieces; pc += 4) {
                             float4 v[4];
 #pragma unroll

@@ -118,7 +118,9 @@ ifa_status choose_kernel(const ifa_params& p, KernelChoice* kc) {
     if (p.kvFormat != IFA_KV_CONTIG) kc->box_rows = (int)gcd64(kc->T, p.blockSize);
     kc->tail_rows = std::min(kc->box_rows, 32);
     const int tile_bytes = 2 * kc->T * kc->dpad * kc->es;
-    kc->piece_cost = std::max(1, (kc->kv_kind == KV_I8 ? kPieceCostBytesI8 : kPieceCostBytes) / tile_bytes);
+    const bool i8 = kc->kv_kind == KV_I8;
+    kc->piece_cost = std::max(1, (int)((16LL * (i8 ? kPieceCostBytesI8 : kPieceCostBytes)) / tile_bytes));
+    kc->cut_cost = std::max(kc->piece_cost, (int)((16LL * (i8 ? kCutCostBytesI8 : kCutCostBytes)) / tile_bytes));
     return IFA_OK;
 }
 
@@ -168,11 +170,71 @@ int choose_grid(const ifa_params& p, int64_t W, int max_seq_tiles, int P_max) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(P_max, (W + min_share - 1) / min_share));
 }
 
-// Without splitTiles, a sequence costs its tiles plus piece_cost tiles of fixed work (the
-// query load and the epilogue), and CTA c starts at the first tile whose cost prefix reaches
-// c * total / P.  A boundary that lands in a sequence's fixed cost moves to that sequence's
-// start, so it does not cut it.  With splitTiles the shares are equal (c W / P).  Every CTA
-// gets at least one tile (P <= W), so the CTAs a sequence spans each hold one of its pieces.
+// Without splitTiles the CTA ranges balance a cost in 1/16 tiles: 16 per tile, plus
+// piece_cost for a sequence that one CTA holds whole and cut_cost for each piece of a
+// sequence that a range boundary cuts.  A greedy walk fills each range up to a cap X,
+// closing it when the next piece would exceed X: it cuts the sequence when at least one tile
+// still fits after the cut cost, and otherwise ends the range at the sequence start.  X is
+// the smallest cap (binary search) with which P ranges suffice, so the costliest range is as
+// cheap as this walk can make it.  The RS sequences of a batch have equal length, so a walk
+// costs O(B + P).  With splitTiles the shares are equal (c W / P).  Every CTA gets at least
+// one tile (P <= W), so the CTAs a sequence spans each hold one of its pieces.
+namespace {
+// Ranges the walk needs under cap X (stops counting past P); writes bounds[1..] when given.
+int split_walk(const int32_t* bd, int B, int64_t RS, int T, int64_t Ec, int64_t Ex, int64_t X, int P,
+               int32_t* bounds) {
+    int n = 1;          // ranges opened so far
+    int64_t cur = 0;    // cost of the open range
+    int64_t g0 = 0;     // first tile of batch b
+    auto close = [&](int64_t at) -> bool {
+        if (bounds && n < P) bounds[n] = (int32_t)at;
+        ++n;
+        cur = 0;
+        return n <= P;
+    };
+    for (int b = 0; b < B; ++b) {
+        const int64_t t = ((int64_t)bd[B + b] + T - 1) / T;
+        if (t == 0) continue;
+        const int64_t whole = 16 * t + Ec;
+        int64_t r = 0, pos = 0;  // sequences of b finished; tiles of sequence r in closed ranges
+        while (r < RS) {
+            if (pos == 0) {
+                const int64_t fit = std::min(RS - r, std::max<int64_t>(0, X - cur) / whole);
+                cur += fit * whole;
+                r += fit;
+                if (r == RS) break;
+            }
+            const int64_t g = g0 + r * t;  // first tile of sequence r
+            const int64_t left = t - pos;
+            const int64_t piece = 16 * left + (pos > 0 ? Ex : Ec);
+            if (cur + piece <= X) {  // a continuation piece that fits
+                cur += piece;
+                ++r;
+                pos = 0;
+                continue;
+            }
+            const int64_t k = (X - cur - Ex) / 16;  // tiles a cut piece may take here
+            if ((k >= 1 && k < left) || cur == 0) {
+                if (cur == 0 && left == 1) {  // a single tile larger than the cap: take it
+                    cur += piece;
+                    ++r;
+                    pos = 0;
+                    continue;
+                }
+                const int64_t kk = std::max<int64_t>(1, std::min(k, left - 1));
+                cur += 16 * kk + Ex;
+                pos += kk;
+                if (!close(g + pos)) return n;
+            } else {
+                if (!close(g + pos)) return n;  // pos is 0: the range ends at the sequence start
+            }
+        }
+        g0 += RS * t;
+    }
+    return n;
+}
+}  // namespace
+
 void build_bounds(const ifa_params& p, const KernelChoice& kc, const int32_t* bd, int64_t W, int P, int32_t* bounds) {
     const int B = (int)p.B;
     bounds[0] = 0;
@@ -182,32 +244,21 @@ void build_bounds(const ifa_params& p, const KernelChoice& kc, const int32_t* bd
         return;
     }
     const int64_t RS = (int64_t)kc.KV_N * kc.NGS;
-    const int64_t E = kc.piece_cost;
-    auto tiles_of = [&](int b) { return ((int64_t)bd[B + b] + kc.T - 1) / kc.T; };
-    int64_t total = W;
+    const int64_t Ec = kc.piece_cost, Ex = std::max<int64_t>(kc.cut_cost, kc.piece_cost);
+    int64_t nseq = 0;
     for (int b = 0; b < B; ++b)
-        if (bd[B + b] > 0) total += E * RS;
-    int b = 0;
-    int64_t C0 = 0, G0 = 0;  // cost and tiles of the batches before b
-    for (int c = 1; c < P; ++c) {
-        const int64_t X = (int64_t)c * total / P;
-        while (b < B) {
-            const int64_t t = tiles_of(b);
-            const int64_t cb = t > 0 ? RS * (t + E) : 0;
-            if (C0 + cb > X) break;
-            C0 += cb;
-            G0 += t * RS;
-            ++b;
-        }
-        int64_t g = W;
-        if (b < B) {
-            const int64_t t = tiles_of(b);
-            const int64_t off = X - C0;
-            const int64_t k = off / (t + E), rem = off - k * (t + E);
-            g = G0 + k * t + (rem <= E ? 0 : rem - E);
-        }
-        bounds[c] = (int32_t)g;
+        if (bd[B + b] > 0) nseq += RS;
+    const int64_t base = 16 * W + Ec * nseq;
+    // Every range but the last ends with less than Ex + 16 of its cap unused, so P ranges of at
+    // least the mean cost with a cut at every boundary, plus that slack, always suffice.
+    int64_t lo = std::max<int64_t>(1, base / P), hi = (base + 2 * Ex * (int64_t)P) / P + Ex + 17;
+    while (lo < hi) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (split_walk(bd, B, RS, kc.T, Ec, Ex, mid, P, nullptr) <= P) hi = mid;
+        else lo = mid + 1;
     }
+    for (int c = 1; c < P; ++c) bounds[c] = (int32_t)W;
+    split_walk(bd, B, RS, kc.T, Ec, Ex, lo, P, bounds);
     for (int c = 1; c < P; ++c) bounds[c] = std::max(bounds[c], bounds[c - 1] + 1);
     for (int c = P - 1; c >= 1; --c) bounds[c] = std::min(bounds[c], bounds[c + 1] - 1);
 }
@@ -334,6 +385,8 @@ void fill_decode_params(DecodeParams& dp, const ifa_params& p, const KernelChoic
     dp.mask_bstride = (p.has_mask && p.maskB > 1) ? p.maskN * p.maskS : 0;
     dp.mask_nstride = (p.has_mask && p.maskN > 1) ? p.maskS : 0;
     dp.aq_per_channel = p.antiquant == IFA_ANTIQUANT_PER_CHANNEL;
+    // a bulk copy moves a key scale row: 16-byte aligned source (rows are D * 2 bytes, D % 8 == 0)
+    dp.aq_stage = dp.aq_per_channel && aligned(antiquantScale, 16);
     dp.scale_log2 = (float)(p.scaleValue * 1.4426950408889634);
     dp.slot_floats = kc.slot_floats;
 }

@@ -83,8 +83,28 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// L2 prefetch of one box of a 4-D tensor map: a hint with no effect on values, so it may be
+// issued before the inputs are known to be final (lines that a writer changes later are
+// updated in L2, the coherence point).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------- inter-CTA arrival
+// Atomic add at GPU scope with acquire-release semantics: the writes that precede it in this
+// thread (and, through a CTA barrier before it, in the CTA) are visible to whoever observes
+// the new count, and the writes that preceded earlier additions are visible after it.
+__device__ __forceinline__ unsigned int atom_add_acq_rel_gpu(unsigned int* addr, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
 }
 
 // ---------------------------------------------------------------- programmatic dependent launch

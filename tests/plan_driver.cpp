@@ -4,7 +4,8 @@
 // kernel launchers are stubs, nothing touches a GPU.
 //
 // input line:  B N KV_N D kv_dtype(0 bf16, 2 int8) split_tiles P_max len_0 ... len_{B-1}
-// output line: W P T piece_cost bounds_0 ... bounds_P   (or "error <status>")
+// output line: W P T piece_cost cut_cost bounds_0 ... bounds_P   (or "error <status>");
+//              the costs are in 1/16 tiles
 #include <cstdio>
 #include <cstring>
 #include <iostream>
@@ -66,7 +67,7 @@ int main() {
         const int P = choose_grid(p, W, mst, (int)pmax);
         std::vector<int32_t> bounds(P + 1);
         if (W > 0) build_bounds(p, kc, bd.data(), W, P, bounds.data());
-        std::printf("%lld %d %d %d", (long long)W, P, kc.T, kc.piece_cost);
+        std::printf("%lld %d %d %d %d", (long long)W, P, kc.T, kc.piece_cost, kc.cut_cost);
         for (int c = 0; c <= P; ++c) std::printf(" %d", W > 0 ? bounds[c] : 0);
         std::printf("\n");
     }

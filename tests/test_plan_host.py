@@ -1,8 +1,9 @@
 """CPU checks of the split planner (plan.cu: build_windows, choose_grid, build_bounds)
 through a host-only driver (tests/plan_driver.cpp) compiled against it: the CTA tile
 bounds partition the tiles, every CTA gets a tile, splitTiles gives equal shares, and the
-cost-weighted split (tiles + piece_cost per sequence piece) is better balanced than equal
-shares on mixes of short and long sequences."""
+cost-weighted split (16 per tile, plus piece_cost per whole sequence and cut_cost per
+piece of a cut sequence, in 1/16 tiles) is better balanced than equal shares on mixes of
+short and long sequences."""
 import math
 import os
 import shutil
@@ -33,28 +34,32 @@ def run(driver, problems):
     for line in res:
         f = line.split()
         assert f[0] != "error", line
-        W, P, T, E = map(int, f[:4])
-        out.append((W, P, T, E, np.array(list(map(int, f[4:])), dtype=np.int64)))
+        W, P, T, Ec, Ex = map(int, f[:5])
+        out.append((W, P, T, (Ec, Ex), np.array(list(map(int, f[5:])), dtype=np.int64)))
     return out
 
 
 def piece_costs(bounds, lens, T, RS, E):
-    """tiles + E x pieces of every CTA range, pieces counted on the real sequence layout."""
+    """Cost of every CTA range in 1/16 tiles: 16 per tile, Ec per whole sequence, Ex per piece
+    of a sequence the range boundaries cut, on the real sequence layout."""
+    Ec, Ex = E
     tiles = [(l + T - 1) // T for l in lens]
-    starts = []  # global tile index where each sequence starts
+    seqs = []  # (first tile, end tile) of every sequence
     g = 0
     for t in tiles:
         for _ in range(RS):
             if t > 0:
-                starts.append(g)
+                seqs.append((g, g + t))
             g += t
-    starts = np.array(starts, dtype=np.int64)
     costs = []
     for c in range(len(bounds) - 1):
         lo, hi = bounds[c], bounds[c + 1]
-        inside = int(((starts >= lo) & (starts < hi)).sum())
-        mid = 0 if (lo == 0 or (starts == lo).any()) else 1
-        costs.append((hi - lo) + E * (inside + mid))
+        cost = 16 * (hi - lo)
+        for s, e in seqs:
+            if e <= lo or s >= hi:
+                continue
+            cost += Ec if (s >= lo and e <= hi) else Ex
+        costs.append(cost)
     return np.array(costs)
 
 
@@ -105,8 +110,8 @@ def test_weighted_split_balances_piece_costs(driver, mix):
         weighted = piece_costs(b, lens, T, RS, E)
         equal = piece_costs(np.array([c * W // P for c in range(P + 1)]), lens, T, RS, E)
         assert weighted.max() <= equal.max()
-        # every range sits within two pieces' fixed cost (plus rounding) of the mean
-        assert weighted.max() - weighted.mean() <= 2 * E + 2
+        # every range sits within two cut pieces' fixed cost (plus a tile) of the mean
+        assert weighted.max() - weighted.mean() <= 2 * E[1] + 16
 
 
 def test_planner_is_deterministic(driver):
