@@ -51,6 +51,15 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+class _SfaArgs(ctypes.Structure):
+    """Mirror of the oracle's orc_sfa argument block (ifa_oracle.c)."""
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "B", "Q_S", "Q_T", "Q_N", "D", "Dr", "layout_q", "layout_kv", "kv_s", "block_size", "block_num",
+        "bt_cols", "sparse_size", "sparse_block_size", "sparse_mode", "dtype")] + [("scale", ctypes.c_double)] + [
+        (n, ctypes.c_void_p) for n in ("q", "q_rope", "k", "k_rope", "v", "indices", "block_table", "lens_kv",
+                                       "lens_q", "out", "softmax_max", "softmax_sum")]
+
+
 def _load():
     global _lib
     with _lock:
@@ -62,8 +71,7 @@ def _load():
                                            vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, vp, ip,
                                            vp, vp, dp, vp]
             lib.sfa_oracle_run.restype = ctypes.c_int
-            lib.sfa_oracle_run.argtypes = [i64, i64, i64, i64, i64, ip, i64, i64, i64, i64, i64, i64,
-                                           vp, vp, vp, vp, vp, vp, vp, vp, vp, dp, vp]
+            lib.sfa_oracle_run.argtypes = [ctypes.POINTER(_SfaArgs)]
             _lib = lib
     return _lib
 
@@ -145,34 +153,75 @@ def ifa_ref(query, key, value, *, num_heads, num_kv_heads=0, scale, layout="BNSD
     return out
 
 
-def sfa_ref(query, query_rope, key, key_rope, value, sparse_indices, block_table,
-            actual_seq_lengths_kv, *, scale, sparse_block_size=1, sparse_mode=0, actual_seq_lengths_query=None):
-    """Reference sparse MLA-absorb decode output, float64 (B, Q_S, Q_N, D); (B, Q_N, D) when Q_S = 1.
+SFA_LAYOUT_Q = {"BSND": 0, "TND": 1}
+SFA_LAYOUT_KV = {"PA_BSND": 0, "BSND": 1, "TND": 2}
 
-    query (B,Q_S,Q_N,D), query_rope (B,Q_S,Q_N,Dr), key/value (block_num, block_size, 1, D),
-    key_rope (block_num, block_size, 1, Dr), sparse_indices (B,Q_S,1,sparse_size) int32,
-    block_table (B, cols) int32, actual_seq_lengths_kv (B,) int32; sparse_block_size > 1: each
-    index selects that many consecutive tokens (block-wise); sparse_mode 3: right-down causal
-    over the Q_S query tokens; actual_seq_lengths_query (B,) int32 or None.
+
+def sfa_ref(query, query_rope, key, key_rope, value, sparse_indices, block_table,
+            actual_seq_lengths_kv, *, scale, sparse_block_size=1, sparse_mode=0, actual_seq_lengths_query=None,
+            layout_query="BSND", layout_kv="PA_BSND", return_softmax_lse=False):
+    """Reference sparse MLA-absorb decode output, float64.
+
+    layout_query BSND: query (B,Q_S,Q_N,D), query_rope (B,Q_S,Q_N,Dr), sparse_indices
+    (B,Q_S,1,sparse_size), output (B,Q_S,Q_N,D), or (B,Q_N,D) when Q_S = 1;
+    actual_seq_lengths_query (B,) int32 or None.  TND: query (Q_T,Q_N,D), query_rope
+    (Q_T,Q_N,Dr), sparse_indices (Q_T,1,sparse_size), output (Q_T,Q_N,D);
+    actual_seq_lengths_query holds prefix sums (its length is B).
+    layout_kv PA_BSND: key/value (block_num, block_size, 1, D), key_rope (block_num,
+    block_size, 1, Dr), block_table (B, cols), actual_seq_lengths_kv (B,).  BSND: key
+    (B, KV_S, 1, D), actual_seq_lengths_kv (B,) or None; TND: key (KV_T, 1, D),
+    actual_seq_lengths_kv prefix sums.  sparse_block_size > 1: each index selects that many
+    consecutive tokens; sparse_mode 3: right-down causal over each batch's query tokens.
+    return_softmax_lse: also return softmax_max and softmax_sum, one value per (row, head),
+    shaped like the output without its last axis.
     """
     lib = _load()
+    lq_code, lkv_code = SFA_LAYOUT_Q[layout_query], SFA_LAYOUT_KV[layout_kv]
     q = _c(query)
     qr = _c(query_rope)
     k = _c(key)
     kr = _c(key_rope)
     v = _c(value)
     idx = _c(sparse_indices, np.int32)
-    bt = _c(block_table, np.int32)
-    lens = _c(actual_seq_lengths_kv, np.int32)
+    bt = None if block_table is None else _c(block_table, np.int32)
+    lens = None if actual_seq_lengths_kv is None else _c(actual_seq_lengths_kv, np.int32)
     lq = None if actual_seq_lengths_query is None else _c(actual_seq_lengths_query, np.int32)
-    B, Q_S, Q_N, D = q.shape[0], q.shape[1], q.shape[2], q.shape[3]
-    Dr = qr.shape[3]
-    block_num, block_size = k.shape[0], k.shape[1]
-    out = np.zeros((B, Q_S, Q_N, D), dtype=np.float64)
-    rc = lib.sfa_oracle_run(B, Q_S, Q_N, D, Dr, _dtype_code(q), block_size, block_num, bt.shape[1],
-                            idx.shape[-1], int(sparse_block_size), int(sparse_mode), _ptr(q), _ptr(qr), _ptr(k),
-                            _ptr(kr), _ptr(v), _ptr(idx), _ptr(bt), _ptr(lens),
-                            None if lq is None else _ptr(lq), float(scale), _ptr(out))
+    a = _SfaArgs()
+    if lq_code == 0:
+        a.B, a.Q_S, a.Q_N, a.D = q.shape[0], q.shape[1], q.shape[2], q.shape[3]
+        rows = a.B * a.Q_S
+        Dr = qr.shape[3]
+        lead = (a.B, a.Q_S)
+    else:
+        a.Q_T, a.Q_N, a.D = q.shape[0], q.shape[1], q.shape[2]
+        a.B = lq.shape[0]
+        rows = a.Q_T
+        Dr = qr.shape[2]
+        lead = (a.Q_T,)
+    a.Dr = Dr
+    a.layout_q, a.layout_kv = lq_code, lkv_code
+    if lkv_code == 0:
+        a.block_num, a.block_size = k.shape[0], k.shape[1]
+        a.bt_cols = bt.shape[1]
+    elif lkv_code == 1:
+        a.kv_s = k.shape[1]
+    else:
+        a.kv_s = k.shape[0]
+    a.sparse_size = idx.shape[-1]
+    a.sparse_block_size = int(sparse_block_size)
+    a.sparse_mode = int(sparse_mode)
+    a.dtype = _dtype_code(q)
+    a.scale = float(scale)
+    out = np.zeros(lead + (a.Q_N, a.D), dtype=np.float64)
+    smax = np.zeros(lead + (a.Q_N,), dtype=np.float64)
+    ssum = np.zeros(lead + (a.Q_N,), dtype=np.float64)
+    a.q, a.q_rope, a.k, a.k_rope, a.v = _ptr(q), _ptr(qr), _ptr(k), _ptr(kr), _ptr(v)
+    a.indices, a.block_table, a.lens_kv, a.lens_q = _ptr(idx), _ptr(bt), _ptr(lens), _ptr(lq)
+    a.out, a.softmax_max, a.softmax_sum = _ptr(out), _ptr(smax), _ptr(ssum)
+    assert idx.size == rows * a.sparse_size
+    rc = lib.sfa_oracle_run(ctypes.byref(a))
     if rc < 0:
         raise ValueError("oracle rejected its arguments")
-    return out[:, 0] if Q_S == 1 else out
+    if lq_code == 0 and a.Q_S == 1:
+        out, smax, ssum = out[:, 0], smax[:, 0], ssum[:, 0]
+    return (out, smax, ssum) if return_softmax_lse else out

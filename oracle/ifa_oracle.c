@@ -254,87 +254,154 @@ int ifa_oracle_run(int64_t B, int64_t N, int64_t KV_N, int64_t D, int q_dtype, i
 /*
  * Sparse-index MLA-absorb decode (SparseFlashAttention README: formula in
  * "功能说明"; query/key/value/query_rope/key_rope/sparse_indices/block_table/
- * actual_seq_lengths_kv in "参数说明").  PA_BSND storage with KV_N = 1:
- *   key   (block_num, block_size, 1, D)   key_rope (block_num, block_size, 1, Dr)
- *   value (block_num, block_size, 1, D)   query (B, 1, Q_N, D), query_rope (B, 1, Q_N, Dr)
- *   sparse_indices (B, 1, 1, sparse_size), block_table (B, bt_cols)
- * s_j = scale * (q . k[idx_j] + q_rope . k_rope[idx_j]);  out = softmax(s) . v[idx_j].
- * sparse_block_size (README "sparse_block_size", 1 = token-wise): entry j of a row selects
- * the tokens idx_j * sparse_block_size + o, o = 0 .. sparse_block_size - 1 (block-wise:
- * the tokens of a block share the selection); a token at or past actual_seq_lengths_kv[b],
- * or any token of a negative entry, is skipped.
- * Q_S query tokens per batch (query (B, Q_S, Q_N, D), sparse_indices (B, Q_S, 1, sparse_size),
- * out (B, Q_S, Q_N, D)): each (b, s) row is its own problem over its own index row.
- * lens_q (nullable: every row valid) gives the valid query tokens of each batch; rows s at or
- * past it are all zero.  sparse_mode 3 (README "sparse_mode", rightDownCausal): query token s
- * sits at key position lens_kv[b] - lens_q[b] + s and selected tokens past it are skipped;
- * sparse_mode 0 masks nothing.
+ * actual_seq_lengths_query/actual_seq_lengths_kv/layout_query/layout_kv in "参数说明").
+ * KV_N = 1 throughout.
+ *
+ * Query rows.  layout_query BSND: query (B, Q_S, Q_N, D), query_rope (B, Q_S, Q_N, Dr),
+ * sparse_indices (B, Q_S, 1, sparse_size), out (B, Q_S, Q_N, D): row r = b * Q_S + s, and
+ * lens_q (nullable) gives each batch's valid query tokens qlen (Q_S when NULL).  layout_query
+ * TND: the same arrays with Q_T rows in place of (B, Q_S); lens_q (required) holds prefix
+ * sums, so batch b owns rows [lens_q[b-1], lens_q[b]) (lens_q[-1] = 0), s counts from the
+ * batch's first row and qlen = lens_q[b] - lens_q[b-1]; rows past lens_q[B-1] belong to no
+ * batch and are zero.
+ * Key rows.  layout_kv PA_BSND: key/value (block_num, block_size, 1, D), key_rope (..., Dr);
+ * token t of batch b is row block_table[b][t / block_size] * block_size + t % block_size and
+ * len = lens_kv[b].  BSND: key (B, KV_S, 1, D); token t is row b * KV_S + t and len =
+ * lens_kv[b] (KV_S when lens_kv is NULL).  TND: key (KV_T, 1, D); lens_kv holds prefix sums,
+ * token t of batch b is row lens_kv[b-1] + t and len = lens_kv[b] - lens_kv[b-1].  Tokens
+ * past the batch's rows in the key tensor (t >= KV_S; row >= KV_T) are skipped.
+ * Selection.  Entry j of a row's indices selects tokens idx_j * sparse_block_size + o,
+ * o = 0 .. sparse_block_size - 1 (README "sparse_block_size"; 1 = token-wise); a negative
+ * entry selects nothing; a token at or past len is skipped; duplicates count once per
+ * occurrence.  Rows s >= qlen select nothing.  sparse_mode 3 (README "sparse_mode",
+ * rightDownCausal): row s sees only tokens below len - qlen + s + 1; sparse_mode 0 masks
+ * nothing.
+ * s_j = scale * (q . k[j] + q_rope . k_rope[j]);  out = softmax(s) . v (zero when nothing
+ * survives).  softmax_max / softmax_sum (nullable, one value per (row, head) at r * Q_N + n,
+ * i.e. the README's (B, 1, Q_S, Q_N) or (1, Q_T, Q_N)): the largest s_j, and the sum of
+ * exp(s_j - softmax_max); -inf and 0 when nothing survives.
  * Returns the number of skipped out-of-range block-table entries, -1 on bad arguments.
  */
-int sfa_oracle_run(int64_t B, int64_t Q_S, int64_t Q_N, int64_t D, int64_t Dr, int dtype, int64_t block_size,
-                   int64_t block_num, int64_t bt_cols, int64_t sparse_size, int64_t sparse_block_size,
-                   int64_t sparse_mode, const void* q, const void* q_rope, const void* k, const void* k_rope,
-                   const void* v, const int32_t* sparse_indices, const int32_t* block_table,
-                   const int32_t* lens_kv, const int32_t* lens_q, double scale, double* out) {
-    if (B < 0 || Q_S <= 0 || Q_N <= 0 || D <= 0 || Dr < 0 || block_size <= 0 || sparse_size <= 0 ||
-        sparse_block_size <= 0 || (sparse_mode != 0 && sparse_mode != 3))
+typedef struct {
+    int64_t B, Q_S, Q_T, Q_N, D, Dr;
+    int64_t layout_q;  /* 0 BSND, 1 TND */
+    int64_t layout_kv; /* 0 PA_BSND, 1 BSND, 2 TND */
+    int64_t kv_s;      /* BSND: KV_S; TND: KV_T; PA_BSND: unused */
+    int64_t block_size, block_num, bt_cols;
+    int64_t sparse_size, sparse_block_size, sparse_mode, dtype;
+    double scale;
+    const void *q, *q_rope, *k, *k_rope, *v;
+    const int32_t *indices, *block_table, *lens_kv, *lens_q;
+    double *out, *softmax_max, *softmax_sum;
+} orc_sfa;
+
+int sfa_oracle_run(const orc_sfa* a) {
+    if (a->B < 0 || a->Q_N <= 0 || a->D <= 0 || a->Dr < 0 || a->sparse_size <= 0 || a->sparse_block_size <= 0 ||
+        (a->sparse_mode != 0 && a->sparse_mode != 3) || a->layout_q < 0 || a->layout_q > 1 || a->layout_kv < 0 ||
+        a->layout_kv > 2)
         return -1;
+    if (a->layout_q == 0 && a->Q_S <= 0) return -1;
+    if (a->layout_q == 1 && (a->Q_T < 0 || !a->lens_q)) return -1;
+    if (a->layout_kv == 0 && (a->block_size <= 0 || !a->block_table || !a->lens_kv)) return -1;
+    if (a->layout_kv == 2 && !a->lens_kv) return -1;
+    const int64_t R = a->layout_q == 0 ? a->B * a->Q_S : a->Q_T;
+    const int64_t npos = a->sparse_size * a->sparse_block_size; /* selected token positions per row */
     int bad = 0;
-    const int64_t npos = sparse_size * sparse_block_size; /* selected token positions per row */
-    double* s = (double*)malloc((size_t)npos * sizeof(double));
-    int64_t* row = (int64_t*)malloc((size_t)npos * sizeof(int64_t));
+    double* s = (double*)malloc((size_t)(npos > 0 ? npos : 1) * sizeof(double));
+    int64_t* row = (int64_t*)malloc((size_t)(npos > 0 ? npos : 1) * sizeof(int64_t));
     if (!s || !row) {
         free(s);
         free(row);
         return -1;
     }
-    for (int64_t bs_row = 0; bs_row < B * Q_S; bs_row++) {
-        const int64_t b = bs_row / Q_S, sq = bs_row % Q_S;
-        const int64_t qlen = lens_q ? lens_q[b] : Q_S;
+    for (int64_t r = 0; r < R; r++) {
+        /* the row's batch b, query token sq and the batch's valid query tokens qlen */
+        int64_t b = -1, sq = 0, qlen = 0;
+        if (a->layout_q == 0) {
+            b = r / a->Q_S;
+            sq = r % a->Q_S;
+            qlen = a->lens_q ? a->lens_q[b] : a->Q_S;
+        } else {
+            for (int64_t bb = 0; bb < a->B; bb++) {
+                if (r < a->lens_q[bb]) {
+                    b = bb;
+                    break;
+                }
+            }
+            if (b >= 0) {
+                const int64_t first = b > 0 ? a->lens_q[b - 1] : 0;
+                sq = r - first;
+                qlen = a->lens_q[b] - first;
+            }
+        }
+        /* the batch's keys: length, first row (BSND, TND), and the rows the key tensor holds */
+        int64_t len = 0, base = 0, avail = INT64_MAX;
+        if (b >= 0) {
+            if (a->layout_kv == 0) {
+                len = a->lens_kv[b];
+            } else if (a->layout_kv == 1) {
+                len = a->lens_kv ? a->lens_kv[b] : a->kv_s;
+                base = b * a->kv_s;
+                avail = a->kv_s;
+            } else {
+                base = b > 0 ? a->lens_kv[b - 1] : 0;
+                len = a->lens_kv[b] - base;
+                avail = a->kv_s - base;
+            }
+        }
         /* keys this query row may use: [0, limit) */
-        int64_t limit = lens_kv[b];
-        if (sq >= qlen) limit = 0;
-        else if (sparse_mode == 3) limit = lens_kv[b] - qlen + sq + 1;
-        /* resolve the selected rows once per query row: physical row = blk * block_size + slot */
+        int64_t limit = len;
+        if (b < 0 || sq >= qlen) limit = 0;
+        else if (a->sparse_mode == 3) limit = len - qlen + sq + 1;
+        if (limit > len) limit = len;
+        if (limit > avail) limit = avail;
         for (int64_t j = 0; j < npos; j++) {
-            int64_t idx = sparse_indices[bs_row * sparse_size + j / sparse_block_size];
+            const int64_t idx = a->indices[r * a->sparse_size + j / a->sparse_block_size];
             row[j] = -1;
             if (idx < 0) continue;
-            int64_t tok = idx * sparse_block_size + j % sparse_block_size;
-            if (tok >= lens_kv[b] || tok >= limit) continue;
-            int64_t blk = block_table[b * bt_cols + tok / block_size];
-            if (blk < 0 || blk >= block_num) {
-                bad++;
-                continue;
+            const int64_t tok = idx * a->sparse_block_size + j % a->sparse_block_size;
+            if (tok >= limit) continue;
+            if (a->layout_kv == 0) {
+                const int64_t blk = a->block_table[b * a->bt_cols + tok / a->block_size];
+                if (blk < 0 || blk >= a->block_num) {
+                    bad++;
+                    continue;
+                }
+                row[j] = blk * a->block_size + tok % a->block_size;
+            } else {
+                row[j] = base + tok;
             }
-            row[j] = blk * block_size + tok % block_size;
         }
-        for (int64_t n = 0; n < Q_N; n++) {
-            double* o = out + (bs_row * Q_N + n) * D;
-            for (int64_t d = 0; d < D; d++) o[d] = 0.0;
+        for (int64_t n = 0; n < a->Q_N; n++) {
+            double* o = a->out + (r * a->Q_N + n) * a->D;
+            for (int64_t d = 0; d < a->D; d++) o[d] = 0.0;
             double smax = -INFINITY;
             int any = 0;
             for (int64_t j = 0; j < npos; j++) {
                 if (row[j] < 0) continue;
                 double dot = 0.0;
-                for (int64_t d = 0; d < D; d++)
-                    dot += load_value(q, (bs_row * Q_N + n) * D + d, dtype) * load_value(k, row[j] * D + d, dtype);
-                for (int64_t d = 0; d < Dr; d++)
-                    dot += load_value(q_rope, (bs_row * Q_N + n) * Dr + d, dtype) *
-                           load_value(k_rope, row[j] * Dr + d, dtype);
-                s[j] = scale * dot;
+                for (int64_t d = 0; d < a->D; d++)
+                    dot += load_value(a->q, (r * a->Q_N + n) * a->D + d, (int)a->dtype) *
+                           load_value(a->k, row[j] * a->D + d, (int)a->dtype);
+                for (int64_t d = 0; d < a->Dr; d++)
+                    dot += load_value(a->q_rope, (r * a->Q_N + n) * a->Dr + d, (int)a->dtype) *
+                           load_value(a->k_rope, row[j] * a->Dr + d, (int)a->dtype);
+                s[j] = a->scale * dot;
                 if (s[j] > smax) smax = s[j];
                 any = 1;
             }
-            if (!any) continue;
             double denom = 0.0;
-            for (int64_t j = 0; j < npos; j++) {
-                if (row[j] < 0) continue;
-                double w = exp(s[j] - smax);
-                denom += w;
-                for (int64_t d = 0; d < D; d++) o[d] += w * load_value(v, row[j] * D + d, dtype);
+            if (any) {
+                for (int64_t j = 0; j < npos; j++) {
+                    if (row[j] < 0) continue;
+                    const double w = exp(s[j] - smax);
+                    denom += w;
+                    for (int64_t d = 0; d < a->D; d++) o[d] += w * load_value(a->v, row[j] * a->D + d, (int)a->dtype);
+                }
+                for (int64_t d = 0; d < a->D; d++) o[d] /= denom;
             }
-            for (int64_t d = 0; d < D; d++) o[d] /= denom;
+            if (a->softmax_max) a->softmax_max[r * a->Q_N + n] = smax;
+            if (a->softmax_sum) a->softmax_sum[r * a->Q_N + n] = denom;
         }
     }
     free(s);

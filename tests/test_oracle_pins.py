@@ -623,3 +623,130 @@ def test_sfa_causal_mode_equals_explicit_index_pruning():
     full = oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
                           lens, scale=c.scale, sparse_mode=0, actual_seq_lengths_query=lq)
     assert not np.array_equal(full[0, 0], causal[0, 0])
+
+
+# ------------------------------------------- TND / BSND layouts and the softmax_max / softmax_sum outputs
+
+def _contig_kv(c, kv_len=64, bs=16):
+    """The paged caches of an SFA case rewritten as BSND (B, KV_S, 1, d) tensors."""
+    B = c.B
+    def gather(t):
+        outp = np.zeros((B, kv_len) + t.shape[2:], dtype=t.dtype)
+        for b in range(B):
+            for tok in range(kv_len):
+                outp[b, tok] = t[c.block_table[b, tok // bs], tok % bs]
+        return outp
+    return gather(c.key), gather(c.key_rope), gather(c.value)
+
+
+@pytest.mark.parametrize("mode", [0, 3])
+def test_sfa_bsnd_and_tnd_kv_equal_the_paged_cache(mode):
+    """layout_kv BSND (row b * KV_S + t) and TND (row lens_kv[b-1] + t, prefix-sum lengths)
+    address the same tokens as PA_BSND through the block table: identical outputs."""
+    c = _sfa_mtp(50, 2, sparse_mode=mode)
+    lens = np.array([64, 41], dtype=np.int32)
+    paged = oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
+                           lens, scale=c.scale, sparse_mode=mode)
+    k, kr, v = _contig_kv(c)
+    bsnd = oracle.sfa_ref(c.query, c.query_rope, k, kr, v, c.sparse_indices, None, lens, scale=c.scale,
+                          sparse_mode=mode, layout_kv="BSND")
+    assert np.array_equal(paged, bsnd)
+    # TND: batch 1 packed right after batch 0's 64 rows
+    kt = np.concatenate([k[0, :64], k[1, :41]])
+    krt = np.concatenate([kr[0, :64], kr[1, :41]])
+    vt = np.concatenate([v[0, :64], v[1, :41]])
+    tnd = oracle.sfa_ref(c.query, c.query_rope, kt, krt, vt, c.sparse_indices, None,
+                         np.array([64, 105], dtype=np.int32), scale=c.scale, sparse_mode=mode, layout_kv="TND")
+    assert np.array_equal(paged, tnd)
+    # BSND without lengths uses KV_S for every batch
+    full = oracle.sfa_ref(c.query, c.query_rope, k, kr, v, c.sparse_indices, None, None, scale=c.scale,
+                          sparse_mode=mode, layout_kv="BSND")
+    ref = oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
+                         np.array([64, 64], dtype=np.int32), scale=c.scale, sparse_mode=mode)
+    assert np.array_equal(full, ref)
+
+
+@pytest.mark.parametrize("mode", [0, 3])
+def test_sfa_tnd_query_rows_match_bsnd_rows_and_torch(mode):
+    """layout_query TND packs each batch's qlen valid query rows (prefix-sum
+    actual_seq_lengths_query); each packed row equals the BSND row (b, s) with the same
+    qlen, and matches the dense library attention over its selected tokens."""
+    Q_S = 3
+    c = _sfa_mtp(51, Q_S, sparse_mode=mode, nvalid_lo=16, nvalid_hi=16)
+    qlen = np.array([3, 2], dtype=np.int32)
+    bsnd = oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
+                          c.actual_seq_lengths_kv, scale=c.scale, sparse_mode=mode, actual_seq_lengths_query=qlen)
+    rows = [(b, s) for b in range(2) for s in range(qlen[b])]
+    qt = np.stack([c.query[b, s] for b, s in rows])
+    qrt = np.stack([c.query_rope[b, s] for b, s in rows])
+    it = np.stack([c.sparse_indices[b, s] for b, s in rows])
+    tnd = oracle.sfa_ref(qt, qrt, c.key, c.key_rope, c.value, it, c.block_table, c.actual_seq_lengths_kv,
+                         scale=c.scale, sparse_mode=mode, actual_seq_lengths_query=np.cumsum(qlen).astype(np.int32),
+                         layout_query="TND")
+    assert tnd.shape == (5, 4, 32)
+    for t, (b, s) in enumerate(rows):
+        assert np.array_equal(tnd[t], bsnd[b, s])
+    q = as_f64(qt, "bf16")
+    qr = as_f64(qrt, "bf16")
+    k = as_f64(c.key, "bf16").reshape(-1, 32)
+    kr = as_f64(c.key_rope, "bf16").reshape(-1, 8)
+    v = as_f64(c.value, "bf16").reshape(-1, 32)
+    L = 64
+    for t, (b, s) in enumerate(rows):
+        lim = L - qlen[b] + s + 1 if mode == 3 else L
+        sel = [i for i in it[t, 0] if 0 <= i < lim]
+        r_ = _rows(c, b, sel)
+        for n in range(4):
+            ref = torch_attention(np.concatenate([q[t, n], qr[t, n]]), np.concatenate([k[r_], kr[r_]], axis=1),
+                                  v[r_], c.scale)
+            np.testing.assert_allclose(tnd[t, n], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_sfa_tnd_rows_past_the_last_prefix_are_zero():
+    c = _sfa_mtp(52, 1)
+    qt = c.query[:, 0]
+    qrt = c.query_rope[:, 0]
+    it = c.sparse_indices[:, 0]
+    out, mx, sm = oracle.sfa_ref(qt, qrt, c.key, c.key_rope, c.value, it, c.block_table, c.actual_seq_lengths_kv,
+                                 scale=c.scale, actual_seq_lengths_query=np.array([1], dtype=np.int32),
+                                 layout_query="TND", return_softmax_lse=True)
+    # one batch of one row: row 1 belongs to no batch
+    assert np.all(out[1] == 0.0) and np.all(mx[1] == -np.inf) and np.all(sm[1] == 0.0)
+    assert np.all(np.isfinite(out[0])) and np.any(out[0] != 0.0)
+
+
+def test_sfa_softmax_max_and_sum_closed_forms():
+    """Q = 0: every score is 0, so softmax_max = 0 and softmax_sum = the number of valid
+    selected tokens (exact); rows with nothing selected give -inf and 0.  Random Q: max and
+    max + log(sum) equal numpy's max and logsumexp of the scaled scores."""
+    from scipy.special import logsumexp
+    c = _sfa_mtp(53, 2, sparse_mode=3)
+    lens = np.array([64, 30], dtype=np.int32)
+    c.sparse_indices[1, 1] = -1
+    zq = np.zeros_like(c.query)
+    zr = np.zeros_like(c.query_rope)
+    _, mx, sm = oracle.sfa_ref(zq, zr, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table, lens,
+                               scale=c.scale, sparse_mode=3, return_softmax_lse=True)
+    for b in range(2):
+        for s in range(2):
+            lim = lens[b] - 2 + s + 1
+            cnt = int(sum(1 for i in c.sparse_indices[b, s, 0] if 0 <= i < lim))
+            if cnt == 0:
+                assert np.all(mx[b, s] == -np.inf) and np.all(sm[b, s] == 0.0)
+            else:
+                assert np.all(mx[b, s] == 0.0) and np.all(sm[b, s] == float(cnt)), (b, s)
+    out, mx, sm = oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices,
+                                 c.block_table, lens, scale=c.scale, sparse_mode=3, return_softmax_lse=True)
+    q = as_f64(c.query, "bf16")
+    qr = as_f64(c.query_rope, "bf16")
+    k = as_f64(c.key, "bf16").reshape(-1, 32)
+    kr = as_f64(c.key_rope, "bf16").reshape(-1, 8)
+    for b in range(2):
+        s = 0
+        lim = lens[b] - 2 + s + 1
+        r_ = _rows(c, b, [i for i in c.sparse_indices[b, s, 0] if 0 <= i < lim])
+        kk = np.concatenate([k[r_], kr[r_]], axis=1)
+        for n in range(4):
+            sc = (kk @ np.concatenate([q[b, s, n], qr[b, s, n]])) * c.scale
+            assert mx[b, s, n] == pytest.approx(sc.max(), rel=1e-13, abs=1e-13)
+            assert mx[b, s, n] + math.log(sm[b, s, n]) == pytest.approx(logsumexp(sc), rel=1e-12, abs=1e-12)
