@@ -72,6 +72,9 @@ def _load():
                                            vp, vp, dp, vp]
             lib.sfa_oracle_run.restype = ctypes.c_int
             lib.sfa_oracle_run.argtypes = [ctypes.POINTER(_SfaArgs)]
+            lib.kv_append_oracle.restype = ctypes.c_int
+            lib.kv_append_oracle.argtypes = [i64, i64, i64, ip, ip, ip, ip, i64, i64, i64, i64, vp, vp, vp, vp, ip,
+                                             vp, vp, vp, vp]
             _lib = lib
     return _lib
 
@@ -225,3 +228,40 @@ def sfa_ref(query, query_rope, key, key_rope, value, sparse_indices, block_table
     if lq_code == 0 and a.Q_S == 1:
         out, smax, ssum = out[:, 0], smax[:, 0], ssum[:, 0]
     return (out, smax, ssum) if return_softmax_lse else out
+
+
+def kv_append_ref(key_new, value_new, positions, key_cache, value_cache, *, layout="BNSD", kv_format=CONTIG,
+                  block_size=0, block_table=None, antiquant=AQ_NONE, antiquant_scale=None, antiquant_offset=None):
+    """Caches after appending one token per batch, as new arrays (the inputs are not modified),
+    and the number of batches whose position lies outside the cache.
+
+    key_new/value_new: (B, KV_N, D) in memory (any query-style layout with S = 1), fp16 or
+    bf16.  key_cache/value_cache: contiguous (B,KV_N,Smax,D) BNSD, (B,Smax,KV_N,D) BSND or
+    (B,Smax,H) BSH; or paged (blocknum, KV_N, blockSize, D) / (blocknum, blockSize, H); fp16,
+    bf16 or int8.  positions: (B,) int64 token index of the new token.
+    """
+    lib = _load()
+    kn = _c(key_new)
+    vn = _c(value_new)
+    kc = np.array(key_cache, copy=True, order="C")
+    vc = np.array(value_cache, copy=True, order="C")
+    pos = _c(positions, np.int64)
+    bt = _c(block_table, np.int32) if block_table is not None else None
+    sc = _c(antiquant_scale)
+    of = _c(antiquant_offset)
+    B = pos.shape[0]
+    lay = _LAYOUT[layout]
+    if kv_format == CONTIG:
+        kvn = kc.shape[1] if lay == BNSD else (kc.shape[2] if lay == BSND else kn.size // (B * kn.shape[-1]))
+        smax = kc.shape[2] if lay == BNSD else kc.shape[1]
+        block_num, cols = 0, 0
+    else:
+        kvn = kn.size // (B * kn.shape[-1])
+        smax, block_num, cols = 0, kc.shape[0], bt.shape[1]
+    D = kn.size // (B * kvn)
+    rc = lib.kv_append_oracle(B, kvn, D, _dtype_code(kn), _dtype_code(kc), lay, kv_format, smax, int(block_size),
+                              cols, block_num, _ptr(kn), _ptr(vn), _ptr(pos), _ptr(bt), int(antiquant), _ptr(sc),
+                              _ptr(of), _ptr(kc), _ptr(vc))
+    if rc < 0:
+        raise ValueError("oracle rejected its arguments")
+    return kc, vc, rc

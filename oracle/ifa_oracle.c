@@ -252,6 +252,83 @@ int ifa_oracle_run(int64_t B, int64_t N, int64_t KV_N, int64_t D, int q_dtype, i
 }
 
 /*
+ * int8 code of x read back as (code + offset) * scale: the inverse of the antiquant reading,
+ * taken in single precision (x, scale and offset are 16-bit values, exact in float):
+ * rint(x / scale - offset), ties to even, saturated to [-128, 127]; NaN gives 0.
+ */
+static int8_t quantize_i8(double x, double scale, double offset) {
+    const float xf = (float)x, sf = (float)scale, of = (float)offset;
+    const float t = xf / sf;
+    const float u = t - of;
+    if (isnan(u)) return 0;
+    float r = rintf(u);
+    if (r > 127.0f) r = 127.0f;
+    if (r < -128.0f) r = -128.0f;
+    return (int8_t)r;
+}
+
+/*
+ * KV-cache append: the cache grows by one token per decode step (IncreFlashAttention README,
+ * incremental inference; aclnnIncreFlashAttentionV2, the key/value cache arguments).  The key
+ * and value rows of the new token of every batch, (B, KV_N, D) in memory in any query-style
+ * layout (S = 1), are written at token position pos[b] of the cache: contiguous BNSD, BSND or
+ * BSH with Smax rows per batch, or paged through the block table (block
+ * block_table[b][pos / block_size], slot pos % block_size) in the NBSD or BSH block format --
+ * the addresses the attention reads.  A 16-bit cache receives the values unchanged; an int8
+ * cache receives quantize_i8 of each element with the antiquant parameter it is read back
+ * with (per channel: entry (0 key | 1 value, h, d); per tensor: entry 0 | 1).  A position
+ * outside the cache (negative, >= Smax, past the block table, or a block id outside
+ * [0, blocknum)) writes nothing for that batch.
+ * Returns the number of batches skipped, -1 on bad arguments.
+ */
+int kv_append_oracle(int64_t B, int64_t KV_N, int64_t D, int new_dtype, int kv_dtype, int layout, int kv_format,
+                     int64_t Smax, int64_t block_size, int64_t block_table_cols, int64_t block_num,
+                     const void* k_new, const void* v_new, const int64_t* pos, const int32_t* block_table,
+                     int antiquant, const void* aq_scale, const void* aq_offset, void* k_cache, void* v_cache) {
+    if (B < 0 || KV_N <= 0 || D <= 0 || !pos) return -1;
+    if (kv_format != ORC_CONTIG && (!block_table || block_size <= 0)) return -1;
+    if ((kv_dtype == ORC_I8) != (antiquant != ORC_AQ_NONE)) return -1;
+    if (kv_dtype != ORC_I8 && kv_dtype != new_dtype) return -1;
+    orc_ifa a;
+    memset(&a, 0, sizeof a);
+    a.B = B; a.N = KV_N; a.KV_N = KV_N; a.D = D;
+    a.q_dtype = new_dtype; a.kv_dtype = kv_dtype; a.layout = layout; a.kv_format = kv_format;
+    a.Smax = Smax; a.block_size = block_size; a.block_table_cols = block_table_cols; a.block_num = block_num;
+    a.block_table = block_table;
+    int skipped = 0;
+    for (int64_t b = 0; b < B; b++) {
+        const int64_t t = pos[b];
+        int ok = t >= 0;
+        if (ok && kv_format == ORC_CONTIG) ok = t < Smax;
+        if (ok && kv_format != ORC_CONTIG) ok = t / block_size < block_table_cols;
+        if (ok && kv_offset(&a, b, 0, t, 0) < 0) ok = 0; /* block id outside [0, blocknum) */
+        if (!ok) {
+            skipped++;
+            continue;
+        }
+        for (int64_t h = 0; h < KV_N; h++) {
+            for (int64_t d = 0; d < D; d++) {
+                const int64_t src = (b * KV_N + h) * D + d;
+                const int64_t dst = kv_offset(&a, b, h, t, d);
+                for (int which = 0; which < 2; which++) {
+                    const void* from = which == 0 ? k_new : v_new;
+                    void* to = which == 0 ? k_cache : v_cache;
+                    if (kv_dtype == ORC_I8) {
+                        const int64_t pidx = antiquant == ORC_AQ_PER_TENSOR ? which : (which * KV_N + h) * D + d;
+                        ((int8_t*)to)[dst] = quantize_i8(load_value(from, src, new_dtype),
+                                                         load_value(aq_scale, pidx, new_dtype),
+                                                         load_value(aq_offset, pidx, new_dtype));
+                    } else {
+                        ((uint16_t*)to)[dst] = ((const uint16_t*)from)[src];
+                    }
+                }
+            }
+        }
+    }
+    return skipped;
+}
+
+/*
  * Sparse-index MLA-absorb decode (SparseFlashAttention README: formula in
  * "功能说明"; query/key/value/query_rope/key_rope/sparse_indices/block_table/
  * actual_seq_lengths_query/actual_seq_lengths_kv/layout_query/layout_kv in "参数说明").

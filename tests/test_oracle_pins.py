@@ -750,3 +750,125 @@ def test_sfa_softmax_max_and_sum_closed_forms():
             sc = (kk @ np.concatenate([q[b, s, n], qr[b, s, n]])) * c.scale
             assert mx[b, s, n] == pytest.approx(sc.max(), rel=1e-13, abs=1e-13)
             assert mx[b, s, n] + math.log(sm[b, s, n]) == pytest.approx(logsumexp(sc), rel=1e-12, abs=1e-12)
+
+
+# ------------------------------------------- KV-cache append
+
+def _place(cache, new, pos, layout, kv_format, block_size=0, block_table=None):
+    """numpy placement of the new token rows (B, KV_N, D) at positions pos."""
+    c = cache.copy()
+    B, KVN, D = new.shape
+    for b in range(B):
+        t = int(pos[b])
+        if kv_format == oracle.CONTIG:
+            if layout == "BNSD":
+                c[b, :, t, :] = new[b]
+            elif layout == "BSND":
+                c[b, t, :, :] = new[b]
+            else:
+                c[b, t, :] = new[b].reshape(-1)
+        else:
+            blk, slot = block_table[b, t // block_size], t % block_size
+            if kv_format == oracle.PAGED_NBSD:
+                c[blk, :, slot, :] = new[b]
+            else:
+                c[blk, slot, :] = new[b].reshape(-1)
+    return c
+
+
+@pytest.mark.parametrize("layout,kv_format", [("BNSD", oracle.CONTIG), ("BSND", oracle.CONTIG), ("BSH", oracle.CONTIG),
+                                              ("BNSD", oracle.PAGED_NBSD), ("BSH", oracle.PAGED_BSH)])
+def test_kv_append_16bit_places_rows_exactly(layout, kv_format):
+    rng = np.random.default_rng(60)
+    B, KVN, D, S, bs = 3, 2, 16, 40, 16
+    kn = rng.standard_normal((B, KVN, D)).astype(np.float16)
+    vn = rng.standard_normal((B, KVN, D)).astype(np.float16)
+    pos = np.array([0, 17, 39])
+    bt = None
+    if kv_format == oracle.CONTIG:
+        shape = {"BNSD": (B, KVN, S, D), "BSND": (B, S, KVN, D), "BSH": (B, S, KVN * D)}[layout]
+    else:
+        bt = rng.permutation(B * 3).astype(np.int32).reshape(B, 3)
+        shape = (B * 3, KVN, bs, D) if kv_format == oracle.PAGED_NBSD else (B * 3, bs, KVN * D)
+    kc = rng.standard_normal(shape).astype(np.float16)
+    vc = rng.standard_normal(shape).astype(np.float16)
+    k2, v2, bad = oracle.kv_append_ref(kn, vn, pos, kc, vc, layout=layout, kv_format=kv_format, block_size=bs,
+                                       block_table=bt)
+    assert bad == 0
+    assert np.array_equal(k2.view(np.uint16), _place(kc, kn, pos, layout, kv_format, bs, bt).view(np.uint16))
+    assert np.array_equal(v2.view(np.uint16), _place(vc, vn, pos, layout, kv_format, bs, bt).view(np.uint16))
+
+
+def test_kv_append_then_attend_equals_attention_over_the_longer_cache():
+    """Appending at position len and attending over len + 1 tokens equals attention over a
+    cache that held the token from the start (IncreFlashAttention's incremental step)."""
+    c = gen.paged_gqa(61, B=2, N=8, KV_N=2, D=32, block_size=16, len_lo=20, len_hi=40)
+    rng = np.random.default_rng(61)
+    lens = c.actual_seq_lengths.astype(np.int64)
+    kn = gen.to_storage(rng.standard_normal((2, 2, 32)).astype(np.float32), "bf16")
+    vn = gen.to_storage(rng.standard_normal((2, 2, 32)).astype(np.float32), "bf16")
+    k2, v2, bad = oracle.kv_append_ref(kn, vn, lens, c.key, c.value, kv_format=oracle.PAGED_NBSD,
+                                       block_size=16, block_table=c.block_table)
+    assert bad == 0
+    got = oracle.ifa_ref(c.query, k2, v2, num_heads=8, num_kv_heads=2, scale=c.scale, kv_format=oracle.PAGED_NBSD,
+                         block_size=16, block_table=c.block_table, actual_seq_lengths=lens + 1)
+    q = as_f64(c.query, "bf16").reshape(2, 8, 32)
+    for b in range(2):
+        L = int(lens[b])
+        rows = [c.block_table[b, t // 16] for t in range(L)]
+        k = np.stack([as_f64(c.key[rows[t], :, t % 16], "bf16") for t in range(L)] + [as_f64(kn[b], "bf16")])
+        v = np.stack([as_f64(c.value[rows[t], :, t % 16], "bf16") for t in range(L)] + [as_f64(vn[b], "bf16")])
+        for n in range(8):
+            ref = torch_attention(q[b, n], k[:, n // 4], v[:, n // 4], c.scale)
+            np.testing.assert_allclose(got[b, n], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_kv_append_int8_codes_invert_the_antiquant_reading():
+    """int8 caches: the code c of x satisfies (c + offset) * scale = x exactly when x is such a
+    value; otherwise |(c + offset) * scale - x| <= scale / 2 unless saturated at -128 / 127;
+    an exact half rounds to the even code."""
+    B, KVN, D = 2, 2, 8
+    sc = np.full((2, KVN, D), 2.0 ** -6, dtype=np.float16)
+    of = np.broadcast_to(np.arange(D, dtype=np.float16) - 4, (2, KVN, D)).copy()
+    codes = np.arange(-60, 60, 15)[:D]
+    x = ((codes[None, None, :] + of[0].astype(np.float64)) * 2.0 ** -6).astype(np.float16)
+    x = np.broadcast_to(x, (B, KVN, D)).copy()
+    kc = np.zeros((B, KVN, 4, D), dtype=np.int8)
+    k2, v2, bad = oracle.kv_append_ref(x, x, np.array([1, 3]), kc, kc, antiquant=oracle.AQ_PER_CHANNEL,
+                                       antiquant_scale=sc, antiquant_offset=of)
+    assert bad == 0 and np.array_equal(k2[0, :, 1], np.broadcast_to(codes, (KVN, D)))
+    rng = np.random.default_rng(62)
+    xr = rng.uniform(-2.5, 2.5, (B, KVN, D)).astype(np.float16)
+    sc2 = rng.uniform(0.005, 0.02, (2, KVN, D)).astype(np.float16)
+    of2 = rng.uniform(-4, 4, (2, KVN, D)).astype(np.float16)
+    k3, v3, _ = oracle.kv_append_ref(xr, xr, np.array([0, 0]), kc, kc, antiquant=oracle.AQ_PER_CHANNEL,
+                                     antiquant_scale=sc2, antiquant_offset=of2)
+    for which, cache in ((0, k3), (1, v3)):
+        c = cache[:, :, 0].astype(np.float64)
+        s = sc2[which].astype(np.float64)
+        o = of2[which].astype(np.float64)
+        back = (c + o) * s
+        inside = (c > -128) & (c < 127)
+        err = np.abs(back - xr.astype(np.float64))
+        assert np.all(err[inside] <= s[None].repeat(B, 0)[inside] / 2 * (1 + 1e-6))
+    # saturation and ties (per-tensor parameters: scale 1, offset 0 -> code = rint(x))
+    one = np.array([1.0, 1.0], dtype=np.float16)
+    zero = np.zeros(2, dtype=np.float16)
+    xt = np.array([[[300.0, -300.0, 2.5, 3.5, -2.5, 0.5, 126.5, -128.5]]], dtype=np.float16)
+    k4, _, _ = oracle.kv_append_ref(xt, xt, np.array([0]), kc[:1, :1], kc[:1, :1], antiquant=oracle.AQ_PER_TENSOR,
+                                    antiquant_scale=one, antiquant_offset=zero)
+    assert list(k4[0, 0, 0]) == [127, -128, 2, 4, -2, 0, 126, -128]
+
+
+def test_kv_append_skips_positions_outside_the_cache():
+    rng = np.random.default_rng(63)
+    kn = rng.standard_normal((3, 1, 8)).astype(np.float16)
+    kc = rng.standard_normal((3, 1, 5, 8)).astype(np.float16)
+    k2, v2, bad = oracle.kv_append_ref(kn, kn, np.array([-1, 5, 2]), kc, kc)
+    assert bad == 2
+    assert np.array_equal(k2[:2], kc[:2]) and np.array_equal(k2[2, 0, 2], kn[2, 0])
+    bt = np.array([[0, -1], [7, 1], [2, 3]], dtype=np.int32)  # block 7 >= blocknum 4
+    pc = rng.standard_normal((4, 1, 4, 8)).astype(np.float16)
+    k3, _, bad = oracle.kv_append_ref(kn, kn, np.array([5, 1, 9]), pc, pc, kv_format=oracle.PAGED_NBSD,
+                                      block_size=4, block_table=bt)
+    assert bad == 3 and np.array_equal(k3, pc)  # entry -1, block 7, and a position past the table
