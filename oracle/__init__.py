@@ -72,6 +72,8 @@ def _load():
                                            vp, vp, dp, vp]
             lib.sfa_oracle_run.restype = ctypes.c_int
             lib.sfa_oracle_run.argtypes = [ctypes.POINTER(_SfaArgs)]
+            lib.ifa_quantize_output.restype = ctypes.c_int
+            lib.ifa_quantize_output.argtypes = [i64, i64, i64, vp, ip, ip, vp, vp, vp]
             lib.kv_append_oracle.restype = ctypes.c_int
             lib.kv_append_oracle.argtypes = [i64, i64, i64, ip, ip, ip, ip, i64, i64, i64, i64, vp, vp, vp, vp, ip,
                                              vp, vp, vp, vp]
@@ -265,3 +267,26 @@ def kv_append_ref(key_new, value_new, positions, key_cache, value_cache, *, layo
     if rc < 0:
         raise ValueError("oracle rejected its arguments")
     return kc, vc, rc
+
+
+def quantize_output_ref(y, scale2, offset2=None):
+    """int8 codes of an attention output y (B, N, D) (float64, rounded to float32 first):
+    saturate(rint(y * scale2 + offset2)) with single-precision product and sum.  scale2 /
+    offset2: float32 or bf16 bit patterns (uint16); one entry (per tensor) or N * D entries
+    (per channel, head-major)."""
+    lib = _load()
+    yy = np.ascontiguousarray(y, dtype=np.float64)
+    B, N, D = yy.shape
+    sc = np.ascontiguousarray(scale2)
+    of = None if offset2 is None else np.ascontiguousarray(offset2)
+    code = 3 if sc.dtype == np.float32 else (BF16 if sc.dtype == np.uint16 else None)
+    if code is None or (of is not None and of.dtype != sc.dtype):
+        raise TypeError("scale2/offset2 must be float32 or bf16 bit patterns, of one dtype")
+    per_channel = sc.size != 1
+    if per_channel and sc.size != N * D:
+        raise ValueError("per-channel scale2 needs N * D entries")
+    out = np.zeros((B, N, D), dtype=np.int8)
+    rc = lib.ifa_quantize_output(B, N, D, _ptr(yy), int(per_channel), code, _ptr(sc), _ptr(of), _ptr(out))
+    if rc < 0:
+        raise ValueError("oracle rejected its arguments")
+    return out

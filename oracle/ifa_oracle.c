@@ -252,6 +252,46 @@ int ifa_oracle_run(int64_t B, int64_t N, int64_t KV_N, int64_t D, int q_dtype, i
 }
 
 /*
+ * int8 output quantisation (IncreFlashAttention README: int8 output with quantScale2 and the
+ * optional quantOffset2, per-tensor or per-channel, FLOAT32 or BFLOAT16; the formula is not
+ * on the pages).  Reading: code = saturate(rint(y * scale2 + offset2)) to [-128, 127], ties
+ * to even, NaN -> 0, with the product and the sum each rounded to single precision (no fused
+ * multiply-add), y the attention output rounded to single precision.  Per channel, element
+ * (b, n, d) of the (B, N, D) output uses entry n * D + d (N query heads: the README's
+ * N * D, which also equals H for BSH); per tensor, entry 0.  offset2 NULL means 0.
+ * q2_dtype: 3 = FLOAT32, 1 = BFLOAT16.  Returns -1 on bad arguments.
+ */
+int ifa_quantize_output(int64_t B, int64_t N, int64_t D, const double* y, int per_channel, int q2_dtype,
+                        const void* scale2, const void* offset2, int8_t* out) {
+    if (B < 0 || N <= 0 || D <= 0 || !y || !scale2 || !out || (q2_dtype != 3 && q2_dtype != ORC_BF16)) return -1;
+    for (int64_t b = 0; b < B; b++) {
+        for (int64_t c = 0; c < N * D; c++) {
+            const int64_t pi = per_channel ? c : 0;
+            float sf, of = 0.0f;
+            if (q2_dtype == 3) {
+                sf = ((const float*)scale2)[pi];
+                if (offset2) of = ((const float*)offset2)[pi];
+            } else {
+                sf = (float)bf16_bits_to_double(((const uint16_t*)scale2)[pi]);
+                if (offset2) of = (float)bf16_bits_to_double(((const uint16_t*)offset2)[pi]);
+            }
+            const float yf = (float)y[b * N * D + c];
+            const float t = yf * sf;
+            const float u = t + of;
+            int8_t code = 0;
+            if (!isnan(u)) {
+                float r = rintf(u);
+                if (r > 127.0f) r = 127.0f;
+                if (r < -128.0f) r = -128.0f;
+                code = (int8_t)r;
+            }
+            out[b * N * D + c] = code;
+        }
+    }
+    return 0;
+}
+
+/*
  * int8 code of x read back as (code + offset) * scale: the inverse of the antiquant reading,
  * taken in single precision (x, scale and offset are 16-bit values, exact in float):
  * rint(x / scale - offset), ties to even, saturated to [-128, 127]; NaN gives 0.

@@ -872,3 +872,48 @@ def test_kv_append_skips_positions_outside_the_cache():
     k3, _, bad = oracle.kv_append_ref(kn, kn, np.array([5, 1, 9]), pc, pc, kv_format=oracle.PAGED_NBSD,
                                       block_size=4, block_table=bt)
     assert bad == 3 and np.array_equal(k3, pc)  # entry -1, block 7, and a position past the table
+
+
+# ------------------------------------------- int8 output quantisation (quantScale2 / quantOffset2)
+
+def test_output_quantisation_of_integer_outputs_is_exact():
+    """Value rows constant per channel make the attention output that constant (to rounding far
+    below a code's width), so the codes are c * scale2 + offset2 by hand: scale 1, offset 0
+    gives c itself."""
+    case = gen.gqa_padded(70, B=2, N=4, KV_N=2, D=16, Smax=30, layout="BNSD", dtype="fp16", mask=False)
+    consts = np.arange(-8, 8, dtype=np.float64)  # channel d carries the integer d - 8
+    case.value = np.broadcast_to(consts.astype(np.float16), case.value.shape).copy()
+    y = run(case)
+    np.testing.assert_allclose(y, np.broadcast_to(consts, y.shape), rtol=1e-13, atol=1e-13)
+    codes = oracle.quantize_output_ref(y, np.array([1.0], np.float32))
+    assert np.array_equal(codes, np.broadcast_to(consts.astype(np.int8), codes.shape))
+    codes = oracle.quantize_output_ref(y, np.array([2.0], np.float32), np.array([3.0], np.float32))
+    assert np.array_equal(codes, np.broadcast_to((consts * 2 + 3).astype(np.int8), codes.shape))
+    codes = oracle.quantize_output_ref(y, np.array([40.0], np.float32), np.array([-1.0], np.float32))
+    assert np.array_equal(codes, np.broadcast_to(np.clip(consts * 40 - 1, -128, 127).astype(np.int8), codes.shape))
+
+
+def test_output_quantisation_per_channel_ties_saturation_and_dtypes():
+    rng = np.random.default_rng(71)
+    y = rng.standard_normal((3, 4, 16))
+    s = rng.uniform(10, 40, 64).astype(np.float32)
+    o = rng.uniform(-5, 5, 64).astype(np.float32)
+    pc = oracle.quantize_output_ref(y, s, o)
+    # per-channel with every entry equal is per-tensor
+    same = oracle.quantize_output_ref(y, np.full(64, s[0], np.float32), np.full(64, o[0], np.float32))
+    assert np.array_equal(same, oracle.quantize_output_ref(y, s[:1], o[:1]))
+    # per-channel entry n * D + d scales output channel (n, d)
+    y1 = np.zeros((1, 4, 16))
+    y1[0, 2, 5] = 1.0
+    c1 = oracle.quantize_output_ref(y1, np.arange(1, 65, dtype=np.float32))
+    assert c1[0, 2, 5] == 2 * 16 + 5 + 1 and np.count_nonzero(c1) == 1
+    # bf16 parameters equal float32 ones holding the same values
+    sb = gen.to_storage(s, "bf16")
+    ob = gen.to_storage(o, "bf16")
+    sf = (sb.astype(np.uint32) << 16).view(np.float32)
+    of = (ob.astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(oracle.quantize_output_ref(y, sb, ob), oracle.quantize_output_ref(y, sf, of))
+    # ties to even, saturation, no offset
+    yt = np.array([[[0.5, 1.5, 2.5, -0.5, -1.5, 200.0, -200.0, 127.4]]])
+    assert list(oracle.quantize_output_ref(yt, np.array([1.0], np.float32))[0, 0]) == [0, 2, 2, 0, -2, 127, -128, 127]
+    assert pc.dtype == np.int8 and np.all(np.abs(pc.astype(np.int64)) <= 128)
