@@ -62,7 +62,7 @@ typedef enum { IFA_LAYOUT_BSH = 0, IFA_LAYOUT_BSND = 1, IFA_LAYOUT_BNSD = 2 } if
  * ("IncreFlashAttention" README, page attention constraints.) */
 typedef enum { IFA_KV_CONTIG = 0, IFA_KV_PAGED_NBSD = 1, IFA_KV_PAGED_BSH = 2 } ifa_kv_format;
 
-typedef enum { IFA_F16 = 0, IFA_BF16 = 1, IFA_I8 = 2, IFA_U8 = 3, IFA_BOOL = 4 } ifa_dtype;
+typedef enum { IFA_F16 = 0, IFA_BF16 = 1, IFA_I8 = 2, IFA_U8 = 3, IFA_BOOL = 4, IFA_F32 = 5 } ifa_dtype;
 
 typedef enum {
     IFA_ANTIQUANT_NONE = 0,
@@ -97,6 +97,15 @@ typedef struct ifa_params {
     double scaleValue;        /* the scale applied to q . k (typically 1/sqrt(D)) */
     int64_t splitTiles;       /* 0: automatic split plan; > 0: at most this many 64-token tiles per
                                  CTA (testing split invariance); negative is invalid */
+    /* Output quantisation ("IncreFlashAttention" README: int8 output with quantScale2 and the
+     * optional quantOffset2; the formula is not on the pages).  With out_dtype IFA_I8 each
+     * output element y becomes saturate(rint(y * scale2 + offset2)) in [-128, 127], the
+     * product and the sum rounded to single precision, ties to even (NaN gives 0); an
+     * all-zero row quantises y = 0.  Per channel, output element (n, d) takes entry
+     * n * headDim + d of numHeads * headDim (the README's N * D, or H); per tensor, entry 0. */
+    int32_t out_dtype;        /* IFA_I8: int8 attentionOut; any other value: q_dtype */
+    int32_t quant2;           /* ifa_antiquant values: PER_CHANNEL or PER_TENSOR with an int8 output, else NONE */
+    int32_t quant2_dtype;     /* IFA_F32, or IFA_BF16 with a bf16 query (the README's rule) */
 } ifa_params;
 
 typedef struct ifa_plan ifa_plan;
@@ -124,7 +133,10 @@ ifa_status ifa_create(const ifa_params* params, ifa_plan** plan, size_t* workspa
  *                    entries of blocks a batch does not reach are never read
  *   antiquantScale   per-channel (2, KV_N, D) or per-tensor (2), of q_dtype, 2-byte aligned
  *   antiquantOffset  same shape and dtype
- *   attentionOut     same shape and dtype as query
+ *   quantScale2      int8 output only: quant2_dtype, 1 or numHeads * headDim entries, 4-byte
+ *                    (f32) or 2-byte (bf16) aligned
+ *   quantOffset2     nullable (0): same dtype and entries as quantScale2
+ *   attentionOut     same shape as query; q_dtype, or int8 with out_dtype IFA_I8
  *   workspace        >= workspace_bytes from ifa_create (nullable when that is 0)
  * Host pointers:
  *   actualSeqLengths int64 (B); NULL means every batch uses maxSeqLen (contiguous only);
@@ -143,8 +155,9 @@ ifa_status ifa_create(const ifa_params* params, ifa_plan** plan, size_t* workspa
 ifa_status ifa_run(ifa_plan* plan, const void* query, const void* key, const void* value,
                    const void* attenMask, const int64_t* actualSeqLengths,
                    const int64_t* kvPaddingSize, int64_t n_kv_padding, const int32_t* blockTable,
-                   const void* antiquantScale, const void* antiquantOffset, void* attentionOut,
-                   void* workspace, size_t workspace_bytes, void* stream);
+                   const void* antiquantScale, const void* antiquantOffset, const void* quantScale2,
+                   const void* quantOffset2, void* attentionOut, void* workspace, size_t workspace_bytes,
+                   void* stream);
 
 /* Release a plan (NULL is accepted). Waits for nothing; do not free while a run is in flight. */
 ifa_status ifa_destroy(ifa_plan* plan);
@@ -190,8 +203,9 @@ ifa_status ifa_get_device_errors(ifa_plan* plan, void* stream, int64_t* flags);
 ifa_status ifa_run_noalloc(const ifa_params* params, const void* query, const void* key, const void* value,
                            const void* attenMask, const int64_t* actualSeqLengths,
                            const int64_t* kvPaddingSize, int64_t n_kv_padding, const int32_t* blockTable,
-                           const void* antiquantScale, const void* antiquantOffset, void* attentionOut,
-                           int32_t* deviceErrorFlags, void* stream);
+                           const void* antiquantScale, const void* antiquantOffset, const void* quantScale2,
+                           const void* quantOffset2, void* attentionOut, int32_t* deviceErrorFlags,
+                           void* stream);
 
 /*
  * Number of CUDA kernels the most recent ifa_run on `plan` enqueued: 1 (the split-KV
@@ -205,37 +219,55 @@ int64_t ifa_last_launch_count(const ifa_plan* plan);
  * Sparse-index MLA-absorb decode ("SparseFlashAttention" README: formula in 功能说明,
  * arguments in 参数说明, limits in 约束说明):
  *
- *     out[b, n, :] = softmax_j( scale_value * (q[b,n] . k[i_j] + q_rope[b,n] . k_rope[i_j]) ) . v[i_j]
+ *     out[r, n, :] = softmax_j( scale_value * (q[r,n] . k[i_j] + q_rope[r,n] . k_rope[i_j]) ) . v[i_j]
  *
- * for every query token s of batch b (the line holds with q[b,s,n], i_j from row (b, s) and
- * out[b,s,n]), over the selected tokens i_j with 0 <= i_j < limit(b, s) (tokens outside that
- * range, e.g. from the -1 tail, are skipped wherever they sit; duplicates count once per
- * occurrence; an empty selection gives an all-zero row).  Token-wise (sparse_block_size 1):
- * i_j = sparse_indices[b, s, 0, j].  Block-wise (sparse_block_size = t > 1, README
- * "sparse_block_size"): entry j selects the t tokens sparse_indices[b, s, 0, j] * t + o,
- * o = 0 .. t - 1.  Token i lives in block block_table[b][i / block_size], slot
- * i % block_size of the PA_BSND caches.  With len = actual_seq_lengths_kv[b] and
- * qlen = actual_seq_lengths_query[b] (Q_S when that array is NULL; README: 0 <= qlen <= Q_S):
- * limit(b, s) = 0 for s >= qlen (an all-zero row); otherwise len under sparse_mode 0, and
- * len - qlen + s + 1 under sparse_mode 3 (rightDownCausal: the last valid query token is
- * aligned with the last key).  Only the layouts and modes the README lists for this case are
- * accepted: query layout BSND, key/value layout PA_BSND, KV_N = 1, D = 512, Dr = 64,
- * attention_mode 2 (MLA-absorb), sparse_mode 0 or 3, Q_N in 1..128.
+ * for every query row r (a (batch b, query token s) pair), over the tokens i_j its index row
+ * selects with 0 <= i_j < limit(r) (tokens outside that range, e.g. from the -1 tail, are
+ * skipped wherever they sit; duplicates count once per occurrence; an empty selection gives
+ * an all-zero row).  Token-wise (sparse_block_size 1): i_j = sparse_indices[r, 0, j].
+ * Block-wise (sparse_block_size = t > 1, README "sparse_block_size"): entry j selects the
+ * t tokens sparse_indices[r, 0, j] * t + o, o = 0 .. t - 1.
+ *
+ * Query rows (layout_query): SFA_LAYOUT_BSND: query (B,Q_S,Q_N,D), row r = b * Q_S + s, and
+ * qlen = actual_seq_lengths_query[b] (Q_S when that array is NULL; README: 0 <= qlen <= Q_S).
+ * SFA_LAYOUT_TND: query (Q_T,Q_N,D); actual_seq_lengths_query (required) holds B prefix sums
+ * (README: cumulative counts), batch b owns rows [cum[b-1], cum[b]) with s counted from its
+ * first row and qlen = cum[b] - cum[b-1]; rows past cum[B-1] belong to no batch (zero rows).
+ * Key rows (layout_kv): SFA_KV_PA_BSND: caches (block_num, block_size, 1, D); token t of batch
+ * b lives in block block_table[b][t / block_size], slot t % block_size; len =
+ * actual_seq_lengths_kv[b] (required).  SFA_KV_BSND: key/value (B, KV_S, 1, D), token t of
+ * batch b at row b * KV_S + t, len = actual_seq_lengths_kv[b] (KV_S when NULL).  SFA_KV_TND:
+ * key/value (KV_S, 1, D) (KV_S = the README's KV_T), actual_seq_lengths_kv (required) holds
+ * prefix sums, token t of batch b at row cum[b-1] + t, len = cum[b] - cum[b-1].  Tokens past
+ * a batch's rows in the key tensor are skipped.
+ * limit(r) = 0 for s >= qlen; otherwise len under sparse_mode 0, and len - qlen + s + 1
+ * under sparse_mode 3 (rightDownCausal: the last valid query token is aligned with the last
+ * key).  Only what the README lists for this operator is accepted: KV_N = 1, D = 512,
+ * Dr = 64, attention_mode 2 (MLA-absorb), sparse_mode 0 or 3, Q_N in 1..128.
  */
+#define SFA_LAYOUT_BSND 0
+#define SFA_LAYOUT_TND 1
+#define SFA_KV_PA_BSND 0
+#define SFA_KV_BSND 1
+#define SFA_KV_TND 2
 typedef struct sfa_params {
-    int64_t B;               /* batch, 1..65536 */
-    int64_t Q_S;             /* query tokens per batch, 1..1024, B * Q_S <= 2^20 */
+    int64_t B;               /* batch (entries of the length arrays), 1..65536 */
+    int64_t Q_S;             /* BSND queries: query tokens per batch, 1..1024, B * Q_S <= 2^20 */
+    int64_t Q_T;             /* TND queries: query rows, 0..2^20 */
     int64_t Q_N;             /* query heads, 1..128 */
     int64_t KV_N;            /* must be 1 */
     int64_t D;               /* 512: head dim of query, key and value */
     int64_t Dr;              /* 64: rope dim of query_rope and key_rope */
-    int64_t block_size;      /* tokens per cache block: a multiple of 16, <= 1024 */
-    int64_t block_num;       /* blocks in the caches */
-    int64_t block_table_cols;/* second dimension of block_table */
+    int64_t KV_S;            /* key rows per batch (SFA_KV_BSND) or in all (SFA_KV_TND); unused when paged */
+    int64_t block_size;      /* SFA_KV_PA_BSND: tokens per cache block, a multiple of 16, <= 1024 */
+    int64_t block_num;       /* SFA_KV_PA_BSND: blocks in the caches */
+    int64_t block_table_cols;/* SFA_KV_PA_BSND: second dimension of block_table */
     int64_t sparse_size;     /* indices per query row, >= 1 */
-    int64_t sparse_block_size; /* 1 (token-wise) or a power of two <= 128 dividing block_size */
+    int64_t sparse_block_size; /* 1 (token-wise) or a power of two <= 128 (dividing block_size when paged) */
     int32_t dtype;           /* IFA_BF16 or IFA_F16, shared by every tensor and the output */
     int32_t sparse_mode;     /* 0 or 3 */
+    int32_t layout_query;    /* SFA_LAYOUT_BSND or SFA_LAYOUT_TND */
+    int32_t layout_kv;       /* SFA_KV_PA_BSND, SFA_KV_BSND or SFA_KV_TND */
     double scale_value;      /* scale applied to the scores (typically 1/sqrt(D + Dr)) */
 } sfa_params;
 
@@ -245,12 +277,15 @@ ifa_status sfa_workspace_size(const sfa_params* params, size_t* workspace_bytes)
 
 /*
  * Enqueue one sparse decode call on `stream` (cudaStream_t, NULL = legacy default).
- * Device pointers, 16-byte aligned unless noted:
- *   query (B,Q_S,Q_N,D), query_rope (B,Q_S,Q_N,Dr), key and value (block_num, block_size, 1, D),
- *   key_rope (block_num, block_size, 1, Dr), attention_out (B,Q_S,Q_N,D), all of `dtype`;
- *   sparse_indices int32 (B,Q_S,1,sparse_size), block_table int32 (B, block_table_cols),
- *   actual_seq_lengths_kv int32 (B) and actual_seq_lengths_query int32 (B, nullable)
- *   (4-byte aligned); workspace of at least
+ * Device pointers, 16-byte aligned unless noted (R = B * Q_S or Q_T query rows):
+ *   query (R,Q_N,D), query_rope (R,Q_N,Dr), attention_out (R,Q_N,D); key and value
+ *   (rows, D) and key_rope (rows, Dr) in the layout_kv shapes above, all of `dtype`;
+ *   sparse_indices int32 (R,1,sparse_size); block_table int32 (B, block_table_cols), paged
+ *   only (nullable otherwise); actual_seq_lengths_kv and actual_seq_lengths_query int32 (B),
+ *   nullable where the layout allows (4-byte aligned); softmax_max and softmax_sum float32
+ *   (R, Q_N), nullable (README softmax_max_out / softmax_sum_out, accepted with every
+ *   layout): the largest scaled score and the sum of exp(score - softmax_max) of each
+ *   (row, head), -inf and 0 for an empty selection; workspace of at least
  *   sfa_workspace_size bytes; deviceErrorFlags (int32, nullable) receives device error
  *   bits (1: a needed block_table entry outside [0, block_num); 2: a wait timed out).
  * `value` may alias `key`.  Calls that share a workspace must not overlap on the GPU.
@@ -260,8 +295,50 @@ ifa_status sfa_workspace_size(const sfa_params* params, size_t* workspace_bytes)
 ifa_status sfa_run(const sfa_params* params, const void* query, const void* query_rope, const void* key,
                    const void* key_rope, const void* value, const int32_t* sparse_indices,
                    const int32_t* block_table, const int32_t* actual_seq_lengths_kv,
-                   const int32_t* actual_seq_lengths_query, void* attention_out, void* workspace,
-                   size_t workspace_bytes, int32_t* deviceErrorFlags, void* stream);
+                   const int32_t* actual_seq_lengths_query, void* attention_out, float* softmax_max,
+                   float* softmax_sum, void* workspace, size_t workspace_bytes, int32_t* deviceErrorFlags,
+                   void* stream);
+
+/*
+ * KV-cache append: the step before the attention in incremental decode (IncreFlashAttention
+ * README: each step attends over the cache grown by the new token).  The key and value rows
+ * of one new token per batch are written at token position positions[b] of the caches,
+ * through the addressing ifa_run reads: contiguous (B,KV_N,Smax,D) BNSD, (B,Smax,KV_N,D) BSND
+ * or (B,Smax,H) BSH (maxSeqLen = Smax), or paged (blockNum, KV_N, blockSize, D) /
+ * (blockNum, blockSize, H) through blockTable (block blockTable[b][t / blockSize], slot
+ * t % blockSize).  A 16-bit cache (kv_dtype = new_dtype) receives the values unchanged.  An
+ * int8 cache receives, per element, rint(x / scale - offset) computed in single precision
+ * (ties to even) and saturated to [-128, 127] (NaN gives 0), with the antiquant scale and
+ * offset the element is read back with (per channel: (2, KV_N, D) memory, entry 0 for key and
+ * 1 for value; per tensor: (2,)) -- the inverse of the reading x = (code + offset) * scale.
+ */
+typedef struct ifa_append_params {
+    int64_t B;                /* batch, 0..2^20 */
+    int64_t numKeyValueHeads; /* KV_N, 1..256 */
+    int64_t headDim;          /* D: a multiple of 8 (16 for int8 caches), <= 512 */
+    int64_t maxSeqLen;        /* contiguous caches: Smax */
+    int64_t blockSize, blockNum, blockTableCols; /* paged caches */
+    int32_t new_dtype;        /* IFA_F16 or IFA_BF16: the new rows and the antiquant parameters */
+    int32_t kv_dtype;         /* = new_dtype, or IFA_I8 (requires antiquant) */
+    int32_t inputLayout;      /* ifa_layout of a contiguous cache */
+    int32_t kvFormat;         /* ifa_kv_format */
+    int32_t antiquant;        /* ifa_antiquant; not NONE exactly when kv_dtype is IFA_I8 */
+} ifa_append_params;
+
+/*
+ * Enqueue one append on `stream` (cudaStream_t, NULL = legacy default); one kernel launch.
+ * Device pointers: keyNew and valueNew (B, KV_N, D) in memory (any layout with S = 1) of
+ * new_dtype, 16-byte aligned; positions int64 (B), 8-byte aligned; blockTable int32
+ * (B, blockTableCols), paged only; antiquantScale / antiquantOffset (int8 caches) of
+ * new_dtype; keyCache and valueCache 16-byte aligned; deviceErrorFlags (int32, nullable)
+ * receives bit 1 for a batch whose position lies outside the cache (negative, >= Smax, past
+ * the block table, or a block id outside [0, blockNum)): that batch writes nothing.
+ * Returns IFA_ERR_PARAM_NULLPTR / IFA_ERR_PARAM_INVALID / IFA_ERR_RUNTIME as ifa_run does.
+ */
+ifa_status ifa_kv_append(const ifa_append_params* params, const void* keyNew, const void* valueNew,
+                         const int64_t* positions, const int32_t* blockTable, const void* antiquantScale,
+                         const void* antiquantOffset, void* keyCache, void* valueCache, int32_t* deviceErrorFlags,
+                         void* stream);
 
 /* Static text for a status code. */
 const char* ifa_status_string(ifa_status status);

@@ -61,6 +61,11 @@ struct alignas(128) DecodeParams {
     int mask_tma;              // the producer stages each tile's mask bytes (per-batch masks)
     int aq_per_channel;
     int aq_stage;              // per-channel key scales reach shared memory with each piece's query
+    int out_i8;                // int8 output: code = saturate(rint(y * scale2 + offset2))
+    int q2_per_channel;        // scale2/offset2 entry n * D + d (else entry 0)
+    int q2_bf16;               // scale2/offset2 are bf16 (else fp32)
+    const void* q2_scale;
+    const void* q2_offset;     // nullable: 0
     float scale_log2;          // scaleValue * log2(e)
     int slot_floats;
     unsigned int gen;          // call number: picks the counter set, and the set the call clears
@@ -150,7 +155,8 @@ void build_bounds(const ifa_params& p, const KernelChoice& kc, const int32_t* bd
 ifa_status check_run_pointers(const ifa_params& p, const void* query, const void* key, const void* value,
                               const void* attenMask, const int64_t* actualSeqLengths, const int64_t* kvPaddingSize,
                               int64_t n_kv_padding, const int32_t* blockTable, const void* antiquantScale,
-                              const void* antiquantOffset, const void* attentionOut);
+                              const void* antiquantOffset, const void* quantScale2, const void* quantOffset2,
+                              const void* attentionOut);
 bool encode_kv_map(const ifa_params& p, const KernelChoice& kc, const void* base, int box_rows, CUtensorMap* map);
 // The four maps a call needs (key/value x full/tail boxes).
 bool encode_kv_maps(const ifa_params& p, const KernelChoice& kc, const void* key, const void* value, DecodeParams& dp);
@@ -160,7 +166,8 @@ bool encode_mask_map(const ifa_params& p, const KernelChoice& kc, const void* ma
 // Everything but the tensor maps, the scratch pointers and the window table.
 void fill_decode_params(DecodeParams& dp, const ifa_params& p, const KernelChoice& kc, const void* query,
                         const void* attenMask, const int32_t* blockTable, const void* antiquantScale,
-                        const void* antiquantOffset, void* attentionOut, int64_t W, int P);
+                        const void* antiquantOffset, const void* quantScale2, const void* quantOffset2,
+                        void* attentionOut, int64_t W, int P);
 
 DecodeLaunchFn decode_launcher(int kv_kind, int dpad, int nt);
 bool decode_cfg(int kv_kind, int dpad, int nt, int* slot_floats, int* smem, int* tile_tokens, int* threads);

@@ -125,6 +125,32 @@ __device__ __forceinline__ void st_out(void* out, long long idx, float v, int is
     else reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
 }
 
+// int8 output code saturate(rint(v * scale2 + offset2)) of element idx (product and sum rounded
+// apart, ties to even, NaN -> 0).
+__device__ __forceinline__ void st_i8(const DecodeParams& p, long long idx, float v) {
+    // idx = (b * N + n) * D + d, so the per-channel entry n * D + d is idx mod N * D
+    const long long pi = p.q2_per_channel ? idx % ((long long)p.N * p.D) : 0;
+    float s, o = 0.f;
+    if (p.q2_bf16) {
+        s = __bfloat162float(__ushort_as_bfloat16(__ldg(reinterpret_cast<const unsigned short*>(p.q2_scale) + pi)));
+        if (p.q2_offset)
+            o = __bfloat162float(__ushort_as_bfloat16(__ldg(reinterpret_cast<const unsigned short*>(p.q2_offset) + pi)));
+    } else {
+        s = __ldg(reinterpret_cast<const float*>(p.q2_scale) + pi);
+        if (p.q2_offset) o = __ldg(reinterpret_cast<const float*>(p.q2_offset) + pi);
+    }
+    const float u = __fadd_rn(__fmul_rn(v, s), o);
+    int code = 0;
+    if (u == u) code = (int)fminf(fmaxf(rintf(u), -128.f), 127.f);
+    reinterpret_cast<int8_t*>(p.out)[idx] = (int8_t)code;
+}
+
+// Output element idx = (b * N + n) * D + d in the output dtype, or its int8 code.
+__device__ __forceinline__ void st_final(const DecodeParams& p, long long idx, float v) {
+    if (p.out_i8) st_i8(p, idx, v);
+    else st_out(p.out, idx, v, p.q_bf16);
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     if constexpr (BF16) {
@@ -291,7 +317,8 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     for (int b = blockIdx.x; b < B; b += p.P) {
         if (bd[B + b] != 0) continue;
         const long long base = (long long)b * p.N * p.D;
-        for (int idx = threadIdx.x; idx < p.N * p.D; idx += C::THREADS) st_out(p.out, base + idx, 0.f, p.q_bf16);
+        for (int idx = threadIdx.x; idx < p.N * p.D; idx += C::THREADS)
+            st_final(p, base + idx, 0.f);
     }
     if (lo >= hi) return;
 
@@ -773,7 +800,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                 if (gg < GTv && d < p.D) {
                     float y = v[e];
                     if constexpr (KV == KV_I8) y = ((e & 1) ? live1 : live0) ? (y + vof[n][e >> 1]) * vsc[n][e >> 1] : 0.f;
-                    st_out(p.out, obase + (long long)gg * p.D + d, y, p.q_bf16);
+                    st_final(p, obase + (long long)gg * p.D + d, y);
                 }
             }
         };

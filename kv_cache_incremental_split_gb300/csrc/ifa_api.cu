@@ -115,12 +115,14 @@ extern "C" ifa_status ifa_get_device_errors(ifa_plan* plan, void* stream, int64_
 extern "C" ifa_status ifa_run(ifa_plan* pl, const void* query, const void* key, const void* value,
                               const void* attenMask, const int64_t* actualSeqLengths,
                               const int64_t* kvPaddingSize, int64_t n_kv_padding, const int32_t* blockTable,
-                              const void* antiquantScale, const void* antiquantOffset, void* attentionOut,
-                              void* workspace, size_t workspace_bytes, void* stream) {
+                              const void* antiquantScale, const void* antiquantOffset, const void* quantScale2,
+                              const void* quantOffset2, void* attentionOut, void* workspace, size_t workspace_bytes,
+                              void* stream) {
     if (!pl) return IFA_ERR_PARAM_NULLPTR;
     const ifa_params& p = pl->prm;
     ifa_status st = check_run_pointers(p, query, key, value, attenMask, actualSeqLengths, kvPaddingSize,
-                                       n_kv_padding, blockTable, antiquantScale, antiquantOffset, attentionOut);
+                                       n_kv_padding, blockTable, antiquantScale, antiquantOffset, quantScale2,
+                                       quantOffset2, attentionOut);
     if (st != IFA_OK) return st;
     if (pl->ws_bytes > 0 && !workspace) return IFA_ERR_PARAM_NULLPTR;
     if (workspace_bytes < pl->ws_bytes) return IFA_ERR_PARAM_INVALID;
@@ -150,8 +152,8 @@ extern "C" ifa_status ifa_run(ifa_plan* pl, const void* query, const void* key, 
         if (!encode_mask_map(p, pl->kc, attenMask, dp)) return IFA_ERR_RUNTIME;
         pl->last_mask = attenMask;
     }
-    fill_decode_params(dp, p, pl->kc, query, attenMask, blockTable, antiquantScale, antiquantOffset, attentionOut, W,
-                       P);
+    fill_decode_params(dp, p, pl->kc, query, attenMask, blockTable, antiquantScale, antiquantOffset, quantScale2,
+                       quantOffset2, attentionOut, W, P);
     build_bounds(p, pl->kc, bd.data(), W, P, dp.bounds);
     dp.partials = reinterpret_cast<float*>(workspace);
     dp.err = pl->d_state;

@@ -59,7 +59,8 @@ extern "C" ifa_status ifa_run_noalloc(const ifa_params* params, const void* quer
                                       const void* value, const void* attenMask, const int64_t* actualSeqLengths,
                                       const int64_t* kvPaddingSize, int64_t n_kv_padding,
                                       const int32_t* blockTable, const void* antiquantScale,
-                                      const void* antiquantOffset, void* attentionOut, int32_t* deviceErrorFlags,
+                                      const void* antiquantOffset, const void* quantScale2,
+                                      const void* quantOffset2, void* attentionOut, int32_t* deviceErrorFlags,
                                       void* stream) {
     if (!params) return IFA_ERR_PARAM_NULLPTR;
     const ifa_params& p = *params;
@@ -68,7 +69,7 @@ extern "C" ifa_status ifa_run_noalloc(const ifa_params* params, const void* quer
     if (st != IFA_OK) return st;
     if (p.B > IFA_NOALLOC_MAX_BATCH) return IFA_ERR_PARAM_INVALID;  // windows must fit the launch parameters
     st = check_run_pointers(p, query, key, value, attenMask, actualSeqLengths, kvPaddingSize, n_kv_padding,
-                            blockTable, antiquantScale, antiquantOffset, attentionOut);
+                            blockTable, antiquantScale, antiquantOffset, quantScale2, quantOffset2, attentionOut);
     if (st != IFA_OK) return st;
     if (deviceErrorFlags && (reinterpret_cast<uintptr_t>(deviceErrorFlags) % 4) != 0) return IFA_ERR_PARAM_INVALID;
     const int B = (int)p.B;
@@ -97,7 +98,8 @@ extern "C" ifa_status ifa_run_noalloc(const ifa_params* params, const void* quer
     if (st != IFA_OK) return st;
     const int P = choose_grid(p, W, max_seq_tiles, P_max);
     if (!encode_kv_maps(p, kc, key, value, dp) || !encode_mask_map(p, kc, attenMask, dp)) return IFA_ERR_RUNTIME;
-    fill_decode_params(dp, p, kc, query, attenMask, blockTable, antiquantScale, antiquantOffset, attentionOut, W, P);
+    fill_decode_params(dp, p, kc, query, attenMask, blockTable, antiquantScale, antiquantOffset, quantScale2,
+                       quantOffset2, attentionOut, W, P);
     build_bounds(p, kc, dp.bdata_inline, W, P, dp.bounds);
     dp.partials = reinterpret_cast<float*>(scratch + kPartialOffset);
     dp.counters = reinterpret_cast<unsigned int*>(scratch + kCounterOffset);

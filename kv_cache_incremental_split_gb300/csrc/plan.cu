@@ -84,6 +84,13 @@ bool params_are_valid(const ifa_params& p) {
     }
     if (!std::isfinite(p.scaleValue)) return false;
     if (p.splitTiles < 0) return false;
+    if (p.out_dtype == IFA_I8) {
+        // README: FLOAT32 parameters, or BFLOAT16 ones with a bf16 query
+        if (p.quant2 != IFA_ANTIQUANT_PER_CHANNEL && p.quant2 != IFA_ANTIQUANT_PER_TENSOR) return false;
+        if (p.quant2_dtype != IFA_F32 && !(p.quant2_dtype == IFA_BF16 && p.q_dtype == IFA_BF16)) return false;
+    } else if (p.quant2 != IFA_ANTIQUANT_NONE) {
+        return false;
+    }
     return true;
 }
 
@@ -268,7 +275,8 @@ static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 ifa_status check_run_pointers(const ifa_params& p, const void* query, const void* key, const void* value,
                               const void* attenMask, const int64_t* actualSeqLengths, const int64_t* kvPaddingSize,
                               int64_t n_kv_padding, const int32_t* blockTable, const void* antiquantScale,
-                              const void* antiquantOffset, const void* attentionOut) {
+                              const void* antiquantOffset, const void* quantScale2, const void* quantOffset2,
+                              const void* attentionOut) {
     const bool paged = p.kvFormat != IFA_KV_CONTIG;
     if (!query || !key || !value || !attentionOut) return IFA_ERR_PARAM_NULLPTR;
     if (p.has_mask && !attenMask) return IFA_ERR_PARAM_NULLPTR;
@@ -282,6 +290,11 @@ ifa_status check_run_pointers(const ifa_params& p, const void* query, const void
         return IFA_ERR_PARAM_INVALID;
     if (p.has_kv_padding && actualSeqLengths && n_kv_padding != 1 && n_kv_padding != p.B)
         return IFA_ERR_PARAM_INVALID;
+    if (p.out_dtype == IFA_I8) {
+        if (!quantScale2) return IFA_ERR_PARAM_NULLPTR;
+        const uintptr_t a = p.quant2_dtype == IFA_F32 ? 4 : 2;
+        if (!aligned(quantScale2, a) || (quantOffset2 && !aligned(quantOffset2, a))) return IFA_ERR_PARAM_INVALID;
+    }
     return IFA_OK;
 }
 
@@ -358,7 +371,8 @@ bool encode_mask_map(const ifa_params& p, const KernelChoice& kc, const void* ma
 
 void fill_decode_params(DecodeParams& dp, const ifa_params& p, const KernelChoice& kc, const void* query,
                         const void* attenMask, const int32_t* blockTable, const void* antiquantScale,
-                        const void* antiquantOffset, void* attentionOut, int64_t W, int P) {
+                        const void* antiquantOffset, const void* quantScale2, const void* quantOffset2,
+                        void* attentionOut, int64_t W, int P) {
     dp.q = query;
     dp.out = attentionOut;
     dp.mask = reinterpret_cast<const uint8_t*>(attenMask);
@@ -389,6 +403,11 @@ void fill_decode_params(DecodeParams& dp, const ifa_params& p, const KernelChoic
     dp.aq_stage = dp.aq_per_channel && aligned(antiquantScale, 16);
     dp.scale_log2 = (float)(p.scaleValue * 1.4426950408889634);
     dp.slot_floats = kc.slot_floats;
+    dp.out_i8 = p.out_dtype == IFA_I8;
+    dp.q2_per_channel = dp.out_i8 && p.quant2 == IFA_ANTIQUANT_PER_CHANNEL;
+    dp.q2_bf16 = dp.out_i8 && p.quant2_dtype == IFA_BF16;
+    dp.q2_scale = dp.out_i8 ? quantScale2 : nullptr;
+    dp.q2_offset = dp.out_i8 ? quantOffset2 : nullptr;
 }
 
 }  // namespace ifa

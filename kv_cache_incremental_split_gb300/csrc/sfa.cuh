@@ -23,12 +23,13 @@ constexpr int kSfaRSlots = 8;       // resolved tiles the resolver warp may run 
 constexpr int kSfaRSlotBytes = 288; // rows[64], valid mask, flag (16-byte aligned)
 constexpr int kSfaIssuers = 4;     // warps that issue the ring's gathers (a stage's 16 row groups split evenly)
 constexpr int kSfaThreads = 10 * 32;  // producer, MMA issuer, four softmax warps, resolver, three more gatherers
-constexpr int kSfaSlotFloats = 128 * kSfaHalf + 2 * 128;  // normalised O of one piece + M + L
+constexpr int kSfaSlotFloats = 128 * kSfaHalf + 3 * 128;  // normalised O of one piece + M + L + largest score
 constexpr int kSfaBarBytes = 512;
 constexpr int kSfaSmem = 1024 + kSfaQBytes + kSfaStages * kSfaStageBytes + kSfaRSlots * kSfaRSlotBytes + kSfaBarBytes;
 constexpr size_t kSfaPartialOffset = 4096;  // workspace: [0,256) error word, partial slots from here
 constexpr float kSfaRescaleSlack = 8.0f;    // log2 units the running max may trail before O is rescaled
 constexpr int kSfaCombineRows = 16;         // query heads per combine CTA
+constexpr float kLn2 = 0.6931471805599453f;  // scores in log2 units -> natural units
 
 struct alignas(128) SfaParams {
     CUtensorMap tmQ;    // 3-D (d, head, query row) over query, 64 x 128 x 1 boxes
@@ -41,15 +42,21 @@ struct alignas(128) SfaParams {
     CUtensorMap tmVb;
     const int32_t* indices;
     const int32_t* block_table;
-    const int32_t* lens;
-    const int32_t* lens_q;  // valid query tokens per batch (nullable: all Q_S)
+    const int32_t* lens;    // key lengths per batch; prefix sums when the key layout is TND
+    const int32_t* lens_q;  // valid query tokens per batch (nullable: all Q_S); prefix sums for TND queries
     void* out;
+    float* lse_max;         // nullable: largest scaled score of each (query row, head)
+    float* lse_sum;         // nullable: sum of exp(score - lse_max) of each (query row, head)
     float* partials;
     int* err;
     long long W;        // tiles: 2 * R * tiles_per_seq
     int P;
-    int R, QS, QN, S_sp, tiles_per_seq;  // R = B * QS query rows (row r: batch r / QS, query token r % QS);
-                                         // S_sp: indices per row; tiles cover S_sp << sbs_log2 positions
+    int R, QS, QN, S_sp, tiles_per_seq;  // R query rows: B * QS (row r: batch r / QS, query token r % QS), or
+                                         // the TND rows; S_sp: indices per row; tiles cover S_sp << sbs_log2
+    int B;                           // batches (entries of the length arrays)
+    int q_tnd;                       // query rows packed per batch (prefix-sum lens_q)
+    int kv_layout;                   // 0 PA_BSND (block table), 1 BSND (row b * kv_s + t), 2 TND (prefix-sum lens)
+    int kv_s;                        // BSND: tokens per batch in the key tensor; TND: key rows
     int causal;                      // sparse_mode 3: query token s of a batch sees keys up to len - qlen + s
     int sbs_log2;                    // log2(sparse_block_size): position p reads index p >> sbs_log2
     int block_size, bt_cols, block_num, total_rows;

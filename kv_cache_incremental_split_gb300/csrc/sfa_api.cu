@@ -1,8 +1,8 @@
 // C ABI of the sparse MLA-absorb decode (sfa_workspace_size, sfa_run).  The
 // checks follow the "SparseFlashAttention" README's 参数说明 and 约束说明 for
-// the decode case this library implements (BSND query with Q_S query tokens,
-// PA_BSND key/value, KV_N = 1, D = 512, Dr = 64, token-wise or block-wise
-// sparsity, sparse_mode 0 or 3, MLA-absorb).
+// the decode case this library implements (BSND or TND queries, PA_BSND, BSND
+// or TND key/value, KV_N = 1, D = 512, Dr = 64, token-wise or block-wise
+// sparsity, sparse_mode 0 or 3, MLA-absorb, optional softmax_max/softmax_sum).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -21,17 +21,32 @@ namespace {
 
 bool sfa_valid(const sfa_params& p) {
     if (p.B < 0 || p.B > 65536) return false;
-    if (p.Q_S < 1 || p.Q_S > 1024 || p.B * p.Q_S > (1 << 20)) return false;
+    if (p.layout_query == SFA_LAYOUT_BSND) {
+        if (p.Q_S < 1 || p.Q_S > 1024 || p.B * p.Q_S > (1 << 20)) return false;
+    } else if (p.layout_query == SFA_LAYOUT_TND) {
+        if (p.Q_T < 0 || p.Q_T > (1 << 20) || (p.B < 1 && p.Q_T > 0)) return false;
+    } else {
+        return false;
+    }
     if (p.Q_N < 1 || p.Q_N > 128) return false;
     if (p.KV_N != 1 || p.D != kSfaD || p.Dr != kSfaDr) return false;
-    if (p.block_size < 16 || p.block_size > 1024 || p.block_size % 16 != 0) return false;
-    if (p.block_num < 1 || p.block_table_cols < 1 || p.sparse_size < 1) return false;
-    if (p.block_num * p.block_size >= INT32_MAX) return false;
-    if (p.sparse_size > INT32_MAX / 2 || p.block_table_cols > INT32_MAX / 2) return false;
-    // token-wise (1) or block-wise: a power of two up to 128 that divides block_size
+    if (p.sparse_size < 1 || p.sparse_size > INT32_MAX / 2) return false;
+    // token-wise (1) or block-wise: a power of two up to 128 (that divides block_size when paged)
     if (p.sparse_block_size < 1 || p.sparse_block_size > 128 || (p.sparse_block_size & (p.sparse_block_size - 1)) != 0)
         return false;
-    if (p.block_size % p.sparse_block_size != 0) return false;
+    if (p.layout_kv == SFA_KV_PA_BSND) {
+        if (p.block_size < 16 || p.block_size > 1024 || p.block_size % 16 != 0) return false;
+        if (p.block_num < 1 || p.block_table_cols < 1) return false;
+        if (p.block_num * p.block_size >= INT32_MAX) return false;
+        if (p.block_table_cols > INT32_MAX / 2) return false;
+        if (p.block_size % p.sparse_block_size != 0) return false;
+    } else if (p.layout_kv == SFA_KV_BSND) {
+        if (p.KV_S < 1 || p.KV_S >= INT32_MAX || p.B * p.KV_S >= INT32_MAX) return false;
+    } else if (p.layout_kv == SFA_KV_TND) {
+        if (p.KV_S < 1 || p.KV_S >= INT32_MAX) return false;
+    } else {
+        return false;
+    }
     if (p.sparse_size * p.sparse_block_size > INT32_MAX / 2) return false;
     if (p.sparse_mode != 0 && p.sparse_mode != 3) return false;
     if (p.dtype != IFA_BF16 && p.dtype != IFA_F16) return false;
@@ -95,25 +110,33 @@ extern "C" ifa_status sfa_workspace_size(const sfa_params* params, size_t* works
 extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const void* query_rope, const void* key,
                               const void* key_rope, const void* value, const int32_t* sparse_indices,
                               const int32_t* block_table, const int32_t* actual_seq_lengths_kv,
-                              const int32_t* actual_seq_lengths_query, void* attention_out, void* workspace,
-                              size_t workspace_bytes, int32_t* deviceErrorFlags, void* stream) {
+                              const int32_t* actual_seq_lengths_query, void* attention_out, float* softmax_max,
+                              float* softmax_sum, void* workspace, size_t workspace_bytes, int32_t* deviceErrorFlags,
+                              void* stream) {
     if (!params) return IFA_ERR_PARAM_NULLPTR;
     const sfa_params& p = *params;
     if (!sfa_valid(p)) return IFA_ERR_PARAM_INVALID;
-    if (!query || !query_rope || !key || !key_rope || !value || !sparse_indices || !block_table ||
-        !actual_seq_lengths_kv || !attention_out || !workspace)
+    const bool paged = p.layout_kv == SFA_KV_PA_BSND;
+    if (!query || !query_rope || !key || !key_rope || !value || !sparse_indices || !attention_out || !workspace)
         return IFA_ERR_PARAM_NULLPTR;
+    if (paged && !block_table) return IFA_ERR_PARAM_NULLPTR;
+    if (p.layout_kv != SFA_KV_BSND && !actual_seq_lengths_kv) return IFA_ERR_PARAM_NULLPTR;
+    if (p.layout_query == SFA_LAYOUT_TND && !actual_seq_lengths_query) return IFA_ERR_PARAM_NULLPTR;
+    if ((softmax_max == nullptr) != (softmax_sum == nullptr)) return IFA_ERR_PARAM_NULLPTR;
     if (!aligned(query, 16) || !aligned(query_rope, 16) || !aligned(key, 16) || !aligned(key_rope, 16) ||
-        !aligned(value, 16) || !aligned(attention_out, 16) || !aligned(workspace, 16) ||
-        !aligned(sparse_indices, 4) || !aligned(block_table, 4) || !aligned(actual_seq_lengths_kv, 4))
+        !aligned(value, 16) || !aligned(attention_out, 16) || !aligned(workspace, 16) || !aligned(sparse_indices, 4))
         return IFA_ERR_PARAM_INVALID;
-    if (actual_seq_lengths_query && !aligned(actual_seq_lengths_query, 4)) return IFA_ERR_PARAM_INVALID;
+    if ((paged && !aligned(block_table, 4)) || (actual_seq_lengths_kv && !aligned(actual_seq_lengths_kv, 4)) ||
+        (actual_seq_lengths_query && !aligned(actual_seq_lengths_query, 4)) ||
+        (softmax_max && (!aligned(softmax_max, 4) || !aligned(softmax_sum, 4))))
+        return IFA_ERR_PARAM_INVALID;
     if (deviceErrorFlags && !aligned(deviceErrorFlags, 4)) return IFA_ERR_PARAM_INVALID;
     size_t need = 0;
     const ifa_status st = sfa_workspace_size(&p, &need);
     if (st != IFA_OK) return st;
     if (workspace_bytes < need) return IFA_ERR_PARAM_INVALID;
-    if (p.B == 0) return IFA_OK;
+    const int64_t R = p.layout_query == SFA_LAYOUT_TND ? p.Q_T : p.B * p.Q_S;  // query rows, each its own problem
+    if (p.B == 0 || R == 0) return IFA_OK;
 
     const int sms = sm_count();
     const int P_max = std::min(kMaxCtas, sms);
@@ -121,8 +144,8 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
     std::memset(&sp, 0, sizeof(sp));
     const bool bf = p.dtype == IFA_BF16;
     const uint64_t es = 2;
-    const int64_t R = p.B * p.Q_S;  // query rows: (batch, query token) pairs, each its own problem
-    const uint64_t rows = (uint64_t)(p.block_num * p.block_size);
+    const uint64_t rows = (uint64_t)(paged ? p.block_num * p.block_size
+                                           : (p.layout_kv == SFA_KV_BSND ? p.B * p.KV_S : p.KV_S));
     {
         cuuint64_t dq[3] = {(cuuint64_t)kSfaD, (cuuint64_t)p.Q_N, (cuuint64_t)R};
         cuuint64_t sq[2] = {kSfaD * es, (cuuint64_t)p.Q_N * kSfaD * es};
@@ -158,22 +181,28 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
     sp.block_table = block_table;
     sp.lens = actual_seq_lengths_kv;
     sp.lens_q = actual_seq_lengths_query;
+    sp.lse_max = softmax_max;
+    sp.lse_sum = softmax_sum;
+    sp.B = (int)p.B;
+    sp.q_tnd = p.layout_query == SFA_LAYOUT_TND;
+    sp.kv_layout = p.layout_kv;
+    sp.kv_s = paged ? 0 : (int)p.KV_S;
     sp.out = attention_out;
     sp.partials = reinterpret_cast<float*>(ws + kSfaPartialOffset);
     sp.err = deviceErrorFlags ? deviceErrorFlags : reinterpret_cast<int*>(ws);
     sp.W = W;
     sp.P = P;
     sp.R = (int)R;
-    sp.QS = (int)p.Q_S;
+    sp.QS = p.layout_query == SFA_LAYOUT_TND ? 1 : (int)p.Q_S;
     sp.causal = p.sparse_mode == 3;
     sp.QN = (int)p.Q_N;
     sp.S_sp = (int)p.sparse_size;
     sp.sbs_log2 = 0;
     while ((1LL << sp.sbs_log2) < p.sparse_block_size) ++sp.sbs_log2;
     sp.tiles_per_seq = tps;
-    sp.block_size = (int)p.block_size;
-    sp.bt_cols = (int)p.block_table_cols;
-    sp.block_num = (int)p.block_num;
+    sp.block_size = paged ? (int)p.block_size : 1;
+    sp.bt_cols = paged ? (int)p.block_table_cols : 0;
+    sp.block_num = paged ? (int)p.block_num : 0;
     sp.total_rows = (int)rows;
     sp.is_bf16 = bf;
     sp.scale_log2 = (float)(p.scale_value * 1.4426950408889634);

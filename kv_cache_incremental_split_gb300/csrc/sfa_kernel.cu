@@ -165,36 +165,76 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             if (idx < 0 || idx / p.block_size >= p.bt_cols) return -1;
             return __ldg(p.block_table + (long long)b * p.bt_cols + idx / p.block_size);
         };
-        // keys query row r may use: [0, limit).  Rows past the batch's valid query tokens use
-        // none; under the right-down causal mode token s sits at key len - qlen + s.
-        auto row_limit = [&](int b, int r) -> int {
-            const int len = __ldg(p.lens + b);
-            if (p.QS == 1 && !p.lens_q) return len;
-            const int s = r - b * p.QS;
-            const int qlen = p.lens_q ? __ldg(p.lens_q + b) : p.QS;
-            if (s >= qlen) return 0;
-            if (!p.causal) return len;
-            const long long lim = (long long)len - qlen + s + 1;  // <= len since s < qlen
-            return lim < 0 ? 0 : (int)lim;
+        // TND query rows: the batch of a row is the first whose prefix sum exceeds it.  Rows only
+        // rise within a CTA's range, so a binary search places the first and the rest step on.
+        const bool paged = p.kv_layout == 0;
+        int tnd_b = 0;
+        if (p.q_tnd) {
+            const int r_first = (int)(lo / tps) >> 1;
+            int a = 0, z = p.B;  // first b in [a, z] with lens_q[b] > r_first (z = B: none)
+            while (a < z) {
+                const int mid = (a + z) >> 1;
+                if (__ldg(p.lens_q + mid) > r_first) z = mid;
+                else a = mid + 1;
+            }
+            tnd_b = a;
+        }
+        // Batch of query row r (-1: none), the keys it may use ([0, limit): rows past the
+        // batch's valid query tokens use none; under the right-down causal mode token s sits at
+        // key len - qlen + s), and the batch's first key row (BSND and TND key layouts).
+        auto row_info = [&](int r, int& b, int& limit, int& base) {
+            int s, qlen;
+            b = -1;
+            limit = 0;
+            base = 0;
+            if (p.q_tnd) {
+                while (tnd_b < p.B && __ldg(p.lens_q + tnd_b) <= r) ++tnd_b;
+                if (tnd_b >= p.B) return;
+                const int first = tnd_b > 0 ? __ldg(p.lens_q + tnd_b - 1) : 0;
+                b = tnd_b;
+                s = r - first;
+                qlen = __ldg(p.lens_q + tnd_b) - first;
+            } else {
+                b = r / p.QS;
+                s = r - b * p.QS;
+                qlen = p.lens_q ? __ldg(p.lens_q + b) : p.QS;
+            }
+            long long len, avail = INT32_MAX;
+            if (paged) {
+                len = __ldg(p.lens + b);
+            } else if (p.kv_layout == 1) {
+                len = p.lens ? __ldg(p.lens + b) : p.kv_s;
+                base = b * p.kv_s;  // < 2^31: the host checks B * KV_S
+                avail = p.kv_s;
+            } else {
+                base = b > 0 ? __ldg(p.lens + b - 1) : 0;
+                len = (long long)__ldg(p.lens + b) - base;
+                avail = (long long)p.kv_s - base;
+                if (base < 0) avail = 0;  // a malformed prefix: nothing to read
+            }
+            long long lim = len;
+            if (s >= qlen) lim = 0;
+            else if (p.causal) lim = len - qlen + s + 1;  // <= len since s < qlen
+            if (lim > avail) lim = avail;
+            limit = lim < 0 ? 0 : (int)lim;
         };
         int i0lo, i0hi, i1lo, i1hi;
         load_idx(lo, i0lo, i0hi);
         load_idx(lo + 1, i1lo, i1hi);
-        int r0 = (int)(lo / tps) >> 1;
-        int b0 = r0 / p.QS;
-        int len0 = row_limit(b0, r0);
-        int bt0lo = load_blk(b0, i0lo), bt0hi = load_blk(b0, i0hi);
+        int b0, len0, base0;
+        row_info((int)(lo / tps) >> 1, b0, len0, base0);
+        int bt0lo = paged && b0 >= 0 ? load_blk(b0, i0lo) : -1, bt0hi = paged && b0 >= 0 ? load_blk(b0, i0hi) : -1;
         long long k = 0;
         for (long long g = lo; g < hi; ++g, ++k) {
             int i2lo, i2hi;
             load_idx(g + 2, i2lo, i2hi);
-            int b1 = 0, len1 = 0, bt1lo = -1, bt1hi = -1;
+            int b1 = -1, len1 = 0, base1 = 0, bt1lo = -1, bt1hi = -1;
             if (g + 1 < hi) {
-                const int r1 = (int)((g + 1) / tps) >> 1;
-                b1 = r1 / p.QS;
-                len1 = row_limit(b1, r1);
-                bt1lo = load_blk(b1, i1lo);
-                bt1hi = load_blk(b1, i1hi);
+                row_info((int)((g + 1) / tps) >> 1, b1, len1, base1);
+                if (paged && b1 >= 0) {
+                    bt1lo = load_blk(b1, i1lo);
+                    bt1hi = load_blk(b1, i1hi);
+                }
             }
             // rows of tile g: invalid (total_rows) outside [0, limit); bad block-table entries are flagged
             int rows2[2];
@@ -205,7 +245,8 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 const int blk = u ? bt0hi : bt0lo;
                 int r = p.total_rows;
                 if (idx >= 0 && idx < len0) {
-                    if (blk < 0 || blk >= p.block_num) bad = true;  // includes a length beyond the block table
+                    if (!paged) r = base0 + idx;  // < total_rows: the limit stops at the tensor's end
+                    else if (blk < 0 || blk >= p.block_num) bad = true;  // includes a length beyond the block table
                     else r = blk * p.block_size + idx % p.block_size;
                 }
                 rows2[u] = r;
@@ -236,6 +277,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             i1hi = i2hi;
             b0 = b1;
             len0 = len1;
+            base0 = base1;
             bt0lo = bt1lo;
             bt0hi = bt1hi;
             if (*abort_flag) break;
@@ -487,6 +529,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const bool bf = p.is_bf16 != 0;
         float m_used = -INFINITY, l_sum = 0.f;
+        float m_top = -INFINITY;  // largest scaled score of the piece (m_used may trail it by the slack)
         int n = 0;        // processed tiles so far
         int n_last = -1;  // last processed tile of the current piece
         auto fail = [&]() {
@@ -499,6 +542,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             const int b = seq >> 1, h = seq & 1;
             if (t == 0 || g == lo) {
                 m_used = -INFINITY;
+                m_top = -INFINITY;
                 l_sum = 0.f;
                 n_last = -1;
             }
@@ -530,6 +574,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                     x[j + 32] = ((vm_hi >> j) & 1) ? __uint_as_float(sb2[j]) * p.scale_log2 : -INFINITY;
                     tmax = fmaxf(tmax, fmaxf(x[j], x[j + 32]));
                 }
+                m_top = fmaxf(m_top, tmax);
                 const float m_new = fmaxf(m_used, tmax);
                 const bool need = m_new > m_used + kSfaRescaleSlack;  // also true when m_used = -inf < m_new
                 if (__any_sync(0xffffffffu, need)) {
@@ -628,6 +673,13 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             if (!complete) {
                 sp[128 * kSfaHalf + row] = m_used;
                 sp[128 * kSfaHalf + 128 + row] = l_sum;
+                sp[128 * kSfaHalf + 256 + row] = m_top;
+            } else if (p.lse_max && h == 0 && row < p.QN) {
+                // the largest score and the sum of exp(score - it), in natural units: the scores
+                // here are log2(e) * scale * q.k
+                const long long li = (long long)b * p.QN + row;
+                p.lse_max[li] = m_top == -INFINITY ? -INFINITY : m_top * kLn2;
+                p.lse_sum[li] = m_top == -INFINITY ? 0.f : l_sum * ex2f_approx(m_used - m_top);
             }
         }
     }
@@ -685,6 +737,19 @@ __global__ void __launch_bounds__(128) sfa_combine(const __grid_constant__ SfaPa
     }
     const float inv = S > 0.f ? 1.f / S : 0.f;
     const bool bf = p.is_bf16 != 0;
+    if (p.lse_max && h == 0 && (threadIdx.x & 7) == 0) {
+        float Mt = -INFINITY;
+        for (int k = 0; k < np; ++k) Mt = fmaxf(Mt, __ldcg(slot_ptr(k) + 128 * kSfaHalf + 256 + row));
+        float St = 0.f;
+        for (int k = 0; k < np; ++k) {
+            const float* pp = slot_ptr(k);
+            const float mk = __ldcg(pp + 128 * kSfaHalf + row);
+            if (mk != -INFINITY) St += __ldcg(pp + 128 * kSfaHalf + 128 + row) * ex2f_approx(mk - Mt);
+        }
+        const long long li = (long long)b * p.QN + row;
+        p.lse_max[li] = Mt == -INFINITY ? -INFINITY : Mt * kLn2;
+        p.lse_sum[li] = Mt == -INFINITY ? 0.f : St;
+    }
     uint32_t wv[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) wv[j] = pack2(acc[2 * j] * inv, acc[2 * j + 1] * inv, bf);

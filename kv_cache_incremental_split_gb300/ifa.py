@@ -28,12 +28,12 @@ IFA_ERR_RUNTIME = 361001
 
 LAYOUTS = {"BSH": 0, "BSND": 1, "BNSD": 2}
 KV_FORMATS = {"contig": 0, "paged_nbsd": 1, "paged_bsh": 2}
-DTYPES = {"fp16": 0, "bf16": 1, "int8": 2, "uint8": 3, "bool": 4}
+DTYPES = {"fp16": 0, "bf16": 1, "int8": 2, "uint8": 3, "bool": 4, "fp32": 5}
 ANTIQUANT = {"none": 0, "per_channel": 1, "per_tensor": 2}
 
 # Every symbol include/ifa.h declares.
 EXPORTED = ("ifa_create", "ifa_run", "ifa_destroy", "ifa_get_device_errors", "ifa_last_launch_count",
-            "ifa_run_noalloc", "sfa_workspace_size", "sfa_run", "ifa_status_string")
+            "ifa_run_noalloc", "sfa_workspace_size", "sfa_run", "ifa_kv_append", "ifa_status_string")
 
 # Fixed scratch of ifa_run_noalloc (include/ifa.h).
 IFA_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -51,17 +51,25 @@ class IfaParams(ctypes.Structure):
         ("maskB", ctypes.c_int64), ("maskN", ctypes.c_int64), ("maskS", ctypes.c_int64),
         ("antiquant", ctypes.c_int32), ("has_kv_padding", ctypes.c_int32),
         ("scaleValue", ctypes.c_double), ("splitTiles", ctypes.c_int64),
+        ("out_dtype", ctypes.c_int32), ("quant2", ctypes.c_int32), ("quant2_dtype", ctypes.c_int32),
     ]
 
 
 class SfaParams(ctypes.Structure):
-    _fields_ = [
-        ("B", ctypes.c_int64), ("Q_S", ctypes.c_int64), ("Q_N", ctypes.c_int64), ("KV_N", ctypes.c_int64), ("D", ctypes.c_int64),
-        ("Dr", ctypes.c_int64), ("block_size", ctypes.c_int64), ("block_num", ctypes.c_int64),
-        ("block_table_cols", ctypes.c_int64), ("sparse_size", ctypes.c_int64),
-        ("sparse_block_size", ctypes.c_int64), ("dtype", ctypes.c_int32), ("sparse_mode", ctypes.c_int32),
-        ("scale_value", ctypes.c_double),
-    ]
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "B", "Q_S", "Q_T", "Q_N", "KV_N", "D", "Dr", "KV_S", "block_size", "block_num", "block_table_cols",
+        "sparse_size", "sparse_block_size")] + [(n, ctypes.c_int32) for n in (
+            "dtype", "sparse_mode", "layout_query", "layout_kv")] + [("scale_value", ctypes.c_double)]
+
+
+class AppendParams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "B", "numKeyValueHeads", "headDim", "maxSeqLen", "blockSize", "blockNum", "blockTableCols")] + [
+        (n, ctypes.c_int32) for n in ("new_dtype", "kv_dtype", "inputLayout", "kvFormat", "antiquant")]
+
+
+SFA_LAYOUT_QUERY = {"BSND": 0, "TND": 1}
+SFA_LAYOUT_KV = {"PA_BSND": 0, "BSND": 1, "TND": 2}
 
 
 _lib = None
@@ -86,7 +94,7 @@ def load_library():
             lib.ifa_create.restype = ctypes.c_int32
             lib.ifa_create.argtypes = [ctypes.POINTER(IfaParams), ctypes.POINTER(vp), ctypes.POINTER(sz)]
             lib.ifa_run.restype = ctypes.c_int32
-            lib.ifa_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]
+            lib.ifa_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp]
             lib.ifa_destroy.restype = ctypes.c_int32
             lib.ifa_destroy.argtypes = [vp]
             lib.ifa_get_device_errors.restype = ctypes.c_int32
@@ -95,12 +103,14 @@ def load_library():
             lib.ifa_last_launch_count.argtypes = [vp]
             lib.ifa_run_noalloc.restype = ctypes.c_int32
             lib.ifa_run_noalloc.argtypes = [ctypes.POINTER(IfaParams), vp, vp, vp, vp, vp, vp, i64, vp, vp, vp,
-                                            vp, vp, vp]
+                                            vp, vp, vp, vp, vp]
             lib.sfa_workspace_size.restype = ctypes.c_int32
             lib.sfa_workspace_size.argtypes = [ctypes.POINTER(SfaParams), ctypes.POINTER(sz)]
+            lib.ifa_kv_append.restype = ctypes.c_int32
+            lib.ifa_kv_append.argtypes = [ctypes.POINTER(AppendParams), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.sfa_run.restype = ctypes.c_int32
-            lib.sfa_run.argtypes = [ctypes.POINTER(SfaParams), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp,
-                                    vp]
+            lib.sfa_run.argtypes = [ctypes.POINTER(SfaParams), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                    sz, vp, vp]
             lib.ifa_status_string.restype = ctypes.c_char_p
             lib.ifa_status_string.argtypes = [ctypes.c_int32]
             _lib = lib
@@ -122,23 +132,23 @@ def ifa_create(params: IfaParams):
 
 def ifa_run(plan, query, key, value, atten_mask, actual_seq_lengths, kv_padding_size, n_kv_padding,
             block_table, antiquant_scale, antiquant_offset, attention_out, workspace, workspace_bytes,
-            stream) -> int:
+            stream, quant_scale2=None, quant_offset2=None) -> int:
     """All pointer arguments are integers (device addresses, or host addresses for
     ``actual_seq_lengths`` / ``kv_padding_size``) or None."""
     return load_library().ifa_run(plan, query, key, value, atten_mask, actual_seq_lengths, kv_padding_size,
-                                   n_kv_padding, block_table, antiquant_scale, antiquant_offset, attention_out,
-                                   workspace, workspace_bytes, stream)
+                                   n_kv_padding, block_table, antiquant_scale, antiquant_offset, quant_scale2,
+                                   quant_offset2, attention_out, workspace, workspace_bytes, stream)
 
 
 def ifa_run_noalloc(params: IfaParams, query, key, value, atten_mask, actual_seq_lengths, kv_padding_size,
                     n_kv_padding, block_table, antiquant_scale, antiquant_offset, attention_out,
-                    device_error_flags, stream) -> int:
+                    device_error_flags, stream, quant_scale2=None, quant_offset2=None) -> int:
     """Plan-less, allocation-free call (include/ifa.h): for callers that cannot
     allocate device memory.  Pointer arguments are integers or None."""
     return load_library().ifa_run_noalloc(ctypes.byref(params), query, key, value, atten_mask,
                                           actual_seq_lengths, kv_padding_size, n_kv_padding, block_table,
-                                          antiquant_scale, antiquant_offset, attention_out,
-                                          device_error_flags, stream)
+                                          antiquant_scale, antiquant_offset, quant_scale2, quant_offset2,
+                                          attention_out, device_error_flags, stream)
 
 
 def ifa_destroy(plan) -> int:
@@ -177,7 +187,8 @@ class IncreFlashAttention:
                  block_num: int = 0, block_table_cols: int = 0,
                  mask_shape: Optional[Sequence[int]] = None, mask_dtype: str = "bool",
                  antiquant: str = "none", kv_padding: bool = False,
-                 scale: Optional[float] = None, split_tiles: int = 0, device=None):
+                 scale: Optional[float] = None, split_tiles: int = 0, out_dtype: Optional[str] = None,
+                 quant2: str = "none", quant2_dtype: str = "fp32", device=None):
         import torch
         p = IfaParams()
         p.B, p.numHeads, p.numKeyValueHeads, p.headDim = batch, num_heads, num_kv_heads, head_dim
@@ -195,6 +206,10 @@ class IncreFlashAttention:
         p.has_kv_padding = int(bool(kv_padding))
         p.scaleValue = (1.0 / math.sqrt(head_dim)) if scale is None else float(scale)
         p.splitTiles = split_tiles
+        self.out_i8 = out_dtype == "int8"
+        p.out_dtype = DTYPES["int8"] if self.out_i8 else p.q_dtype
+        p.quant2 = ANTIQUANT[quant2]
+        p.quant2_dtype = DTYPES[quant2_dtype] if self.out_i8 else 0
         self.params = p
         self.batch, self.num_heads, self.head_dim = batch, num_heads, head_dim
         self.dtype = dtype
@@ -215,17 +230,19 @@ class IncreFlashAttention:
 
     def __call__(self, query, key, value, *, atten_mask=None, actual_seq_lengths=None,
                  kv_padding_size=None, block_table=None, antiquant_scale=None, antiquant_offset=None,
-                 out=None, stream=None):
+                 quant_scale2=None, quant_offset2=None, out=None, stream=None):
         import torch
         if out is None:
-            out = torch.empty_like(query)
+            out = torch.empty(query.shape, dtype=torch.int8, device=query.device) if self.out_i8 \
+                else torch.empty_like(query)
         lens = None if actual_seq_lengths is None else np.ascontiguousarray(actual_seq_lengths, dtype=np.int64)
         pads = None if kv_padding_size is None else np.ascontiguousarray(kv_padding_size, dtype=np.int64).reshape(-1)
         st = ifa_run(self.plan, _ptr(query), _ptr(key), _ptr(value), _ptr(atten_mask),
                      None if lens is None else lens.ctypes.data,
                      None if pads is None else pads.ctypes.data, 0 if pads is None else pads.size,
                      _ptr(block_table), _ptr(antiquant_scale), _ptr(antiquant_offset), _ptr(out),
-                     _ptr(self.workspace), self.workspace.numel(), _stream_handle(stream))
+                     _ptr(self.workspace), self.workspace.numel(), _stream_handle(stream),
+                     quant_scale2=_ptr(quant_scale2), quant_offset2=_ptr(quant_offset2))
         if st != IFA_OK:
             raise IfaError(st, "ifa_run")
         return out
@@ -245,12 +262,12 @@ def sfa_workspace_size(params: SfaParams):
 
 
 def sfa_run(params: SfaParams, query, query_rope, key, key_rope, value, sparse_indices, block_table,
-            actual_seq_lengths_kv, actual_seq_lengths_query, attention_out, workspace, workspace_bytes,
-            device_error_flags, stream) -> int:
+            actual_seq_lengths_kv, actual_seq_lengths_query, attention_out, softmax_max, softmax_sum, workspace,
+            workspace_bytes, device_error_flags, stream) -> int:
     """Pointer arguments are integers (device addresses) or None."""
     return load_library().sfa_run(ctypes.byref(params), query, query_rope, key, key_rope, value, sparse_indices,
                                   block_table, actual_seq_lengths_kv, actual_seq_lengths_query, attention_out,
-                                  workspace, workspace_bytes, device_error_flags, stream)
+                                  softmax_max, softmax_sum, workspace, workspace_bytes, device_error_flags, stream)
 
 
 class SparseFlashAttention:
@@ -258,19 +275,28 @@ class SparseFlashAttention:
 
     Construction validates the static description and allocates the workspace
     with torch; calling the object enqueues ``sfa_run`` on the current (or given)
-    torch stream and returns the output tensor (B, Q_S, Q_N, 512).  ``q_seq_len`` is Q_S,
-    the query tokens per batch (several for multi-token prediction); ``sparse_mode`` 3
-    masks each of them right-down causally.
+    torch stream and returns the output tensor, shaped like the query.  ``q_seq_len`` is
+    Q_S, the query tokens per batch with ``layout_query`` "BSND" (several for multi-token
+    prediction); with "TND", ``q_total`` is Q_T and the query lengths are prefix sums.
+    ``sparse_mode`` 3 masks each query token right-down causally.  ``layout_kv`` "PA_BSND"
+    takes the paged caches (``block_size``, ``block_num``, ``block_table_cols``); "BSND"
+    and "TND" take contiguous key rows, ``kv_rows`` per batch (BSND) or in all (TND).
+    With ``return_softmax_lse`` a call also returns softmax_max and softmax_sum (float32,
+    one value per query row and head).
     """
 
-    def __init__(self, *, batch: int, num_heads: int, block_size: int, block_num: int, block_table_cols: int,
-                 sparse_size: int, dtype: str = "bf16", scale: Optional[float] = None, sparse_mode: int = 0,
-                 sparse_block_size: int = 1, q_seq_len: int = 1, device=None):
+    def __init__(self, *, batch: int, num_heads: int, sparse_size: int, block_size: int = 0, block_num: int = 0,
+                 block_table_cols: int = 0, dtype: str = "bf16", scale: Optional[float] = None, sparse_mode: int = 0,
+                 sparse_block_size: int = 1, q_seq_len: int = 1, layout_query: str = "BSND", q_total: int = 0,
+                 layout_kv: str = "PA_BSND", kv_rows: int = 0, return_softmax_lse: bool = False, device=None):
         import torch
         p = SfaParams()
-        p.B, p.Q_S, p.Q_N, p.KV_N, p.D, p.Dr = batch, q_seq_len, num_heads, 1, 512, 64
+        p.B, p.Q_S, p.Q_T, p.Q_N, p.KV_N, p.D, p.Dr = batch, q_seq_len, q_total, num_heads, 1, 512, 64
+        p.KV_S = kv_rows
         p.block_size, p.block_num, p.block_table_cols = block_size, block_num, block_table_cols
         p.sparse_size, p.sparse_block_size = sparse_size, sparse_block_size
+        p.layout_query, p.layout_kv = SFA_LAYOUT_QUERY[layout_query], SFA_LAYOUT_KV[layout_kv]
+        self.return_softmax_lse = return_softmax_lse
         p.dtype = DTYPES[dtype]
         p.sparse_mode = sparse_mode
         p.scale_value = (1.0 / math.sqrt(576)) if scale is None else float(scale)
@@ -283,17 +309,71 @@ class SparseFlashAttention:
         self.errors = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def __call__(self, query, query_rope, key, key_rope, value, sparse_indices, block_table, actual_seq_lengths_kv,
-                 *, actual_seq_lengths_query=None, out=None, stream=None):
+                 *, actual_seq_lengths_query=None, out=None, softmax_max=None, softmax_sum=None, stream=None):
         import torch
         if out is None:
             out = torch.empty_like(query)
+        if self.return_softmax_lse:
+            lead = query.shape[:-1]
+            if softmax_max is None:
+                softmax_max = torch.empty(lead, dtype=torch.float32, device=query.device)
+            if softmax_sum is None:
+                softmax_sum = torch.empty(lead, dtype=torch.float32, device=query.device)
         st = sfa_run(self.params, _ptr(query), _ptr(query_rope), _ptr(key), _ptr(key_rope), _ptr(value),
                      _ptr(sparse_indices), _ptr(block_table), _ptr(actual_seq_lengths_kv),
-                     _ptr(actual_seq_lengths_query), _ptr(out),
+                     _ptr(actual_seq_lengths_query), _ptr(out), _ptr(softmax_max), _ptr(softmax_sum),
                      _ptr(self.workspace), self.workspace.numel(), _ptr(self.errors), _stream_handle(stream))
         if st != IFA_OK:
             raise IfaError(st, "sfa_run")
-        return out
+        return (out, softmax_max, softmax_sum) if self.return_softmax_lse else out
+
+    def device_errors(self, clear: bool = True) -> int:
+        import torch
+        torch.cuda.synchronize()
+        v = int(self.errors.item())
+        if clear:
+            self.errors.zero_()
+        return v
+
+
+def kv_append(params: AppendParams, key_new, value_new, positions, block_table, antiquant_scale, antiquant_offset,
+              key_cache, value_cache, device_error_flags, stream) -> int:
+    """Pointer arguments are integers (device addresses) or None."""
+    return load_library().ifa_kv_append(ctypes.byref(params), key_new, value_new, positions, block_table,
+                                        antiquant_scale, antiquant_offset, key_cache, value_cache,
+                                        device_error_flags, stream)
+
+
+class KvCacheAppend:
+    """KV-cache append (``ifa_kv_append`` in ``include/ifa.h``): writes one new token's key and
+    value rows per batch into the caches in place.  ``dtype`` is the new rows' dtype,
+    ``kv_dtype`` the cache's ("int8" quantises with ``antiquant`` parameters); ``layout`` and
+    ``kv_format`` as for :class:`IncreFlashAttention`."""
+
+    def __init__(self, *, batch: int, num_kv_heads: int, head_dim: int, max_seq_len: int = 0, dtype: str = "bf16",
+                 kv_dtype: Optional[str] = None, layout: str = "BNSD", kv_format: str = "contig", block_size: int = 0,
+                 block_num: int = 0, block_table_cols: int = 0, antiquant: str = "none", device=None):
+        import torch
+        p = AppendParams()
+        p.B, p.numKeyValueHeads, p.headDim, p.maxSeqLen = batch, num_kv_heads, head_dim, max_seq_len
+        p.blockSize, p.blockNum, p.blockTableCols = block_size, block_num, block_table_cols
+        p.new_dtype = DTYPES[dtype]
+        p.kv_dtype = DTYPES[kv_dtype or dtype]
+        p.inputLayout = LAYOUTS[layout]
+        p.kvFormat = KV_FORMATS[kv_format]
+        p.antiquant = ANTIQUANT[antiquant]
+        self.params = p
+        dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.errors = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def __call__(self, key_new, value_new, positions, key_cache, value_cache, *, block_table=None,
+                 antiquant_scale=None, antiquant_offset=None, stream=None):
+        st = kv_append(self.params, _ptr(key_new), _ptr(value_new), _ptr(positions), _ptr(block_table),
+                       _ptr(antiquant_scale), _ptr(antiquant_offset), _ptr(key_cache), _ptr(value_cache),
+                       _ptr(self.errors), _stream_handle(stream))
+        if st != IFA_OK:
+            raise IfaError(st, "ifa_kv_append")
+        return key_cache, value_cache
 
     def device_errors(self, clear: bool = True) -> int:
         import torch

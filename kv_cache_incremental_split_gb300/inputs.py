@@ -162,6 +162,8 @@ class SfaCase:
     sparse_block_size: int = 1  # > 1: each index selects that many consecutive tokens
     sparse_mode: int = 0        # 3: right-down causal over the Q_S query tokens
     actual_seq_lengths_query: Optional[np.ndarray] = None  # (B,) int32, None: every query token valid
+    layout_query: str = "BSND"  # "TND": query (Q_T, Q_N, D), prefix-sum actual_seq_lengths_query
+    layout_kv: str = "PA_BSND"  # "BSND": key (B, KV_S, 1, D); "TND": key (KV_T, 1, D), prefix-sum lengths
     meta: Dict[str, Any] = field(default_factory=dict)
 
     @property
@@ -304,3 +306,104 @@ def sfa_mla(seed: int = 0, B=32, Q_N=128, D=512, Dr=64, block_size=64, kv_len=32
                    random_storage(seed, 3, (block_num, block_size, 1, D), dtype),
                    idx, bt, lens, scale=1.0 / math.sqrt(D + Dr), dtype=dtype,
                    sparse_block_size=sparse_block_size, sparse_mode=sparse_mode, actual_seq_lengths_query=lq)
+
+
+def sfa_relayout(case: SfaCase, layout_query: str = "BSND", layout_kv: str = "PA_BSND") -> SfaCase:
+    """The same problem with its query rows and/or key rows stored in another layout (data
+    movement only).  Query TND: each batch's valid query rows (actual_seq_lengths_query, or
+    all Q_S) packed in order, the lengths becoming prefix sums.  Key BSND: (B, KV_S, 1, d)
+    with KV_S the longest length; key TND: each batch's tokens packed in order, the lengths
+    becoming prefix sums.  Tokens are read from the paged caches through the block table."""
+    from copy import copy
+    c = copy(case)
+    B, Q_S = case.query.shape[0], case.query.shape[1]
+    if layout_query == "TND":
+        qlen = (np.full(B, Q_S, dtype=np.int64) if case.actual_seq_lengths_query is None
+                else case.actual_seq_lengths_query.astype(np.int64))
+        rows = [(b, s) for b in range(B) for s in range(int(qlen[b]))]
+        c.query = np.stack([case.query[b, s] for b, s in rows]) if rows else case.query[:0, 0]
+        c.query_rope = np.stack([case.query_rope[b, s] for b, s in rows]) if rows else case.query_rope[:0, 0]
+        c.sparse_indices = (np.stack([case.sparse_indices[b, s] for b, s in rows]) if rows
+                            else case.sparse_indices[:0, 0])
+        c.actual_seq_lengths_query = np.cumsum(qlen).astype(np.int32)
+        c.layout_query = "TND"
+    if layout_kv != "PA_BSND":
+        bs = case.key.shape[1]
+        lens = case.actual_seq_lengths_kv.astype(np.int64)
+
+        def rows_of(b, n):
+            t = np.arange(n)
+            return case.block_table[b, t // bs].astype(np.int64) * bs + t % bs
+
+        flat = [a.reshape(-1, a.shape[-1]) for a in (case.key, case.key_rope, case.value)]
+        if layout_kv == "BSND":
+            kv_s = int(lens.max()) if B else 1
+            outs = [np.zeros((B, kv_s, 1, f.shape[-1]), dtype=f.dtype) for f in flat]
+            for b in range(B):
+                r = rows_of(b, int(lens[b]))
+                for o, f in zip(outs, flat):
+                    o[b, :len(r), 0] = f[r]
+            c.key, c.key_rope, c.value = outs
+        else:
+            r = np.concatenate([rows_of(b, int(lens[b])) for b in range(B)]) if B else np.zeros(0, np.int64)
+            c.key, c.key_rope, c.value = [f[r][:, None, :] for f in flat]
+            c.actual_seq_lengths_kv = np.cumsum(lens).astype(np.int32)
+        c.block_table = None
+        c.layout_kv = layout_kv
+    return c
+
+
+@dataclass
+class AppendCase:
+    """One decode step's KV-cache append: the new token's rows of every batch and the caches."""
+    name: str
+    key_new: np.ndarray          # (B, KV_N, D), dtype
+    value_new: np.ndarray
+    positions: np.ndarray        # (B,) int64: token index of the new token
+    key_cache: np.ndarray        # contiguous (B, KV_N, Smax, D) BNSD, or paged (blocknum, KV_N, bs, D)
+    value_cache: np.ndarray
+    layout: str = "BNSD"
+    kv_format: str = "contig"
+    block_size: int = 0
+    block_table: Optional[np.ndarray] = None
+    dtype: str = "bf16"
+    kv_dtype: str = "bf16"
+    antiquant: str = "none"
+    antiquant_scale: Optional[np.ndarray] = None
+    antiquant_offset: Optional[np.ndarray] = None
+    meta: Dict[str, Any] = field(default_factory=dict)
+
+    @property
+    def B(self) -> int:
+        return self.key_new.shape[0]
+
+
+def kv_append_paged(seed: int = 0, B=64, KV_N=8, D=128, block_size=128, len_lo=512, len_hi=4096,
+                    dtype="bf16") -> AppendCase:
+    """Append at each batch's length into a paged (blocknum, KV_N, blockSize, D) cache whose
+    block table (a random permutation of physical blocks) covers length + 1 tokens."""
+    rng = np.random.default_rng(seed)
+    lens = _lengths(rng, B, len_lo, len_hi)
+    cols = (len_hi + 1 + block_size - 1) // block_size
+    bt, blocknum = _block_table(rng, lens + 1, block_size, cols)
+    shape = (blocknum, KV_N, block_size, D)
+    return AppendCase("kv_append_paged", random_storage(seed, 1, (B, KV_N, D), dtype),
+                      random_storage(seed, 2, (B, KV_N, D), dtype), lens.astype(np.int64),
+                      np.zeros(shape, dtype=np.uint16 if dtype == "bf16" else np.float16),
+                      np.zeros(shape, dtype=np.uint16 if dtype == "bf16" else np.float16),
+                      layout="BNSD", kv_format="paged_nbsd", block_size=block_size, block_table=bt,
+                      dtype=dtype, kv_dtype=dtype)
+
+
+def kv_append_int8(seed: int = 0, B=32, KV_N=8, D=128, Smax=8192, dtype="fp16") -> AppendCase:
+    """Append into a contiguous BNSD int8 cache with per-channel antiquant parameters (the
+    int8 workload's shapes and parameter distributions), at positions U{256..Smax-1}."""
+    rng = np.random.default_rng(seed)
+    pos = rng.integers(256, Smax, size=B).astype(np.int64)
+    scale = to_storage(rng.uniform(0.005, 0.02, size=(2, KV_N, 1, D)).astype(np.float32), dtype)
+    offset = to_storage(rng.uniform(-4, 4, size=(2, KV_N, 1, D)).astype(np.float32), dtype)
+    shape = (B, KV_N, Smax, D)
+    return AppendCase("kv_append_int8", random_storage(seed, 1, (B, KV_N, D), dtype),
+                      random_storage(seed, 2, (B, KV_N, D), dtype), pos, np.zeros(shape, dtype=np.int8),
+                      np.zeros(shape, dtype=np.int8), layout="BNSD", kv_format="contig", dtype=dtype,
+                      kv_dtype="int8", antiquant="per_channel", antiquant_scale=scale, antiquant_offset=offset)

@@ -58,7 +58,7 @@ def out_to_f64(t) -> np.ndarray:
     return t.detach().to(torch.float64).cpu().numpy()
 
 
-def make_op(case: gen.IfaCase, split_tiles=0):
+def make_op(case: gen.IfaCase, split_tiles=0, **kw):
     from kv_cache_incremental_split_gb300.ifa import IncreFlashAttention
     m = case.atten_mask
     return IncreFlashAttention(
@@ -70,7 +70,7 @@ def make_op(case: gen.IfaCase, split_tiles=0):
         mask_shape=None if m is None else m.shape,
         mask_dtype="bool" if m is None or m.dtype == np.bool_ else ("int8" if m.dtype == np.int8 else "uint8"),
         antiquant=case.antiquant, kv_padding=case.kv_padding_size is not None, scale=case.scale,
-        split_tiles=split_tiles)
+        split_tiles=split_tiles, **kw)
 
 
 class DeviceCase:
@@ -86,11 +86,11 @@ class DeviceCase:
         self.sc = to_device(case.antiquant_scale)
         self.of = to_device(case.antiquant_offset)
 
-    def run(self, op, out=None):
+    def run(self, op, out=None, **kw):
         c = self.case
         return op(self.q, self.k, self.v, atten_mask=self.mask, actual_seq_lengths=c.actual_seq_lengths,
                   kv_padding_size=c.kv_padding_size, block_table=self.bt, antiquant_scale=self.sc,
-                  antiquant_offset=self.of, out=out)
+                  antiquant_offset=self.of, out=out, **kw)
 
 
 def gpu_ifa(case: gen.IfaCase, split_tiles=0) -> np.ndarray:

@@ -85,7 +85,7 @@ def test_null_arguments(lib):
     assert lib.ifa_create(None, ctypes.byref(plan), ctypes.byref(ws)) == ifa.IFA_ERR_PARAM_NULLPTR
     p = base_params()
     assert lib.ifa_create(ctypes.byref(p), None, ctypes.byref(ws)) == ifa.IFA_ERR_PARAM_NULLPTR
-    assert lib.ifa_run(None, 0, 0, 0, None, None, None, 0, None, None, None, 0, None, 0, None) == \
+    assert lib.ifa_run(None, 0, 0, 0, None, None, None, 0, None, None, None, None, None, 0, None, 0, None) == \
         ifa.IFA_ERR_PARAM_NULLPTR
     assert lib.ifa_destroy(None) == ifa.IFA_OK
     flags = ctypes.c_int64()
@@ -110,6 +110,10 @@ INVALID = [
     dict(has_mask=1, mask_dtype=4, maskB=4, maskN=2, maskS=1024),  # maskN not in {1, N}
     dict(has_mask=1, mask_dtype=4, maskB=4, maskN=8, maskS=0),
     dict(scaleValue=float("nan")), dict(splitTiles=-1),
+    dict(out_dtype=2),  # int8 output without quantisation parameters
+    dict(out_dtype=2, quant2=1, quant2_dtype=0),  # fp16 parameters
+    dict(q_dtype=0, kv_dtype=0, out_dtype=2, quant2=2, quant2_dtype=1),  # bf16 parameters with an fp16 query
+    dict(quant2=2, quant2_dtype=5),  # quantisation without an int8 output
 ]
 
 
@@ -128,6 +132,8 @@ VALID = [
     dict(kvFormat=2, blockSize=16, blockNum=10, blockTableCols=4),
     dict(q_dtype=0, kv_dtype=2, antiquant=2, kvFormat=0, has_kv_padding=1),
     dict(has_mask=1, mask_dtype=4, maskB=1, maskN=8, maskS=1024), dict(headDim=16), dict(headDim=256),
+    dict(out_dtype=2, quant2=2, quant2_dtype=5), dict(out_dtype=2, quant2=1, quant2_dtype=1),
+    dict(q_dtype=0, kv_dtype=0, out_dtype=2, quant2=1, quant2_dtype=5),
 ]
 
 
@@ -153,6 +159,7 @@ def test_sfa_params_struct_layout_matches_header(tmp_path):
 def sfa_params(**kw):
     p = ifa.SfaParams()
     p.B, p.Q_S, p.Q_N, p.KV_N, p.D, p.Dr = 4, 1, 128, 1, 512, 64
+    p.layout_query, p.layout_kv = 0, 0
     p.block_size, p.block_num, p.block_table_cols, p.sparse_size, p.sparse_block_size = 64, 100, 20, 2048, 1
     p.dtype = ifa.DTYPES["bf16"]
     p.sparse_mode = 0
@@ -167,7 +174,10 @@ SFA_INVALID = [dict(KV_N=2), dict(D=256), dict(Dr=32), dict(Q_N=0), dict(Q_N=129
                dict(sparse_block_size=256), dict(sparse_block_size=128),  # 128 does not divide block_size 64
                dict(sparse_size=2**30, sparse_block_size=64), dict(sparse_mode=1), dict(dtype=2),
                dict(sparse_size=0), dict(block_num=0), dict(B=-1), dict(scale_value=float("inf")),
-               dict(Q_S=0), dict(Q_S=1025), dict(B=2048, Q_S=1024)]
+               dict(Q_S=0), dict(Q_S=1025), dict(B=2048, Q_S=1024), dict(layout_query=2), dict(layout_kv=3),
+               dict(layout_query=1, Q_T=-1), dict(layout_query=1, Q_T=2**20 + 1), dict(layout_kv=1, KV_S=0),
+               dict(layout_kv=1, B=65536, KV_S=2**15), dict(layout_kv=2, KV_S=0), dict(layout_kv=1, KV_S=64,
+                                                                                       sparse_block_size=256)]
 
 
 @pytest.mark.parametrize("kw", SFA_INVALID)
@@ -179,7 +189,9 @@ def test_sfa_invalid_descriptions_are_rejected(lib, kw):
 @pytest.mark.parametrize("kw", [dict(), dict(Q_N=16), dict(sparse_mode=3), dict(dtype=0), dict(block_size=16),
                                 dict(sparse_block_size=2), dict(sparse_block_size=64),
                                 dict(block_size=128, sparse_block_size=128), dict(Q_S=2, sparse_mode=3),
-                                dict(Q_S=4, sparse_mode=0)])
+                                dict(Q_S=4, sparse_mode=0), dict(layout_query=1, Q_T=10), dict(layout_query=1, Q_T=0),
+                                dict(layout_kv=1, KV_S=1000, block_size=0, block_num=0, block_table_cols=0),
+                                dict(layout_kv=2, KV_S=5000, sparse_block_size=128)])
 def test_sfa_valid_descriptions_pass_validation(lib, kw):
     st, ws = ifa.sfa_workspace_size(sfa_params(**kw))
     assert st in (ifa.IFA_OK, ifa.IFA_ERR_RUNTIME)
@@ -188,6 +200,62 @@ def test_sfa_valid_descriptions_pass_validation(lib, kw):
 
 
 def test_sfa_run_null_arguments(lib):
-    assert ifa.sfa_run(sfa_params(), None, None, None, None, None, None, None, None, None, None, None, 0, None,
-                       None) in \
+    assert ifa.sfa_run(sfa_params(), None, None, None, None, None, None, None, None, None, None, None, None, None,
+                       0, None, None) in \
         (ifa.IFA_ERR_PARAM_NULLPTR,)
+
+
+# ---------------------------------------------------------------- KV-cache append
+
+def test_append_params_struct_layout_matches_header(tmp_path):
+    src = tmp_path / "append_layout.c"
+    body = "\n".join(f'  printf("%zu\\n", offsetof(ifa_append_params, {f}));' for f, _ in ifa.AppendParams._fields_)
+    src.write_text(f'#include <stdio.h>\n#include <stddef.h>\n#include "ifa.h"\nint main(void) {{\n'
+                   f'  printf("%zu\\n", sizeof(ifa_append_params));\n{body}\n  return 0;\n}}\n')
+    exe = tmp_path / "append_layout"
+    subprocess.check_call(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = [int(x) for x in subprocess.check_output([str(exe)]).split()]
+    assert got[0] == ctypes.sizeof(ifa.AppendParams)
+    for (name, _), off in zip(ifa.AppendParams._fields_, got[1:]):
+        assert getattr(ifa.AppendParams, name).offset == off, name
+
+
+def append_params(**kw):
+    p = ifa.AppendParams()
+    p.B, p.numKeyValueHeads, p.headDim, p.maxSeqLen = 4, 8, 128, 1024
+    p.blockSize, p.blockNum, p.blockTableCols = 0, 0, 0
+    p.new_dtype, p.kv_dtype = ifa.DTYPES["bf16"], ifa.DTYPES["bf16"]
+    p.inputLayout, p.kvFormat, p.antiquant = ifa.LAYOUTS["BNSD"], 0, 0
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+APPEND_INVALID = [dict(B=-1), dict(numKeyValueHeads=0), dict(headDim=12), dict(headDim=1024), dict(new_dtype=2),
+                  dict(kv_dtype=0), dict(kv_dtype=2), dict(antiquant=1), dict(kv_dtype=2, antiquant=1, headDim=24),
+                  dict(inputLayout=5), dict(kvFormat=3), dict(maxSeqLen=0),
+                  dict(kvFormat=1, blockSize=0, blockNum=4, blockTableCols=2)]
+
+
+@pytest.mark.parametrize("kw", APPEND_INVALID)
+def test_append_invalid_descriptions_are_rejected(lib, kw):
+    buf = ctypes.create_string_buffer(64)
+    ptr = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert ifa.kv_append(append_params(**kw), ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, None, None) == \
+        ifa.IFA_ERR_PARAM_INVALID
+
+
+def test_append_null_and_misaligned_arguments(lib):
+    buf = ctypes.create_string_buffer(64)
+    ptr = (ctypes.addressof(buf) + 15) // 16 * 16
+    p = append_params()
+    assert ifa.kv_append(p, None, ptr, ptr, None, None, None, ptr, ptr, None, None) == ifa.IFA_ERR_PARAM_NULLPTR
+    assert ifa.kv_append(p, ptr, ptr, None, None, None, None, ptr, ptr, None, None) == ifa.IFA_ERR_PARAM_NULLPTR
+    assert ifa.kv_append(append_params(kvFormat=1, blockSize=16, blockNum=4, blockTableCols=2), ptr, ptr, ptr,
+                         None, None, None, ptr, ptr, None, None) == ifa.IFA_ERR_PARAM_NULLPTR
+    assert ifa.kv_append(append_params(kv_dtype=2, antiquant=1), ptr, ptr, ptr, None, None, None, ptr, ptr, None,
+                         None) == ifa.IFA_ERR_PARAM_NULLPTR
+    assert ifa.kv_append(p, ptr + 2, ptr, ptr, None, None, None, ptr, ptr, None, None) == ifa.IFA_ERR_PARAM_INVALID
+    assert ifa.kv_append(p, ptr, ptr, ptr + 4, None, None, None, ptr, ptr, None, None) == ifa.IFA_ERR_PARAM_INVALID
+    # B = 0 validates and enqueues nothing
+    assert ifa.kv_append(append_params(B=0), ptr, ptr, ptr, None, None, None, ptr, ptr, None, None) == ifa.IFA_OK

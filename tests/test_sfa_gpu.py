@@ -21,24 +21,42 @@ def _built():
     build.build()
 
 
-def run_gpu(c, sparse_mode=None):
+def sfa_op(c, sparse_mode=None, lse=False):
     from kv_cache_incremental_split_gb300.ifa import SparseFlashAttention
-    Q_S = c.query.shape[1]
-    op = SparseFlashAttention(batch=c.B, num_heads=c.query.shape[2], block_size=c.key.shape[1],
-                              block_num=c.key.shape[0], block_table_cols=c.block_table.shape[1],
-                              sparse_size=c.sparse_indices.shape[-1], dtype=c.dtype, scale=c.scale,
-                              sparse_mode=c.sparse_mode if sparse_mode is None else sparse_mode,
-                              sparse_block_size=c.sparse_block_size, q_seq_len=Q_S)
-    t = [to_device(a) for a in (c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices,
-                                c.block_table, c.actual_seq_lengths_kv)]
+    tnd = c.layout_query == "TND"
+    paged = c.layout_kv == "PA_BSND"
+    B = len(c.actual_seq_lengths_query) if tnd else c.query.shape[0]
+    kw = dict(block_size=c.key.shape[1], block_num=c.key.shape[0], block_table_cols=c.block_table.shape[1]) \
+        if paged else dict(kv_rows=c.key.shape[1] if c.layout_kv == "BSND" else c.key.shape[0])
+    return SparseFlashAttention(batch=B, num_heads=c.query.shape[-2], sparse_size=c.sparse_indices.shape[-1],
+                                dtype=c.dtype, scale=c.scale,
+                                sparse_mode=c.sparse_mode if sparse_mode is None else sparse_mode,
+                                sparse_block_size=c.sparse_block_size, q_seq_len=1 if tnd else c.query.shape[1],
+                                layout_query=c.layout_query, q_total=c.query.shape[0] if tnd else 0,
+                                layout_kv=c.layout_kv, return_softmax_lse=lse, **kw)
+
+
+def run_gpu(c, sparse_mode=None, lse=False):
+    op = sfa_op(c, sparse_mode, lse)
+    t = [to_device(a) for a in (c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices)]
+    bt = None if c.block_table is None else to_device(c.block_table)
+    lk = None if c.actual_seq_lengths_kv is None else to_device(c.actual_seq_lengths_kv)
     lq = None if c.actual_seq_lengths_query is None else to_device(c.actual_seq_lengths_query)
-    out = op(*t, actual_seq_lengths_query=lq)
+    res = op(*t, bt, lk, actual_seq_lengths_query=lq)
     torch.cuda.synchronize()
-    shape = (c.B, c.query.shape[2], 512) if Q_S == 1 else (c.B, Q_S, c.query.shape[2], 512)
-    return out_to_f64(out).reshape(shape), op
+    out = res[0] if lse else res
+    if c.layout_query == "TND":
+        shape = (c.query.shape[0], c.query.shape[1], 512)
+    else:
+        Q_S = c.query.shape[1]
+        shape = (c.B, c.query.shape[2], 512) if Q_S == 1 else (c.B, Q_S, c.query.shape[2], 512)
+    got = out_to_f64(out).reshape(shape)
+    if lse:
+        return got, res[1].double().cpu().numpy().reshape(shape[:-1]), res[2].double().cpu().numpy().reshape(shape[:-1]), op
+    return got, op
 
 
-def run_ref(c, batches=None, sparse_mode=None):
+def run_ref(c, batches=None, sparse_mode=None, lse=False):
     cc = c
     if batches is not None:
         import copy
@@ -53,7 +71,8 @@ def run_ref(c, batches=None, sparse_mode=None):
                           cc.block_table, cc.actual_seq_lengths_kv, scale=cc.scale,
                           sparse_block_size=cc.sparse_block_size,
                           sparse_mode=cc.sparse_mode if sparse_mode is None else sparse_mode,
-                          actual_seq_lengths_query=cc.actual_seq_lengths_query)
+                          actual_seq_lengths_query=cc.actual_seq_lengths_query, layout_query=cc.layout_query,
+                          layout_kv=cc.layout_kv, return_softmax_lse=lse)
 
 
 def check(c, batches=None, sparse_mode=None):
@@ -216,3 +235,53 @@ def test_sfa_multi_token_blockwise_causal(sbs):
     c.actual_seq_lengths_kv = np.array([1024 - sbs // 2, 1000], dtype=np.int32)
     c.sparse_indices[:, :, 0, 0] = 1024 // sbs - 1  # the last block: partly past length and causal limit
     check(c)
+
+
+# ------------------------------------------- TND / BSND layouts and softmax_max / softmax_sum
+
+LAYOUTS = [("BSND", "BSND"), ("BSND", "TND"), ("TND", "PA_BSND"), ("TND", "BSND"), ("TND", "TND")]
+
+
+@pytest.mark.parametrize("lq,lk", LAYOUTS)
+def test_sfa_layouts_match_oracle(lq, lk):
+    c = gen.sfa_mla(30, B=4, Q_N=64, block_size=64, kv_len=900, sparse_size=260, nvalid_lo=100, nvalid_hi=260,
+                    Q_S=3, sparse_mode=3, q_lens=[3, 1, 0, 2])
+    c.actual_seq_lengths_kv = np.array([900, 333, 500, 64], dtype=np.int32)
+    c.sparse_indices[:, :, 0, :3] = np.array([899, 332, 63], dtype=np.int32)
+    check(gen.sfa_relayout(c, lq, lk))
+
+
+@pytest.mark.parametrize("lk", ["BSND", "TND"])
+def test_sfa_contiguous_keys_blockwise_runs(lk):
+    # block-wise runs of 16 tokens as tiled boxes over contiguous key rows (no cache blocks)
+    c = gen.sfa_mla(31, B=3, Q_N=32, block_size=64, kv_len=1024, sparse_size=40, nvalid_lo=20, nvalid_hi=40,
+                    Q_S=2, sparse_mode=3, sparse_block_size=16)
+    c.actual_seq_lengths_kv = np.array([1024, 1000, 250], dtype=np.int32)
+    check(gen.sfa_relayout(c, "BSND", lk))
+
+
+def test_sfa_tnd_long_rows_split_across_ctas():
+    c = gen.sfa_mla(32, B=2, Q_N=128, block_size=64, kv_len=8192, sparse_size=2048, nvalid_lo=1800,
+                    nvalid_hi=2048, Q_S=2, sparse_mode=3, q_lens=[1, 2])
+    check(gen.sfa_relayout(c, "TND", "TND"))
+
+
+@pytest.mark.parametrize("lq,lk,split", [("BSND", "PA_BSND", False), ("BSND", "BSND", True), ("TND", "TND", False),
+                                         ("TND", "PA_BSND", True)])
+def test_sfa_softmax_max_and_sum(lq, lk, split):
+    """softmax_max within 2e-3 (the scores accumulate in fp32 from 16-bit operands), softmax_sum
+    within 1e-3 relative (fp32 sum of exp2 approximations); -inf and 0 on empty rows."""
+    kw = dict(sparse_size=2048, nvalid_lo=1800, nvalid_hi=2048, kv_len=8192) if split else \
+        dict(sparse_size=200, nvalid_lo=1, nvalid_hi=200, kv_len=700)
+    c = gen.sfa_mla(33, B=3, Q_N=128, block_size=64, Q_S=2, sparse_mode=3, q_lens=[2, 0, 1], **kw)
+    c = gen.sfa_relayout(c, lq, lk)
+    got, mx, sm, _ = run_gpu(c, lse=True)
+    ref, rmx, rsm = run_ref(c, lse=True)
+    assert max_abs_err(got, ref) <= TOL[c.dtype]
+    empty = np.isneginf(rmx)
+    assert np.array_equal(np.isneginf(mx), empty)
+    assert np.all(sm[empty] == 0.0)
+    live = ~empty
+    assert live.any()
+    assert np.abs(mx[live] - rmx[live]).max() <= 2e-3
+    assert (np.abs(sm[live] - rsm[live]) / rsm[live]).max() <= 1e-3
