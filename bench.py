@@ -57,6 +57,12 @@ WORKLOADS = {
     "sfa_mla_mtp": ("sparse MLA-absorb decode, two query tokens (multi-token prediction): B=32 Q_S=2 Q_N=128 "
                     "D=512+64 bf16, PA_BSND block 64, KV length 32768, sparse_mode 3 (right-down causal), "
                     "sparse_indices (B,2,1,2048) with U{1024..2048} valid per row then -1"),
+    "kv_append_paged": ("KV-cache append (the step before the attention): B=64 KV_N=8 D=128 bf16 new token rows into "
+                        "a paged (blocknum, 8, 128, 128) cache through a random block table, at each batch's "
+                        "length U{512..4096} minus the step number mod 8"),
+    "kv_append_int8": ("KV-cache append with int8 quantisation: B=32 KV_N=8 D=128 fp16 new token rows into a BNSD "
+                       "int8 cache (Smax 8192) with per-channel scale U[0.005,0.02] and offset U[-4,4], at "
+                       "positions U{256..8191} minus the step number mod 8"),
 }
 
 
@@ -71,6 +77,10 @@ def make_case(name: str, seed: int):
         return gen.sfa_mla(seed, sparse_size=128, nvalid_lo=64, nvalid_hi=128, sparse_block_size=16)
     if name == "sfa_mla_mtp":
         return gen.sfa_mla(seed, Q_S=2, sparse_mode=3)
+    if name == "kv_append_paged":
+        return gen.kv_append_paged(seed)
+    if name == "kv_append_int8":
+        return gen.kv_append_int8(seed)
     return {"gqa_padded": gen.gqa_padded, "tiny_mha": gen.tiny_mha, "paged_gqa": gen.paged_gqa,
             "int8_leftpad": gen.int8_leftpad}[name](seed)
 
@@ -113,6 +123,16 @@ def sfa_valid_counts(case: gen.SfaCase):
 
 
 def algorithmic_bytes(case) -> int:
+    if isinstance(case, gen.AppendCase):
+        rows = case.key_new.size                               # B * KV_N * D elements per tensor
+        es = 1 if case.kv_dtype == "int8" else 2
+        total = 2 * rows * 2 + 2 * rows * es                   # new key/value rows read, cache rows written
+        total += case.positions.nbytes
+        if case.block_table is not None:
+            total += case.B * 4                                # the block-table entry of each position
+        if case.antiquant_scale is not None:
+            total += case.antiquant_scale.nbytes + case.antiquant_offset.nbytes
+        return int(total)
     if isinstance(case, gen.SfaCase):
         n = int(sfa_valid_counts(case).sum())
         QN = case.query.shape[2]
@@ -283,6 +303,16 @@ def _batch_subset(case, b):
     from copy import copy
     c = copy(case)
     sel = np.array([b])
+    if isinstance(case, gen.AppendCase):
+        c.key_new, c.value_new, c.positions = case.key_new[sel], case.value_new[sel], case.positions[sel]
+        if case.block_table is None:
+            c.key_cache, c.value_cache = case.key_cache[sel], case.value_cache[sel]
+        else:  # only batch b's blocks, renumbered
+            blocks = case.block_table[b][case.block_table[b] >= 0]
+            c.key_cache, c.value_cache = case.key_cache[blocks], case.value_cache[blocks]
+            c.block_table = np.where(case.block_table[sel] >= 0, np.arange(case.block_table.shape[1])[None], -1)
+            c.block_table = c.block_table.astype(np.int32)
+        return c
     if isinstance(case, gen.SfaCase):
         c.query, c.query_rope = case.query[sel], case.query_rope[sel]
         c.sparse_indices, c.block_table = case.sparse_indices[sel], case.block_table[sel]
@@ -304,27 +334,38 @@ def _batch_subset(case, b):
     return c
 
 
-def oracle_sample(case, budget_s: float, start_batch: int = 0):
-    """Time the CPU oracle, batch by batch, for about `budget_s` seconds."""
-    import oracle  # test infrastructure: only the CPU-baseline leg of the benchmark uses it
+def _run_oracle(c):
+    """One run of the CPU oracle on case c (test infrastructure: only the CPU-baseline and
+    reference legs of the benchmark call it)."""
+    import oracle
     fmt = {"contig": oracle.CONTIG, "paged_nbsd": oracle.PAGED_NBSD, "paged_bsh": oracle.PAGED_BSH}
     aq = {"none": oracle.AQ_NONE, "per_channel": oracle.AQ_PER_CHANNEL, "per_tensor": oracle.AQ_PER_TENSOR}
+    if isinstance(c, gen.AppendCase):
+        oracle.kv_append_ref(c.key_new, c.value_new, c.positions, c.key_cache, c.value_cache, layout=c.layout,
+                             kv_format=fmt[c.kv_format], block_size=c.block_size, block_table=c.block_table,
+                             antiquant=aq[c.antiquant], antiquant_scale=c.antiquant_scale,
+                             antiquant_offset=c.antiquant_offset)
+    elif isinstance(c, gen.SfaCase):
+        oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
+                       c.actual_seq_lengths_kv, scale=c.scale, sparse_block_size=c.sparse_block_size,
+                       sparse_mode=c.sparse_mode, actual_seq_lengths_query=c.actual_seq_lengths_query)
+    else:
+        oracle.ifa_ref(c.query, c.key, c.value, num_heads=c.num_heads, num_kv_heads=c.num_kv_heads,
+                       scale=c.scale, layout=c.layout, kv_format=fmt[c.kv_format], block_size=c.block_size,
+                       block_table=c.block_table, atten_mask=c.atten_mask,
+                       actual_seq_lengths=c.actual_seq_lengths, kv_padding_size=c.kv_padding_size,
+                       antiquant=aq[c.antiquant], antiquant_scale=c.antiquant_scale,
+                       antiquant_offset=c.antiquant_offset)
+
+
+def oracle_sample(case, budget_s: float, start_batch: int = 0):
+    """Time the CPU oracle, batch by batch, for about `budget_s` seconds."""
     done, nbytes, t_used = [], 0, 0.0
     b = start_batch % case.B
     while True:
         c = _batch_subset(case, b)
         t = time.perf_counter()
-        if isinstance(c, gen.SfaCase):
-            oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
-                           c.actual_seq_lengths_kv, scale=c.scale, sparse_block_size=c.sparse_block_size,
-                           sparse_mode=c.sparse_mode, actual_seq_lengths_query=c.actual_seq_lengths_query)
-        else:
-            oracle.ifa_ref(c.query, c.key, c.value, num_heads=c.num_heads, num_kv_heads=c.num_kv_heads,
-                           scale=c.scale, layout=c.layout, kv_format=fmt[c.kv_format], block_size=c.block_size,
-                           block_table=c.block_table, atten_mask=c.atten_mask,
-                           actual_seq_lengths=c.actual_seq_lengths, kv_padding_size=c.kv_padding_size,
-                           antiquant=aq[c.antiquant], antiquant_scale=c.antiquant_scale,
-                           antiquant_offset=c.antiquant_offset)
+        _run_oracle(c)
         t_used += time.perf_counter() - t
         nbytes += algorithmic_bytes(c)
         done.append(b)
@@ -334,23 +375,59 @@ def oracle_sample(case, budget_s: float, start_batch: int = 0):
     return nbytes, t_used, done
 
 
+_ROWS = {}
+
+
+def _truncated(case, b, frac):
+    """Batch b of the workload with its work cut to about `frac` (0 < frac <= 1): fewer
+    tokens (attention), fewer selected indices (sparse), or the whole row (append).  The
+    batch rows are cut out of the workload once and reused."""
+    from copy import copy
+    key = (id(case), b)
+    if key not in _ROWS:
+        _ROWS[key] = _batch_subset(case, b)
+    c = copy(_ROWS[key])
+    if frac >= 1.0 or isinstance(c, gen.AppendCase):
+        return c
+    if isinstance(c, gen.SfaCase):
+        n = max(1, int(c.sparse_indices.shape[-1] * frac))
+        c.sparse_indices = np.ascontiguousarray(c.sparse_indices[..., :n])
+        return c
+    if c.actual_seq_lengths is not None:
+        c.actual_seq_lengths = np.maximum(1, (c.actual_seq_lengths * frac).astype(np.int64))
+    return c
+
+
+def oracle_unit(case, b, frac):
+    """Bytes and seconds of one oracle run on batch b cut to `frac` of its work."""
+    c = _truncated(case, b, frac)
+    t = time.perf_counter()
+    _run_oracle(c)
+    return algorithmic_bytes(c), time.perf_counter() - t
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     case = make_case(args.workload, args.seed)
-    per_step = args.ref_step_seconds
+    # The whole run takes about --ref-total-seconds: each of the W + K steps runs the oracle on
+    # one batch row cut to the fraction of its work that fits the per-step share (calibrated on
+    # a full row first).
+    per_step = args.ref_total_seconds / max(1, args.warmup + args.steps)
+    _, t_full = oracle_unit(case, 0, 1.0)
+    frac = min(1.0, per_step / max(t_full, 1e-9))
     for w in range(args.warmup):
-        oracle_sample(case, per_step, start_batch=w)
+        oracle_unit(case, w % case.B, frac)
     total_b, total_t, batches = 0, 0.0, 0
     for s in range(args.steps):
-        nb, t, done = oracle_sample(case, per_step, start_batch=args.warmup + s)
+        nb, t = oracle_unit(case, (args.warmup + s) % case.B, frac)
         total_b += nb
         total_t += t
-        batches += len(done)
+        batches += 1
     value = total_b / total_t / 1e9
-    sample = (f"each step: the oracle on whole batches of the workload for about {per_step} s "
-              f"({batches} batch rows over {args.steps} steps, {total_b / 1e6:.1f} MB algorithmic)")
+    sample = (f"each step: the oracle on one batch row of the workload cut to {100 * frac:.1f}% of its work "
+              f"({batches} rows over {args.steps} steps, {total_b / 1e6:.1f} MB algorithmic, {total_t:.1f} s)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -464,6 +541,61 @@ class SfaWorkload:
                        actual_seq_lengths_query=d.get("lq"), stream=stream)
 
 
+class AppendWorkload:
+    """One decode step's KV-cache append on the device: the caches stay resident and are
+    written in place; step i writes at the positions minus i mod 8, so the rows written
+    differ from one step to the next."""
+
+    def __init__(self, case: gen.AppendCase, dev, copies_for):
+        import torch
+        from kv_cache_incremental_split_gb300.ifa import KvCacheAppend
+        self.case, self.dev = case, dev
+        paged = case.kv_format != "contig"
+        KVN, D = case.key_new.shape[1], case.key_new.shape[2]
+        self.op = KvCacheAppend(batch=case.B, num_kv_heads=KVN, head_dim=D,
+                                max_seq_len=0 if paged else case.key_cache.shape[2], dtype=case.dtype,
+                                kv_dtype=case.kv_dtype, layout=case.layout, kv_format=case.kv_format,
+                                block_size=case.block_size, block_num=case.key_cache.shape[0] if paged else 0,
+                                block_table_cols=case.block_table.shape[1] if paged else 0,
+                                antiquant=case.antiquant, device=dev)
+        self.kn, self.vn = _to_dev(case.key_new, dev), _to_dev(case.value_new, dev)
+        self.kc, self.vc = _to_dev(case.key_cache, dev), _to_dev(case.value_cache, dev)
+        self.bt = _to_dev(case.block_table, dev)
+        self.sc, self.of = _to_dev(case.antiquant_scale, dev), _to_dev(case.antiquant_offset, dev)
+        self.copies = copies_for
+        # earlier positions of the same sequences: still inside the cache and the block table
+        self.pos = [_to_dev(case.positions - (i % 8), dev) for i in range(self.copies)]
+        self.q = self.op.errors  # the step's result read back end to end: the device error word
+        self.rotating_bytes = 0
+        self.l2_note = (f"the caches ({2 * self.kc.numel() * self.kc.element_size() / 1e6:.0f} MB) stay resident; "
+                        f"positions shift by the step number mod {self.copies}")
+        self.dtype = case.dtype if case.kv_dtype != "int8" else "int8-kv/" + case.dtype
+        self.call_name = "ifa_kv_append"
+        self.launch_note = ""
+
+    def call(self, i, stream):
+        self.op(self.kn, self.vn, self.pos[i], self.kc, self.vc, block_table=self.bt, antiquant_scale=self.sc,
+                antiquant_offset=self.of, stream=stream)
+        return self.op.errors
+
+    def launches_per_call(self):
+        return 1
+
+    def host_inputs(self):
+        c = self.case
+        d = {"kn": c.key_new, "vn": c.value_new, "pos": c.positions}
+        if c.block_table is not None:
+            d["bt"] = c.block_table
+        if c.antiquant_scale is not None:
+            d["sc"], d["of"] = c.antiquant_scale, c.antiquant_offset
+        return d
+
+    def call_on(self, d, stream):
+        self.op(d["kn"], d["vn"], d["pos"], self.kc, self.vc, block_table=d.get("bt"), antiquant_scale=d.get("sc"),
+                antiquant_offset=d.get("of"), stream=stream)
+        return self.op.errors
+
+
 def run_gpu(args):
     import torch
 
@@ -484,7 +616,12 @@ def run_gpu(args):
     # Rotate through enough input copies that the bytes streamed between two uses of one
     # copy exceed L2 several times (inputs larger than L2: no flush between steps).
     copies = max(1, min(8, math.ceil(6 * L2_BYTES / max(1, alg))))
-    wl = SfaWorkload(case, dev, copies) if isinstance(case, gen.SfaCase) else IfaWorkload(case, dev, copies)
+    if isinstance(case, gen.AppendCase):
+        wl = AppendWorkload(case, dev, copies)
+    elif isinstance(case, gen.SfaCase):
+        wl = SfaWorkload(case, dev, copies)
+    else:
+        wl = IfaWorkload(case, dev, copies)
     stream = torch.cuda.Stream(device=dev)
 
     with torch.cuda.stream(stream):
@@ -599,8 +736,8 @@ def run_gpu(args):
             "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "config": {"workload": WORKLOADS[args.workload], "seed": args.seed,
                        "algorithmic_bytes_per_step": alg,
-                       "l2": f"inputs larger than L2: {copies} rotating cache copies "
-                             f"({copies * wl.rotating_bytes / 1e6:.0f} MB)",
+                       "l2": getattr(wl, "l2_note", None) or (f"inputs larger than L2: {copies} rotating cache "
+                                                              f"copies ({copies * wl.rotating_bytes / 1e6:.0f} MB)"),
                        "launch": f"CUDA graphs of {chunk} consecutive {wl.call_name} calls (one call per step"
                                  f"{wl.launch_note}), replayed {n_chunks} times + {rem} calls",
                        "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
@@ -634,7 +771,8 @@ def parse(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--ref-step-seconds", type=float, default=0.5)
+    ap.add_argument("--ref-total-seconds", type=float, default=120.0,
+                    help="reference arm: about this many seconds of oracle time over all steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
 
