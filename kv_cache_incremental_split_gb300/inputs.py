@@ -407,3 +407,28 @@ def kv_append_int8(seed: int = 0, B=32, KV_N=8, D=128, Smax=8192, dtype="fp16") 
                       random_storage(seed, 2, (B, KV_N, D), dtype), pos, np.zeros(shape, dtype=np.int8),
                       np.zeros(shape, dtype=np.int8), layout="BNSD", kv_format="contig", dtype=dtype,
                       kv_dtype="int8", antiquant="per_channel", antiquant_scale=scale, antiquant_offset=offset)
+
+
+def tensorlist_from(case: IfaCase, seed: int = 0, extra_hi: int = 0) -> IfaCase:
+    """The same problem with key/value as one tensor per batch (data movement, plus random
+    tokens past each length): tensor b holds batch b's first len_b + U{0..extra_hi} tokens of
+    a contiguous case, in its layout, so S_b differs from batch to batch.  The case's
+    key/value become lists and its kv_format "tensorlist"."""
+    from copy import copy
+    assert case.kv_format == "contig" and case.kv_padding_size is None
+    rng = np.random.default_rng(seed)
+    c = copy(case)
+    s_axis = 2 if case.layout == "BNSD" else 1
+    lens = (case.actual_seq_lengths if case.actual_seq_lengths is not None
+            else np.full(case.B, case.key.shape[s_axis], dtype=np.int64))
+    keys, values = [], []
+    for b in range(case.B):
+        S_b = int(min(case.key.shape[s_axis], max(1, int(lens[b]) + int(rng.integers(0, extra_hi + 1)))))
+        sl = [slice(b, b + 1)] + [slice(None)] * (case.key.ndim - 1)
+        sl[s_axis] = slice(0, S_b)
+        keys.append(np.ascontiguousarray(case.key[tuple(sl)]))
+        values.append(np.ascontiguousarray(case.value[tuple(sl)]))
+    c.key, c.value = keys, values
+    c.kv_format = "tensorlist"
+    c.max_seq_len = max(k.shape[s_axis] for k in keys)
+    return c

@@ -290,3 +290,25 @@ def quantize_output_ref(y, scale2, offset2=None):
     if rc < 0:
         raise ValueError("oracle rejected its arguments")
     return out
+
+
+def ifa_ref_tensorlist(query, key_list, value_list, *, num_heads, num_kv_heads=0, scale, layout="BNSD",
+                       atten_mask=None, actual_seq_lengths=None, antiquant=AQ_NONE, antiquant_scale=None,
+                       antiquant_offset=None):
+    """Reference output (B, numHeads, D) with key/value given as one tensor per batch
+    (IncreFlashAttention README, non-contiguous key/value: B tensors of batch 1 whose shapes
+    differ only in S): batch b is the one-batch problem over its own tensor, tokens
+    [0, actual_seq_lengths[b]) (all of its S_b when the lengths are None); a per-batch mask
+    row is batch b's."""
+    B = query.shape[0]
+    outs = []
+    for b in range(B):
+        m = None
+        if atten_mask is not None:
+            m = atten_mask[b:b + 1] if atten_mask.shape[0] > 1 else atten_mask
+        lens = None if actual_seq_lengths is None else np.asarray(actual_seq_lengths, dtype=np.int64)[b:b + 1]
+        outs.append(ifa_ref(query[b:b + 1], key_list[b], value_list[b], num_heads=num_heads,
+                            num_kv_heads=num_kv_heads, scale=scale, layout=layout, atten_mask=m,
+                            actual_seq_lengths=lens, antiquant=antiquant, antiquant_scale=antiquant_scale,
+                            antiquant_offset=antiquant_offset)[0])
+    return np.stack(outs)

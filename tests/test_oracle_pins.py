@@ -917,3 +917,37 @@ def test_output_quantisation_per_channel_ties_saturation_and_dtypes():
     yt = np.array([[[0.5, 1.5, 2.5, -0.5, -1.5, 200.0, -200.0, 127.4]]])
     assert list(oracle.quantize_output_ref(yt, np.array([1.0], np.float32))[0, 0]) == [0, 2, 2, 0, -2, 127, -128, 127]
     assert pc.dtype == np.int8 and np.all(np.abs(pc.astype(np.int64)) <= 128)
+
+
+# ------------------------------------------- key/value as one tensor per batch (tensor list)
+
+@pytest.mark.parametrize("layout", ["BNSD", "BSND", "BSH"])
+def test_tensorlist_equals_the_contiguous_cache(layout):
+    """Per-batch tensors cut from a contiguous cache (each ending at its own S_b past the
+    length) give the contiguous result, with or without a per-batch mask."""
+    case = gen.gqa_padded(90, B=4, N=8, KV_N=2, D=32, Smax=80, layout=layout, dtype="fp16", mask=True)
+    ref = run(case)
+    tl = gen.tensorlist_from(case, seed=1, extra_hi=9)
+    s_axis = 2 if layout == "BNSD" else 1
+    assert len({k.shape[s_axis] for k in tl.key}) > 1  # the extents really differ
+    got = oracle.ifa_ref_tensorlist(tl.query, tl.key, tl.value, num_heads=8, num_kv_heads=2, scale=case.scale,
+                                    layout=layout, atten_mask=tl.atten_mask, actual_seq_lengths=tl.actual_seq_lengths)
+    assert np.array_equal(got, ref)
+
+
+def test_tensorlist_tokens_past_the_length_do_not_count():
+    case = gen.gqa_padded(91, B=3, N=4, KV_N=4, D=16, Smax=40, layout="BNSD", dtype="fp16", mask=False)
+    tl = gen.tensorlist_from(case, seed=2, extra_hi=8)
+    ref = oracle.ifa_ref_tensorlist(tl.query, tl.key, tl.value, num_heads=4, scale=case.scale,
+                                    actual_seq_lengths=tl.actual_seq_lengths)
+    poisoned_k = [k.copy() for k in tl.key]
+    for b, k in enumerate(poisoned_k):
+        k[:, :, int(tl.actual_seq_lengths[b]):, :] = np.float16(np.nan)
+    got = oracle.ifa_ref_tensorlist(tl.query, poisoned_k, tl.value, num_heads=4, scale=case.scale,
+                                    actual_seq_lengths=tl.actual_seq_lengths)
+    assert np.array_equal(got, ref)
+    # without lengths each batch attends over its whole tensor
+    full = oracle.ifa_ref_tensorlist(tl.query, tl.key, tl.value, num_heads=4, scale=case.scale)
+    for b in range(3):
+        one = oracle.ifa_ref(tl.query[b:b + 1], tl.key[b], tl.value[b], num_heads=4, scale=case.scale)
+        assert np.array_equal(full[b], one[0])
