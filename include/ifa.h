@@ -59,8 +59,11 @@ typedef enum { IFA_LAYOUT_BSH = 0, IFA_LAYOUT_BSND = 1, IFA_LAYOUT_BNSD = 2 } if
 /* Key/value storage.  CONTIG: (B,S,H) / (B,S,KV_N,D) / (B,KV_N,S,D) per
  * inputLayout.  PAGED_NBSD: (blockNum, KV_N, blockSize, D), only with a BNSD
  * query.  PAGED_BSH: (blockNum, blockSize, KV_N*D), any query layout.
- * ("IncreFlashAttention" README, page attention constraints.) */
-typedef enum { IFA_KV_CONTIG = 0, IFA_KV_PAGED_NBSD = 1, IFA_KV_PAGED_BSH = 2 } ifa_kv_format;
+ * ("IncreFlashAttention" README, page attention constraints.)  TENSORLIST: one
+ * tensor per batch (the README's non-contiguous case): (1,S_b,H) / (1,S_b,KV_N,D) /
+ * (1,KV_N,S_b,D), S_b the only extent that differs, B <= 256; run with
+ * ifa_run_tensorlist. */
+typedef enum { IFA_KV_CONTIG = 0, IFA_KV_PAGED_NBSD = 1, IFA_KV_PAGED_BSH = 2, IFA_KV_TENSORLIST = 3 } ifa_kv_format;
 
 typedef enum { IFA_F16 = 0, IFA_BF16 = 1, IFA_I8 = 2, IFA_U8 = 3, IFA_BOOL = 4, IFA_F32 = 5 } ifa_dtype;
 
@@ -79,7 +82,7 @@ typedef struct ifa_params {
     int64_t numHeads;         /* query heads N, 1..256 */
     int64_t numKeyValueHeads; /* key/value heads; 0 means numHeads; numHeads % it == 0 */
     int64_t headDim;          /* D, 1..512; a multiple of 8 (fp16/bf16 key/value) or 16 (int8) */
-    int64_t maxSeqLen;        /* CONTIG: the key/value S extent (Smax); ignored when paged */
+    int64_t maxSeqLen;        /* CONTIG: the key/value S extent (Smax); TENSORLIST: the largest S_b; ignored when paged */
     int32_t q_dtype;          /* IFA_F16 | IFA_BF16; attentionOut has this dtype */
     int32_t kv_dtype;         /* = q_dtype, or IFA_I8 (requires antiquant) */
     int32_t inputLayout;      /* ifa_layout */
@@ -158,6 +161,28 @@ ifa_status ifa_run(ifa_plan* plan, const void* query, const void* key, const voi
                    const void* antiquantScale, const void* antiquantOffset, const void* quantScale2,
                    const void* quantOffset2, void* attentionOut, void* workspace, size_t workspace_bytes,
                    void* stream);
+
+/*
+ * ifa_run for a plan whose kvFormat is IFA_KV_TENSORLIST: key and value are given as B
+ * separate tensors ("IncreFlashAttention" README, non-contiguous key/value: the list holds
+ * B tensors of batch 1 whose shapes differ only in S; B <= 256).
+ *   keyList, valueList  host arrays of B device pointers (16-byte aligned), tensor b of shape
+ *                       (1,S_b,H) / (1,S_b,KV_N,D) / (1,KV_N,S_b,D) per inputLayout
+ *   kvSeqLens           host int64 (B): S_b, 1 <= S_b <= maxSeqLen
+ * Batch b attends over tokens [0, actualSeqLengths[b]) of its tensor (all S_b when
+ * actualSeqLengths is NULL; values above S_b return IFA_ERR_PARAM_INVALID); the mask, when
+ * present, is indexed by token as for a contiguous cache (maskS >= the lengths).  Left
+ * padding is not defined here (IFA_ERR_PARAM_INVALID at ifa_create).  The other arguments are
+ * those of ifa_run.  The library keeps one TMA descriptor per tensor in device memory: a call
+ * whose pointers or extents differ from the previous call's re-encodes them and copies them to
+ * the device on `stream` before the kernel, so capture a CUDA graph only after a call with
+ * the same lists has run.
+ */
+ifa_status ifa_run_tensorlist(ifa_plan* plan, const void* query, const void* const* keyList,
+                              const void* const* valueList, const int64_t* kvSeqLens, const void* attenMask,
+                              const int64_t* actualSeqLengths, const void* antiquantScale,
+                              const void* antiquantOffset, const void* quantScale2, const void* quantOffset2,
+                              void* attentionOut, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Release a plan (NULL is accepted). Waits for nothing; do not free while a run is in flight. */
 ifa_status ifa_destroy(ifa_plan* plan);

@@ -61,6 +61,7 @@ struct alignas(128) DecodeParams {
     int mask_tma;              // the producer stages each tile's mask bytes (per-batch masks)
     int aq_per_channel;
     int aq_stage;              // per-channel key scales reach shared memory with each piece's query
+    const CUtensorMap* kv_maps;  // one tensor per batch: 4 maps per batch (K, K tail, V, V tail), else null
     int out_i8;                // int8 output: code = saturate(rint(y * scale2 + offset2))
     int q2_per_channel;        // scale2/offset2 entry n * D + d (else entry 0)
     int q2_bf16;               // scale2/offset2 are bf16 (else fp32)
@@ -143,6 +144,10 @@ struct KernelChoice {
     DecodeLaunchFn launch;
 };
 
+// Paged key/value caches (a block table maps tokens to blocks).
+inline bool kv_paged(const ifa_params& p) {
+    return p.kvFormat == IFA_KV_PAGED_NBSD || p.kvFormat == IFA_KV_PAGED_BSH;
+}
 bool params_are_valid(const ifa_params& p);
 ifa_status choose_kernel(const ifa_params& p, KernelChoice* kc);
 // Fills st/len/pre of every batch into bd (3B+1 ints); returns W and the longest sequence in tiles.

@@ -235,10 +235,12 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == NWC * 32) {  // the descriptor fetches overlap the rest of the prologue
-        prefetch_tensormap(&p.tmK);
-        prefetch_tensormap(&p.tmV);
-        prefetch_tensormap(&p.tmKt);
-        prefetch_tensormap(&p.tmVt);
+        if (!p.kv_maps) {
+            prefetch_tensormap(&p.tmK);
+            prefetch_tensormap(&p.tmV);
+            prefetch_tensormap(&p.tmKt);
+            prefetch_tensormap(&p.tmVt);
+        }
         if (p.mask_tma) prefetch_tensormap(&p.tmM);
     }
     // Programmatic dependent launch: the next kernel on the stream may start its own prologue on
@@ -283,19 +285,26 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         // be written).  The loads after the wait below then start from L2.
         TileCursor pc;
         cursor_init<T>(pc, bd, B, p.NGS, lo);
+        int fenced = -1;  // batch whose per-tensor maps are fenced for the TMA unit
         for (long long g = lo; g < hi && g < lo + C::PREFETCH_TILES; ++g) {
+            if (p.kv_maps && pc.b != fenced) {
+                for (int m = 0; m < 4; ++m) fence_tensormap_acquire(p.kv_maps + 4 * pc.b + m);
+                fenced = pc.b;
+            }
             const int valid = min(T, bd[B + pc.b] - pc.i * T);
             const bool tail = valid < T;
             const int rows_per = tail ? p.tail_rows : p.box_rows;
             const int nbox = tail ? (valid + rows_per - 1) / rows_per : T / p.box_rows;
-            const CUtensorMap* mk = tail ? &p.tmKt : &p.tmK;
-            const CUtensorMap* mv = tail ? &p.tmVt : &p.tmV;
+            // one tensor per batch: its own maps, batch coordinate 0
+            const CUtensorMap* mk = p.kv_maps ? p.kv_maps + 4 * pc.b + (tail ? 1 : 0) : (tail ? &p.tmKt : &p.tmK);
+            const CUtensorMap* mv = p.kv_maps ? p.kv_maps + 4 * pc.b + (tail ? 3 : 2) : (tail ? &p.tmVt : &p.tmV);
+            const int wb = p.kv_maps ? 0 : pc.b;
             for (int k = 0; k < nbox; ++k) {
                 const int y = bd[pc.b] + pc.i * T + k * rows_per;
 #pragma unroll
                 for (int cg = 0; cg < C::NCG; ++cg) {
-                    tma_prefetch_4d(mk, cg * C::CG_ELEMS, y, pc.h, pc.b);
-                    tma_prefetch_4d(mv, cg * C::CG_ELEMS, y, pc.h, pc.b);
+                    tma_prefetch_4d(mk, cg * C::CG_ELEMS, y, pc.h, wb);
+                    tma_prefetch_4d(mv, cg * C::CG_ELEMS, y, pc.h, wb);
                 }
             }
             cursor_next<T>(pc, bd, B, RS, p.NGS);
@@ -334,6 +343,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         TileCursor cur;
         cursor_init<T>(cur, bd, B, p.NGS, lo);
         int my_blk = 0;
+        int fenced = -1;  // batch whose per-tensor maps are fenced for the TMA unit
         int it = 0;  // tiles of this CTA so far (< 2^31)
         for (long long g = lo; g < hi; ++g, ++it) {
             const int kk = it % batch_tiles;
@@ -418,8 +428,13 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                         tma_load_2d(sb + C::MASK_OFF + ml * kMaskBox, &p.tmM, &full[stage], (x0 & ~15) + ml * kMaskBox,
                                     p.mask_bstride ? b : 0);
                 }
-                const CUtensorMap* mk = tail ? &p.tmKt : &p.tmK;
-                const CUtensorMap* mv = tail ? &p.tmVt : &p.tmV;
+                // one tensor per batch: its own maps, batch coordinate 0
+                if (p.kv_maps && b != fenced) {
+                    for (int m = 0; m < 4; ++m) fence_tensormap_acquire(p.kv_maps + 4 * b + m);
+                    fenced = b;
+                }
+                const CUtensorMap* mk = p.kv_maps ? p.kv_maps + 4 * b + (tail ? 1 : 0) : (tail ? &p.tmKt : &p.tmK);
+                const CUtensorMap* mv = p.kv_maps ? p.kv_maps + 4 * b + (tail ? 3 : 2) : (tail ? &p.tmVt : &p.tmV);
                 for (int k = 0; k < nbox; ++k) {
                     const int r0 = k * rows_per;  // first row of the box within the tile
                     const int s = r0 / br;
@@ -430,7 +445,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                         w = blkbuf[s];
                     } else {
                         y = st + cur.i * T + r0;
-                        w = b;
+                        w = p.kv_maps ? 0 : b;
                     }
 #pragma unroll
                     for (int cg = 0; cg < C::NCG; ++cg) {

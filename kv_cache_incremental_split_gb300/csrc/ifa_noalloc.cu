@@ -68,6 +68,7 @@ extern "C" ifa_status ifa_run_noalloc(const ifa_params* params, const void* quer
     ifa_status st = choose_kernel(p, &kc);
     if (st != IFA_OK) return st;
     if (p.B > IFA_NOALLOC_MAX_BATCH) return IFA_ERR_PARAM_INVALID;  // windows must fit the launch parameters
+    if (p.kvFormat == IFA_KV_TENSORLIST) return IFA_ERR_PARAM_INVALID;  // per-tensor descriptors need device memory
     st = check_run_pointers(p, query, key, value, attenMask, actualSeqLengths, kvPaddingSize, n_kv_padding,
                             blockTable, antiquantScale, antiquantOffset, quantScale2, quantOffset2, attentionOut);
     if (st != IFA_OK) return st;

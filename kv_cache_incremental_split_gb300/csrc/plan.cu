@@ -73,6 +73,10 @@ bool params_are_valid(const ifa_params& p) {
         if (p.blockNum < 1 || p.blockNum > INT32_MAX) return false;
         if (p.blockTableCols < 1 || p.blockTableCols * p.blockSize > INT32_MAX / 2) return false;
         if (p.has_kv_padding) return false;  // left padding of a paged cache is not defined
+    } else if (p.kvFormat == IFA_KV_TENSORLIST) {
+        if (p.B > kInlineB) return false;  // README: at most 256 tensors in the list
+        if (p.maxSeqLen < 1 || p.maxSeqLen > INT32_MAX / 2) return false;
+        if (p.has_kv_padding) return false;  // left padding of per-batch tensors is not defined
     } else {
         return false;
     }
@@ -122,7 +126,7 @@ ifa_status choose_kernel(const ifa_params& p, KernelChoice* kc) {
     // Full tiles move in boxes as large as the tile (or the cache block); a window's last
     // tile moves in boxes of at most 32 rows, so rows past the window end are not fetched.
     kc->box_rows = kc->T;
-    if (p.kvFormat != IFA_KV_CONTIG) kc->box_rows = (int)gcd64(kc->T, p.blockSize);
+    if (kv_paged(p)) kc->box_rows = (int)gcd64(kc->T, p.blockSize);
     kc->tail_rows = std::min(kc->box_rows, 32);
     const int tile_bytes = 2 * kc->T * kc->dpad * kc->es;
     const bool i8 = kc->kv_kind == KV_I8;
@@ -134,7 +138,7 @@ ifa_status choose_kernel(const ifa_params& p, KernelChoice* kc) {
 ifa_status build_windows(const ifa_params& p, const KernelChoice& kc, const int64_t* lens, const int64_t* pads,
                          int64_t n_pads, int32_t* bd, int64_t* W_out, int* max_seq_tiles) {
     const int B = (int)p.B;
-    const bool paged = p.kvFormat != IFA_KV_CONTIG;
+    const bool paged = kv_paged(p);
     const bool left_pad = p.has_kv_padding && lens != nullptr;
     const int RS = kc.KV_N * kc.NGS;
     const int64_t cap = paged ? p.blockTableCols * p.blockSize : p.maxSeqLen;
@@ -277,7 +281,7 @@ ifa_status check_run_pointers(const ifa_params& p, const void* query, const void
                               int64_t n_kv_padding, const int32_t* blockTable, const void* antiquantScale,
                               const void* antiquantOffset, const void* quantScale2, const void* quantOffset2,
                               const void* attentionOut) {
-    const bool paged = p.kvFormat != IFA_KV_CONTIG;
+    const bool paged = kv_paged(p);
     if (!query || !key || !value || !attentionOut) return IFA_ERR_PARAM_NULLPTR;
     if (p.has_mask && !attenMask) return IFA_ERR_PARAM_NULLPTR;
     if (paged && (!blockTable || !actualSeqLengths)) return IFA_ERR_PARAM_NULLPTR;
@@ -389,7 +393,7 @@ void fill_decode_params(DecodeParams& dp, const ifa_params& p, const KernelChoic
     dp.GT = kc.GT;
     dp.NGS = kc.NGS;
     dp.q_bf16 = p.q_dtype == IFA_BF16;
-    dp.paged = p.kvFormat != IFA_KV_CONTIG;
+    dp.paged = kv_paged(p);
     dp.block_size = (int)p.blockSize;
     dp.bt_cols = (int)p.blockTableCols;
     dp.block_num = (int)p.blockNum;

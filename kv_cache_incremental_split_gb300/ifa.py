@@ -27,13 +27,14 @@ IFA_ERR_PARAM_INVALID = 161002
 IFA_ERR_RUNTIME = 361001
 
 LAYOUTS = {"BSH": 0, "BSND": 1, "BNSD": 2}
-KV_FORMATS = {"contig": 0, "paged_nbsd": 1, "paged_bsh": 2}
+KV_FORMATS = {"contig": 0, "paged_nbsd": 1, "paged_bsh": 2, "tensorlist": 3}
 DTYPES = {"fp16": 0, "bf16": 1, "int8": 2, "uint8": 3, "bool": 4, "fp32": 5}
 ANTIQUANT = {"none": 0, "per_channel": 1, "per_tensor": 2}
 
 # Every symbol include/ifa.h declares.
 EXPORTED = ("ifa_create", "ifa_run", "ifa_destroy", "ifa_get_device_errors", "ifa_last_launch_count",
-            "ifa_run_noalloc", "sfa_workspace_size", "sfa_run", "ifa_kv_append", "ifa_status_string")
+            "ifa_run_noalloc", "ifa_run_tensorlist", "sfa_workspace_size", "sfa_run", "ifa_kv_append",
+            "ifa_status_string")
 
 # Fixed scratch of ifa_run_noalloc (include/ifa.h).
 IFA_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -95,6 +96,9 @@ def load_library():
             lib.ifa_create.argtypes = [ctypes.POINTER(IfaParams), ctypes.POINTER(vp), ctypes.POINTER(sz)]
             lib.ifa_run.restype = ctypes.c_int32
             lib.ifa_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            lib.ifa_run_tensorlist.restype = ctypes.c_int32
+            lib.ifa_run_tensorlist.argtypes = [vp, vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp, vp, vp, vp,
+                                               vp, vp, vp, vp, sz, vp]
             lib.ifa_destroy.restype = ctypes.c_int32
             lib.ifa_destroy.argtypes = [vp]
             lib.ifa_get_device_errors.restype = ctypes.c_int32
@@ -149,6 +153,19 @@ def ifa_run_noalloc(params: IfaParams, query, key, value, atten_mask, actual_seq
                                           actual_seq_lengths, kv_padding_size, n_kv_padding, block_table,
                                           antiquant_scale, antiquant_offset, quant_scale2, quant_offset2,
                                           attention_out, device_error_flags, stream)
+
+
+def ifa_run_tensorlist(plan, query, key_list, value_list, kv_seq_lens, atten_mask, actual_seq_lengths,
+                       antiquant_scale, antiquant_offset, quant_scale2, quant_offset2, attention_out, workspace,
+                       workspace_bytes, stream) -> int:
+    """key_list / value_list: sequences of B device addresses; kv_seq_lens and
+    actual_seq_lengths: host addresses of int64 arrays (or None); other pointers as ifa_run."""
+    n = len(key_list)
+    karr = (ctypes.c_void_p * max(1, n))(*key_list)
+    varr = (ctypes.c_void_p * max(1, n))(*value_list)
+    return load_library().ifa_run_tensorlist(plan, query, karr, varr, kv_seq_lens, atten_mask, actual_seq_lengths,
+                                             antiquant_scale, antiquant_offset, quant_scale2, quant_offset2,
+                                             attention_out, workspace, workspace_bytes, stream)
 
 
 def ifa_destroy(plan) -> int:
@@ -236,6 +253,18 @@ class IncreFlashAttention:
             out = torch.empty(query.shape, dtype=torch.int8, device=query.device) if self.out_i8 \
                 else torch.empty_like(query)
         lens = None if actual_seq_lengths is None else np.ascontiguousarray(actual_seq_lengths, dtype=np.int64)
+        if self.params.kvFormat == KV_FORMATS["tensorlist"]:
+            # key / value: one tensor per batch; S_b is the token extent of each
+            s_axis = 2 if self.params.inputLayout == LAYOUTS["BNSD"] else 1
+            slen = np.ascontiguousarray([int(t.shape[s_axis]) for t in key], dtype=np.int64)
+            st = ifa_run_tensorlist(self.plan, _ptr(query), [_ptr(t) for t in key], [_ptr(t) for t in value],
+                                    slen.ctypes.data, _ptr(atten_mask), None if lens is None else lens.ctypes.data,
+                                    _ptr(antiquant_scale), _ptr(antiquant_offset), _ptr(quant_scale2),
+                                    _ptr(quant_offset2), _ptr(out), _ptr(self.workspace), self.workspace.numel(),
+                                    _stream_handle(stream))
+            if st != IFA_OK:
+                raise IfaError(st, "ifa_run_tensorlist")
+            return out
         pads = None if kv_padding_size is None else np.ascontiguousarray(kv_padding_size, dtype=np.int64).reshape(-1)
         st = ifa_run(self.plan, _ptr(query), _ptr(key), _ptr(value), _ptr(atten_mask),
                      None if lens is None else lens.ctypes.data,

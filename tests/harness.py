@@ -65,7 +65,7 @@ def make_op(case: gen.IfaCase, split_tiles=0, **kw):
         batch=case.B, num_heads=case.num_heads, num_kv_heads=case.num_kv_heads, head_dim=case.D,
         max_seq_len=case.max_seq_len, dtype=case.q_dtype, kv_dtype=case.kv_dtype, layout=case.layout,
         kv_format=case.kv_format, block_size=case.block_size,
-        block_num=case.key.shape[0] if case.kv_format != "contig" else 0,
+        block_num=case.key.shape[0] if case.kv_format in ("paged_nbsd", "paged_bsh") else 0,
         block_table_cols=case.block_table.shape[1] if case.block_table is not None else 0,
         mask_shape=None if m is None else m.shape,
         mask_dtype="bool" if m is None or m.dtype == np.bool_ else ("int8" if m.dtype == np.int8 else "uint8"),

@@ -98,7 +98,8 @@ INVALID = [
     dict(q_dtype=2), dict(kv_dtype=0),  # bf16 query with fp16 cache
     dict(kv_dtype=2),  # int8 cache without antiquant
     dict(antiquant=1),  # antiquant without an int8 cache
-    dict(inputLayout=3), dict(kvFormat=3), dict(maxSeqLen=0),
+    dict(inputLayout=3), dict(kvFormat=4), dict(maxSeqLen=0),
+    dict(kvFormat=3, B=257), dict(kvFormat=3, has_kv_padding=1), dict(kvFormat=3, maxSeqLen=0),
     dict(kvFormat=1, blockSize=128, blockNum=10, blockTableCols=4),  # NBSD cache needs a BNSD query
     dict(kvFormat=2, blockSize=0, blockNum=10, blockTableCols=4),
     dict(kvFormat=2, blockSize=520, blockNum=10, blockTableCols=4),
@@ -133,6 +134,7 @@ VALID = [
     dict(q_dtype=0, kv_dtype=2, antiquant=2, kvFormat=0, has_kv_padding=1),
     dict(has_mask=1, mask_dtype=4, maskB=1, maskN=8, maskS=1024), dict(headDim=16), dict(headDim=256),
     dict(out_dtype=2, quant2=2, quant2_dtype=5), dict(out_dtype=2, quant2=1, quant2_dtype=1),
+    dict(kvFormat=3), dict(kvFormat=3, inputLayout=2, B=256),
     dict(q_dtype=0, kv_dtype=0, out_dtype=2, quant2=1, quant2_dtype=5),
 ]
 
@@ -259,3 +261,18 @@ def test_append_null_and_misaligned_arguments(lib):
     assert ifa.kv_append(p, ptr, ptr, ptr + 4, None, None, None, ptr, ptr, None, None) == ifa.IFA_ERR_PARAM_INVALID
     # B = 0 validates and enqueues nothing
     assert ifa.kv_append(append_params(B=0), ptr, ptr, ptr, None, None, None, ptr, ptr, None, None) == ifa.IFA_OK
+
+
+def test_tensorlist_entry_point_checks(lib):
+    # a tensor-list plan refuses ifa_run, a contiguous one refuses ifa_run_tensorlist
+    st, plan, ws = ifa.ifa_create(base_params(kvFormat=3))
+    if st != ifa.IFA_OK:  # no device here: validation passed, the device query failed
+        assert st == ifa.IFA_ERR_RUNTIME
+        return
+    try:
+        assert lib.ifa_run(plan, 16, 16, 16, None, None, None, 0, None, None, None, None, None, 16, None, 0,
+                           None) == ifa.IFA_ERR_PARAM_INVALID
+        assert ifa.ifa_run_tensorlist(plan, 16, [], [], None, None, None, None, None, None, None, 16, None, 0,
+                                      None) == ifa.IFA_ERR_PARAM_NULLPTR
+    finally:
+        ifa.ifa_destroy(plan)
