@@ -46,6 +46,9 @@ WORKLOADS = {
                   "random block table, lengths U{512..32768}"),
     "int8_leftpad": ("int8 KV antiquant + left padding: B=32 N=64 KV_N=8 D=128 fp16 query, BNSD int8 K/V, "
                      "per-channel scale/offset, Smax=8192, lengths U{256..8192}, pad Smax-len-U{0..64}"),
+    "gqa_tensorlist": ("GQA decode, key/value as one tensor per batch: B=16 N=32 KV_N=8 D=128 BSH bf16, "
+                       "tensor b of batch 1 holding len_b + U{0..256} tokens, lengths U{1..4096}, bool mask "
+                       "(B,1,1,4096) true past each length, scale 1/sqrt(128)"),
     "paged_gqa_small": ("paged GQA decode, profiling size: B=64 N=32 KV_N=8 D=128 bf16, blockSize 128, "
                         "random block table, lengths U{512..4096}"),
     "sfa_mla": ("sparse MLA-absorb decode: B=32 Q_N=128 KV_N=1 D=512+rope 64 bf16, PA_BSND block 64, "
@@ -77,6 +80,8 @@ def make_case(name: str, seed: int):
         return gen.sfa_mla(seed, sparse_size=128, nvalid_lo=64, nvalid_hi=128, sparse_block_size=16)
     if name == "sfa_mla_mtp":
         return gen.sfa_mla(seed, Q_S=2, sparse_mode=3)
+    if name == "gqa_tensorlist":
+        return gen.tensorlist_from(gen.gqa_padded(seed), seed, extra_hi=256)
     if name == "kv_append_paged":
         return gen.kv_append_paged(seed)
     if name == "kv_append_int8":
@@ -323,6 +328,8 @@ def _batch_subset(case, b):
     c.query = case.query[sel]
     if case.kv_format == "contig":
         c.key, c.value = case.key[sel], case.value[sel]
+    elif case.kv_format == "tensorlist":
+        c.key, c.value = [case.key[b]], [case.value[b]]
     if case.block_table is not None:
         c.block_table = case.block_table[sel]
     if case.atten_mask is not None and case.atten_mask.shape[0] > 1:
@@ -349,6 +356,11 @@ def _run_oracle(c):
         oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices, c.block_table,
                        c.actual_seq_lengths_kv, scale=c.scale, sparse_block_size=c.sparse_block_size,
                        sparse_mode=c.sparse_mode, actual_seq_lengths_query=c.actual_seq_lengths_query)
+    elif c.kv_format == "tensorlist":
+        oracle.ifa_ref_tensorlist(c.query, c.key, c.value, num_heads=c.num_heads, num_kv_heads=c.num_kv_heads,
+                                  scale=c.scale, layout=c.layout, atten_mask=c.atten_mask,
+                                  actual_seq_lengths=c.actual_seq_lengths, antiquant=aq[c.antiquant],
+                                  antiquant_scale=c.antiquant_scale, antiquant_offset=c.antiquant_offset)
     else:
         oracle.ifa_ref(c.query, c.key, c.value, num_heads=c.num_heads, num_kv_heads=c.num_kv_heads,
                        scale=c.scale, layout=c.layout, kv_format=fmt[c.kv_format], block_size=c.block_size,
@@ -449,53 +461,79 @@ def _to_dev(a, dev):
 
 
 class IfaWorkload:
-    """One incremental-attention problem on the device, with rotating key/value copies."""
+    """One incremental-attention problem on the device, with rotating key/value copies.  With
+    key/value as one tensor per batch each copy has its own op (plan), so the per-batch tensor
+    maps of every copy are encoded once, before the graphs are captured."""
 
     def __init__(self, case: gen.IfaCase, dev, copies_for):
         from kv_cache_incremental_split_gb300.ifa import IncreFlashAttention
         self.case, self.dev = case, dev
         m = case.atten_mask
-        self.op = IncreFlashAttention(
-            batch=case.B, num_heads=case.num_heads, num_kv_heads=case.num_kv_heads, head_dim=case.D,
-            max_seq_len=case.max_seq_len, dtype=case.q_dtype, kv_dtype=case.kv_dtype, layout=case.layout,
-            kv_format=case.kv_format, block_size=case.block_size,
-            block_num=case.key.shape[0] if case.kv_format != "contig" else 0,
-            block_table_cols=case.block_table.shape[1] if case.block_table is not None else 0,
-            mask_shape=None if m is None else m.shape, mask_dtype="bool", antiquant=case.antiquant,
-            kv_padding=case.kv_padding_size is not None, scale=case.scale, device=dev)
+        self.tensorlist = case.kv_format == "tensorlist"
+        paged = case.kv_format.startswith("paged")
+
+        def new_op():
+            return IncreFlashAttention(
+                batch=case.B, num_heads=case.num_heads, num_kv_heads=case.num_kv_heads, head_dim=case.D,
+                max_seq_len=case.max_seq_len, dtype=case.q_dtype, kv_dtype=case.kv_dtype, layout=case.layout,
+                kv_format=case.kv_format, block_size=case.block_size,
+                block_num=case.key.shape[0] if paged else 0,
+                block_table_cols=case.block_table.shape[1] if case.block_table is not None else 0,
+                mask_shape=None if m is None else m.shape, mask_dtype="bool", antiquant=case.antiquant,
+                kv_padding=case.kv_padding_size is not None, scale=case.scale, device=dev)
+
+        self.copies = copies_for
+        self.ops = [new_op() for _ in range(self.copies if self.tensorlist else 1)]
+        self.op = self.ops[0]
+        self.e2e_op = new_op() if self.tensorlist else self.op
         self.q = _to_dev(case.query, dev)
-        k, v = _to_dev(case.key, dev), _to_dev(case.value, dev)
         self.mask, self.bt = _to_dev(case.atten_mask, dev), _to_dev(case.block_table, dev)
         self.sc, self.of = _to_dev(case.antiquant_scale, dev), _to_dev(case.antiquant_offset, dev)
-        self.copies = copies_for
-        self.rotating_bytes = k.numel() * k.element_size() + v.numel() * v.element_size()
-        self.ks = [k] + [k.clone() for _ in range(self.copies - 1)]
-        self.vs = [v] + [v.clone() for _ in range(self.copies - 1)]
+        if self.tensorlist:
+            k = [_to_dev(t, dev) for t in case.key]
+            v = [_to_dev(t, dev) for t in case.value]
+            self.rotating_bytes = sum(t.numel() * t.element_size() for t in k + v)
+            self.ks = [k] + [[t.clone() for t in k] for _ in range(self.copies - 1)]
+            self.vs = [v] + [[t.clone() for t in v] for _ in range(self.copies - 1)]
+        else:
+            k, v = _to_dev(case.key, dev), _to_dev(case.value, dev)
+            self.rotating_bytes = k.numel() * k.element_size() + v.numel() * v.element_size()
+            self.ks = [k] + [k.clone() for _ in range(self.copies - 1)]
+            self.vs = [v] + [v.clone() for _ in range(self.copies - 1)]
         self.outs = [self.q.new_empty(self.q.shape) for _ in range(self.copies)]
         self.dtype = case.q_dtype if case.kv_dtype != "int8" else "int8-kv/" + case.q_dtype
-        self.call_name = "ifa_run"
+        self.call_name = "ifa_run_tensorlist" if self.tensorlist else "ifa_run"
         self.launch_note = "; programmatic dependent launch lets each kernel start its prologue as the previous one drains"
 
     def call(self, i, stream):
         c = self.case
-        return self.op(self.q, self.ks[i], self.vs[i], atten_mask=self.mask, actual_seq_lengths=c.actual_seq_lengths,
-                       kv_padding_size=c.kv_padding_size, block_table=self.bt, antiquant_scale=self.sc,
-                       antiquant_offset=self.of, out=self.outs[i], stream=stream)
+        op = self.ops[i] if self.tensorlist else self.op
+        return op(self.q, self.ks[i], self.vs[i], atten_mask=self.mask, actual_seq_lengths=c.actual_seq_lengths,
+                  kv_padding_size=c.kv_padding_size, block_table=self.bt, antiquant_scale=self.sc,
+                  antiquant_offset=self.of, out=self.outs[i], stream=stream)
 
     def launches_per_call(self):
         return self.op.last_launch_count()
 
     def host_inputs(self):
         c = self.case
-        return {n: a for n, a in (("q", c.query), ("k", c.key), ("v", c.value), ("mask", c.atten_mask),
-                                  ("bt", c.block_table), ("sc", c.antiquant_scale), ("of", c.antiquant_offset))
-                if a is not None}
+        named = [("q", c.query), ("mask", c.atten_mask), ("bt", c.block_table), ("sc", c.antiquant_scale),
+                 ("of", c.antiquant_offset)]
+        if self.tensorlist:
+            named += [(f"k{b}", t) for b, t in enumerate(c.key)] + [(f"v{b}", t) for b, t in enumerate(c.value)]
+        else:
+            named += [("k", c.key), ("v", c.value)]
+        return {n: a for n, a in named if a is not None}
 
     def call_on(self, d, stream):
         c = self.case
-        return self.op(d["q"], d["k"], d["v"], atten_mask=d.get("mask"), actual_seq_lengths=c.actual_seq_lengths,
-                       kv_padding_size=c.kv_padding_size, block_table=d.get("bt"), antiquant_scale=d.get("sc"),
-                       antiquant_offset=d.get("of"), stream=stream)
+        if self.tensorlist:
+            k, v = [d[f"k{b}"] for b in range(c.B)], [d[f"v{b}"] for b in range(c.B)]
+        else:
+            k, v = d["k"], d["v"]
+        return self.e2e_op(d["q"], k, v, atten_mask=d.get("mask"), actual_seq_lengths=c.actual_seq_lengths,
+                           kv_padding_size=c.kv_padding_size, block_table=d.get("bt"), antiquant_scale=d.get("sc"),
+                           antiquant_offset=d.get("of"), stream=stream)
 
 
 class SfaWorkload:
@@ -625,7 +663,9 @@ def run_gpu(args):
     stream = torch.cuda.Stream(device=dev)
 
     with torch.cuda.stream(stream):
-        for w in range(max(args.warmup, 3)):
+        # every copy is called at least once before the capture (a tensorlist plan encodes its
+        # per-batch descriptors on its first call, outside the graph)
+        for w in range(max(args.warmup, 3, copies)):
             wl.call(w % copies, stream)
         stream.synchronize()
         launches_per_call = wl.launches_per_call()

@@ -176,7 +176,8 @@ ifa_status ifa_run(ifa_plan* plan, const void* query, const void* key, const voi
  * those of ifa_run.  The library keeps one TMA descriptor per tensor in device memory: a call
  * whose pointers or extents differ from the previous call's re-encodes them and copies them to
  * the device on `stream` before the kernel, so capture a CUDA graph only after a call with
- * the same lists has run.
+ * the same lists has run: under capture, lists that differ from the previous call's return
+ * IFA_ERR_PARAM_INVALID and leave the stream untouched.
  */
 ifa_status ifa_run_tensorlist(ifa_plan* plan, const void* query, const void* const* keyList,
                               const void* const* valueList, const int64_t* kvSeqLens, const void* attenMask,

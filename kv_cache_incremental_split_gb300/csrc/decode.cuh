@@ -174,7 +174,7 @@ void fill_decode_params(DecodeParams& dp, const ifa_params& p, const KernelChoic
                         const void* antiquantOffset, const void* quantScale2, const void* quantOffset2,
                         void* attentionOut, int64_t W, int P);
 
-DecodeLaunchFn decode_launcher(int kv_kind, int dpad, int nt);
+DecodeLaunchFn decode_launcher(int kv_kind, int dpad, int nt, bool tensorlist);
 bool decode_cfg(int kv_kind, int dpad, int nt, int* slot_floats, int* smem, int* tile_tokens, int* threads);
 
 }  // namespace ifa

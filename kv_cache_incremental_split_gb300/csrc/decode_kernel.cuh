@@ -199,7 +199,9 @@ __device__ __forceinline__ uint32_t load_mask_bits(const DecodeParams& p, const 
     return bits;
 }
 
-template <int KV, int DPAD, int NT>
+// TL: key/value given as one tensor per batch; the producer takes each batch's descriptors from
+// p.kv_maps (a separate instantiation, so the other layouts' producer keeps its parameter maps).
+template <int KV, int DPAD, int NT, bool TL>
 __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
     using C = DecodeCfg<KV, DPAD, NT>;
@@ -235,7 +237,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == NWC * 32) {  // the descriptor fetches overlap the rest of the prologue
-        if (!p.kv_maps) {
+        if constexpr (!TL) {
             prefetch_tensormap(&p.tmK);
             prefetch_tensormap(&p.tmV);
             prefetch_tensormap(&p.tmKt);
@@ -285,20 +287,22 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         // be written).  The loads after the wait below then start from L2.
         TileCursor pc;
         cursor_init<T>(pc, bd, B, p.NGS, lo);
-        int fenced = -1;  // batch whose per-tensor maps are fenced for the TMA unit
+        [[maybe_unused]] int fenced = -1;  // batch whose per-tensor maps are fenced for the TMA unit
         for (long long g = lo; g < hi && g < lo + C::PREFETCH_TILES; ++g) {
-            if (p.kv_maps && pc.b != fenced) {
-                for (int m = 0; m < 4; ++m) fence_tensormap_acquire(p.kv_maps + 4 * pc.b + m);
-                fenced = pc.b;
+            if constexpr (TL) {
+                if (pc.b != fenced) {
+                    for (int m = 0; m < 4; ++m) fence_tensormap_acquire(p.kv_maps + 4 * pc.b + m);
+                    fenced = pc.b;
+                }
             }
             const int valid = min(T, bd[B + pc.b] - pc.i * T);
             const bool tail = valid < T;
             const int rows_per = tail ? p.tail_rows : p.box_rows;
             const int nbox = tail ? (valid + rows_per - 1) / rows_per : T / p.box_rows;
             // one tensor per batch: its own maps, batch coordinate 0
-            const CUtensorMap* mk = p.kv_maps ? p.kv_maps + 4 * pc.b + (tail ? 1 : 0) : (tail ? &p.tmKt : &p.tmK);
-            const CUtensorMap* mv = p.kv_maps ? p.kv_maps + 4 * pc.b + (tail ? 3 : 2) : (tail ? &p.tmVt : &p.tmV);
-            const int wb = p.kv_maps ? 0 : pc.b;
+            const CUtensorMap* mk = TL ? p.kv_maps + 4 * pc.b + (tail ? 1 : 0) : (tail ? &p.tmKt : &p.tmK);
+            const CUtensorMap* mv = TL ? p.kv_maps + 4 * pc.b + (tail ? 3 : 2) : (tail ? &p.tmVt : &p.tmV);
+            const int wb = TL ? 0 : pc.b;
             for (int k = 0; k < nbox; ++k) {
                 const int y = bd[pc.b] + pc.i * T + k * rows_per;
 #pragma unroll
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         TileCursor cur;
         cursor_init<T>(cur, bd, B, p.NGS, lo);
         int my_blk = 0;
-        int fenced = -1;  // batch whose per-tensor maps are fenced for the TMA unit
+        [[maybe_unused]] int fenced = -1;  // batch whose per-tensor maps are fenced for the TMA unit
         int it = 0;  // tiles of this CTA so far (< 2^31)
         for (long long g = lo; g < hi; ++g, ++it) {
             const int kk = it % batch_tiles;
@@ -429,12 +433,14 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                                     p.mask_bstride ? b : 0);
                 }
                 // one tensor per batch: its own maps, batch coordinate 0
-                if (p.kv_maps && b != fenced) {
-                    for (int m = 0; m < 4; ++m) fence_tensormap_acquire(p.kv_maps + 4 * b + m);
-                    fenced = b;
+                if constexpr (TL) {
+                    if (b != fenced) {
+                        for (int m = 0; m < 4; ++m) fence_tensormap_acquire(p.kv_maps + 4 * b + m);
+                        fenced = b;
+                    }
                 }
-                const CUtensorMap* mk = p.kv_maps ? p.kv_maps + 4 * b + (tail ? 1 : 0) : (tail ? &p.tmKt : &p.tmK);
-                const CUtensorMap* mv = p.kv_maps ? p.kv_maps + 4 * b + (tail ? 3 : 2) : (tail ? &p.tmVt : &p.tmV);
+                const CUtensorMap* mk = TL ? p.kv_maps + 4 * b + (tail ? 1 : 0) : (tail ? &p.tmKt : &p.tmK);
+                const CUtensorMap* mv = TL ? p.kv_maps + 4 * b + (tail ? 3 : 2) : (tail ? &p.tmVt : &p.tmV);
                 for (int k = 0; k < nbox; ++k) {
                     const int r0 = k * rows_per;  // first row of the box within the tile
                     const int s = r0 / br;
@@ -445,7 +451,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                         w = blkbuf[s];
                     } else {
                         y = st + cur.i * T + r0;
-                        w = p.kv_maps ? 0 : b;
+                        w = TL ? 0 : b;
                     }
 #pragma unroll
                     for (int cg = 0; cg < C::NCG; ++cg) {
@@ -1027,19 +1033,19 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     }
 }
 
-template <int KV, int DPAD, int NT>
+template <int KV, int DPAD, int NT, bool TL = false>
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) {
     using C = DecodeCfg<KV, DPAD, NT>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<KV, DPAD, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<KV, DPAD, NT, TL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM);
         if (e != cudaSuccess) return e;
         if constexpr (C::SPLIT_REGS) {
             // setmaxnreg.inc draws on the registers the block was launched with: refuse to launch
             // a build whose register count cannot cover the split (the increase would never return).
             cudaFuncAttributes fa;
-            e = cudaFuncGetAttributes(&fa, decode_kernel<KV, DPAD, NT>);
+            e = cudaFuncGetAttributes(&fa, decode_kernel<KV, DPAD, NT, TL>);
             if (e != cudaSuccess) return e;
             if ((long long)fa.numRegs * C::THREADS < C::REG_POOL_NEEDED) return cudaErrorInvalidConfiguration;
         }
@@ -1055,7 +1061,7 @@ cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<KV, DPAD, NT>, p);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<KV, DPAD, NT, TL>, p);
 }
 
 }  // namespace ifa

@@ -246,6 +246,14 @@ extern "C" ifa_status ifa_run_tensorlist(ifa_plan* pl, const void* query, const 
     if (!actualSeqLengths && B > 0) lens.assign(kvSeqLens, kvSeqLens + B);
     const int64_t* use_lens = actualSeqLengths ? actualSeqLengths : (B > 0 ? lens.data() : nullptr);
     if (B > 0 && !same) {
+        // The descriptor copy reads pageable host memory, which a CUDA graph cannot replay:
+        // under capture the lists must be those of the plan's previous call.
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cap) != cudaSuccess) {
+            cudaGetLastError();
+            return IFA_ERR_RUNTIME;
+        }
+        if (cap != cudaStreamCaptureStatusNone) return IFA_ERR_PARAM_INVALID;
         // batch b's tensor is a one-batch contiguous cache of extent S_b: encode its four maps
         pl->list_k.clear();
         pl->h_maps.assign((size_t)4 * B, CUtensorMap{});

@@ -18,7 +18,16 @@ DecodeLaunchFn decode_launcher_bf16(int dpad, int nt);
 DecodeLaunchFn decode_launcher_f16(int dpad, int nt);
 DecodeLaunchFn decode_launcher_i8(int dpad, int nt);
 
-DecodeLaunchFn decode_launcher(int kv_kind, int dpad, int nt) {
+DecodeLaunchFn decode_launcher_tl_bf16(int dpad, int nt);
+DecodeLaunchFn decode_launcher_tl_f16(int dpad, int nt);
+DecodeLaunchFn decode_launcher_tl_i8(int dpad, int nt);
+
+DecodeLaunchFn decode_launcher(int kv_kind, int dpad, int nt, bool tensorlist) {
+    if (tensorlist) {
+        if (kv_kind == KV_BF16) return decode_launcher_tl_bf16(dpad, nt);
+        if (kv_kind == KV_F16) return decode_launcher_tl_f16(dpad, nt);
+        return decode_launcher_tl_i8(dpad, nt);
+    }
     if (kv_kind == KV_BF16) return decode_launcher_bf16(dpad, nt);
     if (kv_kind == KV_F16) return decode_launcher_f16(dpad, nt);
     return decode_launcher_i8(dpad, nt);
@@ -120,7 +129,7 @@ ifa_status choose_kernel(const ifa_params& p, KernelChoice* kc) {
     kc->GT = std::min(kc->G, kc->dpad >= 256 ? 8 : 16);
     kc->NT = (kc->GT + 7) / 8;
     kc->NGS = (kc->G + kc->GT - 1) / kc->GT;
-    kc->launch = decode_launcher(kc->kv_kind, kc->dpad, kc->NT);
+    kc->launch = decode_launcher(kc->kv_kind, kc->dpad, kc->NT, p.kvFormat == IFA_KV_TENSORLIST);
     if (!kc->launch || !decode_cfg(kc->kv_kind, kc->dpad, kc->NT, &kc->slot_floats, &kc->smem, &kc->T, &kc->threads))
         return IFA_ERR_PARAM_INVALID;
     // Full tiles move in boxes as large as the tile (or the cache block); a window's last

@@ -20,6 +20,9 @@ static cudaError_t stub_launch(const DecodeParams&, int, cudaStream_t) { return 
 DecodeLaunchFn decode_launcher_bf16(int, int) { return stub_launch; }
 DecodeLaunchFn decode_launcher_f16(int, int) { return stub_launch; }
 DecodeLaunchFn decode_launcher_i8(int, int) { return stub_launch; }
+DecodeLaunchFn decode_launcher_tl_bf16(int, int) { return stub_launch; }
+DecodeLaunchFn decode_launcher_tl_f16(int, int) { return stub_launch; }
+DecodeLaunchFn decode_launcher_tl_i8(int, int) { return stub_launch; }
 }  // namespace ifa
 
 using namespace ifa;

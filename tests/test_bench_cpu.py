@@ -21,7 +21,7 @@ def run_ref(workload, steps, warmup, total):
     return line, time.time() - t
 
 
-@pytest.mark.parametrize("workload", ["tiny_mha", "sfa_mla_small", "kv_append_int8"])
+@pytest.mark.parametrize("workload", ["tiny_mha", "gqa_tensorlist", "sfa_mla_small", "kv_append_int8"])
 def test_reference_arm_line(workload):
     line, _ = run_ref(workload, 20, 3, 2.0)
     assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 20

@@ -87,3 +87,32 @@ def test_tensorlist_new_pointers_between_calls():
     c.value[1] = c.value[1][:, : int(c.actual_seq_lengths[1])].copy()
     got4, _ = run(c, op=op)
     assert max_abs_err(got4, ref_of(c)) <= TOL["bf16"]
+
+
+def test_tensorlist_graph_capture_needs_the_previous_lists():
+    """A captured call replays with the descriptors encoded before the capture; new lists under
+    capture are refused without touching the stream, so the capture stays usable."""
+    from kv_cache_incremental_split_gb300.ifa import IfaError
+    c = gen.tensorlist_from(gen.gqa_padded(105, B=4, Smax=1200), seed=8, extra_hi=50)
+    op = make_op(c)
+    keys = [to_device(k) for k in c.key]
+    values = [to_device(v) for v in c.value]
+    q, mask = to_device(c.query), to_device(c.atten_mask)
+    out = torch.empty_like(q)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        op(q, keys, values, atten_mask=mask, actual_seq_lengths=c.actual_seq_lengths, out=out, stream=stream)
+        stream.synchronize()
+        moved = [k.clone() for k in keys]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            with pytest.raises(IfaError):
+                op(q, moved, values, atten_mask=mask, actual_seq_lengths=c.actual_seq_lengths, out=out,
+                   stream=stream)
+            op(q, keys, values, atten_mask=mask, actual_seq_lengths=c.actual_seq_lengths, out=out, stream=stream)
+        out.zero_()
+        g.replay()
+        stream.synchronize()
+    assert op.device_errors() == 0
+    got = out_to_f64(out).reshape(c.B, c.num_heads, c.D)
+    assert max_abs_err(got, ref_of(c)) <= TOL["bf16"]
