@@ -26,10 +26,25 @@ constexpr int kSfaThreads = 10 * 32;  // producer, MMA issuer, four softmax warp
 constexpr int kSfaSlotFloats = 128 * kSfaHalf + 3 * 128;  // normalised O of one piece + M + L + largest score
 constexpr int kSfaBarBytes = 512;
 constexpr int kSfaSmem = 1024 + kSfaQBytes + kSfaStages * kSfaStageBytes + kSfaRSlots * kSfaRSlotBytes + kSfaBarBytes;
-constexpr size_t kSfaPartialOffset = 4096;  // workspace: [0,256) error word, partial slots from here
+// workspace: [0, 256) error word; [kSfaStartOffset, + 32 * kMaxCtas) each CTA's start (SfaStart);
+// partial slots from kSfaPartialOffset; then live tiles per query row (R ints) and their
+// prefix over rows, two sequences per row (R + 1 ints)
+constexpr size_t kSfaStartOffset = 1024;
+constexpr size_t kSfaPartialOffset = 16384;
+constexpr int kSfaCountCtas = 8;        // the tile-count kernel: one cluster
+constexpr int kSfaCountThreads = 512;
+constexpr int kSfaCountSmemRows = 4096;  // rows whose counts the count kernel scans in shared memory
 constexpr float kSfaRescaleSlack = 8.0f;    // log2 units the running max may trail before O is rescaled
 constexpr int kSfaCombineRows = 16;         // query heads per combine CTA
 constexpr float kLn2 = 0.6931471805599453f;  // scores in log2 units -> natural units
+
+// Where a CTA of the decode kernel starts: tiles [lo, hi) of the live-tile order, the first
+// one tile t of sequence (query row r, value half h), a sequence of n tiles whose first tile
+// has index `first`.
+struct SfaStart {
+    int lo, hi, r, h, t, n, first, pad;
+};
+static_assert(sizeof(SfaStart) == 32, "start table entry");
 
 struct alignas(128) SfaParams {
     CUtensorMap tmQ;    // 3-D (d, head, query row) over query, 64 x 128 x 1 boxes
@@ -49,7 +64,10 @@ struct alignas(128) SfaParams {
     float* lse_sum;         // nullable: sum of exp(score - lse_max) of each (query row, head)
     float* partials;
     int* err;
-    long long W;        // tiles: 2 * R * tiles_per_seq
+    SfaStart* starts;   // per CTA, written by the tile-count kernel
+    int* eff;           // live tiles of each query row (a sequence's tiles), 0 when no index is usable
+    int* pre;           // prefix over rows of 2 * eff (R + 1 entries): the tile order of the decode kernel
+    long long W;        // tiles before the count: 2 * R * tiles_per_seq (an upper bound)
     int P;
     int R, QS, QN, S_sp, tiles_per_seq;  // R query rows: B * QS (row r: batch r / QS, query token r % QS), or
                                          // the TND rows; S_sp: indices per row; tiles cover S_sp << sbs_log2
@@ -64,7 +82,7 @@ struct alignas(128) SfaParams {
     float scale_log2;
 };
 
-// Enqueues the decode kernel and the combine kernel (two launches).
+// Enqueues the tile-count kernel, the decode kernel and the combine kernel (three launches).
 cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream);
 
 }  // namespace ifa

@@ -17,6 +17,8 @@
 
 using namespace ifa;
 
+static_assert(kSfaStartOffset + sizeof(SfaStart) * kMaxCtas <= kSfaPartialOffset, "workspace layout");
+
 namespace {
 
 bool sfa_valid(const sfa_params& p) {
@@ -103,7 +105,9 @@ extern "C" ifa_status sfa_workspace_size(const sfa_params* params, size_t* works
     const int sms = sm_count();
     if (sms <= 0) return IFA_ERR_RUNTIME;
     const int P_max = std::min(kMaxCtas, sms);
-    *workspace_bytes = kSfaPartialOffset + (size_t)2 * P_max * kSfaSlotFloats * sizeof(float);
+    const int64_t R = params->layout_query == SFA_LAYOUT_TND ? params->Q_T : params->B * params->Q_S;
+    *workspace_bytes = kSfaPartialOffset + (size_t)2 * P_max * kSfaSlotFloats * sizeof(float) +
+                       ((size_t)(2 * R + 1) * sizeof(int) + 15) / 16 * 16;
     return IFA_OK;
 }
 
@@ -189,6 +193,9 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
     sp.kv_s = paged ? 0 : (int)p.KV_S;
     sp.out = attention_out;
     sp.partials = reinterpret_cast<float*>(ws + kSfaPartialOffset);
+    sp.starts = reinterpret_cast<SfaStart*>(ws + kSfaStartOffset);
+    sp.eff = reinterpret_cast<int*>(ws + kSfaPartialOffset + (size_t)2 * P_max * kSfaSlotFloats * sizeof(float));
+    sp.pre = sp.eff + R;
     sp.err = deviceErrorFlags ? deviceErrorFlags : reinterpret_cast<int*>(ws);
     sp.W = W;
     sp.P = P;

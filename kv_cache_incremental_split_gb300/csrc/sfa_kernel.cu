@@ -7,10 +7,13 @@
 // value channels (a full 128 x 512 fp32 accumulator would fill all of TMEM, so
 // the two halves are separate sequences; the two CTAs that hold the halves of
 // the same positions run at the same time and share the key rows through L2).
-// A sequence is cut into 64-position tiles of its sparse index row; persistent
-// CTAs take equal contiguous shares of all tiles.  A piece of a sequence that a
-// CTA boundary cuts goes to a partial slot (normalised O, running max M and sum
-// L per head) and the combine kernel merges the pieces of every cut sequence.
+// A sequence is cut into 64-position tiles of its sparse index row.  A first
+// kernel (one cluster) finds each row's live tiles (up to the last tile holding
+// a usable index: the invalid tail after it costs nothing) and the prefix over
+// rows; persistent CTAs take equal contiguous shares of the live tiles.  A piece
+// of a sequence that a CTA boundary cuts goes to a partial slot (normalised O,
+// running max M and sum L per head) and the combine kernel merges the pieces of
+// every cut sequence; it also writes the zero rows of sequences with no live tile.
 //
 // Per CTA:
 //  * resolver (warp 6): for each tile, the cache row of every position (index ->
@@ -34,6 +37,7 @@
 //    units, so P stays below 2^8; P goes to its TMEM buffer as 16-bit pairs.
 // Every wait is bounded; on a timeout the kernel records error bit 2, drains its
 // copies and MMAs, frees TMEM and returns.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -42,6 +46,8 @@
 #include "sfa.cuh"
 
 namespace ifa {
+
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -54,6 +60,14 @@ __device__ __forceinline__ float ex2f_approx(float x) {
 // CTA whose tile range [floor(c W / P), floor((c+1) W / P)) holds global tile t.
 __device__ __forceinline__ int cta_of_tile(long long t, long long W, int P) {
     return (int)(((t + 1) * (long long)P - 1) / W);
+}
+
+// CTAs that share W live tiles: at most the launch's P, and shares of at least
+// min(tiles per sequence, kMinPieceTiles) tiles, so every one of them holds a tile.
+__device__ __forceinline__ int active_ctas(long long W, int P, int tps) {
+    const long long share = max(1, min(tps, kMinPieceTiles));
+    const long long want = (W + share - 1) / share;
+    return (int)max(1LL, min((long long)P, want));
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf) {
@@ -72,6 +86,33 @@ struct RSlot {
     int any;             // some position is valid
 };
 static_assert(sizeof(RSlot) <= kSfaRSlotBytes, "resolver slot");
+
+// Position in the decode kernel's tile order: tile t of the n tiles of sequence (query row r,
+// value half h), whose first tile has index `first`.  Rows with no live tile are stepped over.
+struct SeqCursor {
+    int r, h, t, n;
+    long long first;
+    __device__ __forceinline__ void init(const SfaStart& s) {
+        r = s.r;
+        h = s.h;
+        t = s.t;
+        n = s.n;
+        first = s.first;
+    }
+    __device__ __forceinline__ void next(const int* eff, int R) {
+        if (++t < n) return;
+        t = 0;
+        first += n;
+        if (h == 0) {
+            h = 1;
+            return;
+        }
+        h = 0;
+        n = 0;
+        while (++r < R && (n = __ldcg(eff + r)) == 0) {
+        }
+    }
+};
 
 }  // namespace
 
@@ -93,13 +134,14 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
     uint64_t* done_bar = o_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    static_assert(2 * kSfaStages * 8 + 2 * kSfaRSlots * 8 + 10 * 8 + 8 <= kSfaBarBytes, "barrier area");
+    // this CTA's start, 16-byte aligned past the barriers, the TMEM address and the abort flag
+    SfaStart* sst = reinterpret_cast<SfaStart*>(reinterpret_cast<uint8_t*>(full) + 384);
+    static_assert(2 * kSfaStages * 8 + 2 * kSfaRSlots * 8 + 10 * 8 + 8 <= 384, "barrier area");
+    static_assert(384 + sizeof(SfaStart) <= kSfaBarBytes, "barrier area");
+    static_assert((kSfaQBytes + kSfaStages * kSfaStageBytes + kSfaRSlots * kSfaRSlotBytes) % 16 == 0, "alignment");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const long long lo = (long long)blockIdx.x * p.W / p.P;
-    const long long hi = (long long)(blockIdx.x + 1) * p.W / p.P;
-    const int tps = p.tiles_per_seq;
     auto slot_of = [&](long long k) { return reinterpret_cast<RSlot*>(rbase + (int)(k % kSfaRSlots) * kSfaRSlotBytes); };
 
     if (threadIdx.x == 0) {
@@ -126,9 +168,19 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
+    // The start table and the live-tile counts come from the tile-count kernel (programmatic
+    // dependent launch: everything above overlaps it).
+    pdl_wait_primary();
+    if (threadIdx.x == 0) {
+        const int4* src = reinterpret_cast<const int4*>(p.starts + blockIdx.x);
+        reinterpret_cast<int4*>(sst)[0] = __ldcg(src);
+        reinterpret_cast<int4*>(sst)[1] = __ldcg(src + 1);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    const long long lo = sst->lo;
+    const long long hi = sst->hi;
     const uint32_t tbase = *tmem_slot;
     const uint32_t O_T = tbase + 256;  // columns [256, 512): output accumulator
     // scores: columns [0, 64) and [64, 128); probabilities (16-bit pairs): [128, 160) and [160, 192)
@@ -143,15 +195,13 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         // the tokens index << sbs_log2 .. + (1 << sbs_log2) - 1 (token-wise when sbs_log2 = 0)
         const int npos = p.S_sp << p.sbs_log2;
         const int smask = (1 << p.sbs_log2) - 1;
-        auto load_idx = [&](long long g, int& i_lo, int& i_hi) {
+        auto load_idx = [&](long long g, const SeqCursor& c, int& i_lo, int& i_hi) {
             i_lo = i_hi = -1;
             if (g >= hi) return;
-            const int seq = (int)(g / tps), t = (int)(g % tps);
-            const int b = seq >> 1;
-            const int32_t* row = p.indices + (long long)b * p.S_sp;
+            const int32_t* row = p.indices + (long long)c.r * p.S_sp;
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const int pos = t * kSfaTile + lane + 32 * u;
+                const int pos = c.t * kSfaTile + lane + 32 * u;
                 int tok = -1;
                 if (pos < npos) {
                     const int idx = __ldg(row + (pos >> p.sbs_log2));
@@ -169,8 +219,14 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         // rise within a CTA's range, so a binary search places the first and the rest step on.
         const bool paged = p.kv_layout == 0;
         int tnd_b = 0;
+        SeqCursor c0, c1, c2;  // tiles g, g + 1, g + 2
+        c0.init(*sst);
+        c1 = c0;
+        c1.next(p.eff, p.R);
+        c2 = c1;
+        c2.next(p.eff, p.R);
         if (p.q_tnd) {
-            const int r_first = (int)(lo / tps) >> 1;
+            const int r_first = c0.r;
             int a = 0, z = p.B;  // first b in [a, z] with lens_q[b] > r_first (z = B: none)
             while (a < z) {
                 const int mid = (a + z) >> 1;
@@ -219,18 +275,18 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             limit = lim < 0 ? 0 : (int)lim;
         };
         int i0lo, i0hi, i1lo, i1hi;
-        load_idx(lo, i0lo, i0hi);
-        load_idx(lo + 1, i1lo, i1hi);
+        load_idx(lo, c0, i0lo, i0hi);
+        load_idx(lo + 1, c1, i1lo, i1hi);
         int b0, len0, base0;
-        row_info((int)(lo / tps) >> 1, b0, len0, base0);
+        row_info(c0.r, b0, len0, base0);
         int bt0lo = paged && b0 >= 0 ? load_blk(b0, i0lo) : -1, bt0hi = paged && b0 >= 0 ? load_blk(b0, i0hi) : -1;
         long long k = 0;
         for (long long g = lo; g < hi; ++g, ++k) {
             int i2lo, i2hi;
-            load_idx(g + 2, i2lo, i2hi);
+            load_idx(g + 2, c2, i2lo, i2hi);
             int b1 = -1, len1 = 0, base1 = 0, bt1lo = -1, bt1hi = -1;
             if (g + 1 < hi) {
-                row_info((int)((g + 1) / tps) >> 1, b1, len1, base1);
+                row_info(c1.r, b1, len1, base1);
                 if (paged && b1 >= 0) {
                     bt1lo = load_blk(b1, i1lo);
                     bt1hi = load_blk(b1, i1hi);
@@ -280,6 +336,9 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             base0 = base1;
             bt0lo = bt1lo;
             bt0hi = bt1hi;
+            c0 = c1;
+            c1 = c2;
+            c2.next(p.eff, p.R);
             if (*abort_flag) break;
         }
     } else if ((warp == 0 || warp >= 7) && lo < hi) {
@@ -379,7 +438,9 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             pend = -1;
         };
         long long k = 0;
-        for (long long g = lo; g < hi && ok && !*abort_flag; ++g, ++k) {
+        SeqCursor cur;
+        cur.init(*sst);
+        for (long long g = lo; g < hi && ok && !*abort_flag; ++g, ++k, cur.next(p.eff, p.R)) {
             const int slot = (int)(k % kSfaRSlots);
             if (!mbar_wait_bounded(&r_full[slot], (uint32_t)(k / kSfaRSlots) & 1, kWaitLimitNs)) {
                 if (lane == 0) atomicOr(p.err, kErrTimeout);
@@ -387,8 +448,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 break;
             }
             const RSlot* rs = slot_of(k);
-            const int seq = (int)(g / tps);
-            const int b = seq >> 1, h = seq & 1;
+            const int b = cur.r, h = cur.h;  // query row and value half
             if (!rs->any) {
                 flush();
                 __syncwarp();
@@ -465,10 +525,11 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 umma_commit(&o_full[m & 1]);
             };
             long long kk = 0;
-            for (long long g = lo; g < hi && ok; ++g, ++kk) {
-                const int seq = (int)(g / tps), t = (int)(g % tps);
-                const int b = seq >> 1;
-                if (t == 0 || g == lo) fresh = true;
+            SeqCursor cur;
+            cur.init(*sst);
+            for (long long g = lo; g < hi && ok; ++g, ++kk, cur.next(p.eff, p.R)) {
+                const int b = cur.r;  // query row
+                if (cur.t == 0 || g == lo) fresh = true;
                 const int slot = (int)(kk % kSfaRSlots);
                 if (!mbar_wait_bounded(&r_full[slot], (uint32_t)(kk / kSfaRSlots) & 1, kWaitLimitNs)) {
                     ok = false;
@@ -537,10 +598,11 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             *abort_flag = 1;
         };
         long long kk = 0;
-        for (long long g = lo; g < hi; ++g, ++kk) {
-            const int seq = (int)(g / tps), t = (int)(g % tps);
-            const int b = seq >> 1, h = seq & 1;
-            if (t == 0 || g == lo) {
+        SeqCursor cur;
+        cur.init(*sst);
+        for (long long g = lo; g < hi; ++g, ++kk, cur.next(p.eff, p.R)) {
+            const int b = cur.r, h = cur.h;  // query row and value half
+            if (cur.t == 0 || g == lo) {
                 m_used = -INFINITY;
                 m_top = -INFINITY;
                 l_sum = 0.f;
@@ -626,11 +688,11 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 n_last = n;
                 ++n;
             }
-            const bool last = (t == tps - 1) || (g == hi - 1);
+            const bool last = (cur.t == cur.n - 1) || (g == hi - 1);
             if (!last) continue;
             // ============================================================ piece epilogue
-            const long long seq_first = g - t;
-            const bool complete = seq_first >= lo && seq_first + tps <= hi;
+            const long long seq_first = cur.first;
+            const bool complete = seq_first >= lo && seq_first + cur.n <= hi;
             const long long orow = ((long long)b * p.QN + row) * kSfaD + h * kSfaHalf;
             const int slot_p = 2 * (int)blockIdx.x + (seq_first <= lo ? 0 : 1);
             float* sp = p.partials + (long long)slot_p * kSfaSlotFloats;
@@ -690,21 +752,152 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
     if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
+// Per query row: its live tiles, up to the last tile that holds a usable index (tiles past it
+// hold only invalid positions), and, by the cluster's first CTA after a cluster barrier, the
+// prefix over rows (two sequences per row) and the start of each decode-kernel CTA: equal
+// contiguous shares of the live tiles.  One cluster of kSfaCountCtas CTAs; warp = row.  Up to
+// kSfaCountSmemRows rows, each warp also stores its row's count into the first CTA's shared
+// memory, which then scans and searches there; beyond that the first CTA reads global memory.
+__global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_constant__ SfaParams p) {
+    __shared__ int s_eff[kSfaCountSmemRows];
+    __shared__ int s_pre[kSfaCountSmemRows + 1];
+    __shared__ long long wsum[kSfaCountThreads / 32];
+    __shared__ long long total;
+    pdl_launch_dependents();  // the decode kernel's prologue may start; it waits for this grid's end
+    cg::cluster_group cluster = cg::this_cluster();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int NW = kSfaCountThreads / 32;
+    const int R = p.R;
+    const bool in_smem = R <= kSfaCountSmemRows;
+    int* eff0 = cluster.map_shared_rank(s_eff, 0);  // the first CTA's copy
+    const int idx_max = INT32_MAX >> p.sbs_log2;
+    // rows of whole 16-byte groups: 4 entries per load, 8 loads in flight per lane
+    const bool vec = (p.S_sp & 3) == 0 && (reinterpret_cast<uintptr_t>(p.indices) & 15) == 0;
+    for (int r = blockIdx.x * NW + warp; r < R; r += gridDim.x * NW) {
+        const int32_t* row = p.indices + (long long)r * p.S_sp;
+        int last = -1;  // last entry of the row whose index selects a token
+        if (vec) {
+            const int4* row4 = reinterpret_cast<const int4*>(row);
+            const int n4 = p.S_sp >> 2;
+#pragma unroll 8
+            for (int j = lane; j < n4; j += 32) {
+                const int4 v = __ldg(row4 + j);
+                if (v.x >= 0 && v.x <= idx_max) last = 4 * j;
+                if (v.y >= 0 && v.y <= idx_max) last = 4 * j + 1;
+                if (v.z >= 0 && v.z <= idx_max) last = 4 * j + 2;
+                if (v.w >= 0 && v.w <= idx_max) last = 4 * j + 3;
+            }
+        } else {
+#pragma unroll 8
+            for (int i = lane; i < p.S_sp; i += 32) {
+                const int idx = __ldg(row + i);
+                if (idx >= 0 && idx <= idx_max) last = i;
+            }
+        }
+        last = __reduce_max_sync(0xffffffffu, last);
+        if (lane == 0) {
+            const int e = last < 0 ? 0 : (int)((((long long)last + 1) << p.sbs_log2) + kSfaTile - 1) / kSfaTile;
+            p.eff[r] = e;
+            if (in_smem) eff0[r] = e;
+        }
+    }
+    __threadfence();
+    cluster.sync();
+    if (blockIdx.x != 0) return;
+    auto eff_of = [&](int r) { return in_smem ? s_eff[r] : __ldcg(p.eff + r); };
+    // prefix over rows: thread k sums its contiguous chunk, a block scan places the chunks
+    const int chunk = (R + kSfaCountThreads - 1) / kSfaCountThreads;
+    const int r0 = min(R, (int)threadIdx.x * chunk), r1 = min(R, r0 + chunk);
+    long long mine = 0;
+    for (int r = r0; r < r1; ++r) mine += 2 * eff_of(r);
+    long long incl = mine;  // inclusive scan within the warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        long long run = 0;
+        for (int w = 0; w < NW; ++w) {
+            const long long v = wsum[w];
+            wsum[w] = run;
+            run += v;
+        }
+        total = run;
+    }
+    __syncthreads();
+    long long run = wsum[warp] + incl - mine;  // exclusive prefix of this thread's chunk
+    for (int r = r0; r < r1; ++r) {
+        if (in_smem) s_pre[r] = (int)run;
+        p.pre[r] = (int)run;
+        run += 2 * eff_of(r);
+    }
+    if (threadIdx.x == 0) {
+        p.pre[R] = (int)total;
+        if (in_smem) s_pre[R] = (int)total;
+    }
+    __syncthreads();
+    auto pre_of = [&](int r) { return in_smem ? s_pre[r] : p.pre[r]; };
+    // each decode CTA's share [lo, hi) and where it begins: the last row r < R with pre[r] <= lo
+    // (a row with live tiles, since lo < total)
+    const long long Wl = total;
+    const int Pa = active_ctas(Wl, p.P, p.tiles_per_seq);  // CTAs from Pa on stay idle
+    for (int c = threadIdx.x; c < p.P; c += kSfaCountThreads) {
+        SfaStart st;
+        st.lo = c < Pa ? (int)(c * Wl / Pa) : 0;
+        st.hi = c < Pa ? (int)((c + 1) * Wl / Pa) : 0;
+        st.r = st.h = st.t = st.n = st.first = st.pad = 0;
+        if (st.lo < st.hi) {
+            int a = 0, z = R - 1;
+            while (a < z) {
+                const int mid = (a + z + 1) >> 1;
+                if (pre_of(mid) <= st.lo) a = mid;
+                else z = mid - 1;
+            }
+            const int n = eff_of(a);
+            const int off = st.lo - pre_of(a);
+            st.r = a;
+            st.n = n;
+            st.h = off >= n ? 1 : 0;
+            st.t = off - st.h * n;
+            st.first = pre_of(a) + st.h * n;
+        }
+        p.starts[c] = st;
+    }
+}
+
 // Merges the pieces of every sequence that CTA boundaries cut: grid (2R sequences,
 // 128 / kSfaCombineRows), 128 threads; thread = (head row, 32 channels).  Piece k
-// weighs L_k 2^(M_k - M) / sum_j L_j 2^(M_j - M) with M the largest M_k.
+// weighs L_k 2^(M_k - M) / sum_j L_j 2^(M_j - M) with M the largest M_k.  A sequence with
+// no live tile gets its all-zero output row here (and, for value half 0, max -inf, sum 0).
 __global__ void __launch_bounds__(128) sfa_combine(const __grid_constant__ SfaParams p) {
     const int s = blockIdx.x;
-    const int tps = p.tiles_per_seq;
-    const long long g0 = (long long)s * tps;
-    const int c_first = cta_of_tile(g0, p.W, p.P);
-    const int c_last = cta_of_tile(g0 + tps - 1, p.W, p.P);
-    if (c_first == c_last) return;  // the decode kernel wrote this sequence
     const int row = blockIdx.y * kSfaCombineRows + (threadIdx.x >> 3);
-    if (row >= p.QN) return;
     const int col0 = (threadIdx.x & 7) * 32;
     const int b = s >> 1, h = s & 1;
-    const long long lo_first = (long long)c_first * p.W / p.P;
+    const int n = __ldg(p.eff + b);
+    if (n == 0) {
+        if (row >= p.QN) return;
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + ((long long)b * p.QN + row) * kSfaD +
+                                              h * kSfaHalf + col0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (p.lse_max && h == 0 && (threadIdx.x & 7) == 0) {
+            p.lse_max[(long long)b * p.QN + row] = -INFINITY;
+            p.lse_sum[(long long)b * p.QN + row] = 0.f;
+        }
+        return;
+    }
+    const long long Wl = __ldg(p.pre + p.R);
+    const int Pa = active_ctas(Wl, p.P, p.tiles_per_seq);
+    const long long g0 = __ldg(p.pre + b) + (long long)h * n;
+    const int c_first = cta_of_tile(g0, Wl, Pa);
+    const int c_last = cta_of_tile(g0 + n - 1, Wl, Pa);
+    if (c_first == c_last) return;  // the decode kernel wrote this sequence
+    if (row >= p.QN) return;
+    const long long lo_first = (long long)c_first * Wl / Pa;
     const int slot0 = 2 * c_first + (g0 <= lo_first ? 0 : 1);
     const int np = c_last - c_first + 1;
     auto slot_ptr = [&](int k) {
@@ -766,8 +959,32 @@ cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    sfa_kernel<<<p.P, kSfaThreads, kSfaSmem, stream>>>(p);
-    const cudaError_t e = cudaGetLastError();
+    // tile counts: one cluster, ordered after everything before it on the stream
+    cudaLaunchConfig_t cc = {};
+    cc.gridDim = dim3(kSfaCountCtas);
+    cc.blockDim = dim3(kSfaCountThreads);
+    cc.stream = stream;
+    cudaLaunchAttribute ca[1];
+    ca[0].id = cudaLaunchAttributeClusterDimension;
+    ca[0].val.clusterDim.x = kSfaCountCtas;
+    ca[0].val.clusterDim.y = 1;
+    ca[0].val.clusterDim.z = 1;
+    cc.attrs = ca;
+    cc.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cc, sfa_count, p);
+    if (e != cudaSuccess) return e;
+    // the decode kernel starts its prologue while the counts finish (it waits before reading them)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.P);
+    cfg.blockDim = dim3(kSfaThreads);
+    cfg.dynamicSmemBytes = kSfaSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, sfa_kernel, p);
     if (e != cudaSuccess) return e;
     sfa_combine<<<dim3(2 * p.R, 128 / kSfaCombineRows), 128, 0, stream>>>(p);
     return cudaGetLastError();
