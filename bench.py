@@ -558,7 +558,7 @@ class SfaWorkload:
         self.outs = [self.q.new_empty(self.q.shape) for _ in range(self.copies)]
         self.dtype = case.dtype
         self.call_name = "sfa_run"
-        self.launch_note = ": decode kernel + combine kernel"
+        self.launch_note = ": tile-count kernel + decode kernel + combine kernel"
 
     def call(self, i, stream):
         k, kr, v = self.caches[i]
@@ -566,7 +566,7 @@ class SfaWorkload:
                        out=self.outs[i], stream=stream)
 
     def launches_per_call(self):
-        return 2  # decode kernel + combine kernel
+        return 3  # tile-count kernel, decode kernel (cluster pairs), combine kernel
 
     def host_inputs(self):
         c = self.case

@@ -1,5 +1,5 @@
 // Sparse-index MLA-absorb decode ("SparseFlashAttention" README): launch
-// parameters and fixed sizes of the tcgen05 kernel and its combine kernel
+// parameters and fixed sizes of the tcgen05 kernel, its tile-count and combine kernels
 // (sfa_kernel.cu).
 #pragma once
 #include <cuda.h>
@@ -26,9 +26,9 @@ constexpr int kSfaThreads = 10 * 32;  // producer, MMA issuer, four softmax warp
 constexpr int kSfaSlotFloats = 128 * kSfaHalf + 3 * 128;  // normalised O of one piece + M + L + largest score
 constexpr int kSfaBarBytes = 512;
 constexpr int kSfaSmem = 1024 + kSfaQBytes + kSfaStages * kSfaStageBytes + kSfaRSlots * kSfaRSlotBytes + kSfaBarBytes;
-// workspace: [0, 256) error word; [kSfaStartOffset, + 32 * kMaxCtas) each CTA's start (SfaStart);
-// partial slots from kSfaPartialOffset; then live tiles per query row (R ints) and their
-// prefix over rows, two sequences per row (R + 1 ints)
+// workspace: [0, 256) error word; [kSfaStartOffset, + 32 * kMaxCtas) each pair's start (SfaStart);
+// partial slots from kSfaPartialOffset; then live tiles per query row (R ints) and their prefix
+// over rows (R + 1 ints)
 constexpr size_t kSfaStartOffset = 1024;
 constexpr size_t kSfaPartialOffset = 16384;
 constexpr int kSfaCountCtas = 8;        // the tile-count kernel: one cluster
@@ -66,9 +66,9 @@ struct alignas(128) SfaParams {
     int* err;
     SfaStart* starts;   // per CTA, written by the tile-count kernel
     int* eff;           // live tiles of each query row (a sequence's tiles), 0 when no index is usable
-    int* pre;           // prefix over rows of 2 * eff (R + 1 entries): the tile order of the decode kernel
-    long long W;        // tiles before the count: 2 * R * tiles_per_seq (an upper bound)
-    int P;
+    int* pre;           // prefix over rows of eff (R + 1 entries): the tile order of the decode kernel's pairs
+    long long W;        // tiles before the count: R * tiles_per_seq (an upper bound)
+    int P;              // CTAs: an even count, pairs of CTAs form clusters
     int R, QS, QN, S_sp, tiles_per_seq;  // R query rows: B * QS (row r: batch r / QS, query token r % QS), or
                                          // the TND rows; S_sp: indices per row; tiles cover S_sp << sbs_log2
     int B;                           // batches (entries of the length arrays)
@@ -81,6 +81,9 @@ struct alignas(128) SfaParams {
     int is_bf16;
     float scale_log2;
 };
+
+// CTA pairs of the decode kernel that can be resident at once (0 when the query fails).
+int sfa_max_pairs();
 
 // Enqueues the tile-count kernel, the decode kernel and the combine kernel (three launches).
 cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream);

@@ -13,7 +13,8 @@
 // rows; persistent CTAs take equal contiguous shares of the live tiles.  A piece
 // of a sequence that a CTA boundary cuts goes to a partial slot (normalised O,
 // running max M and sum L per head) and the combine kernel merges the pieces of
-// every cut sequence; it also writes the zero rows of sequences with no live tile.
+// every cut sequence.  The count kernel writes the zero rows of query rows with
+// no live tile.
 //
 // Per CTA:
 //  * resolver (warp 6): for each tile, the cache row of every position (index ->
@@ -44,6 +45,7 @@
 #include "decode.cuh"
 #include "ptx.cuh"
 #include "sfa.cuh"
+#include "sfa_ptx.cuh"
 
 namespace ifa {
 
@@ -87,14 +89,21 @@ struct RSlot {
 };
 static_assert(sizeof(RSlot) <= kSfaRSlotBytes, "resolver slot");
 
-// Position in the decode kernel's tile order: tile t of the n tiles of sequence (query row r,
-// value half h), whose first tile has index `first`.  Rows with no live tile are stepped over.
+// Next ring stage: position stg of round rnd (no division on the hot path).
+__device__ __forceinline__ void ring_next(int& stg, uint32_t& rnd) {
+    if (++stg == kSfaStages) {
+        stg = 0;
+        ++rnd;
+    }
+}
+
+// Position in a pair's tile order: tile t of the n live tiles of query row r, whose first tile
+// has index `first`.  Rows with no live tile are stepped over.
 struct SeqCursor {
-    int r, h, t, n;
+    int r, t, n;
     long long first;
     __device__ __forceinline__ void init(const SfaStart& s) {
         r = s.r;
-        h = s.h;
         t = s.t;
         n = s.n;
         first = s.first;
@@ -103,11 +112,6 @@ struct SeqCursor {
         if (++t < n) return;
         t = 0;
         first += n;
-        if (h == 0) {
-            h = 1;
-            return;
-        }
-        h = 0;
         n = 0;
         while (++r < R && (n = __ldcg(eff + r)) == 0) {
         }
@@ -142,12 +146,15 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // a cluster of two CTAs: rank h takes value half h of the pair's tiles
+    const int h = (int)(blockIdx.x & 1);
+    constexpr uint16_t kPair = 3;  // both CTAs of the cluster
     auto slot_of = [&](long long k) { return reinterpret_cast<RSlot*>(rbase + (int)(k % kSfaRSlots) * kSfaRSlotBytes); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSfaStages; ++s) {
             mbar_init(&full[s], kSfaIssuers);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 2);  // a stage is free once both CTAs' MMAs have read it
         }
         for (int s = 0; s < kSfaRSlots; ++s) {
             mbar_init(&r_full[s], 1);
@@ -172,12 +179,13 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
     // dependent launch: everything above overlaps it).
     pdl_wait_primary();
     if (threadIdx.x == 0) {
-        const int4* src = reinterpret_cast<const int4*>(p.starts + blockIdx.x);
+        const int4* src = reinterpret_cast<const int4*>(p.starts + (blockIdx.x >> 1));
         reinterpret_cast<int4*>(sst)[0] = __ldcg(src);
         reinterpret_cast<int4*>(sst)[1] = __ldcg(src + 1);
     }
+    // both CTAs' barriers are initialised before either CTA copies into or arrives on the other's
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
     const long long lo = sst->lo;
     const long long hi = sst->hi;
@@ -358,11 +366,15 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         }
         const uint64_t pol = policy_evict_first();
         long long it = 0;
+        int stg = 0;  // ring position of stage `it`: stg = it mod kSfaStages, rnd = it / kSfaStages
+        uint32_t rnd = 0;
         int epoch = 0;
         int prev_b = -1;
         bool ok = true;
-        // Gathers column blocks [blk0, blk0 + nblk) of the rows of resolved tile `rs`
-        // (blocks 0..7: key, 8: key rope, 9..12: value half h).
+        // Gathers column blocks [blk0, blk0 + nblk) of the rows of resolved tile `rs` (blocks
+        // 0..7: key, 8: key rope, 9..12: value half h).  The key blocks of a tile alternate
+        // between the two CTAs (by block and tile parity) and land in both CTAs' rings; the
+        // other CTA's blocks only announce their bytes here.  Value blocks are this CTA's own.
         constexpr int kGroups = 16 / kSfaIssuers;  // gather4 row groups per warp and stage
         // Block-wise selections of 8 or more tokens are runs of consecutive cache rows: one tiled
         // box of run_rows rows per run (or per 64-row half of a 128-token run) instead of gathers.
@@ -371,23 +383,25 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         const int nruns = runs ? kSfaTile / run_rows : 0;  // boxes per stage: 8, 4, 2 or 1
         int my_runs = 0;                                    // this warp takes runs gi, gi + 4, ...
         for (int k = gi; k < nruns; k += kSfaIssuers) ++my_runs;
-        auto gather = [&](const RSlot* rs, int blk0, int nblk, int h) {
+        auto gather = [&](const RSlot* rs, int blk0, int nblk, int par) {
             const int grp = gi * kGroups + lane;
             const int4 r4 = lane < kGroups ? reinterpret_cast<const int4*>(rs->rows)[grp] : make_int4(0, 0, 0, 0);
-            for (int blk = blk0; blk < blk0 + nblk; ++blk, ++it) {
-                const int stage = (int)(it % kSfaStages);
-                const uint32_t round = (uint32_t)(it / kSfaStages);
+            for (int blk = blk0; blk < blk0 + nblk; ++blk, ++it, ring_next(stg, rnd)) {
+                const int stage = stg;
+                const uint32_t round = rnd;
                 if (round > 0 && !mbar_wait_bounded(&empty[stage], (round - 1) & 1, kWaitLimitNs)) {
                     if (lane == 0) atomicOr(p.err, kErrTimeout);
                     *abort_flag = 1;
                     ok = false;
                     return;
                 }
+                const bool key = blk < kSfaQBlocks;
+                const bool mine = !key || ((blk + par) & 1) == h;
                 if (runs) {
                     if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)(my_runs * run_rows * 128));
                     __syncwarp();
                     const int k = gi + kSfaIssuers * lane;  // run this lane loads
-                    if (lane < my_runs) {
+                    if (mine && lane < my_runs) {
                         const CUtensorMap* map;
                         int x;
                         if (blk < 8) {
@@ -401,15 +415,16 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                             x = h * kSfaHalf + (blk - kSfaQBlocks) * 64;
                         }
                         // the run's first row; an invalid run starts past the last row (zero fill)
-                        tma_load_2d(ring + stage * kSfaStageBytes + k * run_rows * 128, map, &full[stage], x,
-                                    rs->rows[k * run_rows]);
+                        uint8_t* dst = ring + stage * kSfaStageBytes + k * run_rows * 128;
+                        if (key) tma_load_2d_mc(dst, map, &full[stage], x, rs->rows[k * run_rows], kPair);
+                        else tma_load_2d(dst, map, &full[stage], x, rs->rows[k * run_rows]);
                     }
                     __syncwarp();
                     continue;
                 }
                 if (lane == 0) mbar_arrive_expect_tx(&full[stage], kSfaStageBytes / kSfaIssuers);
                 __syncwarp();
-                if (lane < kGroups) {
+                if (mine && lane < kGroups) {
                     const CUtensorMap* map;
                     int x;
                     if (blk < 8) {
@@ -422,17 +437,17 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                         map = &p.tmV;
                         x = h * kSfaHalf + (blk - kSfaQBlocks) * 64;
                     }
-                    tma_gather4(ring + stage * kSfaStageBytes + grp * 512, map, &full[stage], x, r4.x, r4.y, r4.z,
-                                r4.w, pol);
+                    uint8_t* dst = ring + stage * kSfaStageBytes + grp * 512;
+                    if (key) tma_gather4_mc(dst, map, &full[stage], x, r4.x, r4.y, r4.z, r4.w, kPair, pol);
+                    else tma_gather4(dst, map, &full[stage], x, r4.x, r4.y, r4.z, r4.w, pol);
                 }
                 __syncwarp();
             }
         };
         long long pend = -1;  // resolved tile whose value rows are still to be gathered
-        int pend_h = 0;
         auto flush = [&]() {
             if (pend < 0) return;
-            gather(slot_of(pend), kSfaQBlocks, kSfaVBlocks, pend_h);
+            gather(slot_of(pend), kSfaQBlocks, kSfaVBlocks, 0);
             __syncwarp();
             if (lane == 0) mbar_arrive(&r_empty[(int)(pend % kSfaRSlots)]);
             pend = -1;
@@ -448,7 +463,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 break;
             }
             const RSlot* rs = slot_of(k);
-            const int b = cur.r, h = cur.h;  // query row and value half
+            const int b = cur.r;  // query row
             if (!rs->any) {
                 flush();
                 __syncwarp();
@@ -469,11 +484,10 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 ++epoch;
             }
             prev_b = b;
-            gather(rs, 0, kSfaQBlocks, h);
+            gather(rs, 0, kSfaQBlocks, (int)(k & 1));
             if (!ok) break;
             flush();
             pend = k;
-            pend_h = h;
         }
         if (ok && !*abort_flag) flush();
         // Let every issued copy land before shared memory can be released.
@@ -497,9 +511,11 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             uint32_t pend_acc = 0;
             bool fresh = true;     // no processed tile yet in the current piece
             bool ok = true;
+            int stg = 0;        // ring position of stage `it`: stg = it mod kSfaStages, rnd = it / kSfaStages
+            uint32_t rnd = 0;
             auto wait_stage = [&]() -> int {
-                const int stage = (int)(it % kSfaStages);
-                if (!mbar_wait_bounded(&full[stage], (uint32_t)(it / kSfaStages) & 1, kWaitLimitNs)) {
+                const int stage = stg;
+                if (!mbar_wait_bounded(&full[stage], rnd & 1, kWaitLimitNs)) {
                     ok = false;
                     return -1;
                 }
@@ -512,7 +528,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                     return;
                 }
                 tc_fence_after();
-                for (int vb = 0; vb < kSfaVBlocks; ++vb, ++it) {
+                for (int vb = 0; vb < kSfaVBlocks; ++vb, ++it, ring_next(stg, rnd)) {
                     const int stage = wait_stage();
                     if (stage < 0) return;
 #pragma unroll
@@ -520,7 +536,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                         const uint64_t bd = umma_sdesc(ring_addr + stage * kSfaStageBytes + k * 2048, 8192, 1024);
                         umma_ts(O_T + vb * 64, P_T(m & 1) + k * 8, bd, idesc_pv, (acc != 0 || k > 0) ? 1u : 0u);
                     }
-                    umma_commit(&empty[stage]);
+                    umma_commit_mc(&empty[stage], kPair);
                 }
                 umma_commit(&o_full[m & 1]);
             };
@@ -553,7 +569,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 }
                 tc_fence_after();
                 // ---- S_n = [q | q_rope] . [k | k_rope]^T
-                for (int kb = 0; kb < kSfaQBlocks; ++kb, ++it) {
+                for (int kb = 0; kb < kSfaQBlocks; ++kb, ++it, ring_next(stg, rnd)) {
                     const int stage = wait_stage();
                     if (stage < 0) break;
 #pragma unroll
@@ -562,7 +578,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                         const uint64_t bd = umma_sdesc(ring_addr + stage * kSfaStageBytes + k * 32, 16, 1024);
                         umma_ss(S_T(n & 1), ad, bd, idesc_qk, (kb | k) != 0);
                     }
-                    umma_commit(&empty[stage]);
+                    umma_commit_mc(&empty[stage], kPair);
                 }
                 if (!ok) break;
                 umma_commit(&s_full[n & 1]);
@@ -601,7 +617,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         SeqCursor cur;
         cur.init(*sst);
         for (long long g = lo; g < hi; ++g, ++kk, cur.next(p.eff, p.R)) {
-            const int b = cur.r, h = cur.h;  // query row and value half
+            const int b = cur.r;  // query row
             if (cur.t == 0 || g == lo) {
                 m_used = -INFINITY;
                 m_top = -INFINITY;
@@ -746,16 +762,18 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         }
     }
     // ==================================================================== teardown
+    // Neither CTA leaves while the other may still arrive on its barriers (the MMA issuers
+    // have waited for all their MMAs and so for their commits).
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
 // Per query row: its live tiles, up to the last tile that holds a usable index (tiles past it
 // hold only invalid positions), and, by the cluster's first CTA after a cluster barrier, the
-// prefix over rows (two sequences per row) and the start of each decode-kernel CTA: equal
-// contiguous shares of the live tiles.  One cluster of kSfaCountCtas CTAs; warp = row.  Up to
+// prefix over rows and the start of each CTA pair of the decode kernel: equal contiguous
+// shares of the live tiles (each pair runs its tiles once per value half).  One cluster of kSfaCountCtas CTAs; warp = row.  Up to
 // kSfaCountSmemRows rows, each warp also stores its row's count into the first CTA's shared
 // memory, which then scans and searches there; beyond that the first CTA reads global memory.
 __global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_constant__ SfaParams p) {
@@ -800,7 +818,20 @@ __global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_const
             p.eff[r] = e;
             if (in_smem) eff0[r] = e;
         }
+        if (last < 0) {
+            // no live tile: the decode kernel never visits this row; its output is all zero
+            // (largest score -inf, sum 0)
+            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + (long long)r * p.QN * kSfaD);
+            for (int i = lane; i < p.QN * kSfaD / 8; i += 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (p.lse_max) {
+                for (int i = lane; i < p.QN; i += 32) {
+                    p.lse_max[(long long)r * p.QN + i] = -INFINITY;
+                    p.lse_sum[(long long)r * p.QN + i] = 0.f;
+                }
+            }
+        }
     }
+
     __threadfence();
     cluster.sync();
     if (blockIdx.x != 0) return;
@@ -809,7 +840,7 @@ __global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_const
     const int chunk = (R + kSfaCountThreads - 1) / kSfaCountThreads;
     const int r0 = min(R, (int)threadIdx.x * chunk), r1 = min(R, r0 + chunk);
     long long mine = 0;
-    for (int r = r0; r < r1; ++r) mine += 2 * eff_of(r);
+    for (int r = r0; r < r1; ++r) mine += eff_of(r);
     long long incl = mine;  // inclusive scan within the warp
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -832,7 +863,7 @@ __global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_const
     for (int r = r0; r < r1; ++r) {
         if (in_smem) s_pre[r] = (int)run;
         p.pre[r] = (int)run;
-        run += 2 * eff_of(r);
+        run += eff_of(r);
     }
     if (threadIdx.x == 0) {
         p.pre[R] = (int)total;
@@ -840,11 +871,12 @@ __global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_const
     }
     __syncthreads();
     auto pre_of = [&](int r) { return in_smem ? s_pre[r] : p.pre[r]; };
-    // each decode CTA's share [lo, hi) and where it begins: the last row r < R with pre[r] <= lo
-    // (a row with live tiles, since lo < total)
+    // each pair's share [lo, hi) and where it begins: the last row r < R with pre[r] <= lo (a row
+    // with live tiles, since lo < total)
     const long long Wl = total;
-    const int Pa = active_ctas(Wl, p.P, p.tiles_per_seq);  // CTAs from Pa on stay idle
-    for (int c = threadIdx.x; c < p.P; c += kSfaCountThreads) {
+    const int pairs = p.P >> 1;
+    const int Pa = active_ctas(Wl, pairs, p.tiles_per_seq);  // pairs from Pa on stay idle
+    for (int c = threadIdx.x; c < pairs; c += kSfaCountThreads) {
         SfaStart st;
         st.lo = c < Pa ? (int)(c * Wl / Pa) : 0;
         st.hi = c < Pa ? (int)((c + 1) * Wl / Pa) : 0;
@@ -856,13 +888,10 @@ __global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_const
                 if (pre_of(mid) <= st.lo) a = mid;
                 else z = mid - 1;
             }
-            const int n = eff_of(a);
-            const int off = st.lo - pre_of(a);
             st.r = a;
-            st.n = n;
-            st.h = off >= n ? 1 : 0;
-            st.t = off - st.h * n;
-            st.first = pre_of(a) + st.h * n;
+            st.n = eff_of(a);
+            st.t = st.lo - pre_of(a);
+            st.first = pre_of(a);
         }
         p.starts[c] = st;
     }
@@ -870,38 +899,27 @@ __global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_const
 
 // Merges the pieces of every sequence that CTA boundaries cut: grid (2R sequences,
 // 128 / kSfaCombineRows), 128 threads; thread = (head row, 32 channels).  Piece k
-// weighs L_k 2^(M_k - M) / sum_j L_j 2^(M_j - M) with M the largest M_k.  A sequence with
-// no live tile gets its all-zero output row here (and, for value half 0, max -inf, sum 0).
+// weighs L_k 2^(M_k - M) / sum_j L_j 2^(M_j - M) with M the largest M_k.
 __global__ void __launch_bounds__(128) sfa_combine(const __grid_constant__ SfaParams p) {
     const int s = blockIdx.x;
     const int row = blockIdx.y * kSfaCombineRows + (threadIdx.x >> 3);
     const int col0 = (threadIdx.x & 7) * 32;
     const int b = s >> 1, h = s & 1;
-    const int n = __ldg(p.eff + b);
-    if (n == 0) {
-        if (row >= p.QN) return;
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + ((long long)b * p.QN + row) * kSfaD +
-                                              h * kSfaHalf + col0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (p.lse_max && h == 0 && (threadIdx.x & 7) == 0) {
-            p.lse_max[(long long)b * p.QN + row] = -INFINITY;
-            p.lse_sum[(long long)b * p.QN + row] = 0.f;
-        }
-        return;
-    }
-    const long long Wl = __ldg(p.pre + p.R);
-    const int Pa = active_ctas(Wl, p.P, p.tiles_per_seq);
-    const long long g0 = __ldg(p.pre + b) + (long long)h * n;
+    const int n = __ldcg(p.eff + b);
+    if (n == 0) return;  // the count kernel wrote this row
+    // pairs c_first..c_last hold the row's tiles; CTA 2c + h of pair c holds value half h
+    const long long Wl = __ldcg(p.pre + p.R);
+    const int Pa = active_ctas(Wl, p.P >> 1, p.tiles_per_seq);
+    const long long g0 = __ldcg(p.pre + b);
     const int c_first = cta_of_tile(g0, Wl, Pa);
     const int c_last = cta_of_tile(g0 + n - 1, Wl, Pa);
     if (c_first == c_last) return;  // the decode kernel wrote this sequence
     if (row >= p.QN) return;
     const long long lo_first = (long long)c_first * Wl / Pa;
-    const int slot0 = 2 * c_first + (g0 <= lo_first ? 0 : 1);
+    const int slot0 = 2 * (2 * c_first + h) + (g0 <= lo_first ? 0 : 1);
     const int np = c_last - c_first + 1;
     auto slot_ptr = [&](int k) {
-        const int sl = k == 0 ? slot0 : 2 * (c_first + k);
+        const int sl = k == 0 ? slot0 : 2 * (2 * (c_first + k) + h);
         return p.partials + (long long)sl * kSfaSlotFloats;
     };
     float M = -INFINITY;
@@ -952,6 +970,30 @@ __global__ void __launch_bounds__(128) sfa_combine(const __grid_constant__ SfaPa
     for (int j = 0; j < 4; ++j) dst[j] = make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
 }
 
+int sfa_max_pairs() {
+    static int pairs = -1;
+    if (pairs < 0) {
+        int n = 0;
+        if (cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSfaSmem) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2);
+            cfg.blockDim = dim3(kSfaThreads);
+            cfg.dynamicSmemBytes = kSfaSmem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, sfa_kernel, &cfg) != cudaSuccess) n = 0;
+        }
+        cudaGetLastError();
+        pairs = n;
+    }
+    return pairs;
+}
+
 cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream) {
     static bool configured = false;
     if (!configured) {
@@ -979,13 +1021,19 @@ cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream) {
     cfg.blockDim = dim3(kSfaThreads);
     cfg.dynamicSmemBytes = kSfaSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;  // CTA pairs: the two value halves
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, sfa_kernel, p);
     if (e != cudaSuccess) return e;
+    // An ordinary launch: with programmatic dependent launch (resident early, waiting) the
+    // combine cost the sparse MLA workload 18 us per call on this part.
     sfa_combine<<<dim3(2 * p.R, 128 / kSfaCombineRows), 128, 0, stream>>>(p);
     return cudaGetLastError();
 }
