@@ -285,3 +285,24 @@ def test_sfa_softmax_max_and_sum(lq, lk, split):
     assert live.any()
     assert np.abs(mx[live] - rmx[live]).max() <= 2e-3
     assert (np.abs(sm[live] - rsm[live]) / rsm[live]).max() <= 1e-3
+
+
+def test_sfa_rows_without_live_tiles_and_late_indices():
+    """Rows the tile count leaves out (all -1) get zero rows, max -inf and sum 0; an index that
+    follows a run of -1 (or sits alone far into the row) keeps its tile live."""
+    c = gen.sfa_mla(34, B=6, Q_N=128, block_size=64, sparse_size=2048, nvalid_lo=600, nvalid_hi=1500, kv_len=4096)
+    c.sparse_indices[0] = -1
+    c.sparse_indices[1, 0, 0, 2040] = 123        # after the -1 tail: the last tile stays live
+    c.sparse_indices[2] = -1
+    c.sparse_indices[2, 0, 0, 1500] = 4000       # a single index far into the row
+    c.sparse_indices[4] = -1
+    got, mx, sm, _ = run_gpu(c, lse=True)
+    ref, rmx, rsm = run_ref(c, lse=True)
+    assert max_abs_err(got, ref) <= TOL[c.dtype]
+    assert np.all(got.reshape(6, -1)[[0, 4]] == 0)
+    empty = np.isneginf(rmx)
+    assert np.array_equal(np.isneginf(mx), empty) and np.all(sm[empty] == 0.0)
+    assert empty.reshape(6, -1)[[0, 4]].all() and not empty.reshape(6, -1)[[1, 2, 3, 5]].any()
+    live = ~empty
+    assert np.abs(mx[live] - rmx[live]).max() <= 2e-3
+    assert (np.abs(sm[live] - rsm[live]) / rsm[live]).max() <= 1e-3
