@@ -10,17 +10,17 @@
 
 namespace ifa {
 
-constexpr int kSfaTile = 64;        // sparse positions per tile (the N of S = Q K^T)
+constexpr int kSfaTile = 128;       // sparse positions per tile (the N of S = Q K^T)
 constexpr int kSfaD = 512;          // head dim of query, key and value
 constexpr int kSfaDr = 64;          // rope dim
 constexpr int kSfaHalf = 256;       // value channels per CTA sequence (one half of D)
 constexpr int kSfaQBlocks = 9;      // 64-column blocks of [q | q_rope]
 constexpr int kSfaVBlocks = 4;      // 64-column blocks of one value half
-constexpr int kSfaStages = 8;       // 8 KB ring stages (64 rows x 128 B)
+constexpr int kSfaStages = 4;       // 16 KB ring stages (kSfaTile rows x 128 B)
 constexpr int kSfaStageBytes = kSfaTile * 128;
 constexpr int kSfaQBytes = kSfaQBlocks * 128 * 128;
 constexpr int kSfaRSlots = 8;       // resolved tiles the resolver warp may run ahead
-constexpr int kSfaRSlotBytes = 288; // rows[64], valid mask, flag (16-byte aligned)
+constexpr int kSfaRSlotBytes = 544; // rows[kSfaTile], valid mask, flag (16-byte aligned)
 constexpr int kSfaIssuers = 4;     // warps that issue the ring's gathers (a stage's 16 row groups split evenly)
 constexpr int kSfaThreads = 10 * 32;  // producer, MMA issuer, four softmax warps, resolver, three more gatherers
 constexpr int kSfaSlotFloats = 128 * kSfaHalf + 3 * 128;  // normalised O of one piece + M + L + largest score

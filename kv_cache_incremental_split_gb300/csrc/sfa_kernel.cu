@@ -7,7 +7,7 @@
 // value channels (a full 128 x 512 fp32 accumulator would fill all of TMEM, so
 // the two halves are separate sequences; the two CTAs that hold the halves of
 // the same positions run at the same time and share the key rows through L2).
-// A sequence is cut into 64-position tiles of its sparse index row.  A first
+// A sequence is cut into 128-position tiles of its sparse index row.  A first
 // kernel (one cluster) finds each row's live tiles (up to the last tile holding
 // a usable index: the invalid tail after it costs nothing) and the prefix over
 // rows; persistent CTAs take equal contiguous shares of the live tiles.  A piece
@@ -23,19 +23,22 @@
 //    by every role below.
 //  * producer (warp 0) and gatherers (warps 7-9): warp 0 loads Q of batch b (9
 //    column blocks of [q | q_rope], 128 rows, 147 KB, resident while b does not
-//    change) by 3-D TMA tiles; per tile, the 64 key rows (9 column blocks incl.
-//    rope) and, one tile later, the 64 value rows of half h (4 blocks) go by TMA
-//    tile::gather4 into a ring of 8 KB stages.  The four warps take four of each
-//    stage's 16 groups of 4 rows each (one warp alone cannot issue gathers fast
+//    change) by 3-D TMA tiles; per tile, the 128 key rows (9 column blocks incl.
+//    rope) and, one tile later, the 128 value rows of half h (4 blocks) go by TMA
+//    tile::gather4 into a ring of 16 KB stages.  The four warps take eight of each
+//    stage's 32 groups of 4 rows each (one warp alone cannot issue gathers fast
 //    enough).  Invalid positions gather an out-of-range row (zero fill, no memory
-//    traffic).
-//  * MMA issuer (warp 1): S_n[128 x 64] = Q K_n^T into one of two TMEM score
-//    buffers (36 MMAs, M=128 N=64 K=16), then O += P_{n-1} V_{n-1} with P from
-//    TMEM and V (MN-major) from shared memory, so the scores of tile n are
-//    computed while the softmax warps work on tile n-1.
-//  * softmax warps (2-5): thread = head row.  Masked scores, running max; O is
-//    rescaled (tcgen05.ld/st) only when the max grows by more than 8 in log2
-//    units, so P stays below 2^8; P goes to its TMEM buffer as 16-bit pairs.
+//    traffic).  Key blocks alternate between the two CTAs of a pair and land in both.
+//  * MMA issuer (warp 1): S_n[128 x 128] = Q K_n^T into one of two TMEM score
+//    buffers (36 MMAs, M=128 N=128 K=16: the issuer's instruction stream is what
+//    paces the kernel, and N=128 runs at the full tensor rate), then
+//    O += P_{n-1} V_{n-1} with P from TMEM and V (MN-major) from shared memory, so
+//    the scores of tile n are computed while the softmax warps work on tile n-1.
+//  * softmax warps (2-5): thread = head row.  Masked scores in two passes of
+//    32-column TMEM loads (maximum, then probabilities), running max; O is rescaled
+//    (tcgen05.ld/st) only when the max grows by more than 8 in log2 units, so P
+//    stays below 2^8; P goes as 16-bit pairs over the first half of its own score
+//    buffer, into columns already read.
 // Every wait is bounded; on a timeout the kernel records error bit 2, drains its
 // copies and MMAs, frees TMEM and returns.
 #include <cooperative_groups.h>
@@ -83,11 +86,15 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf) {
 
 // Resolved tile in the resolver ring.
 struct RSlot {
-    int rows[kSfaTile];  // cache row of each position (total_rows = invalid)
-    uint32_t vmask[2];   // valid positions 0..31 and 32..63
+    int rows[kSfaTile];              // cache row of each position (total_rows = invalid)
+    uint32_t vmask[kSfaTile / 32];   // valid positions, 32 per word
     int any;             // some position is valid
 };
 static_assert(sizeof(RSlot) <= kSfaRSlotBytes, "resolver slot");
+constexpr int kPosPerLane = kSfaTile / 32;  // positions of a tile per resolver lane
+struct LaneInts {
+    int v[kPosPerLane];
+};
 
 // Next ring stage: position stg of round rnd (no division on the hot path).
 __device__ __forceinline__ void ring_next(int& stg, uint32_t& rnd) {
@@ -124,7 +131,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sq = smem;                                   // [9][128 rows][128 B]
-    uint8_t* ring = smem + kSfaQBytes;                    // [kSfaStages][64 rows][128 B]
+    uint8_t* ring = smem + kSfaQBytes;                    // [kSfaStages][kSfaTile rows][128 B]
     uint8_t* rbase = ring + kSfaStages * kSfaStageBytes;  // [kSfaRSlots] RSlot
     uint64_t* full = reinterpret_cast<uint64_t*>(rbase + kSfaRSlots * kSfaRSlotBytes);
     uint64_t* empty = full + kSfaStages;
@@ -191,9 +198,12 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
     const long long hi = sst->hi;
     const uint32_t tbase = *tmem_slot;
     const uint32_t O_T = tbase + 256;  // columns [256, 512): output accumulator
-    // scores: columns [0, 64) and [64, 128); probabilities (16-bit pairs): [128, 160) and [160, 192)
-    auto S_T = [&](int buf) { return tbase + 64u * (uint32_t)buf; };
-    auto P_T = [&](int buf) { return tbase + 128u + 32u * (uint32_t)buf; };
+    // TMEM: two score buffers of kSfaTile columns at [0, 256); the softmax writes a tile's
+    // probabilities (16-bit pairs, kSfaTile / 2 columns) over its own score buffer, into columns
+    // it has already read; the output accumulator at [256, 512).
+    auto S_T = [&](int buf) { return tbase + (uint32_t)kSfaTile * (uint32_t)buf; };
+    auto P_T = [&](int buf) { return S_T(buf); };
+    static_assert(2 * kSfaTile + kSfaHalf <= 512, "TMEM columns");
 
     if (warp == 6 && lo < hi) {
         // ================================================================ resolver
@@ -203,20 +213,22 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         // the tokens index << sbs_log2 .. + (1 << sbs_log2) - 1 (token-wise when sbs_log2 = 0)
         const int npos = p.S_sp << p.sbs_log2;
         const int smask = (1 << p.sbs_log2) - 1;
-        auto load_idx = [&](long long g, const SeqCursor& c, int& i_lo, int& i_hi) {
-            i_lo = i_hi = -1;
-            if (g >= hi) return;
+        // tokens of positions lane + 32 u of tile g (u < kPosPerLane), -1 where none
+        auto load_idx = [&](long long g, const SeqCursor& c) {
+            LaneInts tok;
+#pragma unroll
+            for (int u = 0; u < kPosPerLane; ++u) tok.v[u] = -1;
+            if (g >= hi) return tok;
             const int32_t* row = p.indices + (long long)c.r * p.S_sp;
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < kPosPerLane; ++u) {
                 const int pos = c.t * kSfaTile + lane + 32 * u;
-                int tok = -1;
                 if (pos < npos) {
                     const int idx = __ldg(row + (pos >> p.sbs_log2));
-                    if (idx >= 0 && idx <= (INT32_MAX >> p.sbs_log2)) tok = (idx << p.sbs_log2) + (pos & smask);
+                    if (idx >= 0 && idx <= (INT32_MAX >> p.sbs_log2)) tok.v[u] = (idx << p.sbs_log2) + (pos & smask);
                 }
-                (u ? i_hi : i_lo) = tok;
             }
+            return tok;
         };
         // block-table entry of token idx of batch b (read only when it lies inside the table), -1 otherwise
         auto load_blk = [&](int b, int idx) -> int {
@@ -282,31 +294,31 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             if (lim > avail) lim = avail;
             limit = lim < 0 ? 0 : (int)lim;
         };
-        int i0lo, i0hi, i1lo, i1hi;
-        load_idx(lo, c0, i0lo, i0hi);
-        load_idx(lo + 1, c1, i1lo, i1hi);
+        LaneInts i0 = load_idx(lo, c0), i1 = load_idx(lo + 1, c1), bt0, bt1;
         int b0, len0, base0;
         row_info(c0.r, b0, len0, base0);
-        int bt0lo = paged && b0 >= 0 ? load_blk(b0, i0lo) : -1, bt0hi = paged && b0 >= 0 ? load_blk(b0, i0hi) : -1;
+#pragma unroll
+        for (int u = 0; u < kPosPerLane; ++u) bt0.v[u] = paged && b0 >= 0 ? load_blk(b0, i0.v[u]) : -1;
         long long k = 0;
         for (long long g = lo; g < hi; ++g, ++k) {
-            int i2lo, i2hi;
-            load_idx(g + 2, c2, i2lo, i2hi);
-            int b1 = -1, len1 = 0, base1 = 0, bt1lo = -1, bt1hi = -1;
+            const LaneInts i2 = load_idx(g + 2, c2);
+            int b1 = -1, len1 = 0, base1 = 0;
+#pragma unroll
+            for (int u = 0; u < kPosPerLane; ++u) bt1.v[u] = -1;
             if (g + 1 < hi) {
                 row_info(c1.r, b1, len1, base1);
                 if (paged && b1 >= 0) {
-                    bt1lo = load_blk(b1, i1lo);
-                    bt1hi = load_blk(b1, i1hi);
+#pragma unroll
+                    for (int u = 0; u < kPosPerLane; ++u) bt1.v[u] = load_blk(b1, i1.v[u]);
                 }
             }
             // rows of tile g: invalid (total_rows) outside [0, limit); bad block-table entries are flagged
-            int rows2[2];
+            int rows2[kPosPerLane];
             bool bad = false;
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int idx = u ? i0hi : i0lo;
-                const int blk = u ? bt0hi : bt0lo;
+            for (int u = 0; u < kPosPerLane; ++u) {
+                const int idx = i0.v[u];
+                const int blk = bt0.v[u];
                 int r = p.total_rows;
                 if (idx >= 0 && idx < len0) {
                     if (!paged) r = base0 + idx;  // < total_rows: the limit stops at the tensor's end
@@ -316,8 +328,9 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 rows2[u] = r;
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, kErrBadBlock);
-            const uint32_t m_lo = __ballot_sync(0xffffffffu, rows2[0] != p.total_rows);
-            const uint32_t m_hi = __ballot_sync(0xffffffffu, rows2[1] != p.total_rows);
+            uint32_t vm[kPosPerLane];
+#pragma unroll
+            for (int u = 0; u < kPosPerLane; ++u) vm[u] = __ballot_sync(0xffffffffu, rows2[u] != p.total_rows);
             const int slot = (int)(k % kSfaRSlots);
             const uint32_t round = (uint32_t)(k / kSfaRSlots);
             if (round > 0 && !mbar_wait_bounded(&r_empty[slot], (round - 1) & 1, kWaitLimitNs)) {
@@ -326,24 +339,25 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 break;
             }
             RSlot* rs = slot_of(k);
-            rs->rows[lane] = rows2[0];
-            rs->rows[lane + 32] = rows2[1];
+            uint32_t any = 0;
+#pragma unroll
+            for (int u = 0; u < kPosPerLane; ++u) {
+                rs->rows[lane + 32 * u] = rows2[u];
+                any |= vm[u];
+            }
             if (lane == 0) {
-                rs->vmask[0] = m_lo;
-                rs->vmask[1] = m_hi;
-                rs->any = (m_lo | m_hi) != 0;
+#pragma unroll
+                for (int u = 0; u < kPosPerLane; ++u) rs->vmask[u] = vm[u];
+                rs->any = any != 0;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&r_full[slot]);
-            i0lo = i1lo;
-            i0hi = i1hi;
-            i1lo = i2lo;
-            i1hi = i2hi;
+            i0 = i1;
+            i1 = i2;
+            bt0 = bt1;
             b0 = b1;
             len0 = len1;
             base0 = base1;
-            bt0lo = bt1lo;
-            bt0hi = bt1hi;
             c0 = c1;
             c1 = c2;
             c2.next(p.eff, p.R);
@@ -375,12 +389,12 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         // 0..7: key, 8: key rope, 9..12: value half h).  The key blocks of a tile alternate
         // between the two CTAs (by block and tile parity) and land in both CTAs' rings; the
         // other CTA's blocks only announce their bytes here.  Value blocks are this CTA's own.
-        constexpr int kGroups = 16 / kSfaIssuers;  // gather4 row groups per warp and stage
+        constexpr int kGroups = kSfaTile / 4 / kSfaIssuers;  // gather4 row groups per warp and stage
         // Block-wise selections of 8 or more tokens are runs of consecutive cache rows: one tiled
         // box of run_rows rows per run (or per 64-row half of a 128-token run) instead of gathers.
         const bool runs = p.sbs_log2 >= 3;
         const int run_rows = runs ? min(1 << p.sbs_log2, kSfaTile) : 0;
-        const int nruns = runs ? kSfaTile / run_rows : 0;  // boxes per stage: 8, 4, 2 or 1
+        const int nruns = runs ? kSfaTile / run_rows : 0;  // boxes per stage: 16, 8, 4, 2 or 1
         int my_runs = 0;                                    // this warp takes runs gi, gi + 4, ...
         for (int k = gi; k < nruns; k += kSfaIssuers) ++my_runs;
         auto gather = [&](const RSlot* rs, int blk0, int nblk, int par) {
@@ -532,7 +546,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                     const int stage = wait_stage();
                     if (stage < 0) return;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
+                    for (int k = 0; k < kSfaTile / 16; ++k) {
                         const uint64_t bd = umma_sdesc(ring_addr + stage * kSfaStageBytes + k * 2048, 8192, 1024);
                         umma_ts(O_T + vb * 64, P_T(m & 1) + k * 8, bd, idesc_pv, (acc != 0 || k > 0) ? 1u : 0u);
                     }
@@ -630,27 +644,30 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 break;
             }
             const RSlot* rs = slot_of(kk);
-            const uint32_t vm_lo = rs->vmask[0], vm_hi = rs->vmask[1];
             const int any = rs->any;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&r_empty[slot]);
+            if (!any) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&r_empty[slot]);
+            }
             if (any) {
                 if (!mbar_wait_bounded(&s_full[n & 1], (uint32_t)(n >> 1) & 1, kWaitLimitNs)) {
                     fail();
                     break;
                 }
                 tc_fence_after();
-                uint32_t sa[32], sb2[32];
-                tmem_ld32(S_T(n & 1) + lane_off, sa);
-                tmem_ld32(S_T(n & 1) + lane_off + 32, sb2);
-                tmem_wait_ld();
-                float x[64];
+                const uint32_t S0 = S_T(n & 1) + lane_off;
+                // pass 1: the tile's largest scaled score over its valid positions (the valid mask
+                // stays in the resolver slot until pass 2 has read it)
                 float tmax = -INFINITY;
+#pragma unroll 1
+                for (int c = 0; c < kSfaTile / 32; ++c) {
+                    uint32_t sa[32];
+                    tmem_ld32(S0 + 32 * c, sa);
+                    const uint32_t vmc = rs->vmask[c];
+                    tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    x[j] = ((vm_lo >> j) & 1) ? __uint_as_float(sa[j]) * p.scale_log2 : -INFINITY;
-                    x[j + 32] = ((vm_hi >> j) & 1) ? __uint_as_float(sb2[j]) * p.scale_log2 : -INFINITY;
-                    tmax = fmaxf(tmax, fmaxf(x[j], x[j + 32]));
+                    for (int j = 0; j < 32; ++j)
+                        if ((vmc >> j) & 1) tmax = fmaxf(tmax, __uint_as_float(sa[j]) * p.scale_log2);
                 }
                 m_top = fmaxf(m_top, tmax);
                 const float m_new = fmaxf(m_used, tmax);
@@ -688,15 +705,34 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                     tc_fence_after();
                 }
                 const float m_use = m_used == -INFINITY ? 0.f : m_used;
-                uint32_t pk[32];
+                // pass 2: probabilities as 16-bit pairs (column m: positions 2m, 2m + 1), written
+                // over the score buffer 32 columns at a time after the 64 scores they replace
+                // have been read
+#pragma unroll 1
+                for (int c2 = 0; c2 < kSfaTile / 64; ++c2) {
+                    uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float p0 = ex2f_approx(x[2 * c] - m_use);
-                    const float p1 = ex2f_approx(x[2 * c + 1] - m_use);
-                    l_sum += p0 + p1;
-                    pk[c] = pack2(p0, p1, bf);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int c = 2 * c2 + h2;
+                        uint32_t sa[32];
+                        tmem_ld32(S0 + 32 * c, sa);
+                        const uint32_t vmc = rs->vmask[c];
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float x0 = ((vmc >> (2 * j)) & 1) ? __uint_as_float(sa[2 * j]) * p.scale_log2 : -INFINITY;
+                            const float x1 =
+                                ((vmc >> (2 * j + 1)) & 1) ? __uint_as_float(sa[2 * j + 1]) * p.scale_log2 : -INFINITY;
+                            const float p0 = ex2f_approx(x0 - m_use);
+                            const float p1 = ex2f_approx(x1 - m_use);
+                            l_sum += p0 + p1;
+                            pk[16 * h2 + j] = pack2(p0, p1, bf);
+                        }
+                    }
+                    tmem_st32(P_T(n & 1) + lane_off + 32 * c2, pk);
                 }
-                tmem_st32(P_T(n & 1) + lane_off, pk);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&r_empty[slot]);  // the slot's last read was above
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
