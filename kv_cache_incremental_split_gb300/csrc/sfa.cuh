@@ -21,7 +21,7 @@ constexpr int kSfaStageBytes = kSfaTile * 128;
 constexpr int kSfaQBytes = kSfaQBlocks * 128 * 128;
 constexpr int kSfaRSlots = 8;       // resolved tiles the resolver warp may run ahead
 constexpr int kSfaRSlotBytes = 544; // rows[kSfaTile], valid mask, flag (16-byte aligned)
-constexpr int kSfaIssuers = 4;     // warps that issue the ring's gathers (a stage's 16 row groups split evenly)
+constexpr int kSfaIssuers = 4;     // warps that issue the ring's gathers (a stage's kSfaTile / 4 row groups split evenly)
 constexpr int kSfaThreads = 10 * 32;  // producer, MMA issuer, four softmax warps, resolver, three more gatherers
 constexpr int kSfaSlotFloats = 128 * kSfaHalf + 3 * 128;  // normalised O of one piece + M + L + largest score
 constexpr int kSfaBarBytes = 512;
