@@ -210,9 +210,13 @@ ifa_status ifa_get_device_errors(ifa_plan* plan, void* stream, int64_t* flags);
  * Scratch: the split-KV partials and the per-sequence arrival counters live in one
  * fixed array of IFA_NOALLOC_SCRATCH_BYTES in the library's device memory.  Every GPU
  * that loads the library holds that array until the process exits, and every call on
- * a device shares it and finds the previous call's contents there.  Nothing in it
- * needs to start at zero: the counters carry a per-call tag, so a value left by an
- * earlier (even aborted) call is ignored.  Calls whose kernels overlap on the GPU (for
+ * a device shares it and finds the previous call's contents there.  The partial
+ * slots need no clearing.  The per-sequence arrival counters come in two sets: each
+ * device keeps its own call number, a call counts in one set and its kernel clears
+ * the other, which the next call on the same device uses; the number advances only
+ * when a call's kernel was launched, so a call that returns an error leaves the next
+ * call's set as it found it.  A kernel that started always clears that set, even
+ * when it ends early on a device error.  Calls whose kernels overlap on the GPU (for
  * example on two streams) race on the array: serialise them.  The first call on
  * each device looks the array's address up (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.
@@ -317,8 +321,8 @@ ifa_status sfa_workspace_size(const sfa_params* params, size_t* workspace_bytes)
  * `value` may alias `key`.  Calls that share a workspace must not overlap on the GPU.
  * The call enqueues three kernels: a tile-count kernel (one cluster of 8 CTAs; it finds
  * each query row's live tiles, splits them across the decode kernel's CTA pairs and writes
- * the zero output rows of query rows with no usable index), the decode kernel (clusters of
- * 2 CTAs, one per value half, launched with programmatic dependent launch after the count)
+ * the zero output rows of query rows with no usable index), the decode kernel (pairs of
+ * CTAs, one per value half, launched with programmatic dependent launch after the count)
  * and a combine kernel that merges the pieces of the (query row, value half) sequences the
  * decode kernel split across CTA pairs.  The workspace needs no initialisation.  Returns
  * IFA_ERR_RUNTIME when no CTA pair fits on the device or a launch fails.

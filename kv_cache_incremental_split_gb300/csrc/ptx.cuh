@@ -73,6 +73,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return pol;
 }
 
+// The default L2 priority, for data that another CTA reads again shortly after.
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 4-D tiled tensor copy global -> shared with an L2 eviction hint.
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
                                             int c2, int c3, uint64_t policy) {

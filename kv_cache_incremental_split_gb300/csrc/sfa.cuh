@@ -68,7 +68,7 @@ struct alignas(128) SfaParams {
     int* eff;           // live tiles of each query row (a sequence's tiles), 0 when no index is usable
     int* pre;           // prefix over rows of eff (R + 1 entries): the tile order of the decode kernel's pairs
     long long W;        // tiles before the count: R * tiles_per_seq (an upper bound)
-    int P;              // CTAs: an even count, pairs of CTAs form clusters
+    int P;              // CTAs: an even count; CTAs 2c and 2c + 1 (the two value halves) form pair c
     int R, QS, QN, S_sp, tiles_per_seq;  // R query rows: B * QS (row r: batch r / QS, query token r % QS), or
                                          // the TND rows; S_sp: indices per row; tiles cover S_sp << sbs_log2
     int B;                           // batches (entries of the length arrays)

@@ -5,8 +5,9 @@
 //
 // Work: a sequence is (batch b, value half h): 128 query heads x 256 of the 512
 // value channels (a full 128 x 512 fp32 accumulator would fill all of TMEM, so
-// the two halves are separate sequences; the two CTAs that hold the halves of
-// the same positions run at the same time and share the key rows through L2).
+// the two halves are separate sequences; the two CTAs of a pair hold the halves
+// of the same positions, walk them at the same time and each gather the key rows
+// themselves: the second read of a key row mostly hits L2).
 // A sequence is cut into 128-position tiles of its sparse index row.  A first
 // kernel (one cluster) finds each row's live tiles (up to the last tile holding
 // a usable index: the invalid tail after it costs nothing) and the prefix over
@@ -28,7 +29,7 @@
 //    tile::gather4 into a ring of 16 KB stages.  The four warps take eight of each
 //    stage's 32 groups of 4 rows each (one warp alone cannot issue gathers fast
 //    enough).  Invalid positions gather an out-of-range row (zero fill, no memory
-//    traffic).  Key blocks alternate between the two CTAs of a pair and land in both.
+//    traffic).  Every copy lands in this CTA's own shared memory.
 //  * MMA issuer (warp 1): S_n[128 x 128] = Q K_n^T into one of two TMEM score
 //    buffers (36 MMAs, M=128 N=128 K=16: the issuer's instruction stream is what
 //    paces the kernel, and N=128 runs at the full tensor rate), then
@@ -48,7 +49,6 @@
 #include "decode.cuh"
 #include "ptx.cuh"
 #include "sfa.cuh"
-#include "sfa_ptx.cuh"
 
 namespace ifa {
 
@@ -153,15 +153,14 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // a cluster of two CTAs: rank h takes value half h of the pair's tiles
+    // CTAs 2c and 2c + 1 form pair c: CTA 2c + h takes value half h of the pair's tiles
     const int h = (int)(blockIdx.x & 1);
-    constexpr uint16_t kPair = 3;  // both CTAs of the cluster
     auto slot_of = [&](long long k) { return reinterpret_cast<RSlot*>(rbase + (int)(k % kSfaRSlots) * kSfaRSlotBytes); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSfaStages; ++s) {
             mbar_init(&full[s], kSfaIssuers);
-            mbar_init(&empty[s], 2);  // a stage is free once both CTAs' MMAs have read it
+            mbar_init(&empty[s], 1);  // a stage is free once this CTA's MMAs have read it
         }
         for (int s = 0; s < kSfaRSlots; ++s) {
             mbar_init(&r_full[s], 1);
@@ -190,9 +189,9 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         reinterpret_cast<int4*>(sst)[0] = __ldcg(src);
         reinterpret_cast<int4*>(sst)[1] = __ldcg(src + 1);
     }
-    // both CTAs' barriers are initialised before either CTA copies into or arrives on the other's
+    // barriers, the TMEM address and the start are in place before any role uses them
     tc_fence_before();
-    cluster_sync_all();
+    __syncthreads();
     tc_fence_after();
     const long long lo = sst->lo;
     const long long hi = sst->hi;
@@ -378,7 +377,10 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 prefetch_tensormap(&p.tmVb);
             }
         }
-        const uint64_t pol = policy_evict_first();
+        // value rows are read once; key rows twice, by both CTAs of the pair, so they keep the
+        // default L2 priority for the second read
+        const uint64_t pol_v = policy_evict_first();
+        const uint64_t pol_k = policy_evict_normal();
         long long it = 0;
         int stg = 0;  // ring position of stage `it`: stg = it mod kSfaStages, rnd = it / kSfaStages
         uint32_t rnd = 0;
@@ -386,9 +388,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         int prev_b = -1;
         bool ok = true;
         // Gathers column blocks [blk0, blk0 + nblk) of the rows of resolved tile `rs` (blocks
-        // 0..7: key, 8: key rope, 9..12: value half h).  The key blocks of a tile alternate
-        // between the two CTAs (by block and tile parity) and land in both CTAs' rings; the
-        // other CTA's blocks only announce their bytes here.  Value blocks are this CTA's own.
+        // 0..7: key, 8: key rope, 9..12: value half h) into this CTA's ring.
         constexpr int kGroups = kSfaTile / 4 / kSfaIssuers;  // gather4 row groups per warp and stage
         // Block-wise selections of 8 or more tokens are runs of consecutive cache rows: one tiled
         // box of run_rows rows per run (or per 64-row half of a 128-token run) instead of gathers.
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         const int nruns = runs ? kSfaTile / run_rows : 0;  // boxes per stage: 16, 8, 4, 2 or 1
         int my_runs = 0;                                    // this warp takes runs gi, gi + 4, ...
         for (int k = gi; k < nruns; k += kSfaIssuers) ++my_runs;
-        auto gather = [&](const RSlot* rs, int blk0, int nblk, int par) {
+        auto gather = [&](const RSlot* rs, int blk0, int nblk) {
             const int grp = gi * kGroups + lane;
             const int4 r4 = lane < kGroups ? reinterpret_cast<const int4*>(rs->rows)[grp] : make_int4(0, 0, 0, 0);
             for (int blk = blk0; blk < blk0 + nblk; ++blk, ++it, ring_next(stg, rnd)) {
@@ -409,13 +409,11 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                     ok = false;
                     return;
                 }
-                const bool key = blk < kSfaQBlocks;
-                const bool mine = !key || ((blk + par) & 1) == h;
                 if (runs) {
                     if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)(my_runs * run_rows * 128));
                     __syncwarp();
                     const int k = gi + kSfaIssuers * lane;  // run this lane loads
-                    if (mine && lane < my_runs) {
+                    if (lane < my_runs) {
                         const CUtensorMap* map;
                         int x;
                         if (blk < 8) {
@@ -430,15 +428,14 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                         }
                         // the run's first row; an invalid run starts past the last row (zero fill)
                         uint8_t* dst = ring + stage * kSfaStageBytes + k * run_rows * 128;
-                        if (key) tma_load_2d_mc(dst, map, &full[stage], x, rs->rows[k * run_rows], kPair);
-                        else tma_load_2d(dst, map, &full[stage], x, rs->rows[k * run_rows]);
+                        tma_load_2d(dst, map, &full[stage], x, rs->rows[k * run_rows]);
                     }
                     __syncwarp();
                     continue;
                 }
                 if (lane == 0) mbar_arrive_expect_tx(&full[stage], kSfaStageBytes / kSfaIssuers);
                 __syncwarp();
-                if (mine && lane < kGroups) {
+                if (lane < kGroups) {
                     const CUtensorMap* map;
                     int x;
                     if (blk < 8) {
@@ -452,8 +449,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                         x = h * kSfaHalf + (blk - kSfaQBlocks) * 64;
                     }
                     uint8_t* dst = ring + stage * kSfaStageBytes + grp * 512;
-                    if (key) tma_gather4_mc(dst, map, &full[stage], x, r4.x, r4.y, r4.z, r4.w, kPair, pol);
-                    else tma_gather4(dst, map, &full[stage], x, r4.x, r4.y, r4.z, r4.w, pol);
+                    tma_gather4(dst, map, &full[stage], x, r4.x, r4.y, r4.z, r4.w, blk < kSfaQBlocks ? pol_k : pol_v);
                 }
                 __syncwarp();
             }
@@ -461,7 +457,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         long long pend = -1;  // resolved tile whose value rows are still to be gathered
         auto flush = [&]() {
             if (pend < 0) return;
-            gather(slot_of(pend), kSfaQBlocks, kSfaVBlocks, 0);
+            gather(slot_of(pend), kSfaQBlocks, kSfaVBlocks);
             __syncwarp();
             if (lane == 0) mbar_arrive(&r_empty[(int)(pend % kSfaRSlots)]);
             pend = -1;
@@ -498,7 +494,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 ++epoch;
             }
             prev_b = b;
-            gather(rs, 0, kSfaQBlocks, (int)(k & 1));
+            gather(rs, 0, kSfaQBlocks);
             if (!ok) break;
             flush();
             pend = k;
@@ -550,7 +546,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                         const uint64_t bd = umma_sdesc(ring_addr + stage * kSfaStageBytes + k * 2048, 8192, 1024);
                         umma_ts(O_T + vb * 64, P_T(m & 1) + k * 8, bd, idesc_pv, (acc != 0 || k > 0) ? 1u : 0u);
                     }
-                    umma_commit_mc(&empty[stage], kPair);
+                    umma_commit(&empty[stage]);
                 }
                 umma_commit(&o_full[m & 1]);
             };
@@ -592,7 +588,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                         const uint64_t bd = umma_sdesc(ring_addr + stage * kSfaStageBytes + k * 32, 16, 1024);
                         umma_ss(S_T(n & 1), ad, bd, idesc_qk, (kb | k) != 0);
                     }
-                    umma_commit_mc(&empty[stage], kPair);
+                    umma_commit(&empty[stage]);
                 }
                 if (!ok) break;
                 umma_commit(&s_full[n & 1]);
@@ -798,10 +794,10 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         }
     }
     // ==================================================================== teardown
-    // Neither CTA leaves while the other may still arrive on its barriers (the MMA issuers
-    // have waited for all their MMAs and so for their commits).
+    // Every role is done with TMEM (the MMA issuer has waited for all its MMAs and so for
+    // their commits) before it is freed.
     tc_fence_before();
-    cluster_sync_all();
+    __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tbase, 512);
 }
@@ -1009,23 +1005,14 @@ __global__ void __launch_bounds__(128) sfa_combine(const __grid_constant__ SfaPa
 int sfa_max_pairs() {
     static int pairs = -1;
     if (pairs < 0) {
-        int n = 0;
-        if (cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSfaSmem) == cudaSuccess) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(2);
-            cfg.blockDim = dim3(kSfaThreads);
-            cfg.dynamicSmemBytes = kSfaSmem;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, sfa_kernel, &cfg) != cudaSuccess) n = 0;
-        }
+        int n = 0, dev = 0, sms = 0;
+        if (cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSfaSmem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sfa_kernel, kSfaThreads, kSfaSmem) != cudaSuccess ||
+            cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 0;
         cudaGetLastError();
-        pairs = n;
+        pairs = n * sms / 2;
     }
     return pairs;
 }
@@ -1057,15 +1044,11 @@ cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream) {
     cfg.blockDim = dim3(kSfaThreads);
     cfg.dynamicSmemBytes = kSfaSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;  // CTA pairs: the two value halves
-    attr[1].val.clusterDim.x = 2;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, sfa_kernel, p);
     if (e != cudaSuccess) return e;
     // An ordinary launch: with programmatic dependent launch (resident early, waiting) the
