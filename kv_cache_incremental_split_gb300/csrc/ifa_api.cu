@@ -175,7 +175,10 @@ static ifa_status run_planned(ifa_plan* pl, const void* query, const void* key, 
     dp.partials = reinterpret_cast<float*>(workspace);
     dp.err = pl->d_state;
     dp.counters = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(pl->d_state) + 8);
-    dp.gen = ++pl->gen;  // wraps: consecutive calls alternate the counter set
+    // Wraps: consecutive launched calls alternate the counter set.  The plan's call number
+    // advances only once the kernel is launched (below): a call whose launch failed cleared
+    // nothing, so the next call counts in the set this one would have used.
+    dp.gen = pl->gen + 1u;
     if (B <= kInlineB) {
         std::memcpy(dp.bdata_inline, bd.data(), bd.size() * sizeof(int32_t));
         dp.ext_bdata = nullptr;
@@ -192,6 +195,7 @@ static ifa_status run_planned(ifa_plan* pl, const void* query, const void* key, 
         cudaGetLastError();
         return IFA_ERR_RUNTIME;
     }
+    pl->gen = dp.gen;
     pl->last_launches = 1;
     return IFA_OK;
 }

@@ -9,7 +9,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -35,22 +34,31 @@ constexpr int kMaxDevices = 64;
 // name is only a stand-in; the device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-// Device address of the scratch array on the current device, looked up once per
-// device (the first call on a device does this set-up).
+// Per-device state: the scratch array's device address, looked up once per device (the
+// first call on a device does this set-up), and the device's call number, which picks the
+// counter set a call counts in.  Each device alternates its own two sets: a call clears the
+// set the next call on the same device will use, so the number must advance per device.
+struct DeviceSlot {
+    unsigned char* addr = nullptr;
+    unsigned int gen = 0;
+};
+
+std::mutex g_mu;
+DeviceSlot g_dev[kMaxDevices];
+
 unsigned char* scratch_on_current_device(int device) {
-    static std::mutex mu;
-    static unsigned char* addr[kMaxDevices] = {};
     if (device < 0 || device >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[device]) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceSlot& d = g_dev[device];
+    if (!d.addr) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
             cudaGetLastError();
             return nullptr;
         }
-        addr[device] = static_cast<unsigned char*>(p);
+        d.addr = static_cast<unsigned char*>(p);
     }
-    return addr[device];
+    return d.addr;
 }
 
 }  // namespace
@@ -104,13 +112,17 @@ extern "C" ifa_status ifa_run_noalloc(const ifa_params* params, const void* quer
     build_bounds(p, kc, dp.bdata_inline, W, P, dp.bounds);
     dp.partials = reinterpret_cast<float*>(scratch + kPartialOffset);
     dp.counters = reinterpret_cast<unsigned int*>(scratch + kCounterOffset);
-    static std::atomic<unsigned int> generation{0};
-    dp.gen = ++generation;  // wraps: consecutive calls alternate the counter set
     dp.err = deviceErrorFlags ? deviceErrorFlags : reinterpret_cast<int*>(scratch);
     dp.ext_bdata = nullptr;
+    // The device's call number advances only when the kernel was launched: a launch that failed
+    // cleared nothing, so the next call must count in the set this one would have used.  (The
+    // number wraps; consecutive launched calls on a device alternate the counter set.)
+    std::lock_guard<std::mutex> lock(g_mu);
+    dp.gen = g_dev[device].gen + 1u;
     if (kc.launch(dp, P, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return IFA_ERR_RUNTIME;
     }
+    g_dev[device].gen = dp.gen;
     return IFA_OK;
 }
