@@ -2,6 +2,8 @@
 library (via the C-ABI binding) or through the CPU oracle, and compare."""
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 import oracle
@@ -108,3 +110,80 @@ def max_abs_err(a, b) -> float:
     if a.size == 0:
         return 0.0
     return float(np.max(np.abs(a - b)))
+
+
+# ---------------------------------------------------------------- sparse decode probes
+
+_PROBE_BITS = 12  # token-index bits the softmax_sum fingerprint covers
+
+
+def sfa_live_tiles(idx_rows):
+    """Live 128-position tiles of each index row: up to the last entry that holds an index >= 0."""
+    ok = idx_rows >= 0
+    last = np.where(ok.any(axis=1), idx_rows.shape[1] - 1 - np.argmax(ok[:, ::-1], axis=1), -1)
+    return np.where(last < 0, 0, (last + 1 + 127) // 128)
+
+
+def sfa_pieces_per_row(idx_rows, sms):
+    """CTA pairs that hold a part of each index row, under the library's split: pairs take equal
+    contiguous shares (floor(c W / Pa)) of the rows' live tiles in row order, with at most one pair
+    per two SMs and shares of at least min(tiles per row, 4) tiles."""
+    eff = sfa_live_tiles(idx_rows).astype(np.int64)
+    tps = -(-idx_rows.shape[1] // 128)
+    share = max(1, min(tps, 4))
+    launched = max(1, min(min(256, sms) // 2, -(-(len(eff) * tps) // share)))
+    W = int(eff.sum())
+    Pa = max(1, min(launched, -(-W // share)))
+    pre = np.concatenate([[0], np.cumsum(eff)])
+    first = ((pre[:-1] + 1) * Pa - 1) // W
+    last = ((pre[:-1] + eff) * Pa - 1) // W
+    bounds = {c * W // Pa for c in range(1, Pa)}
+    ends_on_boundary = np.array([eff[r] > 0 and int(pre[r] + eff[r]) in bounds for r in range(len(eff))])
+    return np.where(eff > 0, last - first + 1, 0), ends_on_boundary
+
+
+def sfa_selected_tokens(c, r):
+    """Tokens row r (batch b, query token s) attends to, for token-wise indices with every query
+    token valid: its indices in [0, limit), the limit being the length, or len - Q_S + s + 1 under
+    the right-down causal mode."""
+    Q_S = c.query.shape[1]
+    b, s = divmod(r, Q_S)
+    idx = c.sparse_indices[b, s, 0].astype(np.int64)
+    ln = int(c.actual_seq_lengths_kv[b])
+    lim = ln - Q_S + s + 1 if c.sparse_mode == 3 else ln
+    return idx[(idx >= 0) & (idx < lim)]
+
+
+def sfa_bit_probe(c):
+    """Query 0 except query_rope[head n] = -1 at channel n mod 12; key_rope of token t = the bits
+    of t; scale ln 2.  Every score of head n is -bit_{n mod 12}(t), every probability exactly 1 or
+    1/2, so softmax_sum is exact: (count with bit 0) + (count with bit 1) / 2, or the count when no
+    selected token has bit 0.  It pins the selected set, not only its size."""
+    B, Q_S, Q_N = c.query.shape[0], c.query.shape[1], c.query.shape[2]
+    bs = c.key.shape[1]
+    c.query = np.zeros_like(c.query)
+    qr = np.zeros(c.query_rope.shape, dtype=np.float32)
+    for n in range(Q_N):
+        qr[:, :, n, n % _PROBE_BITS] = -1.0
+    c.query_rope = gen.to_storage(qr, c.dtype)
+    cols = c.block_table.shape[1]
+    col_of_block = np.empty(c.key.shape[0], dtype=np.int64)
+    col_of_block[c.block_table.reshape(-1)] = np.tile(np.arange(cols), B)
+    tok = col_of_block[:, None] * bs + np.arange(bs)[None, :]            # (block, slot) -> token
+    kr = np.zeros(c.key_rope.shape, dtype=np.float32)
+    for j in range(_PROBE_BITS):
+        kr[:, :, 0, j] = (tok >> j) & 1
+    c.key_rope = gen.to_storage(kr, c.dtype)
+    c.scale = math.log(2.0)
+    exp_sum = np.zeros((B * Q_S, Q_N))
+    exp_max = np.full((B * Q_S, Q_N), -np.inf)
+    for r in range(B * Q_S):
+        t = sfa_selected_tokens(c, r)
+        for n in range(Q_N):
+            bit = (t >> (n % _PROBE_BITS)) & 1
+            n1 = int(bit.sum())
+            n0 = len(t) - n1
+            exp_sum[r, n] = n0 + 0.5 * n1 if n0 > 0 else float(n1)
+            if len(t):
+                exp_max[r, n] = 0.0 if n0 > 0 else -math.log(2.0)
+    return c, exp_sum, exp_max

@@ -752,6 +752,37 @@ def test_sfa_softmax_max_and_sum_closed_forms():
             assert mx[b, s, n] + math.log(sm[b, s, n]) == pytest.approx(logsumexp(sc), rel=1e-12, abs=1e-12)
 
 
+@pytest.mark.parametrize("Q_S,mode", [(1, 0), (2, 3)])
+def test_sfa_softmax_sum_bit_probe_fingerprint(Q_S, mode):
+    """The probe the GPU split-path test uses: scores -bit_j(t) at scale ln 2 make every
+    probability 1 or 1/2, so softmax_sum is a count-based closed form of the selected set (the
+    number of selected tokens with bit j clear, plus half of those with it set) and softmax_max
+    is 0 or -ln 2.  Checked exactly, including the causal limit's last key."""
+    from harness import sfa_bit_probe
+    c = gen.sfa_mla(5, B=3, Q_N=16, block_size=64, kv_len=4096, sparse_size=300, nvalid_lo=100, nvalid_hi=300,
+                    Q_S=Q_S, sparse_mode=mode)
+    c.sparse_indices[0, :, 0, 0] = 4095  # the last key: visible to the last query token only under mode 3
+    c.sparse_indices[2] = -1             # nothing selected
+    c, exp_sum, exp_max = sfa_bit_probe(c)
+    _, mx, sm = oracle.sfa_ref(c.query, c.query_rope, c.key, c.key_rope, c.value, c.sparse_indices,
+                               c.block_table, c.actual_seq_lengths_kv, scale=c.scale, sparse_mode=mode,
+                               return_softmax_lse=True)
+    sm, mx = sm.reshape(exp_sum.shape), mx.reshape(exp_max.shape)
+    assert np.array_equal(sm, exp_sum)
+    assert np.array_equal(np.isneginf(mx), np.isneginf(exp_max))
+    live = ~np.isneginf(exp_max)
+    assert np.abs(mx[live] - exp_max[live]).max() <= 1e-15
+    # a swapped token changes the fingerprint: move one selected index of batch 1, first query token
+    c2 = c
+    c2.sparse_indices = c.sparse_indices.copy()
+    i0 = int(c2.sparse_indices[1, 0, 0, 1])
+    c2.sparse_indices[1, 0, 0, 1] = i0 ^ 1 if (i0 ^ 1) not in set(c2.sparse_indices[1, 0, 0].tolist()) else i0 ^ 2
+    _, _, sm2 = oracle.sfa_ref(c2.query, c2.query_rope, c2.key, c2.key_rope, c2.value, c2.sparse_indices,
+                               c2.block_table, c2.actual_seq_lengths_kv, scale=c2.scale, sparse_mode=mode,
+                               return_softmax_lse=True)
+    assert not np.array_equal(sm2.reshape(exp_sum.shape)[Q_S], exp_sum[Q_S])
+
+
 # ------------------------------------------- KV-cache append
 
 def _place(cache, new, pos, layout, kv_format, block_size=0, block_table=None):

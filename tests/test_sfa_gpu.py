@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 from kv_cache_incremental_split_gb300 import inputs as gen
-from harness import TOL, max_abs_err, out_to_f64, to_device
+from harness import TOL, max_abs_err, out_to_f64, sfa_bit_probe, sfa_pieces_per_row, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -306,3 +306,59 @@ def test_sfa_rows_without_live_tiles_and_late_indices():
     live = ~empty
     assert np.abs(mx[live] - rmx[live]).max() <= 2e-3
     assert (np.abs(sm[live] - rsm[live]) / rsm[live]).max() <= 1e-3
+
+
+# ------------------------------------------- exact selected sets on rows cut across CTA pairs
+
+@pytest.mark.parametrize("Q_S,mode", [(1, 0), (2, 3)])
+def test_sfa_selected_set_exact_on_split_rows(Q_S, mode):
+    """The sparse MLA workload's shape (B=32, 2048 indices, U{1024..2048} valid per row, keys of
+    32768 tokens; two query tokens with the right-down causal mode): softmax_sum of the bit probe
+    is compared exactly, on every row, with the count-based closed form, and on sampled rows with
+    the oracle rounded to float32.  Rows are cut across CTA pairs (asserted from the live-tile
+    split); one row is re-drawn so that its live tiles end exactly on a pair boundary, and one so
+    that its valid entries end exactly on a tile boundary."""
+    c = gen.sfa_mla(40 + Q_S, Q_S=Q_S, sparse_mode=mode)
+    B = c.query.shape[0]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = c.sparse_indices.reshape(B * Q_S, -1)
+    rng = np.random.default_rng(400 + Q_S)
+
+    def redraw(r, nv):
+        b, s = divmod(r, Q_S)
+        c.sparse_indices[b, s, 0, :] = -1
+        c.sparse_indices[b, s, 0, :nv] = rng.choice(32768, size=nv, replace=False)
+
+    redraw(3, 1280)  # ten whole tiles
+    boundary_row = None
+    for r in range(5, B * Q_S):
+        for nv in range(1024, 2049, 128):
+            keep = c.sparse_indices.copy()
+            redraw(r, nv)
+            pieces, on_b = sfa_pieces_per_row(rows, sms)
+            if on_b[r] and pieces[r] >= 2:
+                boundary_row = r
+                break
+            c.sparse_indices[:] = keep
+        if boundary_row is not None:
+            break
+    assert boundary_row is not None
+    pieces, _ = sfa_pieces_per_row(rows, sms)
+    assert (pieces >= 2).mean() >= 0.75, pieces
+
+    c, exp_sum, exp_max = sfa_bit_probe(c)
+    got, mx, sm, _ = run_gpu(c, lse=True)
+    sm = sm.reshape(B * Q_S, -1)
+    assert np.array_equal(sm, exp_sum), np.argwhere(sm != exp_sum)[:8]
+    # the largest score: 0 when a selected token has the probed bit clear, else -ln 2
+    mx = mx.reshape(B * Q_S, -1)
+    assert np.array_equal(np.isneginf(mx), np.isneginf(exp_max))
+    live = ~np.isneginf(exp_max)
+    assert np.abs(mx[live] - exp_max[live]).max() <= 1e-6
+    # oracle on sampled batches (the boundary row's batch among them): exact sums, tolerance elsewhere
+    bsel = np.unique([boundary_row // Q_S, 3 // Q_S, B - 1])
+    ref, rmx, rsm = run_ref(c, batches=bsel, lse=True)
+    rows_sel = np.concatenate([np.arange(b * Q_S, (b + 1) * Q_S) for b in bsel])
+    assert np.array_equal(sm[rows_sel], rsm.reshape(len(rows_sel), -1).astype(np.float32).astype(np.float64))
+    assert np.abs(mx[rows_sel] - rmx.reshape(len(rows_sel), -1)).max() <= 1e-6
+    assert max_abs_err(got[bsel], ref) <= TOL[c.dtype]
