@@ -1,10 +1,11 @@
 #!/usr/bin/env python3
 """Decode-attention benchmark: KV-cache GB/s read and decode-attention calls/s.
 
-One step = one library call (ifa_run, or sfa_run for the sparse workload) over
-one batch of the workload.  Default workload: GQA decode against a padded
-cache, B=16, N=32, KV_N=8, D=128, BSH bf16, Smax=4096, lengths ~ U{1..4096},
-bool mask (B,1,1,S) true past each length.
+One step = one library call (ifa_run, or sfa_run for the sparse workloads) over
+one batch of the workload.  Default workload: paged GQA decode, B=64, N=32,
+KV_N=8, D=128, bf16, blockSize 128, cache (blocknum, KV_N, 128, D) through a
+random block table, lengths ~ U{512..32768} (about 4.4 GB of keys and values
+per call: the largest single-GPU workload).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -12,7 +13,12 @@ Prints one JSON line on rank 0.  ``value`` is algorithmic bytes per step
 (key/value rows of the valid tokens, query, output, mask over the valid
 windows, block-table entries and sparse indices used, antiquant parameters)
 divided by the device time per step, summed over ranks (weak scaling: every
-rank runs its own rank-seeded copy of the workload).
+rank runs its own rank-seeded copy of the workload).  The K timed steps are
+timed as one region, R times over (at least --repeats, and at least
+--min-timed-seconds of regions in all); ``ms_per_step`` is the median region
+time / K, with the 10th and 90th percentiles beside it.  With --gpus N > 1 and
+no WORLD_SIZE in the environment, the script relaunches itself under
+torch.distributed.run with N ranks, one per GPU.
 """
 from __future__ import annotations
 
@@ -55,6 +61,9 @@ WORKLOADS = {
                 "KV length 32768, sparse_indices (B,1,1,2048) with U{1024..2048} valid then -1, scale 1/sqrt(576)"),
     "sfa_mla_small": ("sparse MLA-absorb decode, profiling size: B=8 Q_N=128 D=512+64 bf16, block 64, "
                       "KV length 8192, 2048 indices with U{1024..2048} valid"),
+    "sfa_mla_vk": ("sparse MLA-absorb decode with value = key (one cache tensor serves both): B=32 Q_N=128 KV_N=1 "
+                   "D=512+rope 64 bf16, PA_BSND block 64, KV length 32768, sparse_indices (B,1,1,2048) with "
+                   "U{1024..2048} valid then -1, scale 1/sqrt(576)"),
     "sfa_mla_blockwise": ("sparse MLA-absorb decode, block-wise: B=32 Q_N=128 D=512+64 bf16, PA_BSND block 64, "
                           "KV length 32768, sparse_block_size 16, 128 block indices with U{64..128} valid then -1"),
     "sfa_mla_mtp": ("sparse MLA-absorb decode, two query tokens (multi-token prediction): B=32 Q_S=2 Q_N=128 "
@@ -76,6 +85,10 @@ def make_case(name: str, seed: int):
         return gen.sfa_mla(seed)
     if name == "sfa_mla_small":
         return gen.sfa_mla(seed, B=8, kv_len=8192)
+    if name == "sfa_mla_vk":
+        c = gen.sfa_mla(seed)
+        c.value = c.key  # the same array: the call receives one tensor as key and value
+        return c
     if name == "sfa_mla_blockwise":
         return gen.sfa_mla(seed, sparse_size=128, nvalid_lo=64, nvalid_hi=128, sparse_block_size=16)
     if name == "sfa_mla_mtp":
@@ -141,7 +154,8 @@ def algorithmic_bytes(case) -> int:
     if isinstance(case, gen.SfaCase):
         n = int(sfa_valid_counts(case).sum())
         QN = case.query.shape[2]
-        total = n * (512 + 64 + 512) * 2                       # key, key_rope and value rows of selected tokens
+        # key, key_rope and value rows of selected tokens; with value = key a row serves both
+        total = n * (512 + 64 + (0 if case.value is case.key else 512)) * 2
         rows = case.B * case.query.shape[1]                    # (batch, query token) rows
         total += rows * QN * (512 + 64) * 2                    # query and query_rope
         total += rows * QN * 512 * 2                           # output
@@ -370,21 +384,61 @@ def _run_oracle(c):
                        antiquant_offset=c.antiquant_offset)
 
 
-def oracle_sample(case, budget_s: float, start_batch: int = 0):
-    """Time the CPU oracle, batch by batch, for about `budget_s` seconds."""
-    done, nbytes, t_used = [], 0, 0.0
-    b = start_batch % case.B
-    while True:
-        c = _batch_subset(case, b)
-        t = time.perf_counter()
-        _run_oracle(c)
-        t_used += time.perf_counter() - t
-        nbytes += algorithmic_bytes(c)
-        done.append(b)
-        b = (b + 1) % case.B
-        if t_used >= budget_s or len(done) >= case.B:
-            break
-    return nbytes, t_used, done
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return max(1, os.cpu_count() or 1)
+
+
+def oracle_sample(case, budget_s: float, threads: int = 1, start_batch: int = 0):
+    """Time the CPU oracle on whole batch rows of the workload for about `budget_s` seconds of
+    wall time, `threads` threads taking rows in turn (the C oracle runs without the GIL).
+    Returns (algorithmic bytes done, wall seconds, rows done in order)."""
+    import threading
+    from concurrent.futures import ThreadPoolExecutor
+    lock = threading.Lock()
+    state = {"next": start_batch, "bytes": 0, "done": []}
+    t0 = time.perf_counter()
+
+    def worker():
+        first = True
+        while True:
+            with lock:
+                if not first and (time.perf_counter() - t0 >= budget_s or len(state["done"]) >= 64 * case.B):
+                    return
+                b = state["next"] % case.B
+                state["next"] += 1
+            first = False
+            c = _batch_subset(case, b)
+            _run_oracle(c)
+            nb = algorithmic_bytes(c)
+            with lock:
+                state["bytes"] += nb
+                state["done"].append(b)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for f in [ex.submit(worker) for _ in range(threads)]:
+            f.result()
+    return state["bytes"], time.perf_counter() - t0, state["done"]
+
+
+def cpu_baseline_legs(case, budget_s: float):
+    """The oracle at one thread and at every host core: the baseline object of the JSON line
+    (its value and cores are the all-core leg's)."""
+    legs = {}
+    for th in sorted({1, host_threads()}):
+        nb, t, done = oracle_sample(case, budget_s, threads=th)
+        legs[th] = (nb / t / 1e9, nb, t, len(done))
+    nmax = max(legs)
+    v, nb, t, rows = legs[nmax]
+    return {"value": v, "unit": UNIT, "cores": nmax, "kind": "oracle",
+            "sample": (f"whole batch rows of the same workload, taken in turn by {nmax} threads for about "
+                       f"{budget_s:.0f} s ({rows} rows, {nb / 1e6:.1f} MB algorithmic, {t:.1f} s wall); "
+                       f"plain C, float64"),
+            "by_threads": {str(th): {"value": lv, "rows": lr, "seconds": round(lt, 2)}
+                           for th, (lv, _, lt, lr) in legs.items()}}
 
 
 _ROWS = {}
@@ -418,33 +472,46 @@ def oracle_unit(case, b, frac):
     return algorithmic_bytes(c), time.perf_counter() - t
 
 
+def line_config(args, case, world):
+    """The `config` object both arms print: the workload, its seed and algorithmic bytes."""
+    return {"workload": WORKLOADS[args.workload], "name": args.workload, "seed": args.seed,
+            "algorithmic_bytes_per_step": algorithmic_bytes(case),
+            "parallelism": f"replica x{world}" if world > 1 else "single GPU"}
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     case = make_case(args.workload, args.seed)
+    threads = args.ref_threads or host_threads()
     # The whole run takes about --ref-total-seconds: each of the W + K steps runs the oracle on
-    # one batch row cut to the fraction of its work that fits the per-step share (calibrated on
-    # a full row first).
+    # `threads` batch rows at once, each cut to the fraction of its work that fits the per-step
+    # share (calibrated on a full row first).
     per_step = args.ref_total_seconds / max(1, args.warmup + args.steps)
     _, t_full = oracle_unit(case, 0, 1.0)
     frac = min(1.0, per_step / max(t_full, 1e-9))
-    for w in range(args.warmup):
-        oracle_unit(case, w % case.B, frac)
-    total_b, total_t, batches = 0, 0.0, 0
-    for s in range(args.steps):
-        nb, t = oracle_unit(case, (args.warmup + s) % case.B, frac)
-        total_b += nb
-        total_t += t
-        batches += 1
+    from concurrent.futures import ThreadPoolExecutor
+    total_b, total_t, rows = 0, 0.0, 0
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for step in range(args.warmup + args.steps):
+            t = time.perf_counter()
+            futs = [ex.submit(oracle_unit, case, (step * threads + i) % case.B, frac) for i in range(threads)]
+            nb = sum(f.result()[0] for f in futs)
+            t = time.perf_counter() - t
+            if step >= args.warmup:
+                total_b += nb
+                total_t += t
+                rows += threads
     value = total_b / total_t / 1e9
-    sample = (f"each step: the oracle on one batch row of the workload cut to {100 * frac:.1f}% of its work "
-              f"({batches} rows over {args.steps} steps, {total_b / 1e6:.1f} MB algorithmic, {total_t:.1f} s)")
+    sample = (f"each step: the oracle on {threads} batch rows of the workload at once ({threads} threads), each "
+              f"cut to {100 * frac:.1f}% of its work ({rows} rows over {args.steps} steps, "
+              f"{total_b / 1e6:.1f} MB algorithmic, {total_t:.1f} s wall)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOADS[args.workload], "seed": args.seed},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "data": "synthetic", "config": line_config(args, case, world),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -551,10 +618,17 @@ class SfaWorkload:
         self.idx, self.bt = _to_dev(case.sparse_indices, dev), _to_dev(case.block_table, dev)
         self.lens = _to_dev(case.actual_seq_lengths_kv, dev)
         self.lq = None if case.actual_seq_lengths_query is None else _to_dev(case.actual_seq_lengths_query, dev)
-        k, kr, v = _to_dev(case.key, dev), _to_dev(case.key_rope, dev), _to_dev(case.value, dev)
+        self.aliased = case.value is case.key  # one tensor passed as key and as value
+        k, kr = _to_dev(case.key, dev), _to_dev(case.key_rope, dev)
+        v = k if self.aliased else _to_dev(case.value, dev)
         self.copies = copies_for
-        self.rotating_bytes = sum(t.numel() * t.element_size() for t in (k, kr, v))
-        self.caches = [(k, kr, v)] + [(k.clone(), kr.clone(), v.clone()) for _ in range(self.copies - 1)]
+        self.rotating_bytes = sum(t.numel() * t.element_size() for t in ((k, kr) if self.aliased else (k, kr, v)))
+
+        def clone3():
+            k2, kr2 = k.clone(), kr.clone()
+            return k2, kr2, (k2 if self.aliased else v.clone())
+
+        self.caches = [(k, kr, v)] + [clone3() for _ in range(self.copies - 1)]
         self.outs = [self.q.new_empty(self.q.shape) for _ in range(self.copies)]
         self.dtype = case.dtype
         self.call_name = "sfa_run"
@@ -570,13 +644,14 @@ class SfaWorkload:
 
     def host_inputs(self):
         c = self.case
-        return {"q": c.query, "qr": c.query_rope, "k": c.key, "kr": c.key_rope, "v": c.value,
+        return {"q": c.query, "qr": c.query_rope, "k": c.key, "kr": c.key_rope,
+                **({} if self.aliased else {"v": c.value}),
                 "idx": c.sparse_indices, "bt": c.block_table, "lens": c.actual_seq_lengths_kv,
                 **({} if c.actual_seq_lengths_query is None else {"lq": c.actual_seq_lengths_query})}
 
     def call_on(self, d, stream):
-        return self.op(d["q"], d["qr"], d["k"], d["kr"], d["v"], d["idx"], d["bt"], d["lens"],
-                       actual_seq_lengths_query=d.get("lq"), stream=stream)
+        return self.op(d["q"], d["qr"], d["k"], d["kr"], d["k"] if self.aliased else d["v"], d["idx"], d["bt"],
+                       d["lens"], actual_seq_lengths_query=d.get("lq"), stream=stream)
 
 
 class AppendWorkload:
@@ -653,7 +728,7 @@ def run_gpu(args):
     alg = algorithmic_bytes(case)
     # Rotate through enough input copies that the bytes streamed between two uses of one
     # copy exceed L2 several times (inputs larger than L2: no flush between steps).
-    copies = max(1, min(8, math.ceil(6 * L2_BYTES / max(1, alg))))
+    copies = args.copies or max(1, min(8, math.ceil(6 * L2_BYTES / max(1, alg))))
     if isinstance(case, gen.AppendCase):
         wl = AppendWorkload(case, dev, copies)
     elif isinstance(case, gen.SfaCase):
@@ -701,19 +776,12 @@ def run_gpu(args):
         e1.synchronize()
         eager_ms = e0.elapsed_time(e1) / n_eager
 
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize()
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-    smi_index = vis.split(",")[local] if vis and len(vis.split(",")) > local else str(local)
-    sampler = ClockSampler(smi_index)
-    with sampler:
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- timed: the K steps as one region (graph replays), R times over; each region is
+    # bracketed by a barrier (multi-rank) and a device synchronisation
+    def region_ms():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        sampler.mark_start()
         start.record(stream)
         with torch.cuda.stream(stream):
             for _ in range(n_chunks):
@@ -722,13 +790,33 @@ def run_gpu(args):
                 graphs[1].replay()
         end.record(stream)
         end.synchronize()
+        return start.elapsed_time(end)
+
+    if world > 1:
+        import torch.distributed as dist
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    est = region_ms()  # untimed: sizes the repeat count
+    reps = max(args.repeats, min(args.max_repeats, math.ceil(args.min_timed_seconds * 1e3 / max(est, 1e-3))))
+    if world > 1:  # every rank runs the same number of regions
+        rt = torch.tensor([reps], dtype=torch.int64, device=dev)
+        dist.all_reduce(rt, op=dist.ReduceOp.MAX)
+        reps = int(rt.item())
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    smi_index = vis.split(",")[local] if vis and len(vis.split(",")) > local else str(local)
+    sampler = ClockSampler(smi_index)
+    with sampler:
+        sampler.mark_start()
+        regions = [region_ms() for _ in range(reps)]
         torch.cuda.synchronize()
         sampler.mark_end()
-    elapsed = start.elapsed_time(end)
-    max_elapsed, total_bytes = aggregate(elapsed, float(alg) * args.steps, world)
+    q10, q50, q90 = (float(x) for x in np.percentile(regions, [10, 50, 90]))
+    # max over ranks of each statistic; bytes summed over ranks
+    max_elapsed, total_bytes = aggregate(q50, float(alg) * args.steps, world)
+    p10_elapsed, _ = aggregate(q10, 0.0, world)
+    p90_elapsed, _ = aggregate(q90, 0.0, world)
     ms_per_step = max_elapsed / args.steps
     value = total_bytes / (max_elapsed * 1e-3) / 1e9
-    local_gbs = alg / (elapsed / args.steps * 1e-3) / 1e9
+    local_gbs = alg / (q50 / args.steps * 1e-3) / 1e9
 
     # ---- end to end through the public API: pinned host inputs -> device -> call -> host output
     host = {n: torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for n, a in wl.host_inputs().items()}
@@ -762,10 +850,7 @@ def run_gpu(args):
     # ---- CPU oracle baseline on a bounded sample (rank 0, single GPU runs only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        nb, t, done = oracle_sample(case, args.cpu_seconds)
-        cpu = {"value": nb / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"batch rows {done} of the same workload ({nb / 1e6:.1f} MB algorithmic, "
-                         f"{t:.1f} s, single-threaded C, float64)"}
+        cpu = cpu_baseline_legs(case, args.cpu_seconds)
 
     peak, peak_kind = measured_peaks()
     clocks = sampler.summary()
@@ -774,13 +859,14 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-            "config": {"workload": WORKLOADS[args.workload], "seed": args.seed,
-                       "algorithmic_bytes_per_step": alg,
+            "config": line_config(args, case, world),
+            "timing": {"regions": reps, "ms_per_step_p10": p10_elapsed / args.steps,
+                       "ms_per_step_p90": p90_elapsed / args.steps,
+                       "statistic": f"median over {reps} timed regions of the {args.steps} steps",
                        "l2": getattr(wl, "l2_note", None) or (f"inputs larger than L2: {copies} rotating cache "
                                                               f"copies ({copies * wl.rotating_bytes / 1e6:.0f} MB)"),
                        "launch": f"CUDA graphs of {chunk} consecutive {wl.call_name} calls (one call per step"
-                                 f"{wl.launch_note}), replayed {n_chunks} times + {rem} calls",
-                       "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
+                                 f"{wl.launch_note}), replayed {n_chunks} times + {rem} calls per region"},
             "calls_per_sec": world * 1e3 / ms_per_step,
             "calls_per_sec_eager": 1e3 / eager_ms,
             "pct_of_hbm_peak": 100.0 * local_gbs / peak,
@@ -805,20 +891,69 @@ def run_gpu(args):
 def parse(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="gqa_padded", choices=sorted(WORKLOADS))
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="paged_gqa", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--copies", type=int, default=0,
+                    help="rotating input copies (0: enough that > 6x L2 streams between two uses of one)")
+    ap.add_argument("--repeats", type=int, default=5, help="timed regions of K steps, at least")
+    ap.add_argument("--min-timed-seconds", type=float, default=1.0,
+                    help="more regions until their estimated total reaches this")
+    ap.add_argument("--max-repeats", type=int, default=5000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="wall seconds of each CPU-baseline leg")
     ap.add_argument("--ref-total-seconds", type=float, default=120.0,
                     help="reference arm: about this many seconds of oracle time over all steps")
+    ap.add_argument("--ref-threads", type=int, default=0, help="reference arm threads (0: every host core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launch-check", action="store_true",
+                    help="check the multi-rank launch and reduction on CPU (gloo): each rank reports its "
+                         "workload's bytes and a stand-in time of rank + 1 ms; measures nothing")
     return ap.parse_args(argv)
+
+
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def relaunch(args, argv) -> int:
+    """--gpus N > 1 without a launcher: run this script under torch.distributed.run with N ranks
+    on this node (one per GPU), the same arguments, rendezvous on 127.0.0.1."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.abspath(__file__)]
+    cmd += list(sys.argv[1:] if argv is None else argv)
+    return subprocess.call(cmd)
+
+
+def run_launch_check(args) -> int:
+    """The multi-rank path without a GPU: process group over gloo, each rank's rank-seeded case,
+    the max/sum reduction, one line from rank 0 (value null: nothing is measured)."""
+    import torch.distributed as dist
+    world, rank, _ = dist_env()
+    if world > 1:
+        dist.init_process_group("gloo")
+    case = make_case(args.workload, args.seed + rank)
+    alg = float(algorithmic_bytes(case))
+    t, b = aggregate(float(rank + 1), alg * args.steps, world)
+    if rank == 0:
+        print(json.dumps({"launch_check": True, "metric": METRIC, "value": None, "n_gpus": world,
+                          "steps": args.steps, "max_rank_ms": t, "bytes_all_ranks": b,
+                          "config": line_config(args, case, world)}))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
 
 
 def main(argv=None):
     args = parse(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return relaunch(args, argv)
+    if args.launch_check:
+        return run_launch_check(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

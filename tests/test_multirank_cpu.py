@@ -72,3 +72,27 @@ def test_algorithmic_bytes_counts_valid_windows_only():
     assert bench.windows(case) == [(90, 10), (0, 0), (0, 0)]
     expect = 2 * 10 * 2 * 128 * 1 + 2 * 3 * 8 * 128 * 2 + 2 * case.antiquant_scale.nbytes
     assert bench.algorithmic_bytes(case) == expect
+
+
+def test_bench_gpus_flag_launches_ranks_and_reduces():
+    """`bench.py --gpus 2` without WORLD_SIZE relaunches itself under torch.distributed.run with two
+    ranks; with --launch-check each rank stands in for its GPU leg (its workload's bytes and a
+    time of rank + 1 ms), so the line checks the launch and the reduction: two ranks, the maximum
+    time, the bytes of both rank-seeded workloads summed."""
+    import json
+    import subprocess
+    import sys
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--launch-check",
+                          "--workload", "tiny_mha", "--steps", "7"], capture_output=True, text=True, cwd=root,
+                         env=env, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [json.loads(l) for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = lines[0]
+    assert line["launch_check"] is True and line["value"] is None
+    assert line["n_gpus"] == 2 and line["max_rank_ms"] == 2.0
+    expect = sum(bench.algorithmic_bytes(bench.make_case("tiny_mha", r)) for r in range(2)) * 7
+    assert line["bytes_all_ranks"] == expect
