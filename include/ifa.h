@@ -119,7 +119,8 @@ typedef struct ifa_plan ifa_plan;
  *   workspace_bytes out: device workspace every ifa_run on this plan needs
  * Returns IFA_ERR_PARAM_NULLPTR for NULL arguments, IFA_ERR_PARAM_INVALID for a
  * description outside the supported range, IFA_ERR_RUNTIME if the device
- * cannot be queried.  Allocates the plan and a 4-byte device error word.
+ * cannot be queried.  Allocates the plan and a small device block: the error
+ * word and the per-sequence arrival counters (zero between calls).
  */
 ifa_status ifa_create(const ifa_params* params, ifa_plan** plan, size_t* workspace_bytes);
 
@@ -154,6 +155,9 @@ ifa_status ifa_create(const ifa_params* params, ifa_plan** plan, size_t* workspa
  * Runs of one plan must not overlap on the GPU (they share the plan's per-sequence
  * arrival counters): use one plan per stream.  The call is one kernel launch and can be
  * captured in a CUDA graph; a captured call replays with the lengths it was captured with.
+ * Each call that runs to the end leaves the counters at zero (the last piece of a split
+ * sequence to arrive resets its counter), so captured and eager calls may be mixed and
+ * replayed in any order and number.
  */
 ifa_status ifa_run(ifa_plan* plan, const void* query, const void* key, const void* value,
                    const void* attenMask, const int64_t* actualSeqLengths,
@@ -191,7 +195,8 @@ ifa_status ifa_destroy(ifa_plan* plan);
 /*
  * Synchronise `stream`, return in *flags the device error bits accumulated by this
  * plan's runs since the last call (1: blockTable entry out of range, 2: a pipeline
- * wait timed out), and clear them.
+ * wait timed out), and clear them.  After bit 2 the arrival counters are cleared too
+ * (a run that gave up may have left some set); outputs of that run are undefined.
  */
 ifa_status ifa_get_device_errors(ifa_plan* plan, void* stream, int64_t* flags);
 
@@ -211,12 +216,12 @@ ifa_status ifa_get_device_errors(ifa_plan* plan, void* stream, int64_t* flags);
  * fixed array of IFA_NOALLOC_SCRATCH_BYTES in the library's device memory.  Every GPU
  * that loads the library holds that array until the process exits, and every call on
  * a device shares it and finds the previous call's contents there.  The partial
- * slots need no clearing.  The per-sequence arrival counters come in two sets: each
- * device keeps its own call number, a call counts in one set and its kernel clears
- * the other, which the next call on the same device uses; the number advances only
- * when a call's kernel was launched, so a call that returns an error leaves the next
- * call's set as it found it.  A kernel that started always clears that set, even
- * when it ends early on a device error.  Calls whose kernels overlap on the GPU (for
+ * slots need no clearing.  The per-sequence arrival counters start at zero when the
+ * library is loaded, and each call that runs to the end leaves them at zero (the last
+ * piece of a split sequence to arrive resets its counter), in any call order.  A call
+ * whose kernel gave up on a wait (error bit 2) may leave counters set, and nothing
+ * here can clear them: after that bit, results of later calls on that device are
+ * undefined until the process restarts.  Calls whose kernels overlap on the GPU (for
  * example on two streams) race on the array: serialise them.  The first call on
  * each device looks the array's address up (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.

@@ -47,7 +47,7 @@ struct alignas(128) DecodeParams {
     const void* aq_scale;
     const void* aq_offset;
     float* partials;           // 2 slots per CTA
-    unsigned int* counters;    // arrival counters [2][kMaxCtas]; a call uses set gen & 1
+    unsigned int* counters;    // arrival counters [kMaxCtas], zero between calls (the last arrival resets)
     int* err;
     const int32_t* ext_bdata;  // per-batch windows in global memory when B > kInlineB
     long long W;               // total tiles
@@ -69,7 +69,6 @@ struct alignas(128) DecodeParams {
     const void* q2_offset;     // nullable: 0
     float scale_log2;          // scaleValue * log2(e)
     int slot_floats;
-    unsigned int gen;          // call number: picks the counter set, and the set the call clears
     int bdata_inline[3 * kInlineB + 1];
     int bounds[kMaxCtas + 1];  // CTA c takes the tiles [bounds[c], bounds[c+1]), strictly increasing
 };

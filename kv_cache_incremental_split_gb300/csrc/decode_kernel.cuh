@@ -19,10 +19,13 @@
 // (no bank conflicts) and sum the fragments normalised by the piece's L.  A
 // piece that starts and ends inside the CTA is written to the output.  A
 // piece cut by a CTA boundary writes its normalised O with (M, L) per head to
-// the CTA's partial slot and bumps the sequence's arrival counter; the piece
-// that arrives last merges all pieces in piece order (deterministic, no float
-// atomics), so one launch finishes the call.  Counters come in two sets: a
-// call counts in set gen & 1 and clears the other set for the next call.
+// the CTA's partial slot and adds one to the sequence's arrival counter (a
+// release add, nothing to wait for); the CTA that holds the sequence's first
+// piece, which ends that CTA's range, waits for the others' arrivals and merges
+// all pieces in piece order (deterministic, no float atomics), so one launch
+// finishes the call.  The merging CTA also resets the counter, so every call
+// that runs to the end leaves all counters at zero for the next one, whatever
+// order calls are launched or replayed in.
 //
 // int8 key/value (antiquant): the per-channel key scale is folded into the
 // query (q'[d] = q[d] * scale_K[d]) and the key offset is dropped, because it
@@ -231,8 +234,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(aux + C::MERGE_BYTES + C::ML_BYTES + C::BD_BYTES + C::INFO_BYTES);
     uint64_t* empty = full + C::STAGES;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::STAGES);
-    volatile int* last_flag = abort_flag + 1;
-    volatile int* blkbuf = last_flag + 1;  // [8] block ids of the current tile's full boxes (producer)
+    volatile int* blkbuf = abort_flag + 2;  // [8] block ids of the current tile's full boxes (producer)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -271,7 +273,6 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
             mbar_init(&empty[s], NWC);
         }
         *abort_flag = 0;
-        *last_flag = 0;
         fence_mbar_init();
     }
     // Query buffers start (and stay) zero outside the rows/columns the bulk copies fill.
@@ -317,14 +318,6 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
     // Inputs, outputs and the workspace may belong to the previous kernel on the stream until it
     // has completed.
     pdl_wait_primary();
-
-    // The next call counts its arrivals in the other counter set: clear that set now
-    // (entry c by CTA c mod P), so no call depends on how an earlier one ended.
-    {
-        unsigned int* next_set = p.counters + ((p.gen + 1u) & 1u) * kMaxCtas;
-        for (long long c = blockIdx.x + (long long)threadIdx.x * p.P; c < kMaxCtas; c += (long long)C::THREADS * p.P)
-            next_set[c] = 0u;
-    }
 
     // Batches with no valid token produce all-zero rows; CTA c takes b = c, c+P, ...
     for (int b = blockIdx.x; b < B; b += p.P) {
@@ -900,13 +893,20 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
         }
         named_bar_sync(1, CONSUMERS);
 
-        // (3) sum the MW normalised fragments: the output of a whole sequence, or this
-        //     piece's partial (normalised O, with M and L per head) for the merge
+        // (3) sum the MW normalised fragments: the output of a whole sequence; for a sequence
+        //     that CTA boundaries cut, this piece's normalised O (with M and L per head): a
+        //     partial in the CTA's slot, or, for the sequence's first piece, kept in registers
+        //     for the merge below.  The first piece ends its CTA's range (the sequence runs on
+        //     past it), so the CTA that holds it merges: the other pieces start their CTAs'
+        //     ranges or fill them, and publish long before it finishes, as a rule.
+        const bool head = seq_first >= lo;
         const int slot = 2 * (int)blockIdx.x + (seq_first <= lo ? 0 : 1);
         float* sp = p.partials + (long long)slot * p.slot_floats;
+        float4 own[NPOS];
 #pragma unroll
         for (int n = 0; n < NPOS; ++n) {
             const int k = tid + n * CONSUMERS;
+            own[n] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (k < FRAG4 * 32) {
                 float4 o = mrg[k];
 #pragma unroll
@@ -921,59 +921,77 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                     for (int jj = 1; jj < NT; ++jj)
                         if (j == jj) l0 = Lh[jj][0], l1 = Lh[jj][1];
                     put(o, k, l0 > 0.f, l1 > 0.f, n);
+                } else if (head) {
+                    own[n] = o;
                 } else {
                     reinterpret_cast<float4*>(sp)[k] = o;
                 }
             }
         }
         if (!complete) {
-            if (warp == 0 && r == 0) {
-#pragma unroll
-                for (int j = 0; j < NT; ++j)
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        sp[GT_PAD * DPAD + 8 * j + 2 * q4 + u] = Mh[j][u];
-                        sp[GT_PAD * DPAD + GT_PAD + 8 * j + 2 * q4 + u] = Lh[j][u];
-                    }
-            }
-            // (4) arrive on the sequence's counter; the piece that arrives last merges all pieces
             const int c_first = cta_of(seq_first, sbounds, p.P);
             const int c_last = cta_of(seq_first + tiles - 1, sbounds, p.P);
-            const int npieces = c_last - c_first + 1;
-            named_bar_sync(1, CONSUMERS);
-            if (tid == 0) {
-                // release: this CTA's partial (written by every consumer thread before the barrier)
-                // is visible before the arrival; acquire: so are the partials of earlier arrivals
-                const unsigned int n =
-                    atom_add_acq_rel_gpu(p.counters + (p.gen & 1u) * kMaxCtas + c_first, 1u) + 1u;
-                *last_flag = n == (unsigned int)npieces;
-            }
-            named_bar_sync(1, CONSUMERS);
-            if (*last_flag) {
-                const long long lo_first = sbounds[c_first];
-                const int slot0 = 2 * c_first + (seq_first <= lo_first ? 0 : 1);
-                // the first two pieces' partial fragments do not depend on the weights: load them now
-                float4 pre[NPOS][2];
+            const int npieces = c_last - c_first + 1;  // >= 2: the sequence runs past a range end
+            unsigned int* ctr = p.counters + c_first;  // CTA c_first starts no other cut sequence
+            if (!head) {
+                // (4) publish: M and L beside the partial, then one release add on the sequence's
+                //     counter (the partial, written by every consumer thread before the barrier,
+                //     is visible before the add); nothing to wait for
+                if (warp == 0 && r == 0) {
+#pragma unroll
+                    for (int j = 0; j < NT; ++j)
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            sp[GT_PAD * DPAD + 8 * j + 2 * q4 + u] = Mh[j][u];
+                            sp[GT_PAD * DPAD + GT_PAD + 8 * j + 2 * q4 + u] = Lh[j][u];
+                        }
+                }
+                named_bar_sync(1, CONSUMERS);
+                if (tid == 0) red_add_release_gpu(ctr, 1u);
+            } else {
+                // (4) merge: wait until the other npieces - 1 pieces have published (acquire),
+                //     then weigh piece k by L_k 2^(M_k - M) / sum_j L_j 2^(M_j - M), in piece
+                //     order (this piece is piece 0); deterministic, no float atomics
+                float* pm = reinterpret_cast<float*>(mrg);  // [npieces][GT_PAD] M, then the head's total
+                float* pw = pm + npieces * GT_PAD;            // [npieces][GT_PAD] L, then the piece weights
+                named_bar_sync(1, CONSUMERS);                 // step (3) has read mrg
+                if (warp == 0 && r == 0) {
+#pragma unroll
+                    for (int j = 0; j < NT; ++j)
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            pm[8 * j + 2 * q4 + u] = Mh[j][u];
+                            pw[8 * j + 2 * q4 + u] = Lh[j][u];
+                        }
+                }
+                if (tid == 0) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (ld_acquire_gpu(ctr) != (unsigned int)(npieces - 1)) {
+                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                            record_error(p, kErrTimeout);
+                            break;
+                        }
+                    }
+                    // every other piece has arrived: no other access to the counter in this call,
+                    // so it goes back to zero for the next call (read after this grid completes)
+                    *reinterpret_cast<volatile unsigned int*>(ctr) = 0u;
+                }
+                named_bar_sync(1, CONSUMERS);
+                // pieces 1.. start the ranges of CTAs c_first + 1, ...: slot 0 of each
+                auto slot_of = [&](int k) { return p.partials + (long long)(2 * (c_first + k)) * p.slot_floats; };
+                // piece 1's fragments do not depend on the weights: load them now
+                float4 pre1[NPOS];
 #pragma unroll
                 for (int n = 0; n < NPOS; ++n) {
                     const int k = tid + n * CONSUMERS;
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        pre[n][t] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (k < FRAG4 * 32 && t < npieces) {
-                            const int sl = t == 0 ? slot0 : 2 * (c_first + t);
-                            pre[n][t] = __ldcg(reinterpret_cast<const float4*>(p.partials + (long long)sl * p.slot_floats) + k);
-                        }
-                    }
+                    pre1[n] = k < FRAG4 * 32 ? __ldcg(reinterpret_cast<const float4*>(slot_of(1)) + k)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                float* pm = reinterpret_cast<float*>(mrg);  // [npieces][GT_PAD] M, then the head's total
-                float* pw = pm + npieces * GT_PAD;            // [npieces][GT_PAD] L, then the piece weights
-                for (int x2 = tid; x2 < npieces * GT_PAD; x2 += CONSUMERS) {
-                    const int k = x2 / GT_PAD, gg = x2 % GT_PAD;
-                    const int sl = k == 0 ? slot0 : 2 * (c_first + k);
-                    const float* pp = p.partials + (long long)sl * p.slot_floats + GT_PAD * DPAD;
-                    pm[x2] = __ldcg(pp + gg);
-                    pw[x2] = __ldcg(pp + GT_PAD + gg);
+                for (int x2 = tid; x2 < (npieces - 1) * GT_PAD; x2 += CONSUMERS) {
+                    const int k = 1 + x2 / GT_PAD, gg = x2 % GT_PAD;
+                    const float* pp = slot_of(k) + GT_PAD * DPAD;
+                    pm[k * GT_PAD + gg] = __ldcg(pp + gg);
+                    pw[k * GT_PAD + gg] = __ldcg(pp + GT_PAD + gg);
                 }
                 named_bar_sync(1, CONSUMERS);
                 if (tid < GT_PAD) {
@@ -996,22 +1014,19 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                     const int k = tid + n * CONSUMERS;
                     if (k < FRAG4 * 32) {
                         const int gg0 = 8 * ((k >> 5) % NT) + 2 * (k & 3);
-                        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                        for (int t = 0; t < 2; ++t) {
-                            if (t < npieces) {
-                                const float w0 = pw[t * GT_PAD + gg0], w1 = pw[t * GT_PAD + gg0 + 1];
-                                o.x += w0 * pre[n][t].x; o.y += w1 * pre[n][t].y; o.z += w0 * pre[n][t].z; o.w += w1 * pre[n][t].w;
-                            }
+                        float4 o;
+                        {
+                            const float w0 = pw[gg0], w1 = pw[gg0 + 1];
+                            const float v0 = pw[GT_PAD + gg0], v1 = pw[GT_PAD + gg0 + 1];
+                            o = make_float4(w0 * own[n].x + v0 * pre1[n].x, w1 * own[n].y + v1 * pre1[n].y,
+                                            w0 * own[n].z + v0 * pre1[n].z, w1 * own[n].w + v1 * pre1[n].w);
                         }
                         int pc = 2;
                         for (; pc + 4 <= npieces; pc += 4) {
                             float4 v[4];
 #pragma unroll
-                            for (int t = 0; t < 4; ++t) {
-                                const int sl = pc + t == 0 ? slot0 : 2 * (c_first + pc + t);
-                                v[t] = __ldcg(reinterpret_cast<const float4*>(p.partials + (long long)sl * p.slot_floats) + k);
-                            }
+                            for (int t = 0; t < 4; ++t)
+                                v[t] = __ldcg(reinterpret_cast<const float4*>(slot_of(pc + t)) + k);
 #pragma unroll
                             for (int t = 0; t < 4; ++t) {
                                 const float w0 = pw[(pc + t) * GT_PAD + gg0], w1 = pw[(pc + t) * GT_PAD + gg0 + 1];
@@ -1019,8 +1034,7 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
                             }
                         }
                         for (; pc < npieces; ++pc) {
-                            const int sl = pc == 0 ? slot0 : 2 * (c_first + pc);
-                            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.partials + (long long)sl * p.slot_floats) + k);
+                            const float4 v = __ldcg(reinterpret_cast<const float4*>(slot_of(pc)) + k);
                             const float w0 = pw[pc * GT_PAD + gg0], w1 = pw[pc * GT_PAD + gg0 + 1];
                             o.x += w0 * v.x; o.y += w1 * v.y; o.z += w0 * v.z; o.w += w1 * v.w;
                         }

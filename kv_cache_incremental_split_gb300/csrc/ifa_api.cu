@@ -20,8 +20,7 @@ struct ifa_plan {
     KernelChoice kc;
     int num_sms, P_max, device;
     size_t partial_bytes, ws_bytes;
-    int* d_state;  // [0]: device error word; from byte 8 on: two sets of kMaxCtas arrival counters
-    unsigned int gen;
+    int* d_state;  // [0]: device error word; from byte 8 on: kMaxCtas arrival counters
     const void* last_k;
     const void* last_v;
     const void* last_mask;
@@ -70,7 +69,7 @@ extern "C" ifa_status ifa_create(const ifa_params* params, ifa_plan** plan, size
     pl->partial_bytes = align_up((size_t)2 * pl->P_max * kc.slot_floats * sizeof(float), 256);
     pl->ws_bytes = pl->partial_bytes;
     if (params->B > kInlineB) pl->ws_bytes += align_up((size_t)(3 * params->B + 1) * sizeof(int32_t), 256);
-    const size_t state_bytes = 8 + (size_t)2 * kMaxCtas * sizeof(unsigned int);
+    const size_t state_bytes = 8 + (size_t)kMaxCtas * sizeof(unsigned int);
     if (cudaMalloc(&pl->d_state, state_bytes) != cudaSuccess ||
         cudaMemset(pl->d_state, 0, state_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -85,7 +84,6 @@ extern "C" ifa_status ifa_create(const ifa_params* params, ifa_plan** plan, size
     }
     pl->last_k = pl->last_v = pl->last_mask = nullptr;
     pl->last_launches = 0;
-    pl->gen = 0;
     pl->d_maps = nullptr;
     if (params->kvFormat == IFA_KV_TENSORLIST && params->B > 0) {
         if (cudaMalloc(&pl->d_maps, (size_t)4 * params->B * sizeof(CUtensorMap)) != cudaSuccess) {
@@ -121,7 +119,10 @@ extern "C" ifa_status ifa_get_device_errors(ifa_plan* plan, void* stream, int64_
         cudaGetLastError();
         return IFA_ERR_RUNTIME;
     }
-    if (cudaMemsetAsync(plan->d_state, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
+    // A call that gave up on a wait (bit 2) may have left arrival counters behind: clear them
+    // with the error word, so the next call starts from zero counters again.
+    const size_t clear = (h & kErrTimeout) ? 8 + (size_t)kMaxCtas * sizeof(unsigned int) : sizeof(int);
+    if (cudaMemsetAsync(plan->d_state, 0, clear, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return IFA_ERR_RUNTIME;
     }
@@ -175,10 +176,6 @@ static ifa_status run_planned(ifa_plan* pl, const void* query, const void* key, 
     dp.partials = reinterpret_cast<float*>(workspace);
     dp.err = pl->d_state;
     dp.counters = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(pl->d_state) + 8);
-    // Wraps: consecutive launched calls alternate the counter set.  The plan's call number
-    // advances only once the kernel is launched (below): a call whose launch failed cleared
-    // nothing, so the next call counts in the set this one would have used.
-    dp.gen = pl->gen + 1u;
     if (B <= kInlineB) {
         std::memcpy(dp.bdata_inline, bd.data(), bd.size() * sizeof(int32_t));
         dp.ext_bdata = nullptr;
@@ -195,7 +192,6 @@ static ifa_status run_planned(ifa_plan* pl, const void* query, const void* key, 
         cudaGetLastError();
         return IFA_ERR_RUNTIME;
     }
-    pl->gen = dp.gen;
     pl->last_launches = 1;
     return IFA_OK;
 }

@@ -21,44 +21,35 @@ using namespace ifa;
 namespace {
 
 constexpr size_t kScratchBytes = IFA_NOALLOC_SCRATCH_BYTES;
-// Layout of the scratch: [0, 256) device error word; [256, 256 + 8*kMaxCtas) two sets of
-// arrival counters (a call counts in set gen & 1 and clears the other set for the next
-// call, so whatever an aborted call left behind is gone two calls later); from
-// kPartialOffset on, the partial slots.
+// Layout of the scratch: [0, 256) device error word; [256, 256 + 4*kMaxCtas) the arrival
+// counters (zero at load time; the last arrival of each cut sequence resets its counter, so
+// every call that runs to the end leaves them at zero); from kPartialOffset on, the partial
+// slots.
 constexpr size_t kCounterOffset = 256;
 constexpr size_t kPartialOffset = 4096;
-static_assert(kCounterOffset + 2 * sizeof(unsigned int) * kMaxCtas <= kPartialOffset, "scratch layout");
+static_assert(kCounterOffset + sizeof(unsigned int) * kMaxCtas <= kPartialOffset, "scratch layout");
 constexpr int kMaxDevices = 64;
 
 // The scratch every ifa_run_noalloc call on a device shares.  In host code this
 // name is only a stand-in; the device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-// Per-device state: the scratch array's device address, looked up once per device (the
-// first call on a device does this set-up), and the device's call number, which picks the
-// counter set a call counts in.  Each device alternates its own two sets: a call clears the
-// set the next call on the same device will use, so the number must advance per device.
-struct DeviceSlot {
-    unsigned char* addr = nullptr;
-    unsigned int gen = 0;
-};
-
-std::mutex g_mu;
-DeviceSlot g_dev[kMaxDevices];
-
+// Device address of the scratch array on the current device, looked up once per device (the
+// first call on a device does this set-up).
 unsigned char* scratch_on_current_device(int device) {
+    static std::mutex mu;
+    static unsigned char* addr[kMaxDevices] = {};
     if (device < 0 || device >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_mu);
-    DeviceSlot& d = g_dev[device];
-    if (!d.addr) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[device]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
             cudaGetLastError();
             return nullptr;
         }
-        d.addr = static_cast<unsigned char*>(p);
+        addr[device] = static_cast<unsigned char*>(p);
     }
-    return d.addr;
+    return addr[device];
 }
 
 }  // namespace
@@ -114,15 +105,9 @@ extern "C" ifa_status ifa_run_noalloc(const ifa_params* params, const void* quer
     dp.counters = reinterpret_cast<unsigned int*>(scratch + kCounterOffset);
     dp.err = deviceErrorFlags ? deviceErrorFlags : reinterpret_cast<int*>(scratch);
     dp.ext_bdata = nullptr;
-    // The device's call number advances only when the kernel was launched: a launch that failed
-    // cleared nothing, so the next call must count in the set this one would have used.  (The
-    // number wraps; consecutive launched calls on a device alternate the counter set.)
-    std::lock_guard<std::mutex> lock(g_mu);
-    dp.gen = g_dev[device].gen + 1u;
     if (kc.launch(dp, P, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return IFA_ERR_RUNTIME;
     }
-    g_dev[device].gen = dp.gen;
     return IFA_OK;
 }

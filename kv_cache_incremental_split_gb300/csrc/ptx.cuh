@@ -121,6 +121,17 @@ __device__ __forceinline__ unsigned int atom_add_acq_rel_gpu(unsigned int* addr,
     return old;
 }
 
+// Adds v at addr with release semantics at GPU scope; returns nothing (no round trip to wait for).
+__device__ __forceinline__ void red_add_release_gpu(unsigned int* addr, unsigned int v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* addr) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -121,6 +121,38 @@ def test_split_invariance_and_run_to_run_determinism():
     assert max_abs_err(outs[0], outs[5]) <= TOL["bf16"]
 
 
+def test_graph_replays_of_odd_call_counts_with_eager_calls_between():
+    """Pieces of a cut sequence meet on a per-sequence arrival counter that all calls of a plan
+    share, so every call that completes must leave the counters at zero, whatever mix of graph
+    replays and eager calls follows: a graph of three calls (an odd count), replayed three
+    times with an eager call after each replay, every sequence cut into pieces."""
+    kw = dict(B=4, N=16, KV_N=4, D=128, Smax=1500, layout="BSH", dtype="bf16")
+    ca, cb = gen.gqa_padded(31, **kw), gen.gqa_padded(32, **kw)
+    da, db = DeviceCase(ca), DeviceCase(cb)
+    op = make_op(ca, split_tiles=3)
+    refa, refb = oracle_ifa(ca), oracle_ifa(cb)
+    outs = [torch.full_like(da.q, float("nan")) for _ in range(3)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        da.run(op, out=outs[0], stream=s)  # eager first call: the plan's workspace exists before capture
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            da.run(op, out=outs[0], stream=s)
+            db.run(op, out=outs[1], stream=s)
+            da.run(op, out=outs[2], stream=s)
+        for rep in range(3):
+            for o in outs:
+                o.fill_(float("nan"))
+            g.replay()
+            eager = db.run(op, stream=s)
+            s.synchronize()
+            for got, ref in ((outs[0], refa), (outs[1], refb), (outs[2], refa), (eager, refb)):
+                got = out_to_f64(got).reshape(ref.shape)
+                assert np.all(np.isfinite(got)), rep
+                assert max_abs_err(got, ref) <= TOL["bf16"], rep
+
+
 # ---------------------------------------------------------------- edge cases
 
 def test_head_groupings():
