@@ -245,7 +245,7 @@ class ClockSampler:
 
 def kernel_sources_digest(family: str) -> str:
     """Digest of the sources that decide one kernel family's DRAM traffic: "decode" (the
-    split-KV decode kernel, its planner and API) or "sfa" (the sparse decode and combine
+    split-KV decode kernel, its planner and API) or "sfa" (the sparse tile-count, decode and combine
     kernels, their API, and the shared constants and PTX helpers)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kv_cache_incremental_split_gb300", "csrc")
@@ -640,7 +640,7 @@ class SfaWorkload:
                        out=self.outs[i], stream=stream)
 
     def launches_per_call(self):
-        return 3  # tile-count kernel, decode kernel (cluster pairs), combine kernel
+        return 3  # tile-count kernel, decode kernel (CTA pairs), combine kernel
 
     def host_inputs(self):
         c = self.case

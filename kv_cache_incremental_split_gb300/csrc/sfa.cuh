@@ -27,15 +27,14 @@ constexpr int kSfaSlotFloats = 128 * kSfaHalf + 3 * 128;  // normalised O of one
 constexpr int kSfaBarBytes = 512;
 constexpr int kSfaSmem = 1024 + kSfaQBytes + kSfaStages * kSfaStageBytes + kSfaRSlots * kSfaRSlotBytes + kSfaBarBytes;
 // workspace: [0, 256) error word; [kSfaStartOffset, + 32 * kMaxCtas) each pair's start (SfaStart);
-// partial slots from kSfaPartialOffset; then live tiles per query row (R ints) and their prefix
-// over rows (R + 1 ints)
+// partial slots from kSfaPartialOffset; then live tiles per query row (R ints), their prefix
+// over rows (R + 1 ints) and, 16-byte aligned, the pieces of each row (R SfaPieces)
 constexpr size_t kSfaStartOffset = 1024;
 constexpr size_t kSfaPartialOffset = 16384;
 constexpr int kSfaCountCtas = 8;        // the tile-count kernel: one cluster
 constexpr int kSfaCountThreads = 512;
 constexpr int kSfaCountSmemRows = 4096;  // rows whose counts the count kernel scans in shared memory
 constexpr float kSfaRescaleSlack = 8.0f;    // log2 units the running max may trail before O is rescaled
-constexpr int kSfaCombineRows = 16;         // query heads per combine CTA
 constexpr float kLn2 = 0.6931471805599453f;  // scores in log2 units -> natural units
 
 // Where a CTA of the decode kernel starts: tiles [lo, hi) of the live-tile order, the first
@@ -45,6 +44,13 @@ struct SfaStart {
     int lo, hi, r, h, t, n, first, pad;
 };
 static_assert(sizeof(SfaStart) == 32, "start table entry");
+
+// Where the pieces of query row r's two sequences sit: pairs c_first .. c_first + np - 1 (np = 0
+// for a row with no live tile, 1 for a row one pair holds whole); the first piece's partial
+// slot within its CTA (0 when the row starts that pair's share, else 1).
+struct alignas(16) SfaPieces {
+    int c_first, np, slot0, pad;
+};
 
 struct alignas(128) SfaParams {
     CUtensorMap tmQ;    // 3-D (d, head, query row) over query, 64 x 128 x 1 boxes
@@ -67,6 +73,7 @@ struct alignas(128) SfaParams {
     SfaStart* starts;   // per CTA, written by the tile-count kernel
     int* eff;           // live tiles of each query row (a sequence's tiles), 0 when no index is usable
     int* pre;           // prefix over rows of eff (R + 1 entries): the tile order of the decode kernel's pairs
+    SfaPieces* pieces;  // per query row, written by the tile-count kernel for the combine kernel
     long long W;        // tiles before the count: R * tiles_per_seq (an upper bound)
     int P;              // CTAs: an even count; CTAs 2c and 2c + 1 (the two value halves) form pair c
     int R, QS, QN, S_sp, tiles_per_seq;  // R query rows: B * QS (row r: batch r / QS, query token r % QS), or

@@ -107,7 +107,7 @@ extern "C" ifa_status sfa_workspace_size(const sfa_params* params, size_t* works
     const int P_max = std::min(kMaxCtas, sms);
     const int64_t R = params->layout_query == SFA_LAYOUT_TND ? params->Q_T : params->B * params->Q_S;
     *workspace_bytes = kSfaPartialOffset + (size_t)2 * P_max * kSfaSlotFloats * sizeof(float) +
-                       ((size_t)(2 * R + 1) * sizeof(int) + 15) / 16 * 16;
+                       ((size_t)(2 * R + 1) * sizeof(int) + 15) / 16 * 16 + (size_t)R * sizeof(SfaPieces);
     return IFA_OK;
 }
 
@@ -199,6 +199,8 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
     sp.starts = reinterpret_cast<SfaStart*>(ws + kSfaStartOffset);
     sp.eff = reinterpret_cast<int*>(ws + kSfaPartialOffset + (size_t)2 * P_max * kSfaSlotFloats * sizeof(float));
     sp.pre = sp.eff + R;
+    sp.pieces = reinterpret_cast<SfaPieces*>(reinterpret_cast<unsigned char*>(sp.eff) +
+                                             ((size_t)(2 * R + 1) * sizeof(int) + 15) / 16 * 16);
     sp.err = deviceErrorFlags ? deviceErrorFlags : reinterpret_cast<int*>(ws);
     sp.W = W;
     sp.P = P;

@@ -821,7 +821,8 @@ __global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_const
     const bool in_smem = R <= kSfaCountSmemRows;
     int* eff0 = cluster.map_shared_rank(s_eff, 0);  // the first CTA's copy
     const int idx_max = INT32_MAX >> p.sbs_log2;
-    // rows of whole 16-byte groups: 4 entries per load, 8 loads in flight per lane
+    // rows of whole 16-byte groups: 4 entries per load, up to 16 loads in flight per lane (a row
+    // of 2048 indices in one round trip)
     const bool vec = (p.S_sp & 3) == 0 && (reinterpret_cast<uintptr_t>(p.indices) & 15) == 0;
     for (int r = blockIdx.x * NW + warp; r < R; r += gridDim.x * NW) {
         const int32_t* row = p.indices + (long long)r * p.S_sp;
@@ -829,7 +830,7 @@ __global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_const
         if (vec) {
             const int4* row4 = reinterpret_cast<const int4*>(row);
             const int n4 = p.S_sp >> 2;
-#pragma unroll 8
+#pragma unroll 16
             for (int j = lane; j < n4; j += 32) {
                 const int4 v = __ldg(row4 + j);
                 if (v.x >= 0 && v.x <= idx_max) last = 4 * j;
@@ -927,60 +928,101 @@ __global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_const
         }
         p.starts[c] = st;
     }
+    // for the combine kernel: where each row's pieces sit (one record instead of a search)
+    for (int r = threadIdx.x; r < R; r += kSfaCountThreads) {
+        const long long g0 = pre_of(r);
+        const int n = eff_of(r);
+        SfaPieces pc;
+        pc.c_first = pc.np = pc.slot0 = pc.pad = 0;
+        if (n > 0) {
+            pc.c_first = cta_of_tile(g0, Wl, Pa);
+            pc.np = cta_of_tile(g0 + n - 1, Wl, Pa) - pc.c_first + 1;
+            pc.slot0 = g0 <= (long long)pc.c_first * Wl / Pa ? 0 : 1;
+        }
+        p.pieces[r] = pc;
+    }
 }
 
-// Merges the pieces of every sequence that CTA boundaries cut: grid (2R sequences,
-// 128 / kSfaCombineRows), 128 threads; thread = (head row, 32 channels).  Piece k
-// weighs L_k 2^(M_k - M) / sum_j L_j 2^(M_j - M) with M the largest M_k.
+// Merges the pieces of every sequence that CTA boundaries cut: grid (2R sequences, 16 blocks
+// of 8 head rows), 128 threads; thread = (head row, 16 channels).  Piece k weighs
+// L_k 2^(M_k - M) / sum_j L_j 2^(M_j - M) with M the largest M_k.  One record from the count
+// kernel says where the pieces sit; then every piece's M, L and channels are loaded at once.
 __global__ void __launch_bounds__(128) sfa_combine(const __grid_constant__ SfaParams p) {
+    constexpr int kCh = 16;                          // channels per thread
+    constexpr int kTpr = kSfaHalf / kCh;             // threads per head row
+    constexpr int kMaxFast = 4;                      // pieces loaded together
     const int s = blockIdx.x;
-    const int row = blockIdx.y * kSfaCombineRows + (threadIdx.x >> 3);
-    const int col0 = (threadIdx.x & 7) * 32;
     const int b = s >> 1, h = s & 1;
-    const int n = __ldcg(p.eff + b);
-    if (n == 0) return;  // the count kernel wrote this row
-    // pairs c_first..c_last hold the row's tiles; CTA 2c + h of pair c holds value half h
-    const long long Wl = __ldcg(p.pre + p.R);
-    const int Pa = active_ctas(Wl, p.P >> 1, p.tiles_per_seq);
-    const long long g0 = __ldcg(p.pre + b);
-    const int c_first = cta_of_tile(g0, Wl, Pa);
-    const int c_last = cta_of_tile(g0 + n - 1, Wl, Pa);
-    if (c_first == c_last) return;  // the decode kernel wrote this sequence
+    const SfaPieces pc = p.pieces[b];
+    if (pc.np < 2) return;  // the count kernel or the decode kernel wrote this sequence
+    const int row = blockIdx.y * (128 / kTpr) + (int)threadIdx.x / kTpr;
+    const int col0 = ((int)threadIdx.x % kTpr) * kCh;
     if (row >= p.QN) return;
-    const long long lo_first = (long long)c_first * Wl / Pa;
-    const int slot0 = 2 * (2 * c_first + h) + (g0 <= lo_first ? 0 : 1);
-    const int np = c_last - c_first + 1;
+    const int np = pc.np;
+    // pairs c_first .. c_first + np - 1 hold the row's tiles; CTA 2c + h of pair c value half h
     auto slot_ptr = [&](int k) {
-        const int sl = k == 0 ? slot0 : 2 * (2 * (c_first + k) + h);
+        const int sl = k == 0 ? 2 * (2 * pc.c_first + h) + pc.slot0 : 2 * (2 * (pc.c_first + k) + h);
         return p.partials + (long long)sl * kSfaSlotFloats;
     };
-    float M = -INFINITY;
-    for (int k = 0; k < np; ++k) M = fmaxf(M, __ldcg(slot_ptr(k) + 128 * kSfaHalf + row));
-    float acc[32];
+    float acc[kCh];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+    for (int j = 0; j < kCh; ++j) acc[j] = 0.f;
     float S = 0.f;
-    for (int k = 0; k < np; ++k) {
-        const float* pp = slot_ptr(k);
-        const float mk = __ldcg(pp + 128 * kSfaHalf + row);
-        const float lk = __ldcg(pp + 128 * kSfaHalf + 128 + row);
-        float4 v[8];
+    if (np <= kMaxFast) {
+        float m[kMaxFast], l[kMaxFast];
+        float4 v[kMaxFast][kCh / 4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            v[j] = __ldcg(reinterpret_cast<const float4*>(pp + (long long)row * kSfaHalf + col0) + j);
-        const float w = mk == -INFINITY ? 0.f : lk * ex2f_approx(mk - M);
-        S += w;
+        for (int k = 0; k < kMaxFast; ++k) {
+            m[k] = -INFINITY;
+            l[k] = 0.f;
+            if (k < np) {
+                const float* pp = slot_ptr(k);
+                m[k] = __ldcg(pp + 128 * kSfaHalf + row);
+                l[k] = __ldcg(pp + 128 * kSfaHalf + 128 + row);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            acc[4 * j] += w * v[j].x;
-            acc[4 * j + 1] += w * v[j].y;
-            acc[4 * j + 2] += w * v[j].z;
-            acc[4 * j + 3] += w * v[j].w;
+                for (int j = 0; j < kCh / 4; ++j)
+                    v[k][j] = __ldcg(reinterpret_cast<const float4*>(pp + (long long)row * kSfaHalf + col0) + j);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kCh / 4; ++j) v[k][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float M = m[0];
+#pragma unroll
+        for (int k = 1; k < kMaxFast; ++k) M = fmaxf(M, m[k]);
+#pragma unroll
+        for (int k = 0; k < kMaxFast; ++k) {
+            const float w = m[k] == -INFINITY ? 0.f : l[k] * ex2f_approx(m[k] - M);
+            S += w;
+#pragma unroll
+            for (int j = 0; j < kCh / 4; ++j) {
+                acc[4 * j] += w * v[k][j].x;
+                acc[4 * j + 1] += w * v[k][j].y;
+                acc[4 * j + 2] += w * v[k][j].z;
+                acc[4 * j + 3] += w * v[k][j].w;
+            }
+        }
+    } else {
+        float M = -INFINITY;
+        for (int k = 0; k < np; ++k) M = fmaxf(M, __ldcg(slot_ptr(k) + 128 * kSfaHalf + row));
+        for (int k = 0; k < np; ++k) {
+            const float* pp = slot_ptr(k);
+            const float mk = __ldcg(pp + 128 * kSfaHalf + row);
+            const float w = mk == -INFINITY ? 0.f : __ldcg(pp + 128 * kSfaHalf + 128 + row) * ex2f_approx(mk - M);
+            S += w;
+#pragma unroll
+            for (int j = 0; j < kCh / 4; ++j) {
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(pp + (long long)row * kSfaHalf + col0) + j);
+                acc[4 * j] += w * x.x;
+                acc[4 * j + 1] += w * x.y;
+                acc[4 * j + 2] += w * x.z;
+                acc[4 * j + 3] += w * x.w;
+            }
         }
     }
     const float inv = S > 0.f ? 1.f / S : 0.f;
     const bool bf = p.is_bf16 != 0;
-    if (p.lse_max && h == 0 && (threadIdx.x & 7) == 0) {
+    if (p.lse_max && h == 0 && col0 == 0) {
         float Mt = -INFINITY;
         for (int k = 0; k < np; ++k) Mt = fmaxf(Mt, __ldcg(slot_ptr(k) + 128 * kSfaHalf + 256 + row));
         float St = 0.f;
@@ -993,13 +1035,13 @@ __global__ void __launch_bounds__(128) sfa_combine(const __grid_constant__ SfaPa
         p.lse_max[li] = Mt == -INFINITY ? -INFINITY : Mt * kLn2;
         p.lse_sum[li] = Mt == -INFINITY ? 0.f : St;
     }
-    uint32_t wv[16];
+    uint32_t wv[kCh / 2];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) wv[j] = pack2(acc[2 * j] * inv, acc[2 * j + 1] * inv, bf);
+    for (int j = 0; j < kCh / 2; ++j) wv[j] = pack2(acc[2 * j] * inv, acc[2 * j + 1] * inv, bf);
     uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + ((long long)b * p.QN + row) * kSfaD +
                                           h * kSfaHalf + col0);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) dst[j] = make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
+    for (int j = 0; j < kCh / 8; ++j) dst[j] = make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
 }
 
 int sfa_max_pairs() {
@@ -1053,7 +1095,7 @@ cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     // An ordinary launch: with programmatic dependent launch (resident early, waiting) the
     // combine cost the sparse MLA workload 18 us per call on this part.
-    sfa_combine<<<dim3(2 * p.R, 128 / kSfaCombineRows), 128, 0, stream>>>(p);
+    sfa_combine<<<dim3(2 * p.R, kSfaHalf / 16), 128, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
