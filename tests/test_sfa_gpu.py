@@ -362,3 +362,33 @@ def test_sfa_selected_set_exact_on_split_rows(Q_S, mode):
     assert np.array_equal(sm[rows_sel], rsm.reshape(len(rows_sel), -1).astype(np.float32).astype(np.float64))
     assert np.abs(mx[rows_sel] - rmx.reshape(len(rows_sel), -1)).max() <= 1e-6
     assert max_abs_err(got[bsel], ref) <= TOL[c.dtype]
+
+
+def test_sfa_value_aliases_key():
+    """`value` may be the same tensor as `key` (one cache serves both, as in MLA-absorb decode):
+    the kernel reads the value half from the key rows; checked against the oracle given the same
+    array for both, on a small case with split rows and on sampled rows of the full-size shape."""
+    c = gen.sfa_mla(11, B=2, Q_N=128, block_size=64, kv_len=8192, sparse_size=2048, nvalid_lo=1500,
+                    nvalid_hi=2048)
+    c.value = c.key
+    op = sfa_op(c)
+    q, qr, k, kr, idx = (to_device(a) for a in (c.query, c.query_rope, c.key, c.key_rope, c.sparse_indices))
+    out = op(q, qr, k, kr, k, idx, to_device(c.block_table), to_device(c.actual_seq_lengths_kv))
+    torch.cuda.synchronize()
+    got = out_to_f64(out).reshape(c.B, c.query.shape[2], 512)
+    ref = run_ref(c)
+    assert np.all(np.isfinite(got)) and max_abs_err(got, ref) <= TOL[c.dtype]
+    assert op.device_errors() == 0
+
+
+def test_sfa_value_aliases_key_full_size_sampled():
+    c = gen.sfa_mla(12)
+    c.value = c.key
+    op = sfa_op(c)
+    q, qr, k, kr, idx = (to_device(a) for a in (c.query, c.query_rope, c.key, c.key_rope, c.sparse_indices))
+    out = op(q, qr, k, kr, k, idx, to_device(c.block_table), to_device(c.actual_seq_lengths_kv))
+    torch.cuda.synchronize()
+    got = out_to_f64(out).reshape(c.B, c.query.shape[2], 512)
+    bsel = np.array([0, 13, 31])
+    ref = run_ref(c, batches=bsel)
+    assert max_abs_err(got[bsel], ref) <= TOL[c.dtype]
