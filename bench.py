@@ -392,9 +392,13 @@ def host_threads() -> int:
         return max(1, os.cpu_count() or 1)
 
 
+ORACLE_MAX_PASSES = 64  # a small workload's sample stops after this many passes over its rows
+
+
 def oracle_sample(case, budget_s: float, threads: int = 1, start_batch: int = 0):
     """Time the CPU oracle on whole batch rows of the workload for about `budget_s` seconds of
-    wall time, `threads` threads taking rows in turn (the C oracle runs without the GIL).
+    wall time (or ORACLE_MAX_PASSES passes over the rows), `threads` threads taking rows in
+    turn (the C oracle runs without the GIL).
     Returns (algorithmic bytes done, wall seconds, rows done in order)."""
     import threading
     from concurrent.futures import ThreadPoolExecutor
@@ -406,7 +410,8 @@ def oracle_sample(case, budget_s: float, threads: int = 1, start_batch: int = 0)
         first = True
         while True:
             with lock:
-                if not first and (time.perf_counter() - t0 >= budget_s or len(state["done"]) >= 64 * case.B):
+                if not first and (time.perf_counter() - t0 >= budget_s or
+                                  len(state["done"]) >= ORACLE_MAX_PASSES * case.B):
                     return
                 b = state["next"] % case.B
                 state["next"] += 1
@@ -434,9 +439,9 @@ def cpu_baseline_legs(case, budget_s: float):
     nmax = max(legs)
     v, nb, t, rows = legs[nmax]
     return {"value": v, "unit": UNIT, "cores": nmax, "kind": "oracle",
-            "sample": (f"whole batch rows of the same workload, taken in turn by {nmax} threads for about "
-                       f"{budget_s:.0f} s ({rows} rows, {nb / 1e6:.1f} MB algorithmic, {t:.1f} s wall); "
-                       f"plain C, float64"),
+            "sample": (f"whole batch rows of the same workload, taken in turn by {nmax} threads until about "
+                       f"{budget_s:.0f} s or {ORACLE_MAX_PASSES} passes over the batch rows, whichever comes "
+                       f"first ({rows} rows, {nb / 1e6:.1f} MB algorithmic, {t:.2f} s wall); plain C, float64"),
             "by_threads": {str(th): {"value": lv, "rows": lr, "seconds": round(lt, 2)}
                            for th, (lv, _, lt, lr) in legs.items()}}
 
