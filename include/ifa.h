@@ -155,8 +155,8 @@ ifa_status ifa_create(const ifa_params* params, ifa_plan** plan, size_t* workspa
  * Runs of one plan must not overlap on the GPU (they share the plan's per-sequence
  * arrival counters): use one plan per stream.  The call is one kernel launch and can be
  * captured in a CUDA graph; a captured call replays with the lengths it was captured with.
- * Each call that runs to the end leaves the counters at zero (the last piece of a split
- * sequence to arrive resets its counter), so captured and eager calls may be mixed and
+ * Each call that runs to the end leaves the counters at zero (the CTA that merges a split
+ * sequence resets its counter once the other pieces have arrived), so captured and eager calls may be mixed and
  * replayed in any order and number.
  */
 ifa_status ifa_run(ifa_plan* plan, const void* query, const void* key, const void* value,
@@ -217,8 +217,8 @@ ifa_status ifa_get_device_errors(ifa_plan* plan, void* stream, int64_t* flags);
  * that loads the library holds that array until the process exits, and every call on
  * a device shares it and finds the previous call's contents there.  The partial
  * slots need no clearing.  The per-sequence arrival counters start at zero when the
- * library is loaded, and each call that runs to the end leaves them at zero (the last
- * piece of a split sequence to arrive resets its counter), in any call order.  A call
+ * library is loaded, and each call that runs to the end leaves them at zero (the CTA
+ * that merges a split sequence resets its counter), in any call order.  A call
  * whose kernel gave up on a wait (error bit 2) may leave counters set, and nothing
  * here can clear them: after that bit, results of later calls on that device are
  * undefined until the process restarts.  Calls whose kernels overlap on the GPU (for

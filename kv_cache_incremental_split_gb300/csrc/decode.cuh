@@ -47,7 +47,7 @@ struct alignas(128) DecodeParams {
     const void* aq_scale;
     const void* aq_offset;
     float* partials;           // 2 slots per CTA
-    unsigned int* counters;    // arrival counters [kMaxCtas], zero between calls (the last arrival resets)
+    unsigned int* counters;    // arrival counters [kMaxCtas], zero between calls (the merging CTA resets)
     int* err;
     const int32_t* ext_bdata;  // per-batch windows in global memory when B > kInlineB
     long long W;               // total tiles
@@ -107,7 +107,7 @@ struct DecodeCfg {
     static constexpr int MW = NWC < 4 ? NWC : 4;               // warps the merge buffer holds at once
     static constexpr int FRAG4 = (DPAD / 16) * NT;             // float4 accumulator groups per lane
     // merge buffer: MW warps' accumulator fragments, lane-contiguous float4; also holds the
-    // (M, L) of up to kMaxCtas pieces when the last piece merges a sequence
+    // (M, L) of up to kMaxCtas pieces when a cut sequence's first CTA merges it
     static constexpr int MERGE_BYTES = MW * FRAG4 * 32 * 16 > 2 * kMaxCtas * GT_PAD * 4 ? MW * FRAG4 * 32 * 16
                                                                                           : 2 * kMaxCtas * GT_PAD * 4;
     static constexpr int ML_BYTES = 2 * NWC * GT_PAD * 4;      // per-warp running max and sum of each head

@@ -22,7 +22,7 @@ namespace {
 
 constexpr size_t kScratchBytes = IFA_NOALLOC_SCRATCH_BYTES;
 // Layout of the scratch: [0, 256) device error word; [256, 256 + 4*kMaxCtas) the arrival
-// counters (zero at load time; the last arrival of each cut sequence resets its counter, so
+// counters (zero at load time; the CTA that merges each cut sequence resets its counter, so
 // every call that runs to the end leaves them at zero); from kPartialOffset on, the partial
 // slots.
 constexpr size_t kCounterOffset = 256;
