@@ -153,8 +153,11 @@ ifa_status ifa_create(const ifa_params* params, ifa_plan** plan, size_t* workspa
  * Device-side data errors (a needed blockTable entry outside [0, blockNum)) leave the
  * affected tokens out and set a flag readable with ifa_get_device_errors.
  * Runs of one plan must not overlap on the GPU (they share the plan's per-sequence
- * arrival counters): use one plan per stream.  The call is one kernel launch and can be
- * captured in a CUDA graph; a captured call replays with the lengths it was captured with.
+ * arrival counters): use one plan per stream.  Up to B = 256 the call is one kernel launch
+ * and can be captured in a CUDA graph; a captured call replays with the lengths it was
+ * captured with.  Above B = 256 the per-batch windows are copied from pageable host memory
+ * into the workspace on `stream` before the kernel; such a call cannot be captured: under
+ * capture it returns IFA_ERR_PARAM_INVALID and leaves the stream untouched.
  * Each call that runs to the end leaves the counters at zero (the CTA that merges a split
  * sequence resets its counter once the other pieces have arrived), so captured and eager calls may be mixed and
  * replayed in any order and number.

@@ -147,6 +147,18 @@ static ifa_status run_planned(ifa_plan* pl, const void* query, const void* key, 
     pl->last_launches = 0;
     const int B = (int)p.B;
     if (B == 0) return IFA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (B > kInlineB) {
+        // Beyond kInlineB batches the windows reach the device by a copy from pageable host
+        // memory that the plan reuses, which a CUDA graph cannot hold: under capture the call
+        // is refused before it touches the stream, so the capture stays usable.
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+            cudaGetLastError();
+            return IFA_ERR_RUNTIME;
+        }
+        if (cap != cudaStreamCaptureStatusNone) return IFA_ERR_PARAM_INVALID;
+    }
 
     std::vector<int32_t>& bd = pl->bdata;
     bd.assign((size_t)3 * B + 1, 0);
@@ -156,7 +168,6 @@ static ifa_status run_planned(ifa_plan* pl, const void* query, const void* key, 
     if (st != IFA_OK) return st;
     const int P = choose_grid(p, W, max_seq_tiles, pl->P_max);
 
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     DecodeParams& dp = *pl->dp;
     if (!kv_maps && (key != pl->last_k || value != pl->last_v)) {
         pl->last_k = pl->last_v = nullptr;

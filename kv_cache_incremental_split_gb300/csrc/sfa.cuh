@@ -23,7 +23,9 @@ constexpr int kSfaRSlots = 8;       // resolved tiles the resolver warp may run 
 constexpr int kSfaRSlotBytes = 544; // rows[kSfaTile], valid mask, flag (16-byte aligned)
 constexpr int kSfaIssuers = 4;     // warps that issue the ring's gathers (a stage's kSfaTile / 4 row groups split evenly)
 constexpr int kSfaThreads = 10 * 32;  // producer, MMA issuer, four softmax warps, resolver, three more gatherers
-constexpr int kSfaSlotFloats = 128 * kSfaHalf + 3 * 128;  // normalised O of one piece + M + L + largest score
+// partial slot: the normalised O of one piece as [64 channel quads][128 head rows][4 floats],
+// then M, L and the largest score of each head row
+constexpr int kSfaSlotFloats = 128 * kSfaHalf + 3 * 128;
 constexpr int kSfaBarBytes = 512;
 constexpr int kSfaSmem = 1024 + kSfaQBytes + kSfaStages * kSfaStageBytes + kSfaRSlots * kSfaRSlotBytes + kSfaBarBytes;
 // workspace: [0, 256) error word; [kSfaStartOffset, + 32 * kMaxCtas) each pair's start (SfaStart);

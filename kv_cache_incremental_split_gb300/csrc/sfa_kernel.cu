@@ -387,6 +387,17 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
         int epoch = 0;
         int prev_b = -1;
         bool ok = true;
+        if (gi == 0) {
+            // the first row's query: its row is in the start record, so it need not wait for the
+            // first resolved tile (index and block-table loads)
+            prev_b = sst->r;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(q_full, kSfaQBytes);
+                for (int kb = 0; kb < 8; ++kb) tma_load_3d(sq + kb * 16384, &p.tmQ, q_full, kb * 64, 0, prev_b);
+                tma_load_3d(sq + 8 * 16384, &p.tmQr, q_full, 0, 0, prev_b);
+            }
+            epoch = 1;
+        }
         // Gathers column blocks [blk0, blk0 + nblk) of the rows of resolved tile `rs` (blocks
         // 0..7: key, 8: key rope, 9..12: value half h) into this CTA's ring.
         constexpr int kGroups = kSfaTile / 4 / kSfaIssuers;  // gather4 row groups per warp and stage
@@ -515,11 +526,14 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
             const uint32_t sq_addr = smem_u32(sq);
             const uint32_t ring_addr = smem_u32(ring);
             long long it = 0;
-            int epoch = 0, prev_b = -1;
+            int epoch = 0;             // query loads waited for
+            int prev_b = sst->r;       // row of the query in place (the producer loads the first at once)
+            bool q_waited = false;     // that query has been waited for
             int n = 0;             // processed (non-empty) tiles so far
             int pending = -1;      // processed tile whose P . V is still to be issued
             uint32_t pend_acc = 0;
             bool fresh = true;     // no processed tile yet in the current piece
+            bool q_freed = false;  // the query blocks were released after the current row's last scores
             bool ok = true;
             int stg = 0;        // ring position of stage `it`: stg = it mod kSfaStages, rnd = it / kSfaStages
             uint32_t rnd = 0;
@@ -569,13 +583,27 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                     continue;
                 }
                 if (b != prev_b) {
-                    if (prev_b >= 0) umma_commit(q_empty);
+                    // the query in place may never have been used (its row's tiles here were all
+                    // empty): it must have landed before the producer overwrites it
+                    if (!q_waited) {
+                        if (!mbar_wait_bounded(q_full, epoch & 1, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        ++epoch;
+                    }
+                    if (!q_freed) umma_commit(q_empty);
+                    q_freed = false;
+                    q_waited = false;
+                    prev_b = b;
+                }
+                if (!q_waited) {
                     if (!mbar_wait_bounded(q_full, epoch & 1, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     ++epoch;
-                    prev_b = b;
+                    q_waited = true;
                 }
                 tc_fence_after();
                 // ---- S_n = [q | q_rope] . [k | k_rope]^T
@@ -592,6 +620,13 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 }
                 if (!ok) break;
                 umma_commit(&s_full[n & 1]);
+                // The row's last tile: once these score MMAs finish, the query blocks may take the
+                // next row's query, which then lands while this row's last P . V waits for its
+                // probabilities.
+                if (cur.t + 1 >= cur.n && g + 1 < hi) {
+                    umma_commit(q_empty);
+                    q_freed = true;
+                }
                 // ---- O += P_{n-1} . V_{n-1} while the softmax warps work on S_n
                 if (pending >= 0) do_pv(pending, pend_acc);
                 pending = n;
@@ -772,10 +807,12 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                         for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                     }
                 } else {
-                    float4* dst = reinterpret_cast<float4*>(sp + (long long)row * kSfaHalf + c * 32);
+                    // slot layout [channel quad][head row]: the warp's 32 rows store 512
+                    // contiguous bytes per instruction
+                    float4* dst = reinterpret_cast<float4*>(sp) + c * 8 * 128 + row;
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                        dst[j * 128] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
                                              __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
                 }
             }
@@ -955,8 +992,9 @@ __global__ void __launch_bounds__(128) sfa_combine(const __grid_constant__ SfaPa
     const int b = s >> 1, h = s & 1;
     const SfaPieces pc = p.pieces[b];
     if (pc.np < 2) return;  // the count kernel or the decode kernel wrote this sequence
-    const int row = blockIdx.y * (128 / kTpr) + (int)threadIdx.x / kTpr;
-    const int col0 = ((int)threadIdx.x % kTpr) * kCh;
+    // rows vary fastest across the threads: a slot holds channel quads of consecutive head rows
+    const int row = blockIdx.y * (128 / kTpr) + (int)threadIdx.x % (128 / kTpr);
+    const int col0 = ((int)threadIdx.x / (128 / kTpr)) * kCh;
     if (row >= p.QN) return;
     const int np = pc.np;
     // pairs c_first .. c_first + np - 1 hold the row's tiles; CTA 2c + h of pair c value half h
@@ -981,7 +1019,7 @@ __global__ void __launch_bounds__(128) sfa_combine(const __grid_constant__ SfaPa
                 l[k] = __ldcg(pp + 128 * kSfaHalf + 128 + row);
 #pragma unroll
                 for (int j = 0; j < kCh / 4; ++j)
-                    v[k][j] = __ldcg(reinterpret_cast<const float4*>(pp + (long long)row * kSfaHalf + col0) + j);
+                    v[k][j] = __ldcg(reinterpret_cast<const float4*>(pp) + (col0 / 4 + j) * 128 + row);
             } else {
 #pragma unroll
                 for (int j = 0; j < kCh / 4; ++j) v[k][j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1012,7 +1050,7 @@ __global__ void __launch_bounds__(128) sfa_combine(const __grid_constant__ SfaPa
             S += w;
 #pragma unroll
             for (int j = 0; j < kCh / 4; ++j) {
-                const float4 x = __ldcg(reinterpret_cast<const float4*>(pp + (long long)row * kSfaHalf + col0) + j);
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(pp) + (col0 / 4 + j) * 128 + row);
                 acc[4 * j] += w * x.x;
                 acc[4 * j + 1] += w * x.y;
                 acc[4 * j + 2] += w * x.z;

@@ -185,6 +185,33 @@ def test_batch_above_inline_limit():
     check(case)
 
 
+def test_batch_above_inline_limit_is_refused_under_capture():
+    """Above 256 batches the per-batch windows reach the device by a pageable host copy, which a
+    graph cannot hold: under capture the call is refused without touching the stream, the
+    capture stays usable, and an eager call afterwards still matches the oracle."""
+    from kv_cache_incremental_split_gb300.ifa import IFA_ERR_PARAM_INVALID, IfaError
+    case = gen.gqa_padded(16, B=260, N=4, KV_N=2, D=64, Smax=70, layout="BSH", dtype="bf16", mask=False)
+    dc = DeviceCase(case)
+    op = make_op(case)
+    s = torch.cuda.Stream()
+    x = torch.zeros(8, device="cuda")
+    with torch.cuda.stream(s):
+        dc.run(op, stream=s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            with pytest.raises(IfaError) as e:
+                dc.run(op, stream=s)
+            x.add_(1.0)
+        g.replay()
+        out = dc.run(op, stream=s)
+        s.synchronize()
+    assert e.value.status == IFA_ERR_PARAM_INVALID
+    assert float(x.sum()) == 8.0
+    ref = oracle_ifa(case)
+    assert max_abs_err(out_to_f64(out).reshape(ref.shape), ref) <= TOL["bf16"]
+
+
 def test_fully_masked_rows_and_per_head_mask():
     case = gen.gqa_padded(14, B=3, N=8, KV_N=2, D=128, Smax=200, layout="BNSD", dtype="bf16", mask=False)
     m = (np.random.default_rng(1).random((3, 8, 1, 200)) < 0.5)
