@@ -327,12 +327,13 @@ ifa_status sfa_workspace_size(const sfa_params* params, size_t* workspace_bytes)
  *   sfa_workspace_size bytes; deviceErrorFlags (int32, nullable) receives device error
  *   bits (1: a needed block_table entry outside [0, block_num); 2: a wait timed out).
  * `value` may alias `key`.  Calls that share a workspace must not overlap on the GPU.
- * The call enqueues three kernels: a tile-count kernel (one cluster of 8 CTAs; it finds
- * each query row's live tiles, splits them across the decode kernel's CTA pairs and writes
- * the zero output rows of query rows with no usable index), the decode kernel (pairs of
- * CTAs, one per value half, launched with programmatic dependent launch after the count)
- * and a combine kernel that merges the pieces of the (query row, value half) sequences the
- * decode kernel split across CTA pairs.  The workspace needs no initialisation.  Returns
+ * The call enqueues three kernels: a tile-count kernel that finds each query row's live
+ * tiles and writes the zero output rows of query rows with no usable index (one warp per
+ * row; above 1024 query rows one cluster of 8 CTAs, which also splits the live tiles across
+ * the decode kernel's CTA pairs), the decode kernel (pairs of CTAs, one per value half,
+ * launched with programmatic dependent launch after the count; up to 1024 query rows each
+ * CTA derives its pair's share from the counts itself) and a combine kernel that merges the
+ * pieces of the (query row, value half) sequences the decode kernel split across CTA pairs.  The workspace needs no initialisation.  Returns
  * IFA_ERR_RUNTIME when no CTA pair fits on the device or a launch fails.
  */
 ifa_status sfa_run(const sfa_params* params, const void* query, const void* query_rope, const void* key,

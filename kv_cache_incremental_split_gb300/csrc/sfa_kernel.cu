@@ -125,6 +125,138 @@ struct SeqCursor {
     }
 };
 
+// Last entry of query row r's index row whose index selects a token, or -1 (one warp; lanes
+// stride the row, whole 16-byte groups when the rows allow it).
+__device__ __forceinline__ int row_last_usable(const SfaParams& p, int r, int lane) {
+    const int idx_max = INT32_MAX >> p.sbs_log2;
+    const int32_t* row = p.indices + (long long)r * p.S_sp;
+    const bool vec = (p.S_sp & 3) == 0 && (reinterpret_cast<uintptr_t>(p.indices) & 15) == 0;
+    int last = -1;
+    if (vec) {
+        const int4* row4 = reinterpret_cast<const int4*>(row);
+        const int n4 = p.S_sp >> 2;
+#pragma unroll 16
+        for (int j = lane; j < n4; j += 32) {
+            const int4 v = __ldg(row4 + j);
+            if (v.x >= 0 && v.x <= idx_max) last = 4 * j;
+            if (v.y >= 0 && v.y <= idx_max) last = 4 * j + 1;
+            if (v.z >= 0 && v.z <= idx_max) last = 4 * j + 2;
+            if (v.w >= 0 && v.w <= idx_max) last = 4 * j + 3;
+        }
+    } else {
+#pragma unroll 8
+        for (int i = lane; i < p.S_sp; i += 32) {
+            const int idx = __ldg(row + i);
+            if (idx >= 0 && idx <= idx_max) last = i;
+        }
+    }
+    return __reduce_max_sync(0xffffffffu, last);
+}
+
+// Live tiles of a row whose last usable entry is `last`.
+__device__ __forceinline__ int live_tiles(const SfaParams& p, int last) {
+    return last < 0 ? 0 : (int)((((long long)last + 1) << p.sbs_log2) + kSfaTile - 1) / kSfaTile;
+}
+
+// A query row with no live tile: the decode kernel never visits it, so its output is all zero
+// (largest score -inf, sum 0), written here by one warp.
+__device__ __forceinline__ void write_empty_row(const SfaParams& p, int r, int lane) {
+    uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + (long long)r * p.QN * kSfaD);
+    for (int i = lane; i < p.QN * kSfaD / 8; i += 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (p.lse_max) {
+        for (int i = lane; i < p.QN; i += 32) {
+            p.lse_max[(long long)r * p.QN + i] = -INFINITY;
+            p.lse_sum[(long long)r * p.QN + i] = 0.f;
+        }
+    }
+}
+
+// The share of pair c when every decode CTA derives the split itself (up to kSfaLocalRows query
+// rows): the prefix of the live-tile counts over rows, the same equal contiguous shares as the
+// tile-count kernel computes for more rows, and this pair's start.  The pair's first CTA also
+// writes the piece record of every row whose first tile its share holds.  All threads; s_pre
+// holds R + 1 ints, s_wsum one entry per warp and the total.
+__device__ void local_split(const SfaParams& p, int* s_pre, long long* s_wsum, SfaStart* sst, int c,
+                            bool write_pieces) {
+    constexpr int NT = kSfaThreads, NW = kSfaThreads / 32;
+    constexpr int kMaxChunk = (kSfaLocalRows + NT - 1) / NT;
+    const int R = p.R;
+    const int tid = (int)threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int chunk = (R + NT - 1) / NT;
+    const int r0 = min(R, tid * chunk), r1 = min(R, r0 + chunk);
+    int e[kMaxChunk];
+    long long mine = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxChunk; ++k) {
+        e[k] = r0 + k < r1 ? __ldcg(p.eff + r0 + k) : 0;
+        mine += e[k];
+    }
+    long long incl = mine;  // inclusive scan within the warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        long long run = 0;
+        for (int w = 0; w < NW; ++w) {
+            const long long v = s_wsum[w];
+            s_wsum[w] = run;
+            run += v;
+        }
+        s_wsum[NW] = run;
+    }
+    __syncthreads();
+    long long run = s_wsum[warp] + incl - mine;  // exclusive prefix of this thread's rows
+#pragma unroll
+    for (int k = 0; k < kMaxChunk; ++k)
+        if (r0 + k < r1) {
+            s_pre[r0 + k] = (int)run;
+            run += e[k];
+        }
+    const long long Wl = s_wsum[NW];
+    if (tid == 0) s_pre[R] = (int)Wl;
+    __syncthreads();
+    const int Pa = active_ctas(Wl, p.P >> 1, p.tiles_per_seq);  // pairs from Pa on stay idle
+    const int lo = c < Pa ? (int)(c * Wl / Pa) : 0;
+    const int hi = c < Pa ? (int)((c + 1) * Wl / Pa) : 0;
+    if (tid == 0) {
+        SfaStart st;
+        st.lo = lo;
+        st.hi = hi;
+        st.r = st.h = st.t = st.n = st.first = st.pad = 0;
+        if (lo < hi) {
+            // the last row with pre <= lo: a row with live tiles, since lo < the total
+            int a = 0, z = R - 1;
+            while (a < z) {
+                const int mid = (a + z + 1) >> 1;
+                if (s_pre[mid] <= lo) a = mid;
+                else z = mid - 1;
+            }
+            st.r = a;
+            st.n = s_pre[a + 1] - s_pre[a];
+            st.t = lo - s_pre[a];
+            st.first = s_pre[a];
+        }
+        *sst = st;
+    }
+    if (write_pieces && lo < hi) {
+        for (int r = tid; r < R; r += NT) {
+            const int g0 = s_pre[r], n = s_pre[r + 1] - g0;
+            if (n > 0 && g0 >= lo && g0 < hi) {
+                SfaPieces pc;
+                pc.c_first = c;
+                pc.np = cta_of_tile((long long)g0 + n - 1, Wl, Pa) - c + 1;
+                pc.slot0 = g0 == lo ? 0 : 1;
+                pc.pad = 0;
+                p.pieces[r] = pc;
+            }
+        }
+    }
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_constant__ SfaParams p) {
@@ -184,7 +316,14 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
     // The start table and the live-tile counts come from the tile-count kernel (programmatic
     // dependent launch: everything above overlaps it).
     pdl_wait_primary();
-    if (threadIdx.x == 0) {
+    if (p.R <= kSfaLocalRows) {
+        // the resolver slots serve as scratch until the roles start
+        static_assert((kSfaLocalRows + 1) * sizeof(int) + (kSfaThreads / 32 + 1) * sizeof(long long) <=
+                          kSfaRSlots * kSfaRSlotBytes, "split scratch");
+        int* s_pre = reinterpret_cast<int*>(rbase);
+        long long* s_wsum = reinterpret_cast<long long*>(rbase + ((kSfaLocalRows + 1) * sizeof(int) + 7) / 8 * 8);
+        local_split(p, s_pre, s_wsum, sst, (int)(blockIdx.x >> 1), h == 0);
+    } else if (threadIdx.x == 0) {
         const int4* src = reinterpret_cast<const int4*>(p.starts + (blockIdx.x >> 1));
         reinterpret_cast<int4*>(sst)[0] = __ldcg(src);
         reinterpret_cast<int4*>(sst)[1] = __ldcg(src + 1);
@@ -857,49 +996,14 @@ __global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_const
     const int R = p.R;
     const bool in_smem = R <= kSfaCountSmemRows;
     int* eff0 = cluster.map_shared_rank(s_eff, 0);  // the first CTA's copy
-    const int idx_max = INT32_MAX >> p.sbs_log2;
-    // rows of whole 16-byte groups: 4 entries per load, up to 16 loads in flight per lane (a row
-    // of 2048 indices in one round trip)
-    const bool vec = (p.S_sp & 3) == 0 && (reinterpret_cast<uintptr_t>(p.indices) & 15) == 0;
     for (int r = blockIdx.x * NW + warp; r < R; r += gridDim.x * NW) {
-        const int32_t* row = p.indices + (long long)r * p.S_sp;
-        int last = -1;  // last entry of the row whose index selects a token
-        if (vec) {
-            const int4* row4 = reinterpret_cast<const int4*>(row);
-            const int n4 = p.S_sp >> 2;
-#pragma unroll 16
-            for (int j = lane; j < n4; j += 32) {
-                const int4 v = __ldg(row4 + j);
-                if (v.x >= 0 && v.x <= idx_max) last = 4 * j;
-                if (v.y >= 0 && v.y <= idx_max) last = 4 * j + 1;
-                if (v.z >= 0 && v.z <= idx_max) last = 4 * j + 2;
-                if (v.w >= 0 && v.w <= idx_max) last = 4 * j + 3;
-            }
-        } else {
-#pragma unroll 8
-            for (int i = lane; i < p.S_sp; i += 32) {
-                const int idx = __ldg(row + i);
-                if (idx >= 0 && idx <= idx_max) last = i;
-            }
-        }
-        last = __reduce_max_sync(0xffffffffu, last);
+        const int last = row_last_usable(p, r, lane);
         if (lane == 0) {
-            const int e = last < 0 ? 0 : (int)((((long long)last + 1) << p.sbs_log2) + kSfaTile - 1) / kSfaTile;
+            const int e = live_tiles(p, last);
             p.eff[r] = e;
             if (in_smem) eff0[r] = e;
         }
-        if (last < 0) {
-            // no live tile: the decode kernel never visits this row; its output is all zero
-            // (largest score -inf, sum 0)
-            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + (long long)r * p.QN * kSfaD);
-            for (int i = lane; i < p.QN * kSfaD / 8; i += 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (p.lse_max) {
-                for (int i = lane; i < p.QN; i += 32) {
-                    p.lse_max[(long long)r * p.QN + i] = -INFINITY;
-                    p.lse_sum[(long long)r * p.QN + i] = 0.f;
-                }
-            }
-        }
+        if (last < 0) write_empty_row(p, r, lane);
     }
 
     __threadfence();
@@ -978,6 +1082,26 @@ __global__ void __launch_bounds__(kSfaCountThreads) sfa_count(const __grid_const
         }
         p.pieces[r] = pc;
     }
+}
+
+// Per query row, up to kSfaLocalRows rows: its live tiles (the decode CTAs derive the split from
+// them), and for a row without one the all-zero output and an empty piece record.  One warp per
+// row and few rows per CTA, so that the index rows spread over many SMs.
+__global__ void __launch_bounds__(kSfaRowCountWarps * 32) sfa_count_rows(const __grid_constant__ SfaParams p) {
+    pdl_launch_dependents();  // the decode kernel's prologue may start; it waits for this grid's end
+    const int lane = (int)threadIdx.x & 31;
+    const int r = (int)blockIdx.x * kSfaRowCountWarps + ((int)threadIdx.x >> 5);
+    if (r >= p.R) return;
+    const int last = row_last_usable(p, r, lane);
+    if (lane == 0) {
+        p.eff[r] = live_tiles(p, last);
+        if (last < 0) {
+            SfaPieces pc;
+            pc.c_first = pc.np = pc.slot0 = pc.pad = 0;
+            p.pieces[r] = pc;
+        }
+    }
+    if (last < 0) write_empty_row(p, r, lane);
 }
 
 // Merges the pieces of every sequence that CTA boundaries cut: grid (2R sequences, 16 blocks
@@ -1097,27 +1221,7 @@ int sfa_max_pairs() {
     return pairs;
 }
 
-cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream) {
-    static bool configured = false;
-    if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSfaSmem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    // tile counts: one cluster, ordered after everything before it on the stream
-    cudaLaunchConfig_t cc = {};
-    cc.gridDim = dim3(kSfaCountCtas);
-    cc.blockDim = dim3(kSfaCountThreads);
-    cc.stream = stream;
-    cudaLaunchAttribute ca[1];
-    ca[0].id = cudaLaunchAttributeClusterDimension;
-    ca[0].val.clusterDim.x = kSfaCountCtas;
-    ca[0].val.clusterDim.y = 1;
-    ca[0].val.clusterDim.z = 1;
-    cc.attrs = ca;
-    cc.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cc, sfa_count, p);
-    if (e != cudaSuccess) return e;
+static cudaError_t launch_sfa_decode_and_combine(const SfaParams& p, cudaStream_t stream) {
     // the decode kernel starts its prologue while the counts finish (it waits before reading them)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.P);
@@ -1129,7 +1233,7 @@ cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, sfa_kernel, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, sfa_kernel, p);
     if (e != cudaSuccess) return e;
     // An ordinary launch: with programmatic dependent launch (resident early, waiting) the
     // combine cost the sparse MLA workload 18 us per call on this part.
@@ -1137,4 +1241,39 @@ cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream) {
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSfaSmem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    cudaError_t e;
+    if (p.R <= kSfaLocalRows) {
+        // live tiles per row, ordered after everything before it on the stream; the decode CTAs
+        // derive the split themselves
+        sfa_count_rows<<<(p.R + kSfaRowCountWarps - 1) / kSfaRowCountWarps, kSfaRowCountWarps * 32, 0, stream>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_sfa_decode_and_combine(p, stream);
+    }
+    // tile counts, prefix, split and piece records: one cluster, ordered after everything
+    // before it on the stream
+    cudaLaunchConfig_t cc = {};
+    cc.gridDim = dim3(kSfaCountCtas);
+    cc.blockDim = dim3(kSfaCountThreads);
+    cc.stream = stream;
+    cudaLaunchAttribute ca[1];
+    ca[0].id = cudaLaunchAttributeClusterDimension;
+    ca[0].val.clusterDim.x = kSfaCountCtas;
+    ca[0].val.clusterDim.y = 1;
+    ca[0].val.clusterDim.z = 1;
+    cc.attrs = ca;
+    cc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cc, sfa_count, p);
+    if (e != cudaSuccess) return e;
+    return launch_sfa_decode_and_combine(p, stream);
+}
+
 }  // namespace ifa
+

@@ -86,6 +86,16 @@ def check(c, batches=None, sparse_mode=None):
     return got, op
 
 
+@pytest.mark.parametrize("B,Q_S", [(512, 2), (1025, 1)])
+def test_sfa_many_rows_both_split_paths(B, Q_S):
+    """Up to 1024 query rows every decode CTA derives its share from the per-row live-tile
+    counts; above that the tile-count cluster computes the prefix, the shares and the piece
+    records.  1024 rows (the limit) and 1025 rows, short rows (some empty), against the oracle."""
+    c = gen.sfa_mla(40 + B, B=B, Q_N=16, block_size=64, kv_len=128, sparse_size=32, nvalid_lo=0, nvalid_hi=32,
+                    Q_S=Q_S)
+    check(c)
+
+
 @pytest.mark.parametrize("seed", [0, 1])
 def test_sfa_small(seed):
     check(gen.sfa_mla(seed, B=3, Q_N=128, block_size=64, kv_len=1000, sparse_size=300, nvalid_lo=1,
