@@ -33,7 +33,7 @@ constexpr int kSfaSmem = 1024 + kSfaQBytes + kSfaStages * kSfaStageBytes + kSfaR
 // over rows (R + 1 ints) and, 16-byte aligned, the pieces of each row (R SfaPieces)
 constexpr size_t kSfaStartOffset = 1024;
 constexpr size_t kSfaPartialOffset = 16384;
-constexpr int kSfaCountCtas = 8;        // the tile-count kernel: one cluster
+constexpr int kSfaCountCtas = 8;        // the cluster tile-count kernel (above kSfaLocalRows query rows)
 constexpr int kSfaCountThreads = 512;
 constexpr int kSfaCountSmemRows = 4096;  // rows whose counts the count kernel scans in shared memory
 constexpr int kSfaLocalRows = 1024;  // up to this many query rows each decode CTA derives the split itself
@@ -74,10 +74,11 @@ struct alignas(128) SfaParams {
     float* lse_sum;         // nullable: sum of exp(score - lse_max) of each (query row, head)
     float* partials;
     int* err;
-    SfaStart* starts;   // per CTA, written by the tile-count kernel
+    SfaStart* starts;   // per pair, written by the cluster tile-count kernel (above kSfaLocalRows rows)
     int* eff;           // live tiles of each query row (a sequence's tiles), 0 when no index is usable
-    int* pre;           // prefix over rows of eff (R + 1 entries): the tile order of the decode kernel's pairs
-    SfaPieces* pieces;  // per query row, written by the tile-count kernel for the combine kernel
+    int* pre;           // prefix over rows of eff (R + 1 entries), written by the cluster tile-count kernel
+    SfaPieces* pieces;  // per query row, for the combine kernel: written by the tile-count kernel (rows with
+                        // no live tile, and every row above kSfaLocalRows rows) or by the decode kernel's pairs
     long long W;        // tiles before the count: R * tiles_per_seq (an upper bound)
     int P;              // CTAs: an even count; CTAs 2c and 2c + 1 (the two value halves) form pair c
     int R, QS, QN, S_sp, tiles_per_seq;  // R query rows: B * QS (row r: batch r / QS, query token r % QS), or

@@ -9,22 +9,26 @@
 // of the same positions, walk them at the same time and each gather the key rows
 // themselves: the second read of a key row mostly hits L2).
 // A sequence is cut into 128-position tiles of its sparse index row.  A first
-// kernel (one cluster) finds each row's live tiles (up to the last tile holding
-// a usable index: the invalid tail after it costs nothing) and the prefix over
-// rows; persistent CTAs take equal contiguous shares of the live tiles.  A piece
-// of a sequence that a CTA boundary cuts goes to a partial slot (normalised O,
-// running max M and sum L per head) and the combine kernel merges the pieces of
-// every cut sequence.  The count kernel writes the zero rows of query rows with
-// no live tile.
+// kernel finds each row's live tiles (up to the last tile holding a usable index:
+// the invalid tail after it costs nothing); persistent CTA pairs take equal
+// contiguous shares of the live tiles.  Up to kSfaLocalRows query rows every
+// decode CTA derives its pair's share from the counts itself; above that the
+// count kernel (one cluster) computes the prefix over rows and every share.  A
+// piece of a sequence that a CTA boundary cuts goes to a partial slot (normalised
+// O, running max M and sum L per head) and the combine kernel merges the pieces
+// of every cut sequence.  The count kernel writes the zero rows of query rows
+// with no live tile.
 //
 // Per CTA:
 //  * resolver (warp 6): for each tile, the cache row of every position (index ->
 //    block table, software-pipelined over three tiles) and the valid mask, into a
 //    ring of kSfaRSlots resolved tiles.  A tile with no valid position is skipped
 //    by every role below.
-//  * producer (warp 0) and gatherers (warps 7-9): warp 0 loads Q of batch b (9
-//    column blocks of [q | q_rope], 128 rows, 147 KB, resident while b does not
-//    change) by 3-D TMA tiles; per tile, the 128 key rows (9 column blocks incl.
+//  * producer (warp 0) and gatherers (warps 7-9): warp 0 loads Q of query row b
+//    (9 column blocks of [q | q_rope], 128 rows, 147 KB, resident while b does not
+//    change) by 3-D TMA tiles, the first row's before any tile is resolved and each
+//    next one once the MMA issuer has released the buffer after the previous row's
+//    last score MMAs; per tile, the 128 key rows (9 column blocks incl.
 //    rope) and, one tile later, the 128 value rows of half h (4 blocks) go by TMA
 //    tile::gather4 into a ring of 16 KB stages.  The four warps take eight of each
 //    stage's 32 groups of 4 rows each (one warp alone cannot issue gathers fast
@@ -630,7 +634,7 @@ __global__ void __launch_bounds__(kSfaThreads, 1) sfa_kernel(const __grid_consta
                 if (lane == 0) mbar_arrive(&r_empty[slot]);
                 continue;
             }
-            if (b != prev_b && gi == 0) {  // new query batch: wait until the MMAs using the old one are done
+            if (b != prev_b && gi == 0) {  // new query row: wait until the MMAs using the old query are done
                 if (epoch > 0 && !mbar_wait_bounded(q_empty, (epoch - 1) & 1, kWaitLimitNs)) {
                     if (lane == 0) atomicOr(p.err, kErrTimeout);
                     *abort_flag = 1;
