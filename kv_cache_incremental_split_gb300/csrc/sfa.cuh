@@ -37,6 +37,10 @@ constexpr int kSfaCountCtas = 8;        // the cluster tile-count kernel (above 
 constexpr int kSfaCountThreads = 512;
 constexpr int kSfaCountSmemRows = 4096;  // rows whose counts the count kernel scans in shared memory
 constexpr int kSfaLocalRows = 1024;  // up to this many query rows each decode CTA derives the split itself
+// The smallest share of live tiles a CTA pair takes.  A pair's first tile costs about as much
+// as two more (the query and the first key stages land together), so small problems run
+// fastest spread over every pair, one tile each.
+constexpr int kSfaMinShareTiles = 1;
 constexpr int kSfaRowCountWarps = 2;  // rows (one per warp) of a CTA of the per-row count kernel
 constexpr float kSfaRescaleSlack = 8.0f;    // log2 units the running max may trail before O is rescaled
 constexpr float kLn2 = 0.6931471805599453f;  // scores in log2 units -> natural units

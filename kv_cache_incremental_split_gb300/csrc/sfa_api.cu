@@ -177,10 +177,10 @@ extern "C" ifa_status sfa_run(const sfa_params* params, const void* query, const
     // tiles of the query rows (each runs once per value half, on the two CTAs of a pair)
     const long long W = (long long)R * tps;
     if (W > INT32_MAX) return IFA_ERR_PARAM_INVALID;
-    // pairs: as many as fit at once, with contiguous shares of at least min(tiles per row, 4) tiles
+    // pairs: as many as fit at once, with contiguous shares of at least min(tiles per row, kSfaMinShareTiles) tiles
     const int fit = std::min(P_max / 2, sfa_max_pairs());
     if (fit < 1) return IFA_ERR_RUNTIME;
-    const long long min_share = std::max(1, std::min(tps, kMinPieceTiles));
+    const long long min_share = std::max(1, std::min(tps, kSfaMinShareTiles));
     const int P = 2 * (int)std::max<long long>(1, std::min<long long>(fit, (W + min_share - 1) / min_share));
 
     unsigned char* ws = static_cast<unsigned char*>(workspace);

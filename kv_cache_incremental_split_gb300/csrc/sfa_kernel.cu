@@ -71,10 +71,10 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long W, int P) {
     return (int)(((t + 1) * (long long)P - 1) / W);
 }
 
-// CTAs that share W live tiles: at most the launch's P, and shares of at least
-// min(tiles per sequence, kMinPieceTiles) tiles, so every one of them holds a tile.
+// CTA pairs that share W live tiles: at most the launch's P, and shares of at least
+// min(tiles per sequence, kSfaMinShareTiles) tiles, so every one of them holds a tile.
 __device__ __forceinline__ int active_ctas(long long W, int P, int tps) {
-    const long long share = max(1, min(tps, kMinPieceTiles));
+    const long long share = max(1, min(tps, kSfaMinShareTiles));
     const long long want = (W + share - 1) / share;
     return (int)max(1LL, min((long long)P, want));
 }
