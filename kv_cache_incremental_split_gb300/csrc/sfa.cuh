@@ -42,6 +42,7 @@ constexpr int kSfaLocalRows = 1024;  // up to this many query rows each decode C
 // fastest spread over every pair, one tile each.
 constexpr int kSfaMinShareTiles = 1;
 constexpr int kSfaRowCountWarps = 2;  // rows (one per warp) of a CTA of the per-row count kernel
+constexpr int kSfaCombineThreads = 256;  // threads of a combine block: 8 head rows x 32 groups of 8 channels
 constexpr float kSfaRescaleSlack = 8.0f;    // log2 units the running max may trail before O is rescaled
 constexpr float kLn2 = 0.6931471805599453f;  // scores in log2 units -> natural units
 
