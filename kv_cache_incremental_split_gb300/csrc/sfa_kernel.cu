@@ -1108,13 +1108,117 @@ __global__ void __launch_bounds__(kSfaRowCountWarps * 32) sfa_count_rows(const _
     if (last < 0) write_empty_row(p, r, lane);
 }
 
-// Merges the pieces of every sequence that CTA boundaries cut: grid (2R sequences, 16 blocks
-// of 8 head rows), 256 threads; thread = (head row, 8 channels).  Piece k weighs
+// Merges the pieces of every sequence that CTA boundaries cut, for problems whose shares average
+// four tiles or more (rows of a few pieces): grid (2R sequences, 16 blocks of 8 head rows), 128
+// threads; thread = (head row, 16 channels).  Piece k weighs
+// L_k 2^(M_k - M) / sum_j L_j 2^(M_j - M) with M the largest M_k.  One record from the count
+// kernel says where the pieces sit; then every piece's M, L and channels are loaded at once.
+__global__ void __launch_bounds__(128) sfa_combine_few(const __grid_constant__ SfaParams p) {
+    constexpr int kCh = 16;                          // channels per thread
+    constexpr int kTpr = kSfaHalf / kCh;             // threads per head row
+    constexpr int kMaxFast = 4;                      // pieces loaded together
+    const int s = blockIdx.x;
+    const int b = s >> 1, h = s & 1;
+    const SfaPieces pc = p.pieces[b];
+    if (pc.np < 2) return;  // the count kernel or the decode kernel wrote this sequence
+    // rows vary fastest across the threads: a slot holds channel quads of consecutive head rows
+    const int row = blockIdx.y * (128 / kTpr) + (int)threadIdx.x % (128 / kTpr);
+    const int col0 = ((int)threadIdx.x / (128 / kTpr)) * kCh;
+    if (row >= p.QN) return;
+    const int np = pc.np;
+    // pairs c_first .. c_first + np - 1 hold the row's tiles; CTA 2c + h of pair c value half h
+    auto slot_ptr = [&](int k) {
+        const int sl = k == 0 ? 2 * (2 * pc.c_first + h) + pc.slot0 : 2 * (2 * (pc.c_first + k) + h);
+        return p.partials + (long long)sl * kSfaSlotFloats;
+    };
+    float acc[kCh];
+#pragma unroll
+    for (int j = 0; j < kCh; ++j) acc[j] = 0.f;
+    float S = 0.f;
+    if (np <= kMaxFast) {
+        float m[kMaxFast], l[kMaxFast];
+        float4 v[kMaxFast][kCh / 4];
+#pragma unroll
+        for (int k = 0; k < kMaxFast; ++k) {
+            m[k] = -INFINITY;
+            l[k] = 0.f;
+            if (k < np) {
+                const float* pp = slot_ptr(k);
+                m[k] = __ldcg(pp + 128 * kSfaHalf + row);
+                l[k] = __ldcg(pp + 128 * kSfaHalf + 128 + row);
+#pragma unroll
+                for (int j = 0; j < kCh / 4; ++j)
+                    v[k][j] = __ldcg(reinterpret_cast<const float4*>(pp) + (col0 / 4 + j) * 128 + row);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kCh / 4; ++j) v[k][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float M = m[0];
+#pragma unroll
+        for (int k = 1; k < kMaxFast; ++k) M = fmaxf(M, m[k]);
+#pragma unroll
+        for (int k = 0; k < kMaxFast; ++k) {
+            const float w = m[k] == -INFINITY ? 0.f : l[k] * ex2f_approx(m[k] - M);
+            S += w;
+#pragma unroll
+            for (int j = 0; j < kCh / 4; ++j) {
+                acc[4 * j] += w * v[k][j].x;
+                acc[4 * j + 1] += w * v[k][j].y;
+                acc[4 * j + 2] += w * v[k][j].z;
+                acc[4 * j + 3] += w * v[k][j].w;
+            }
+        }
+    } else {
+        float M = -INFINITY;
+        for (int k = 0; k < np; ++k) M = fmaxf(M, __ldcg(slot_ptr(k) + 128 * kSfaHalf + row));
+        for (int k = 0; k < np; ++k) {
+            const float* pp = slot_ptr(k);
+            const float mk = __ldcg(pp + 128 * kSfaHalf + row);
+            const float w = mk == -INFINITY ? 0.f : __ldcg(pp + 128 * kSfaHalf + 128 + row) * ex2f_approx(mk - M);
+            S += w;
+#pragma unroll
+            for (int j = 0; j < kCh / 4; ++j) {
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(pp) + (col0 / 4 + j) * 128 + row);
+                acc[4 * j] += w * x.x;
+                acc[4 * j + 1] += w * x.y;
+                acc[4 * j + 2] += w * x.z;
+                acc[4 * j + 3] += w * x.w;
+            }
+        }
+    }
+    const float inv = S > 0.f ? 1.f / S : 0.f;
+    const bool bf = p.is_bf16 != 0;
+    if (p.lse_max && h == 0 && col0 == 0) {
+        float Mt = -INFINITY;
+        for (int k = 0; k < np; ++k) Mt = fmaxf(Mt, __ldcg(slot_ptr(k) + 128 * kSfaHalf + 256 + row));
+        float St = 0.f;
+        for (int k = 0; k < np; ++k) {
+            const float* pp = slot_ptr(k);
+            const float mk = __ldcg(pp + 128 * kSfaHalf + row);
+            if (mk != -INFINITY) St += __ldcg(pp + 128 * kSfaHalf + 128 + row) * ex2f_approx(mk - Mt);
+        }
+        const long long li = (long long)b * p.QN + row;
+        p.lse_max[li] = Mt == -INFINITY ? -INFINITY : Mt * kLn2;
+        p.lse_sum[li] = Mt == -INFINITY ? 0.f : St;
+    }
+    uint32_t wv[kCh / 2];
+#pragma unroll
+    for (int j = 0; j < kCh / 2; ++j) wv[j] = pack2(acc[2 * j] * inv, acc[2 * j + 1] * inv, bf);
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + ((long long)b * p.QN + row) * kSfaD +
+                                          h * kSfaHalf + col0);
+#pragma unroll
+    for (int j = 0; j < kCh / 8; ++j) dst[j] = make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
+}
+
+// Merges the pieces of every sequence that CTA boundaries cut, for problems with smaller shares
+// (rows of many pieces): grid (2R sequences, 16 blocks of 8 head rows), 256 threads; thread =
+// (head row, 8 channels).  Piece k weighs
 // L_k 2^(M_k - M) / sum_j L_j 2^(M_j - M) with M the largest M_k.  One record says where the
 // pieces sit; then the pieces are merged four at a time (their M, L and channels loaded
 // together, one round trip per group) against the running largest M, the running sums rescaled
 // when a group raises it: up to four pieces, one group with M the largest M_k.
-__global__ void __launch_bounds__(kSfaCombineThreads) sfa_combine(const __grid_constant__ SfaParams p) {
+__global__ void __launch_bounds__(kSfaCombineThreads) sfa_combine_many(const __grid_constant__ SfaParams p) {
     constexpr int kCh = 8;                                   // channels per thread
     constexpr int kRows = kSfaCombineThreads * kCh / kSfaHalf;  // head rows per block
     constexpr int kGroup = 4;                                // pieces loaded together
@@ -1249,7 +1353,12 @@ static cudaError_t launch_sfa_decode_and_combine(const SfaParams& p, cudaStream_
     if (e != cudaSuccess) return e;
     // An ordinary launch: with programmatic dependent launch (resident early, waiting) the
     // combine cost the sparse MLA workload 18 us per call on this part.
-    sfa_combine<<<dim3(2 * p.R, 128 * kSfaHalf / (8 * kSfaCombineThreads)), kSfaCombineThreads, 0, stream>>>(p);
+    // Shares of four tiles and more (so rows of a few pieces): 16 channels a thread, every block
+    // resident at once; smaller shares cut rows into many pieces, merged four at a time.
+    if (p.W >= 4LL * (p.P >> 1))
+        sfa_combine_few<<<dim3(2 * p.R, kSfaHalf / 16), 128, 0, stream>>>(p);
+    else
+        sfa_combine_many<<<dim3(2 * p.R, 128 * kSfaHalf / (8 * kSfaCombineThreads)), kSfaCombineThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
