@@ -34,6 +34,11 @@
  * owns every tensor, the workspace and the stream.  Results are deterministic:
  * the same inputs give bitwise-identical outputs.
  *
+ * Devices: every call works on the device current on the calling thread.  A plan's
+ * device state lives on the device current at ifa_create, so run a plan with that
+ * device current.  One process may use several devices (device indices below 64): the
+ * kernels' launch attributes are set on each device's first call.
+ *
  * Errors: no exception or abort crosses this ABI.  Return codes follow the
  * aclnnIncreFlashAttentionV2 page's Return Value table.
  */

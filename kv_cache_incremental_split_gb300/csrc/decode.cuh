@@ -23,6 +23,19 @@ constexpr int kCutCostBytes = 160 * 1024;
 constexpr int kPieceCostBytesI8 = 192 * 1024;
 constexpr int kCutCostBytesI8 = 320 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded spin-waits: 2 s
+constexpr int kMaxDevices = 64;      // devices whose one-time kernel set-up is tracked
+
+// The current device as an index for per-device one-time set-up (kernel attributes such as the
+// dynamic shared-memory limit are set per device), or -1 when it cannot be read or is kMaxDevices
+// or beyond.
+inline int current_device_slot() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return (dev >= 0 && dev < kMaxDevices) ? dev : -1;
+}
 
 // Device error word bits (OR-ed into the error word).
 constexpr int kErrBadBlock = 1;      // a needed blockTable entry outside [0, blockNum)

@@ -38,6 +38,8 @@
 // the row sums l add up the same fp16-rounded probabilities the P.V MMAs use,
 // so -1152 joins offset_V.
 #pragma once
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -1060,8 +1062,10 @@ __global__ void __launch_bounds__(DecodeCfg<KV, DPAD, NT>::THREADS, 1)
 template <int KV, int DPAD, int NT, bool TL = false>
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) {
     using C = DecodeCfg<KV, DPAD, NT>;
-    static bool configured = false;
-    if (!configured) {
+    static std::atomic<bool> configured[kMaxDevices];  // per device: the attributes are set per device
+    const int dev = current_device_slot();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    if (!configured[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(decode_kernel<KV, DPAD, NT, TL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM);
         if (e != cudaSuccess) return e;
@@ -1073,7 +1077,7 @@ cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) 
             if (e != cudaSuccess) return e;
             if ((long long)fa.numRegs * C::THREADS < C::REG_POOL_NEEDED) return cudaErrorInvalidConfiguration;
         }
-        configured = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

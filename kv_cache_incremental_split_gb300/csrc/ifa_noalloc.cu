@@ -28,7 +28,6 @@ constexpr size_t kScratchBytes = IFA_NOALLOC_SCRATCH_BYTES;
 constexpr size_t kCounterOffset = 256;
 constexpr size_t kPartialOffset = 4096;
 static_assert(kCounterOffset + sizeof(unsigned int) * kMaxCtas <= kPartialOffset, "scratch layout");
-constexpr int kMaxDevices = 64;
 
 // The scratch every ifa_run_noalloc call on a device shares.  In host code this
 // name is only a stand-in; the device address comes from cudaGetSymbolAddress.

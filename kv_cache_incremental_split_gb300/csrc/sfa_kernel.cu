@@ -46,6 +46,8 @@
 //    buffer, into columns already read.
 // Every wait is bounded; on a timeout the kernel records error bit 2, drains its
 // copies and MMAs, frees TMEM and returns.
+#include <atomic>
+
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -1323,18 +1325,21 @@ __global__ void __launch_bounds__(kSfaCombineThreads) sfa_combine_many(const __g
 }
 
 int sfa_max_pairs() {
-    static int pairs = -1;
-    if (pairs < 0) {
-        int n = 0, dev = 0, sms = 0;
+    static std::atomic<int> pairs[kMaxDevices];  // per device; 0 until known
+    const int dev = current_device_slot();
+    if (dev < 0) return 0;
+    int known = pairs[dev].load(std::memory_order_acquire);
+    if (known == 0) {
+        int n = 0, sms = 0;
         if (cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSfaSmem) != cudaSuccess ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sfa_kernel, kSfaThreads, kSfaSmem) != cudaSuccess ||
-            cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             n = 0;
         cudaGetLastError();
-        pairs = n * sms / 2;
+        known = n * sms / 2;
+        if (known > 0) pairs[dev].store(known, std::memory_order_release);
     }
-    return pairs;
+    return known;
 }
 
 static cudaError_t launch_sfa_decode_and_combine(const SfaParams& p, cudaStream_t stream) {
@@ -1363,11 +1368,13 @@ static cudaError_t launch_sfa_decode_and_combine(const SfaParams& p, cudaStream_
 }
 
 cudaError_t launch_sfa(const SfaParams& p, cudaStream_t stream) {
-    static bool configured = false;
-    if (!configured) {
+    static std::atomic<bool> configured[kMaxDevices];  // per device: the attribute is set per device
+    const int dev = current_device_slot();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    if (!configured[dev].load(std::memory_order_acquire)) {
         const cudaError_t e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSfaSmem);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     cudaError_t e;
     if (p.R <= kSfaLocalRows) {
