@@ -105,8 +105,9 @@ def _c(a, dtype=None):
 def ifa_ref(query, key, value, *, num_heads, num_kv_heads=0, scale, layout="BNSD",
             kv_format=CONTIG, block_size=0, block_table=None, atten_mask=None,
             actual_seq_lengths=None, kv_padding_size=None, antiquant=AQ_NONE,
-            antiquant_scale=None, antiquant_offset=None):
-    """Reference output, float64 array of shape (B, numHeads, D).
+            antiquant_scale=None, antiquant_offset=None, return_bad_tokens=False):
+    """Reference output, float64 array of shape (B, numHeads, D); with return_bad_tokens,
+    also the number of window tokens whose block-table entry lies outside [0, blocknum).
 
     query: (B,N,1,D) BNSD, (B,1,N,D) BSND or (B,1,H) BSH.
     key/value: contiguous in the same layout, or a paged cache
@@ -155,7 +156,7 @@ def ifa_ref(query, key, value, *, num_heads, num_kv_heads=0, scale, layout="BNSD
                             _ptr(sc), _ptr(of), float(scale), _ptr(out))
     if rc < 0:
         raise ValueError("oracle rejected its arguments")
-    return out
+    return (out, rc) if return_bad_tokens else out
 
 
 SFA_LAYOUT_Q = {"BSND": 0, "TND": 1}

@@ -25,6 +25,9 @@
  *    for key, 1 for value; per-channel tensors are (2, KV_N, D) in memory.
  *  - sparse indices outside [0, actual_seq_lengths_kv[b]) are skipped;
  *    duplicates count once per occurrence.
+ *  - lengths: negative, or (right padding, paging) above the cache's S or
+ *    blockTableCols * blockSize, are refused; kvPaddingSize applies only with
+ *    actualSeqLengths; a paged cache takes no left padding.
  *
  * No code, header or table is shared with the CUDA path.
  */
@@ -141,14 +144,20 @@ static double kv_value(const orc_ifa* a, int which, int64_t off, int64_t h, int6
 
 /*
  * Valid window [*st, *en) of batch b in the S coordinate.  Returns 0 when the
- * output row is all zeros by rule (out-of-range left-pad window).
+ * output row is all zeros by rule (out-of-range left-pad window), -1 for a
+ * length the cache cannot hold: negative, or, without left padding, above the
+ * cache's S (contiguous) or above blockTableCols * blockSize (paged) -- a batch's
+ * valid tokens are tokens of its cache (aclnnIncreFlashAttentionV2,
+ * actualSeqLengths; IncreFlashAttention README, page attention: the block table
+ * holds every block a sequence uses).
  * Left padding: IncreFlashAttention README, "kv左padding" constraints.
  */
 static int resolve_window(const orc_ifa* a, int64_t b, int64_t* st, int64_t* en) {
     int64_t len;
     if (a->lens) len = a->lens[b];
     else len = a->Smax;
-    if (a->pads) {
+    if (len < 0) return -1;
+    if (a->pads && a->lens) { /* without lengths the window is right padded */
         int64_t pad = a->pads[a->n_pads == 1 ? 0 : b];
         if (pad < 0) pad = 0;
         int64_t s0 = a->Smax - pad - len;
@@ -158,8 +167,8 @@ static int resolve_window(const orc_ifa* a, int64_t b, int64_t* st, int64_t* en)
         *en = e0;
         return 1;
     }
-    if (len < 0) len = 0;
-    if (a->kv_format == ORC_CONTIG && len > a->Smax) len = a->Smax;
+    const int64_t cap = a->kv_format == ORC_CONTIG ? a->Smax : a->block_table_cols * a->block_size;
+    if (len > cap) return -1;
     *st = 0;
     *en = len;
     return 1;
@@ -173,8 +182,9 @@ static int masked(const orc_ifa* a, int64_t b, int64_t n, int64_t t) {
 }
 
 /*
- * Returns the number of block-table lookups that fell outside [0, blocknum)
- * (those tokens are left out of the softmax), or -1 on bad arguments.
+ * Returns the number of tokens of the batches' windows whose block-table entry lies
+ * outside [0, blocknum) (those tokens are left out of the softmax of every head),
+ * or -1 on bad arguments.
  */
 int ifa_oracle_run(int64_t B, int64_t N, int64_t KV_N, int64_t D, int q_dtype, int kv_dtype,
                    int layout, int kv_format, int64_t Smax, int64_t block_size,
@@ -195,9 +205,17 @@ int ifa_oracle_run(int64_t B, int64_t N, int64_t KV_N, int64_t D, int q_dtype, i
     a.scale = scale;
     if (a.KV_N <= 0 || N % a.KV_N != 0) return -1;
     if (kv_format != ORC_CONTIG && (!lens || !block_table || block_size <= 0)) return -1;
+    if (kv_format != ORC_CONTIG && pads) return -1; /* left padding of a paged cache is not defined */
     int64_t G = N / a.KV_N;
     int bad = 0;
 
+    for (int64_t b = 0; b < B; b++) {
+        int64_t st = 0, en = 0;
+        const int live = resolve_window(&a, b, &st, &en);
+        if (live < 0) return -1;
+        for (int64_t t = st; live && t < en; t++)
+            if (kv_offset(&a, b, 0, t, 0) < 0) bad++;
+    }
     double* s = NULL;
     int64_t cap = 0;
     for (int64_t b = 0; b < B; b++) {
@@ -222,10 +240,7 @@ int ifa_oracle_run(int64_t B, int64_t N, int64_t KV_N, int64_t D, int q_dtype, i
                 *sc = NAN;
                 if (masked(&a, b, n, t)) continue;
                 int64_t off0 = kv_offset(&a, b, h, t, 0);
-                if (off0 < 0) {
-                    if (n == 0) bad++;
-                    continue;
-                }
+                if (off0 < 0) continue; /* counted above */
                 double dot = 0.0;
                 for (int64_t d = 0; d < D; d++)
                     dot += load_value(q, q_offset(&a, b, n, d), q_dtype) * kv_value(&a, 0, off0 + d, h, d);

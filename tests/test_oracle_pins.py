@@ -982,3 +982,101 @@ def test_tensorlist_tokens_past_the_length_do_not_count():
     for b in range(3):
         one = oracle.ifa_ref(tl.query[b:b + 1], tl.key[b], tl.value[b], num_heads=4, scale=case.scale)
         assert np.array_equal(full[b], one[0])
+
+
+# ---------------------------------------------------------------- value decoding and argument rules
+
+def test_every_finite_16bit_pattern_decodes_exactly():
+    """With one valid token the softmax weight is exactly 1, so the output is that token's
+    value row: checked for every finite fp16 bit pattern (subnormals included) against numpy's
+    float16, and for every finite bf16 pattern against the float32 with those upper 16 bits."""
+    D = 64
+    for dtype in ("fp16", "bf16"):
+        bits = np.arange(65536, dtype=np.uint32)
+        exp_mask, exp_shift = (0x7C00, 10) if dtype == "fp16" else (0x7F80, 7)
+        finite = bits[((bits & exp_mask) >> exp_shift) != (exp_mask >> exp_shift)].astype(np.uint16)
+        rows = -(-finite.size // D)
+        vals = np.zeros(rows * D, dtype=np.uint16)
+        vals[:finite.size] = finite
+        vals = vals.reshape(rows, 1, 1, D)  # BNSD (B=rows, KV_N=1, S=1, D)
+        if dtype == "fp16":
+            v = vals.view(np.float16)
+            expect = v.astype(np.float64)
+        else:
+            v = vals
+            expect = (vals.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+        q = np.zeros((rows, 1, 1, D), dtype=v.dtype)
+        out = oracle.ifa_ref(q, v, v, num_heads=1, scale=1.0, layout="BNSD",
+                             actual_seq_lengths=np.ones(rows, dtype=np.int64))
+        assert np.array_equal(out.reshape(-1), expect.reshape(-1)), dtype
+
+
+def test_lengths_the_cache_cannot_hold_are_rejected():
+    """Reading 10: a batch's valid tokens are tokens of its cache.  A negative length, or
+    (without left padding) one above the cache's S or above blockTableCols * blockSize, is
+    refused, as the library refuses it; exactly S is accepted.  Left padding of a paged cache
+    is refused too (reading 9)."""
+    c = gen.gqa_padded(3, B=2, N=4, KV_N=2, D=16, Smax=40, layout="BNSD", dtype="fp16", mask=False)
+    run(c, actual_seq_lengths=np.array([40, 7], dtype=np.int64))
+    for lens in ([41, 7], [-1, 7]):
+        with pytest.raises(ValueError):
+            run(c, actual_seq_lengths=np.array(lens, dtype=np.int64))
+    p = gen.paged_gqa(4, B=2, N=4, KV_N=2, D=16, block_size=16, len_lo=1, len_hi=64, dtype="fp16")
+    cols = p.block_table.shape[1]
+    kw = dict(num_heads=4, num_kv_heads=2, scale=p.scale, layout="BNSD", kv_format=oracle.PAGED_NBSD,
+              block_size=16, block_table=p.block_table)
+    oracle.ifa_ref(p.query, p.key, p.value, actual_seq_lengths=np.array([cols * 16, 5], np.int64), **kw)
+    with pytest.raises(ValueError):
+        oracle.ifa_ref(p.query, p.key, p.value, actual_seq_lengths=np.array([cols * 16 + 1, 5], np.int64), **kw)
+    with pytest.raises(ValueError):
+        oracle.ifa_ref(p.query, p.key, p.value, actual_seq_lengths=p.actual_seq_lengths,
+                       kv_padding_size=np.array([0], np.int64), **kw)
+
+
+def test_padding_sizes_without_lengths_leave_the_window_right_padded():
+    """Reading 5: without actualSeqLengths every batch uses the whole cache, and kvPaddingSize
+    has nothing to place."""
+    c = gen.gqa_padded(5, B=2, N=4, KV_N=2, D=16, Smax=24, layout="BSND", dtype="bf16", mask=False)
+    plain = run(c, actual_seq_lengths=None)
+    padded = run(c, actual_seq_lengths=None, kv_padding_size=np.array([5, 9], dtype=np.int64))
+    assert np.array_equal(plain, padded)
+    assert np.array_equal(plain, run(c, actual_seq_lengths=np.array([24, 24], dtype=np.int64)))
+
+
+def test_out_of_range_block_entries_are_counted_once_per_token_and_left_out():
+    """Reading 11: a needed block-table entry outside [0, blockNum) leaves its tokens out for
+    every head (the result equals the cache with those tokens masked) and the oracle counts
+    each such token of the windows once, whatever the number of heads."""
+    p = gen.paged_gqa(6, B=2, N=8, KV_N=2, D=16, block_size=16, len_lo=40, len_hi=64, dtype="bf16")
+    bt = p.block_table.copy()
+    lens = p.actual_seq_lengths
+    bt[0, 1] = p.key.shape[0] + 3     # tokens 16..31 of batch 0
+    bt[1, 0] = -7                     # tokens 0..15 of batch 1
+    kw = dict(num_heads=8, num_kv_heads=2, scale=p.scale, layout="BNSD", kv_format=oracle.PAGED_NBSD,
+              block_size=16, actual_seq_lengths=lens)
+    out, nbad = oracle.ifa_ref(p.query, p.key, p.value, block_table=bt, return_bad_tokens=True, **kw)
+    assert nbad == 32
+    mask = np.zeros((2, 1, 1, bt.shape[1] * 16), dtype=bool)
+    mask[0, :, :, 16:32] = True
+    mask[1, :, :, 0:16] = True
+    ref, none_bad = oracle.ifa_ref(p.query, p.key, p.value, block_table=p.block_table, atten_mask=mask,
+                                   return_bad_tokens=True, **kw)
+    assert none_bad == 0
+    assert np.array_equal(out, ref)
+
+
+def test_sfa_bsnd_tokens_past_the_key_tensor_are_skipped():
+    """layout_kv BSND with a length above KV_S: selected tokens at or past KV_S are not in
+    the batch's rows of the key tensor and select nothing, exactly as if their indices were -1
+    (they must not reach the next batch's rows)."""
+    c = _sfa(60, B=2, sparse_size=16, nvalid_lo=16, nvalid_hi=16)
+    k, kr, v = _contig_kv(c, kv_len=64)
+    idx = c.sparse_indices.copy()
+    idx[0, 0, 0, :4] = [64, 66, 70, 71]  # past KV_S = 64 for batch 0, inside its length of 72
+    lens = np.array([72, 64], dtype=np.int32)
+    got = oracle.sfa_ref(c.query, c.query_rope, k, kr, v, idx, None, lens, scale=c.scale, layout_kv="BSND")
+    pruned = idx.copy()
+    pruned[0, 0, 0, :4] = -1
+    ref = oracle.sfa_ref(c.query, c.query_rope, k, kr, v, pruned, None, np.array([64, 64], np.int32),
+                         scale=c.scale, layout_kv="BSND")
+    assert np.array_equal(got, ref)
