@@ -227,6 +227,18 @@ def test_broadcast_mask_1N1S():
     check(case)
 
 
+def test_padding_sizes_without_lengths_leave_the_cache_right_padded():
+    """Without actualSeqLengths every batch uses its whole cache and kvPaddingSize has nothing to
+    place: the call equals the one without padding sizes bit for bit, and the oracle."""
+    case = gen.gqa_padded(24, B=3, N=8, KV_N=2, D=128, Smax=700, layout="BSND", dtype="bf16", mask=False)
+    case.actual_seq_lengths = None
+    plain = gpu_ifa(case)
+    case.kv_padding_size = np.array([5, 300, 0], dtype=np.int64)
+    padded = gpu_ifa(case)
+    assert np.array_equal(plain, padded)
+    assert max_abs_err(padded, oracle_ifa(case)) <= TOL["bf16"]
+
+
 def test_left_pad_edge_windows():
     case = gen.int8_leftpad(16, B=4, N=8, KV_N=2, D=128, Smax=256, len_lo=1, len_hi=256)
     case.actual_seq_lengths = np.array([200, 10, 256, 100], dtype=np.int64)

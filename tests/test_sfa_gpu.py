@@ -261,6 +261,34 @@ def test_sfa_layouts_match_oracle(lq, lk):
     check(gen.sfa_relayout(c, lq, lk))
 
 
+def test_sfa_bsnd_lengths_above_the_key_rows_skip_tokens_past_them():
+    """BSND keys with a batch length above KV_S (the key tensor's rows per batch): selected tokens
+    at or past KV_S select nothing and must not reach the next batch's rows.  Outputs against the
+    oracle; with a zero query every score is 0, so softmax_sum is the exact count of the tokens
+    that count, compared exactly."""
+    c = gen.sfa_mla(36, B=3, Q_N=64, block_size=64, kv_len=512, sparse_size=256, nvalid_lo=120, nvalid_hi=256)
+    c.actual_seq_lengths_kv = np.array([512, 512, 512], dtype=np.int32)
+    c = gen.sfa_relayout(c, "BSND", "BSND")
+    kv_s = c.key.shape[1]
+    assert kv_s == 512
+    c.actual_seq_lengths_kv = np.array([kv_s + 40, kv_s, kv_s - 100], dtype=np.int32)
+    c.sparse_indices[0, 0, 0, :6] = [kv_s, kv_s + 1, kv_s + 17, kv_s + 39, kv_s - 1, 0]
+    c.sparse_indices[1, 0, 0, :2] = [kv_s - 1, 3]
+    # batch 2: every entry selects a token at or past its length, so its tiles are live but empty
+    nv2 = int((c.sparse_indices[2, 0, 0] >= 0).sum())
+    c.sparse_indices[2, 0, 0, :nv2] = kv_s - 100 + np.arange(nv2) % 100
+    got, mx, sm, op = run_gpu(c, lse=True)
+    ref, rmx, rsm = run_ref(c, lse=True)
+    assert max_abs_err(got, ref) <= TOL[c.dtype]
+    assert np.all(got[2] == 0) and np.all(np.isneginf(mx[2])) and np.all(sm[2] == 0)
+    assert op.device_errors() == 0
+    c.query = np.zeros_like(c.query)
+    c.query_rope = np.zeros_like(c.query_rope)
+    _, _, sm0, _ = run_gpu(c, lse=True)
+    _, _, rsm0 = run_ref(c, lse=True)
+    assert np.array_equal(sm0, rsm0), np.argwhere(sm0 != rsm0)[:8]
+
+
 @pytest.mark.parametrize("lk", ["BSND", "TND"])
 def test_sfa_contiguous_keys_blockwise_runs(lk):
     # block-wise runs of 16 tokens as tiled boxes over contiguous key rows (no cache blocks)
