@@ -119,3 +119,65 @@ def test_planner_is_deterministic(driver):
     pr = [32, 64, 8, 128, 2, 0, 152] + list(r.integers(256, 8193, 32))
     a, b = run(driver, [pr, pr])
     assert a[:4] == b[:4] and (a[4] == b[4]).all()
+
+
+# ---------------------------------------------------------------- window resolution (build_windows)
+
+def windows(driver, B, smax, lens, pads=None, paged=False, cols=0, bs=128):
+    lens = [-9] * B if lens is None else list(lens)
+    pads = [] if pads is None else list(pads)
+    line = f"w {B} {smax} {int(paged)} {cols} {bs} {len(pads)} " + " ".join(map(str, pads + lens)) + "\n"
+    out = subprocess.run([driver], input=line, capture_output=True, text=True, check=True).stdout.split()
+    if out[0] == "error":
+        return int(out[1])
+    W, T = int(out[0]), int(out[1])
+    v = np.array(list(map(int, out[2:])), dtype=np.int64)
+    return W, T, v[:B], v[B:]
+
+
+def expected_window(smax, length, pad):
+    """The IncreFlashAttention README's kv left padding rule: tokens [Smax - pad - len, Smax - pad),
+    a negative pad counting as 0, an all-zero row (empty window) when the start or the end falls
+    below 0; without padding sizes the first len tokens."""
+    if pad is None:
+        return 0, length
+    pad = max(pad, 0)
+    st, en = smax - pad - length, smax - pad
+    if st < 0 or en < 0:
+        return 0, 0
+    return st, length
+
+
+def test_windows_follow_the_left_padding_rule(driver):
+    r = np.random.default_rng(11)
+    smax = 1000
+    lens = [0, 1, 1000, 999, 500, 700, 37, 1000] + list(r.integers(0, 1001, 24))
+    pads = [0, 999, 0, 1, -5, 301, 963, 1] + list(r.integers(-20, 1001, 24))
+    B = len(lens)
+    W, T, st, ln = windows(driver, B, smax, lens, pads)
+    for b in range(B):
+        assert (st[b], ln[b]) == expected_window(smax, lens[b], pads[b]), b
+    assert W == sum((int(x) + T - 1) // T for x in ln) * 2  # tiles of every (batch, kv head)
+    # one broadcast padding size
+    W1, _, st1, ln1 = windows(driver, 4, smax, [10, 200, 990, 995], [7])
+    for b, L in enumerate([10, 200, 990, 995]):
+        assert (st1[b], ln1[b]) == expected_window(smax, L, 7)
+
+
+def test_windows_without_padding_and_rejected_lengths(driver):
+    # right padding: the first len tokens; without lengths every batch uses maxSeqLen
+    _, _, st, ln = windows(driver, 3, 300, [0, 17, 300])
+    assert list(st) == [0, 0, 0] and list(ln) == [0, 17, 300]
+    _, _, st, ln = windows(driver, 2, 300, None)
+    assert list(ln) == [300, 300]
+    # padding sizes without lengths leave the window right padded
+    _, _, st, ln = windows(driver, 2, 300, None, [5, 9])
+    assert list(st) == [0, 0] and list(ln) == [300, 300]
+    # a length above the cache, or negative, is refused (161002)
+    assert windows(driver, 2, 300, [301, 1]) == 161002
+    assert windows(driver, 2, 300, [-1, 1]) == 161002
+    assert windows(driver, 2, 300, [-1, 1], [0]) == 161002
+    # paged: up to blockTableCols * blockSize tokens
+    _, _, st, ln = windows(driver, 2, 0, [512, 1], paged=True, cols=4, bs=128)
+    assert list(ln) == [512, 1]
+    assert windows(driver, 2, 0, [513, 1], paged=True, cols=4, bs=128) == 161002
