@@ -477,11 +477,32 @@ def oracle_unit(case, b, frac):
     return algorithmic_bytes(c), time.perf_counter() - t
 
 
+def input_copies(args, alg):
+    """Input copies the device arm rotates through: enough that the bytes streamed between two
+    uses of one copy exceed L2 several times (inputs larger than L2: no flush between steps)."""
+    return args.copies or max(1, min(8, math.ceil(6 * L2_BYTES / max(1, alg))))
+
+
+def l2_method(args, case):
+    """How the device arm keeps L2 from serving repeated inputs, stated for `config`."""
+    if isinstance(case, gen.AppendCase):
+        return "no flush: the append caches stay resident (launch-bound calls)"
+    alg = algorithmic_bytes(case)
+    copies = input_copies(args, alg)
+    if copies * alg >= L2_BYTES:
+        return (f"inputs larger than L2, no flush: {copies} input cop{'y' if copies == 1 else 'ies'} in "
+                f"rotation, {copies * alg / 1e6:.0f} MB of algorithmic bytes between two uses of a copy")
+    return (f"inputs resident in L2 ({copies} input copies in rotation, {copies * alg / 1e6:.1f} MB): "
+            f"a latency-bound workload")
+
+
 def line_config(args, case, world):
-    """The `config` object both arms print: the workload, its seed and algorithmic bytes."""
+    """The `config` object both arms print: the workload, its seed, algorithmic bytes and the
+    device arm's L2 method."""
     return {"workload": WORKLOADS[args.workload], "name": args.workload, "seed": args.seed,
             "algorithmic_bytes_per_step": algorithmic_bytes(case),
-            "parallelism": f"replica x{world}" if world > 1 else "single GPU"}
+            "parallelism": f"replica x{world}" if world > 1 else "single GPU",
+            "l2": l2_method(args, case)}
 
 
 def run_reference(args):
@@ -731,9 +752,7 @@ def run_gpu(args):
 
     case = make_case(args.workload, args.seed + rank)
     alg = algorithmic_bytes(case)
-    # Rotate through enough input copies that the bytes streamed between two uses of one
-    # copy exceed L2 several times (inputs larger than L2: no flush between steps).
-    copies = args.copies or max(1, min(8, math.ceil(6 * L2_BYTES / max(1, alg))))
+    copies = input_copies(args, alg)
     if isinstance(case, gen.AppendCase):
         wl = AppendWorkload(case, dev, copies)
     elif isinstance(case, gen.SfaCase):
