@@ -27,6 +27,12 @@ def test_reference_arm_line(workload):
     assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 20
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    # the config both arms print, L2 method included
+    sys.path.insert(0, ROOT)
+    import bench
+    args = bench.parse(["--workload", workload])
+    assert line["config"] == bench.line_config(args, bench.make_case(workload, 0), 1)
+    assert line["config"]["l2"]
 
 
 def test_reference_arm_time_is_bounded_for_many_steps():
