@@ -127,10 +127,10 @@ def sfa_live_tiles(idx_rows):
 def sfa_pieces_per_row(idx_rows, sms):
     """CTA pairs that hold a part of each index row, under the library's split: pairs take equal
     contiguous shares (floor(c W / Pa)) of the rows' live tiles in row order, with at most one pair
-    per two SMs and shares of at least min(tiles per row, 4) tiles."""
+    per two SMs and shares of at least one tile (the library's smallest share)."""
     eff = sfa_live_tiles(idx_rows).astype(np.int64)
     tps = -(-idx_rows.shape[1] // 128)
-    share = max(1, min(tps, 4))
+    share = 1
     launched = max(1, min(min(256, sms) // 2, -(-(len(eff) * tps) // share)))
     W = int(eff.sum())
     Pa = max(1, min(launched, -(-W // share)))

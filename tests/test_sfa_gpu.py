@@ -128,6 +128,18 @@ def test_sfa_full_size_sampled(seed):
     check(c, batches=np.sort(rng.choice(c.B, size=3, replace=False)))
 
 
+@pytest.mark.parametrize("Q_S,mode", [(1, 0), (2, 3)])
+def test_sfa_fp16_full_size_sampled(Q_S, mode):
+    """fp16 operands and output at the sparse MLA workload's full size (rows cut across CTA pairs,
+    so the merge runs), sampled batches within the fp16 bound of 2e-3."""
+    c = gen.sfa_mla(14 + Q_S, Q_S=Q_S, sparse_mode=mode, dtype="fp16")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pieces, _ = sfa_pieces_per_row(c.sparse_indices.reshape(c.B * Q_S, -1), sms)
+    assert (pieces >= 2).mean() >= 0.75
+    got, _ = check(c, batches=np.array([0, 9, 31]))
+    assert TOL["fp16"] == 2e-3
+
+
 def test_sfa_mtp_full_size_sampled():
     # the multi-token workload at full size (B=32, Q_S=2, 2048 indices per row, causal), sampled batches
     c = gen.sfa_mla(0, Q_S=2, sparse_mode=3)
