@@ -1080,3 +1080,47 @@ def test_sfa_bsnd_tokens_past_the_key_tensor_are_skipped():
     ref = oracle.sfa_ref(c.query, c.query_rope, k, kr, v, pruned, None, np.array([64, 64], np.int32),
                          scale=c.scale, layout_kv="BSND")
     assert np.array_equal(got, ref)
+
+
+def test_kv_append_bounds_at_the_edges_of_the_cache():
+    """A position of -1 in a later batch, and a paged position exactly at blockTableCols *
+    blockSize (whose entry would be the next row's first), write nothing: the neighbouring
+    batch's rows and blocks stay as they were."""
+    rng = np.random.default_rng(64)
+    kn = rng.standard_normal((2, 1, 8)).astype(np.float16)
+    kc = rng.standard_normal((2, 1, 5, 8)).astype(np.float16)
+    k2, _, bad = oracle.kv_append_ref(kn, kn, np.array([0, -1]), kc, kc)
+    assert bad == 1
+    assert np.array_equal(k2[1], kc[1]) and np.array_equal(k2[0, 0, 1:], kc[0, 0, 1:])
+    assert np.array_equal(k2[0, 0, 0], kn[0, 0])
+    bt = np.array([[0, 1], [2, 3]], dtype=np.int32)
+    pc = rng.standard_normal((4, 1, 4, 8)).astype(np.float16)
+    k3, _, bad = oracle.kv_append_ref(kn, kn, np.array([8, 3]), pc, pc, kv_format=oracle.PAGED_NBSD,
+                                      block_size=4, block_table=bt)
+    assert bad == 1
+    # batch 1's position 3 is slot 3 of its first block (block 2); nothing else changes
+    assert np.array_equal(k3[[0, 1, 3]], pc[[0, 1, 3]]) and np.array_equal(k3[2, 0, :3], pc[2, 0, :3])
+    assert np.array_equal(k3[2, 0, 3], kn[1, 0])
+
+
+def test_output_quantisation_of_nan_is_zero():
+    """Reading 20: a NaN output quantises to code 0 (finite neighbours are unaffected)."""
+    y = np.array([[[np.nan, 1.0, -2.0, np.nan]]])
+    assert list(oracle.quantize_output_ref(y, np.array([3.0], np.float32))[0, 0]) == [0, 3, -6, 0]
+
+
+def test_sfa_tnd_tokens_past_the_key_tensor_are_skipped():
+    """layout_kv TND whose last prefix sum runs past KV_T (the key tensor's rows): the last
+    batch's tokens at or past its remaining rows select nothing, as if their indices were -1."""
+    c = _sfa(61, B=2, sparse_size=16, nvalid_lo=16, nvalid_hi=16)
+    k, kr, v = _contig_kv(c, kv_len=64)
+    kt, krt, vt = (np.concatenate([t[0, :64], t[1, :40]]) for t in (k, kr, v))  # KV_T = 104
+    idx = c.sparse_indices.copy()
+    idx[1, 0, 0, :4] = [40, 41, 50, 39]  # batch 1 owns rows 64..103: tokens 40+ are past KV_T
+    got = oracle.sfa_ref(c.query, c.query_rope, kt, krt, vt, idx, None, np.array([64, 124], np.int32),
+                         scale=c.scale, layout_kv="TND")
+    pruned = idx.copy()
+    pruned[1, 0, 0, :3] = -1
+    ref = oracle.sfa_ref(c.query, c.query_rope, kt, krt, vt, pruned, None, np.array([64, 104], np.int32),
+                         scale=c.scale, layout_kv="TND")
+    assert np.array_equal(got, ref)
