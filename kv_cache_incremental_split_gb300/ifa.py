@@ -196,6 +196,11 @@ class IncreFlashAttention:
     Construction validates the description (``ifa_create``) and allocates the
     device workspace with torch.  Calling the object enqueues ``ifa_run`` on
     the current (or given) torch stream and returns the output tensor.
+
+    Devices: the plan's device state is created on the CUDA device current at
+    construction, so construct and call the object with the same device current
+    (``device``, when given, must be that device), and pass tensors and streams
+    of that device.
     """
 
     def __init__(self, *, batch: int, num_heads: int, num_kv_heads: int = 0, head_dim: int,
