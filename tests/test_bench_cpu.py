@@ -40,3 +40,30 @@ def test_reference_arm_time_is_bounded_for_many_steps():
     line, wall = run_ref("gqa_padded", 20000, 20, 5.0)
     assert line["steps"] == 20000
     assert wall < 180
+
+
+def test_algorithmic_bytes_closed_forms():
+    """The bytes behind every reported GB/s: only what the method must move.  The tiny MHA
+    workload is exactly K + V (262 144 B) plus query and output (2 x 1 024 B); GQA counts the
+    valid tokens' key/value rows, query, output and the mask over the valid windows; paging adds
+    one block-table entry per block used; the sparse decode moves 2 176 B per selected token
+    (key 1 024 + rope 128 + value 1 024; 1 152 B when value is key) plus one block-table entry,
+    the query, the output and the index rows."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    from kv_cache_incremental_split_gb300 import inputs as gen
+    assert bench.algorithmic_bytes(bench.make_case("tiny_mha", 0)) == 264_192
+    g = gen.gqa_padded(3, B=4, N=32, KV_N=8, D=128, Smax=512)
+    toks = int(g.actual_seq_lengths.sum())
+    assert bench.algorithmic_bytes(g) == 2 * toks * 8 * 128 * 2 + 2 * 4 * 32 * 128 * 2 + toks
+    p = gen.paged_gqa(4, B=5, N=32, KV_N=8, D=128, block_size=128, len_lo=100, len_hi=1000)
+    lens = p.actual_seq_lengths.astype(np.int64)
+    assert bench.algorithmic_bytes(p) == (2 * int(lens.sum()) * 8 * 128 * 2 + 2 * 5 * 32 * 128 * 2
+                                          + int(((lens + 127) // 128).sum()) * 4)
+    s = gen.sfa_mla(5, B=3, Q_N=128, block_size=64, kv_len=4096, sparse_size=512, nvalid_lo=100, nvalid_hi=512)
+    n = int(((s.sparse_indices >= 0) & (s.sparse_indices < s.actual_seq_lengths_kv[:, None, None, None])).sum())
+    fixed = 3 * 128 * (512 + 64) * 2 + 3 * 128 * 512 * 2 + s.sparse_indices.nbytes
+    assert bench.algorithmic_bytes(s) == n * (2_176 + 4) + fixed
+    s.value = s.key
+    assert bench.algorithmic_bytes(s) == n * (1_152 + 4) + fixed
